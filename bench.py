@@ -1,0 +1,491 @@
+#!/usr/bin/env python3
+"""Benchmark of one tree-verification step on GB300.
+
+A step is the whole hot path over one batch: the Hydra draft heads fill the
+64-node candidate tree (hidden 4096, vocabulary 32000, 4 sequentially
+dependent heads, top-k 8/4/2/1), the tree tokens attend over a 1024-token KV
+prefix (32 heads x 128, bf16), and greedy acceptance picks the longest accepted
+path (target logits planted so the mean accepted length is about 2.5).  Batch 1,
+synthetic seeded inputs resident in HBM; L2 is flushed between timed steps.
+
+Prints one JSON line (rank 0).  `--impl reference` times the CPU oracle on the
+same workload instead (the oracle is a deliberately plain NumPy fp64 program).
+Multi-GPU runs (torchrun) give every rank its own independent batch: no data
+exchange, weak scaling; the reported time is the maximum over ranks.
+"""
+
+import argparse
+import hashlib
+import json
+import os
+import resource
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np
+
+METRIC = "verify steps/s & tree-node tokens/s per step; achieved HBM GB/s vs GB300 peak"
+UNIT = "verify steps/s"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def workload(seed):
+    import spec_workloads as wl
+    base = wl.WORKLOADS[2]
+    return wl.Workload("vicuna7b-verify-step", "bf16", B=1, seed=seed, tree=base.tree,
+                       d=4096, V=32000, cond=(1, 1, 1, 1), topk=(8, 4, 2, 1),
+                       Hq=32, Hkv=32, D=128, Lmax=1024, prefix=(1024, 1024),
+                       accept="greedy", accept_lengths=(1, 2, 3, 4))
+
+
+def config_of(w, T):
+    return {
+        "workload": "vicuna7b-verify-step: Hydra draft heads (hidden 4096, vocab 32000, 4 heads, top-k 8/4/2/1) "
+                    "+ tree attention (32x128 heads, prefix 1024) + greedy acceptance, 64-node sparse tree, batch 1",
+        "batch": w.B, "tree_nodes": T, "prefix": w.Lmax, "hidden": w.d, "vocab": w.V,
+        "attention_heads": f"{w.Hq}x{w.D}", "draft_heads": len(w.cond), "topk": list(w.topk),
+        "acceptance": "greedy", "l2": "flushed between timed steps (256 MB write)",
+    }
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def init_dist(backend):
+    import torch.distributed as dist
+    rank, local, world = dist_info()
+    if world > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        os.environ.setdefault("MASTER_PORT", "29511")
+        dist.init_process_group(backend=backend, rank=rank, world_size=world)
+    return rank, local, world
+
+
+def max_over_ranks(x, device=None):
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None:
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons, every 200 ms."""
+
+    FIELDS = ["index", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+        self.marks = {}
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + ",".join(self.FIELDS),
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == len(self.FIELDS):
+                self.samples.append((time.time(), parts))
+
+    def mark(self, name):
+        self.marks[name] = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0, t1):
+        if not self.samples:
+            return None
+        inside = [p for (t, p) in self.samples if t0 - 0.25 <= t <= t1 + 0.25]
+        if len(inside) < 2:
+            inside = [p for (_, p) in self.samples[-5:]]
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(p[1]) for p in inside if num(p[1]) is not None]
+        mx = [num(p[2]) for p in inside if num(p[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in inside for i in range(4) if p[5 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(inside)}
+
+
+# ---------------------------------------------------------------- roofline bookkeeping
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def algorithmic_bytes(name, ctx):
+    """Algorithmic HBM bytes per launch of each kernel of the step (what the math must move)."""
+    w, rows = ctx["w"], ctx["rows"]
+    s = 2  # bf16
+    d, V = w.d, w.V
+    heads = [k for k in range(len(w.cond)) if rows[k] > 0]
+    if name.startswith("draft_proj"):
+        return sum(V * d * s + rows[k] * d * s for k in heads) / len(heads)
+    if name.startswith("draft_mlp"):
+        return sum(d * 2 * d * s + d * s + rows[k] * 2 * d * s + rows[k] * d * s for k in heads) / len(heads)
+    if name.startswith("attn_") and name != "attn_combine":
+        T = ctx["T"]
+        return (sum(ctx["prefix_len"]) * w.Hkv * w.D * 2 * s + w.B * w.Hq * T * w.D * s
+                + w.B * w.Hkv * T * w.D * 2 * s)
+    if name == "attn_combine":
+        return w.B * w.Hq * ctx["T"] * w.D * 4
+    if name == "accept_rows_greedy":
+        return w.B * ctx["T"] * w.V * 4
+    return None
+
+
+def recorded_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary, if its source is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    for line in lines:
+        if line.startswith("#") or not line.strip():
+            continue
+        parts = line.split()
+        if len(parts) >= 3 and parts[0] == kernel:
+            src = os.path.join(ROOT, "tree_speculative_decoding_spec_gb300", "csrc", parts[2].split(":")[0])
+            want = parts[2].split(":")[1] if ":" in parts[2] else ""
+            try:
+                have = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+            except OSError:
+                return None
+            return float(parts[1]) if have == want else None
+    return None
+
+
+# ---------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    rank, local, world = init_dist("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import oracle  # noqa: F401  (cpu baseline leg only)
+    import spec_workloads as wl
+    import tree_speculative_decoding_spec_gb300 as st
+
+    w = workload(seed=2 + 1000 * rank)
+    parent, rank_arr = wl.make_tree(w.tree)
+    T = len(parent)
+    dx = wl.draft_inputs(w)
+    ax = wl.attention_inputs(w, T)
+
+    def dev_t(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    tree = st.spec_tree_build(parent, rank_arr, device=dev)
+    h, E = dev_t(dx["h"]), dev_t(dx["E"])
+    W1 = [dev_t(a) for a in dx["W1"]]
+    b1 = [dev_t(a) for a in dx["b1"]]
+    W2 = [dev_t(a) for a in dx["W2"]]
+    root_tok = dev_t(dx["root_tok"])
+    q, kc, vc = dev_t(ax["q"]), dev_t(ax["k_cache"]), dev_t(ax["v_cache"])
+    plen, kt, vt = dev_t(ax["prefix_len"]), dev_t(ax["k_tree"]), dev_t(ax["v_tree"])
+    cond, topk = list(w.cond), list(w.topk)
+    B = w.B
+
+    node_tok = torch.empty(B, T, dtype=torch.int32, device=dev)
+    node_logit = torch.empty(B, T, dtype=torch.float32, device=dev)
+    node_logprob = torch.empty(B, T, dtype=torch.float32, device=dev)
+    out = torch.empty(B, w.Hq, T, w.D, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, w.Hq, T, dtype=torch.float32, device=dev)
+    alen = torch.empty(B, dtype=torch.int32, device=dev)
+    apath = torch.empty(B, tree.max_depth + 1, dtype=torch.int32, device=dev)
+    nxt = torch.empty(B, dtype=torch.int32, device=dev)
+    mg = torch.empty(B, dtype=torch.float32, device=dev)
+    ws_d = torch.empty(st.hydra_draft_workspace_size(tree, B, w.d, w.V, cond, topk, 1), dtype=torch.uint8, device=dev)
+    ws_a = torch.empty(st.tree_attention_workspace_size(tree, B, w.Hq, w.Hkv, w.Lmax, w.D, 1), dtype=torch.uint8, device=dev)
+    ws_c = torch.empty(st.tree_accept_workspace_size(0, tree, B, w.V), dtype=torch.uint8, device=dev)
+
+    def draft():
+        st.hydra_draft(h, E, W1, b1, W2, cond, topk, root_tok, tree, node_tok=node_tok, node_logit=node_logit,
+                       node_logprob=node_logprob, ws=ws_d)
+
+    # plant the target logits on the draft's own tokens (the target model itself is out of scope)
+    draft()
+    torch.cuda.synchronize()
+    gx = wl.greedy_inputs(w, parent, node_tok=node_tok.cpu().numpy())
+    logits_p = dev_t(gx["logits_p"])
+
+    def attention():
+        st.tree_attention(q, kc, vc, plen, kt, vt, tree, out=out, lse=lse, ws=ws_a)
+
+    def accept():
+        st.tree_accept(0, logits_p, None, node_tok, tree, accept_len=alen, accept_path=apath, next_token=nxt,
+                       margin=mg, ws=ws_c)
+
+    def step():
+        draft()
+        attention()
+        accept()
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    for _ in range(max(args.warmup, 0)):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+
+    # per-phase times (separate pass, not the headline)
+    phase_ms = {}
+    for name, fn in [("draft", draft), ("attention", attention), ("accept", accept)]:
+        evs = []
+        for _ in range(5):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        phase_ms[name] = statistics.median([a.elapsed_time(b) for a, b in evs])
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    launches0 = st.spec_launch_count()
+    st.spec_trace_begin(100000)
+    barrier(dev)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    evs = []
+    for _ in range(args.steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        step()
+        b.record(stream)
+        evs.append((a, b))
+        flush.zero_()
+    torch.cuda.synchronize()
+    barrier(dev)
+    t_wall1 = time.time()
+    kernels = st.spec_trace_end(256)
+    launches = st.spec_launch_count() - launches0
+    time.sleep(0.3)
+    clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in evs]
+    ms_per_step = max_over_ranks(sum(step_ms) / len(step_ms), dev)
+    value = world * 1000.0 / ms_per_step
+
+    # roofline of the dominant kernel
+    hbm, tf_burst, tf_sust, peak_src = peaks()
+    total_k = sum(v[1] for v in kernels.values())
+    dom = max(kernels.items(), key=lambda kv: kv[1][1])
+    dom_name, (dom_n, dom_ms) = dom
+    rows = [(B * tree.struct.n_internal_at_depth[k] if cond[k] else B) if tree.struct.n_internal_at_depth[k] else 0
+            for k in range(len(cond))]
+    ctx = {"w": w, "rows": rows, "T": T, "prefix_len": [int(x) for x in ax["prefix_len"]]}
+    abytes = algorithmic_bytes(dom_name, ctx)
+    per_launch_s = dom_ms / dom_n / 1000.0
+    achieved = abytes / per_launch_s / 1e9 if abytes else None
+    roofline = {"kernel": dom_name, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm if achieved else None, "traffic": recorded_traffic(dom_name),
+                "algorithmic_bytes_per_launch": abytes, "launch_us": per_launch_s * 1e6,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs, copy bandwidth)" if peak_src == "measured"
+                else "fallback 6.8 TB/s", "frac_of_nominal_8TBs": achieved / 8000.0 if achieved else None}
+    kern_table = {k: {"launches": n, "ms_per_launch": ms / n, "share": ms / total_k if total_k else None,
+                      "algorithmic_GBps": (algorithmic_bytes(k, ctx) / (ms / n / 1000.0) / 1e9)
+                      if algorithmic_bytes(k, ctx) else None}
+                  for k, (n, ms) in sorted(kernels.items(), key=lambda kv: -kv[1][1])}
+
+    # end-to-end through the public API with host buffers (pinned), copies inside the timed region
+    e2e = None
+    if not args.no_e2e:
+        host_in = {"h": h.cpu().pin_memory(), "root_tok": root_tok.cpu().pin_memory(), "q": q.cpu().pin_memory(),
+                   "k_tree": kt.cpu().pin_memory(), "v_tree": vt.cpu().pin_memory(),
+                   "prefix_len": plen.cpu().pin_memory(), "logits_p": logits_p.cpu().pin_memory()}
+        dev_in = {"h": h, "root_tok": root_tok, "q": q, "k_tree": kt, "v_tree": vt, "prefix_len": plen,
+                  "logits_p": logits_p}
+        host_out = {"node_tok": torch.empty_like(node_tok, device="cpu").pin_memory(),
+                    "accept_len": torch.empty_like(alen, device="cpu").pin_memory(),
+                    "accept_path": torch.empty_like(apath, device="cpu").pin_memory(),
+                    "next_token": torch.empty_like(nxt, device="cpu").pin_memory()}
+        dev_out = {"node_tok": node_tok, "accept_len": alen, "accept_path": apath, "next_token": nxt}
+        bi = sum(t.numel() * t.element_size() for t in host_in.values())
+        bo = sum(t.numel() * t.element_size() for t in host_out.values())
+        e_ms = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for k in host_in:
+                dev_in[k].copy_(host_in[k], non_blocking=True)
+            step()
+            for k in host_out:
+                host_out[k].copy_(dev_out[k], non_blocking=True)
+            b.record(stream)
+            b.synchronize()
+            if i >= args.warmup:
+                e_ms.append(a.elapsed_time(b))
+        e_mean = max_over_ranks(sum(e_ms) / len(e_ms), dev)
+        e2e = {"value": world * 1000.0 / e_mean, "unit": UNIT, "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo,
+               "ms_per_step": e_mean}
+
+    # CPU baseline: the oracle as it stands, one full step of the same workload
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = time_oracle_step(w, parent, rank_arr, dx, ax, gx)
+
+    if rank != 0:
+        return
+    accepted = float(alen.float().mean().item())
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init head weights, N(0,1) KV)",
+        "config": config_of(w, T),
+        "tree_node_tokens_per_s": value * B * T,
+        "accepted_tokens_per_s": value * B * (accepted + 1),
+        "phases_ms": phase_ms,
+        "kernels": kern_table,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "gpu_launches_per_step": launches / max(args.steps, 1),
+        "clocks": clocks.summary(t_wall0, t_wall1),
+        "wall_s_timed": t_wall1 - t_wall0,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def time_oracle_step(w, parent, rank_arr, dx, ax, gx):
+    import oracle
+    to = oracle.tree_encode(parent, rank_arr)
+    c0 = resource.getrusage(resource.RUSAGE_SELF)
+    t0 = time.perf_counter()
+    ref = oracle.hydra_draft(dx["h"], dx["E"], dx["W1"], dx["b1"], dx["W2"], dx["cond"], dx["topk"],
+                             dx["root_tok"], to, w.dtype)
+    oracle.tree_attention(**ax, tree=to, dtype=w.dtype)
+    oracle.greedy_accept(gx["logits_p"], ref["node_tok"], to)
+    t1 = time.perf_counter()
+    c1 = resource.getrusage(resource.RUSAGE_SELF)
+    cpu_s = (c1.ru_utime - c0.ru_utime) + (c1.ru_stime - c0.ru_stime)
+    return {"value": 1.0 / (t1 - t0), "unit": UNIT, "cores": round(cpu_s / (t1 - t0), 2),
+            "cores_available": os.cpu_count(), "kind": "oracle",
+            "sample": "one full verification step of the same workload (draft heads, attention, greedy acceptance), "
+                      "NumPy float64 on the host cores; cores = CPU time / wall time"}
+
+
+# ---------------------------------------------------------------- reference arm (the CPU oracle)
+
+def run_reference(args):
+    rank, local, world = dist_info()
+    if rank != 0:
+        return
+    import oracle
+    import spec_workloads as wl
+    w = workload(seed=2)
+    parent, rank_arr = wl.make_tree(w.tree)
+    T = len(parent)
+    dx = wl.draft_inputs(w)
+    ax = wl.attention_inputs(w, T)
+    to = oracle.tree_encode(parent, rank_arr)
+    tok = oracle.hydra_draft(dx["h"], dx["E"], dx["W1"], dx["b1"], dx["W2"], dx["cond"], dx["topk"], dx["root_tok"],
+                             to, w.dtype)["node_tok"]
+    gx = wl.greedy_inputs(w, parent, node_tok=tok)
+    for _ in range(max(args.warmup, 0)):
+        time_oracle_step(w, parent, rank_arr, dx, ax, gx)
+    times, cores = [], []
+    for _ in range(args.steps):
+        r = time_oracle_step(w, parent, rank_arr, dx, ax, gx)
+        times.append(1.0 / r["value"])
+        cores.append(r["cores"])
+    ms = 1000.0 * sum(times) / len(times)
+    value = 1000.0 / ms
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded)", "config": config_of(w, T),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": round(statistics.median(cores), 2),
+                         "cores_available": os.cpu_count(), "kind": "oracle",
+                         "sample": "each step: one full verification step of the workload on the host cores"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,254 @@
+/*
+ * spec_tree.h -- C ABI of a GB300 (sm_103a) library for one tree-verification
+ * step of Medusa/Hydra speculative decoding: draft heads fill a candidate tree,
+ * the tree tokens attend over a KV-cache prefix plus their own ancestors, and
+ * acceptance picks the longest accepted path (greedy, or the min(1, p/q) rule
+ * with residual resampling).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - The caller owns every buffer, device scratch ("workspace") included; its
+ *    size comes from the matching *_workspace_size call.  Apart from
+ *    spec_tree_build (which copies a small host table to the device and waits
+ *    for it) no call allocates, frees or synchronises; all work is queued on
+ *    the given stream in order.  0 selects the legacy default stream.
+ *  - "device" pointers must point to memory of the current CUDA device and be
+ *    16-byte aligned (SPEC_EALIGN otherwise); "host" pointers are read during
+ *    the call only.
+ *  - Every call checks its arguments on the host before it queues anything.
+ *    On failure it returns a non-zero spec_status, queues nothing, writes no
+ *    output, and spec_last_error() describes the problem (per host thread).
+ *    CUDA launch errors are reported as SPEC_ECUDA.
+ *  - Kernels never trap and never wait without bound.  A failure detected on
+ *    the device (a bounded wait that ran out) is recorded in the first 16 bytes
+ *    of the call's workspace; spec_read_device_status() returns it.
+ *  - Tokens are int32, logits and outputs float32; inputs of the float tensors
+ *    of a call share one spec_dtype (float32 or bfloat16 bit patterns).
+ *  - Tensor shapes are given outermost first and are densely packed (row-major).
+ */
+#ifndef SPEC_TREE_H
+#define SPEC_TREE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); declared opaquely so this header needs no CUDA headers. */
+typedef struct CUstream_st* spec_stream_t;
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_EINVAL = 1,       /* bad argument: null pointer, size out of range, shape mismatch */
+    SPEC_ETREE = 2,        /* malformed tree: parent[0] != -1, parent[i] not in [0, i), duplicate sibling rank */
+    SPEC_EALIGN = 3,       /* a device pointer is not 16-byte aligned */
+    SPEC_EWORKSPACE = 4,   /* workspace missing or smaller than *_workspace_size */
+    SPEC_EUNSUPPORTED = 5, /* a valid combination this build does not implement */
+    SPEC_ECUDA = 6,        /* a CUDA runtime call or launch failed */
+    SPEC_ETIMEOUT = 7      /* device status only: a bounded wait inside a kernel ran out */
+} spec_status;
+
+typedef enum { SPEC_F32 = 0, SPEC_BF16 = 1 } spec_dtype;
+
+#define SPEC_MAX_T 1024      /* tree nodes, root included */
+#define SPEC_MAX_DEPTH 16    /* deepest node; also the most draft heads */
+#define SPEC_MAX_TOPK 16     /* largest top-k per head */
+
+/*
+ * Candidate tree, encoded once per topology by spec_tree_build.
+ *
+ * Hydra Guide: Sequentially-Dependent Speculative AI, sections "Candidate Tree
+ * Construction" (the root is the base token x_t; a depth-k node holds a token
+ * proposed by head k; rank = which of the parent head's top-k candidates it
+ * is) and "Tree Attention Matrix with Topology-Aware Causal Masking" (the tree
+ * is flattened into one sequence; node u may attend to node v iff v is an
+ * ancestor of u or v = u).
+ *
+ * Host fields are filled by spec_tree_build; the pointers point into the
+ * caller's device buffer and stay valid as long as that buffer does.
+ */
+typedef struct {
+    int32_t T;                                   /* nodes, root (node 0) included */
+    int32_t max_depth;                           /* largest depth (root: 0) */
+    int32_t words;                               /* ceil(T / 64): 64-bit words per ancestor mask */
+    int32_t n_internal;                          /* nodes that have at least one child */
+    int32_t n_at_depth[SPEC_MAX_DEPTH + 1];      /* host: nodes of each depth */
+    int32_t n_internal_at_depth[SPEC_MAX_DEPTH + 1]; /* host: nodes of each depth that have children */
+    int32_t max_rank_at_depth[SPEC_MAX_DEPTH + 1];   /* host: largest rank among nodes of each depth (depth >= 1) */
+    const int32_t* parent;        /* device [T]; parent[0] = -1, parent[i] < i */
+    const int32_t* depth;         /* device [T] */
+    const int32_t* rank;          /* device [T]; 0 for the root */
+    const uint64_t* anc;          /* device [T][words]; bit j of row i set iff j is i or an ancestor of i */
+    const int32_t* internal;      /* device [n_internal]: nodes with children, by depth then index */
+    const int32_t* internal_off;  /* device [SPEC_MAX_DEPTH + 2]: depth d's nodes start at internal[internal_off[d]] */
+    const int32_t* row_of;        /* device [T]: position of a node within its depth's internal list, -1 for leaves */
+    const int32_t* child_off;     /* device [T + 1]: children of u are child_idx[child_off[u] .. child_off[u+1]) */
+    const int32_t* child_idx;     /* device [max(T - 1, 1)], ascending per parent */
+} spec_tree;
+
+/* Bytes of device memory spec_tree_build needs for a tree of T nodes (0 if T is out of range). */
+size_t spec_tree_device_bytes(int32_t T);
+
+/*
+ * Validate a parent-index tree and encode it for the other calls.
+ *   parent  host [T]: parent[0] = -1, 0 <= parent[i] < i.
+ *   rank    host [T] or NULL: rank[i] >= 0 is node i's slot among its parent
+ *           head's top-k (0 = most probable); distinct among siblings.  NULL
+ *           numbers each node's children 0, 1, ... in index order.
+ *   T       1 .. SPEC_MAX_T; the tree's depth must be <= SPEC_MAX_DEPTH.
+ *   d_buf   device buffer of at least spec_tree_device_bytes(T) bytes.
+ *   out     host struct filled on success.
+ * Copies the encoded tables to d_buf on stream s and waits for that copy.
+ */
+spec_status spec_tree_build(const int32_t* parent, const int32_t* rank, int32_t T,
+                            void* d_buf, size_t d_bytes, spec_tree* out, spec_stream_t s);
+
+/* Workspace bytes hydra_draft needs for these shapes (0 on invalid arguments). */
+size_t hydra_draft_workspace_size(const spec_tree* tree, int32_t B, int32_t d, int32_t V, int32_t K,
+                                  const int32_t* cond, const int32_t* topk, spec_dtype dt);
+
+/*
+ * Draft heads: fill every candidate node of every sequence with a token.
+ *
+ * Medusa Heads (ultralytics glossary), section "So sagen die Köpfe voraus": a
+ * head is one feed-forward layer with SiLU and a residual, then a projection
+ * onto the vocabulary.  Hydra Guide, sections "1. Embedding Conditioning
+ * Mechanics" and "Candidate Tree Construction": a sequentially dependent head
+ * also reads the base-embedding row of its parent node's token, and each
+ * node's children are the top-k of the head run on that node.  Per head k
+ * (filling depth k + 1) and parent node u of sequence b:
+ *     u_in = h_b                     if cond[k] == 0   (W1[k] is [d, d])
+ *     u_in = [h_b || emb[tok(u)]]    if cond[k] == 1   (W1[k] is [d, 2d])
+ *     z    = h_b + SiLU(W1[k] u_in + b1[k])   (rounded to bf16 when dt is bf16)
+ *     l    = W2[k] z                 ([V] logits, never written to memory)
+ * A child of rank r gets the (r+1)-th largest logit (ties: lower token id).
+ *
+ *   h          device [B, d]                 hidden state of each sequence
+ *   emb        device [V, d]                 base token-embedding table
+ *   K          number of heads, >= tree->max_depth, <= SPEC_MAX_DEPTH
+ *   W1, b1, W2 host arrays [K] of device pointers: W1[k] [d, d_in_k] (out x in),
+ *              b1[k] [d] (a NULL entry or a NULL array means no bias), W2[k] [V, d]
+ *   cond, topk host [K]: cond[k] in {0, 1}; topk[k] in 1 .. SPEC_MAX_TOPK and
+ *              > the largest rank among depth-(k+1) nodes
+ *   root_tok   device [B]                     token of node 0 (the base token x_t)
+ *   node_tok   device [B, T] out: node 0 = root_tok, others = drafted tokens
+ *   node_logit device [B, T] out: the node's logit in its parent's row (root: 0)
+ *   node_logprob device [B, T] out or NULL: cumulative log-probability along
+ *              the node's path, log-softmax of each row (root: 0)
+ * Shapes: 1 <= B, d % 8 == 0, 1 <= d <= 16384, topk[k] <= V <= 2^24.
+ */
+spec_status hydra_draft(const void* h, const void* emb, int32_t K,
+                        const void* const* W1, const void* const* b1, const void* const* W2,
+                        const int32_t* cond, const int32_t* topk, const int32_t* root_tok,
+                        const spec_tree* tree, int32_t B, int32_t d, int32_t V, spec_dtype dt,
+                        int32_t* node_tok, float* node_logit, float* node_logprob,
+                        void* ws, size_t ws_bytes, spec_stream_t s);
+
+/* Workspace bytes tree_attention needs for these shapes on the current device (0 on invalid arguments). */
+size_t tree_attention_workspace_size(const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv,
+                                     int32_t Lmax, int32_t D, spec_dtype dt);
+
+/*
+ * Tree attention of one layer.
+ *
+ * Hydra Guide, section "Tree Attention Matrix with Topology-Aware Causal
+ * Masking": every tree token sees the whole cached prefix and, among the tree
+ * tokens, only itself and its ancestors (M_tree = 0 there, -inf elsewhere), so
+ * its output equals autoregressive attention over [prompt, ancestors, itself].
+ * For query head h (KV head h / (Hq / Hkv)), sequence b and node i:
+ *     keys  = k_cache[b, :prefix_len[b]] followed by k_tree[b, a] for a in anc*(i)
+ *     out   = softmax(scale * q . keys) . values,  lse = log(sum exp(scale * q . keys))
+ *
+ *   q                 device [B, Hq, T, D]
+ *   k_cache, v_cache  device [B, Hkv, Lmax, D]; rows >= prefix_len[b] are not read
+ *   prefix_len        device [B], each in 0 .. Lmax (values outside are clamped to it)
+ *   k_tree, v_tree    device [B, Hkv, T, D]: keys/values of the tree tokens
+ *   scale             > 0 (usually 1/sqrt(D))
+ *   out               device [B, Hq, T, D] float32
+ *   lse               device [B, Hq, T] float32, or NULL
+ * Shapes: Hq % Hkv == 0, D in {64, 128}, 1 <= Lmax <= 2^22.
+ */
+spec_status tree_attention(const void* q, const void* k_cache, const void* v_cache,
+                           const int32_t* prefix_len, const void* k_tree, const void* v_tree,
+                           const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
+                           int32_t D, float scale, spec_dtype dt, float* out, float* lse,
+                           void* ws, size_t ws_bytes, spec_stream_t s);
+
+/* Workspace bytes tree_accept needs (0 on invalid arguments). */
+size_t tree_accept_workspace_size(int32_t mode, const spec_tree* tree, int32_t B, int32_t V);
+
+/*
+ * Acceptance: longest accepted path and the extra token.
+ *
+ * mode 0, greedy -- Hydra Guide, section "Parallel Verification and Greedy
+ *   Acceptance Algorithm": a(u) = argmax logits_p[b, u] (ties: lower id); a
+ *   node is accepted when its parent is and its token equals a(parent); the
+ *   deepest accepted node u* (lowest index on equal depth) ends the path and
+ *   a(u*) is the extra token.  temperature, seed, offset and logits_q unused.
+ * mode 1, rejection -- Speculative Decoding (thegustafson.com), sections "The
+ *   acceptance criterion", "The correctness guarantee" and "A worked example":
+ *   p_u = softmax(logits_p[b, u] / temperature), q_u likewise from logits_q;
+ *   the edge into node c with token x is accepted iff u_c < p_par(x) / q_par(x);
+ *   u* as above; the extra token is drawn from norm(max(p_u* - q_u*, 0)) when u*
+ *   has children (from p_u* if that residual is zero), else from p_u*, by
+ *   inverse CDF in ascending token order with uniform u'.  u_c is word 0 and u'
+ *   word 1 of Philox4x32-10 (Salmon et al., SC'11) with key (seed low, seed
+ *   high) and counter (node, b, offset low, offset high) -- u' from node 0 --
+ *   each word w mapped to (w >> 8) * 2^-24.
+ *
+ *   logits_p     device [B, T, V] float32 target logits (row u predicts the token after u)
+ *   logits_q     device [B, T, V] float32 draft logits (rejection; rows of leaves not read) or NULL
+ *   node_tok     device [B, T]
+ *   accept_len   device [B] out: m, the depth of u*
+ *   accept_path  device [B, max_depth + 1] out: node ids root first, -1 padded
+ *   next_token   device [B] out: the extra token
+ *   margin       device [B] out or NULL: distance of the closest decision to its
+ *                threshold (greedy: smallest top-1 minus top-2 logit gap over accepted
+ *                nodes; rejection: smallest |u_c - ratio| over decided edges with
+ *                ratio < 1, or the sampling draw's distance to a CDF breakpoint over the total)
+ * Shapes: 2 <= V <= 2^24; temperature > 0 for mode 1.
+ */
+spec_status tree_accept(int32_t mode, const float* logits_p, const float* logits_q, const int32_t* node_tok,
+                        const spec_tree* tree, int32_t B, int32_t V, float temperature,
+                        uint64_t seed, uint64_t offset, int32_t* accept_len, int32_t* accept_path,
+                        int32_t* next_token, float* margin, void* ws, size_t ws_bytes, spec_stream_t s);
+
+/*
+ * The uniforms tree_accept draws, for inspection: u_accept [B, T] (entry
+ * [b, c] = word 0 of counter (c, b, offset)), u_sample [B] (word 1 of counter
+ * (0, b, offset)).  Device pointers.  Salmon et al., SC'11, Philox4x32-10.
+ */
+spec_status spec_philox_uniform(uint64_t seed, uint64_t offset, int32_t B, int32_t T,
+                                float* u_accept, float* u_sample, spec_stream_t s);
+
+/* Message of the last failed call on this host thread ("" if none). */
+const char* spec_last_error(void);
+
+/* Copy the device status word kept at the start of a workspace to *status and wait for it (SPEC_OK = no failure). */
+spec_status spec_read_device_status(const void* ws, int32_t* status, spec_stream_t s);
+
+/*
+ * Kernel tracing.  While enabled, every kernel this library launches is
+ * bracketed by a pair of CUDA events on its launch stream (at most `capacity`
+ * launches are recorded).  spec_trace_end waits for them, totals the time per
+ * kernel name into out[0 .. max_entries) and returns the number of entries,
+ * or -1 on error.  spec_launch_count counts every kernel launch of this
+ * library in this process.  Tracing is process-wide and not thread-safe.
+ */
+typedef struct {
+    char name[48];
+    int32_t launches;
+    double total_ms;
+} spec_trace_entry;
+
+spec_status spec_trace_begin(int32_t capacity);
+int32_t spec_trace_end(spec_trace_entry* out, int32_t max_entries);
+int64_t spec_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_TREE_H */

@@ -114,18 +114,53 @@ def tree_depths(parent):
 # tensors
 
 def f32_to_bf16_bits(x):
-    """float32 -> bf16 bit patterns, round to nearest even (storage format only)."""
-    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = u + (((u >> np.uint64(16)) & np.uint64(1)) + np.uint64(0x7FFF))
-    return (u >> np.uint64(16)).astype(np.uint16)
+    """float32 -> bf16 bit patterns, round to nearest even (storage format only; finite inputs)."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32)
+    r = (u >> np.uint32(16)) & np.uint32(1)
+    r += np.uint32(0x7FFF)
+    r += u
+    r >>= np.uint32(16)
+    return r.astype(np.uint16)
 
 
-def normal(rng, shape, std=1.0, dtype="f32"):
-    """N(0, std^2) samples as float32, or as bf16 bits when dtype == 'bf16'."""
-    x = rng.standard_normal(size=shape, dtype=np.float32)
-    if std != 1.0:
-        x *= np.float32(std)
-    return f32_to_bf16_bits(x) if dtype == "bf16" else x
+_CHUNK = 1 << 22
+_POOL = None
+
+
+def _pool():
+    global _POOL
+    if _POOL is None:
+        import concurrent.futures as cf
+        import os
+        _POOL = cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 4))
+    return _POOL
+
+
+def normal(key, shape, std=1.0, dtype="f32"):
+    """N(0, std^2) samples as float32, or as bf16 bits when dtype == 'bf16'.
+
+    ``key`` is a tuple of integers; the array is drawn in chunks of 2^22
+    elements, chunk c from numpy's default generator seeded with key + (c,),
+    so the values do not depend on how many threads fill them.
+    """
+    shape = tuple(int(s) for s in (shape if isinstance(shape, (tuple, list)) else (shape,)))
+    n = int(np.prod(shape)) if shape else 1
+    out = np.empty(n, dtype=np.uint16 if dtype == "bf16" else np.float32)
+
+    def fill(c):
+        lo, hi = c * _CHUNK, min(n, (c + 1) * _CHUNK)
+        x = np.random.default_rng(list(key) + [c]).standard_normal(size=hi - lo, dtype=np.float32)
+        if std != 1.0:
+            x *= np.float32(std)
+        out[lo:hi] = f32_to_bf16_bits(x) if dtype == "bf16" else x
+
+    nchunks = (n + _CHUNK - 1) // _CHUNK
+    if nchunks <= 1:
+        for c in range(nchunks):
+            fill(c)
+    else:
+        list(_pool().map(fill, range(nchunks)))
+    return out.reshape(shape)
 
 
 def sibling_tokens(rng, parent, B, V, root_tok=None):
@@ -142,7 +177,7 @@ def sibling_tokens(rng, parent, B, V, root_tok=None):
     return tok
 
 
-def plant_greedy(rng, parent, node_tok, V, lengths, std=2.0):
+def plant_greedy(rng, key, parent, node_tok, V, lengths, std=2.0):
     """Target logits [B, T, V] ~ N(0, std^2) in which greedy acceptance stops at depth lengths[b].
 
     For each sequence a node u_m of depth m = lengths[b] is drawn uniformly; along
@@ -154,7 +189,7 @@ def plant_greedy(rng, parent, node_tok, V, lengths, std=2.0):
     B, T = node_tok.shape
     depth = tree_depths(parent)
     ch = _children(parent)
-    logits = rng.standard_normal(size=(B, T, V), dtype=np.float32) * np.float32(std)
+    logits = normal(key, (B, T, V), std)
     for b in range(B):
         m = int(lengths[b])
         cands = np.nonzero(depth == m)[0]
@@ -254,20 +289,21 @@ def _rng(seed, part):
 def draft_inputs(w, B=None, seed=None):
     """Draft-head inputs: h [B, d] ~ N(0,1); E [V, d], W1_k [d, d_in_k], b1_k [d], W2_k [V, d] ~ N(0, 0.02^2); root tokens uniform."""
     B = w.B if B is None else B
-    rng = _rng(w.seed if seed is None else seed, 1)
+    s = w.seed if seed is None else seed
     d, V = w.d, w.V
+    rng = _rng(s, 1)
     out = {
-        "h": normal(rng, (B, d), 1.0, w.dtype),
-        "E": normal(rng, (V, d), 0.02, w.dtype),
+        "h": normal((s, 1, 0), (B, d), 1.0, w.dtype),
+        "E": normal((s, 1, 1), (V, d), 0.02, w.dtype),
         "W1": [], "b1": [], "W2": [],
         "cond": np.array(w.cond, dtype=np.int32),
         "topk": np.array(w.topk, dtype=np.int32),
         "root_tok": rng.integers(0, V, size=B).astype(np.int32),
     }
-    for c in w.cond:
-        out["W1"].append(normal(rng, (d, d * (2 if c else 1)), 0.02, w.dtype))
-        out["b1"].append(normal(rng, (d,), 0.02, w.dtype))
-        out["W2"].append(normal(rng, (V, d), 0.02, w.dtype))
+    for k, c in enumerate(w.cond):
+        out["W1"].append(normal((s, 1, 10 + k), (d, d * (2 if c else 1)), 0.02, w.dtype))
+        out["b1"].append(normal((s, 1, 30 + k), (d,), 0.02, w.dtype))
+        out["W2"].append(normal((s, 1, 50 + k), (V, d), 0.02, w.dtype))
     return out
 
 
@@ -277,26 +313,27 @@ def attention_inputs(w, T, B=None, seed=None):
     Cache rows at or beyond prefix_len[b] hold random values too (they must be ignored).
     """
     B = w.B if B is None else B
-    rng = _rng(w.seed if seed is None else seed, 2)
+    s = w.seed if seed is None else seed
     lo, hi = w.prefix
     return {
-        "q": normal(rng, (B, w.Hq, T, w.D), 1.0, w.dtype),
-        "k_cache": normal(rng, (B, w.Hkv, w.Lmax, w.D), 1.0, w.dtype),
-        "v_cache": normal(rng, (B, w.Hkv, w.Lmax, w.D), 1.0, w.dtype),
-        "prefix_len": rng.integers(lo, hi + 1, size=B).astype(np.int32),
-        "k_tree": normal(rng, (B, w.Hkv, T, w.D), 1.0, w.dtype),
-        "v_tree": normal(rng, (B, w.Hkv, T, w.D), 1.0, w.dtype),
+        "q": normal((s, 2, 0), (B, w.Hq, T, w.D), 1.0, w.dtype),
+        "k_cache": normal((s, 2, 1), (B, w.Hkv, w.Lmax, w.D), 1.0, w.dtype),
+        "v_cache": normal((s, 2, 2), (B, w.Hkv, w.Lmax, w.D), 1.0, w.dtype),
+        "prefix_len": _rng(s, 2).integers(lo, hi + 1, size=B).astype(np.int32),
+        "k_tree": normal((s, 2, 3), (B, w.Hkv, T, w.D), 1.0, w.dtype),
+        "v_tree": normal((s, 2, 4), (B, w.Hkv, T, w.D), 1.0, w.dtype),
     }
 
 
 def greedy_inputs(w, parent, B=None, seed=None, node_tok=None):
     """Node tokens (distinct among siblings unless given) and planted target logits [B, T, V] fp32."""
     B = w.B if B is None else B
-    rng = _rng(w.seed if seed is None else seed, 3)
+    s = w.seed if seed is None else seed
+    rng = _rng(s, 3)
     if node_tok is None:
         node_tok = sibling_tokens(rng, parent, B, w.V)
     lengths = rng.choice(np.array(w.accept_lengths), size=B)
-    logits = plant_greedy(rng, parent, node_tok, w.V, lengths)
+    logits = plant_greedy(rng, (s, 3, 0), parent, node_tok, w.V, lengths)
     return {"node_tok": np.asarray(node_tok, dtype=np.int32), "logits_p": logits, "planted": lengths}
 
 
@@ -308,11 +345,12 @@ def rejection_inputs(w, parent, rank, B=None, seed=None):
     logits_q[u] (child of rank r: the (r+1)-th largest, ties to the lower id).
     """
     B = w.B if B is None else B
-    rng = _rng(w.seed if seed is None else seed, 4)
+    s = w.seed if seed is None else seed
+    rng = _rng(s, 4)
     T = len(parent)
     V = w.V
-    zq = rng.standard_normal(size=(B, T, V), dtype=np.float32)
-    eps = rng.standard_normal(size=(B, T, V), dtype=np.float32)
+    zq = normal((s, 4, 0), (B, T, V))
+    eps = normal((s, 4, 1), (B, T, V))
     zp = np.float32(w.rho) * zq + np.float32(np.sqrt(1.0 - w.rho ** 2)) * eps
     lq = (np.float32(w.logit_scale) * zq).astype(np.float32)
     lp = (np.float32(w.logit_scale) * zp).astype(np.float32)

@@ -1,0 +1,101 @@
+"""Tree attention: CUDA path vs the oracle, element by element (GPU)."""
+
+import zlib
+
+import numpy as np
+import pytest
+
+import oracle
+import spec_workloads as wl
+from gpu_util import assert_close, lib, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(st, x, tree, dtype, scale=None):
+    out, lse = st.tree_attention(to_dev(x["q"]), to_dev(x["k_cache"]), to_dev(x["v_cache"]),
+                                 to_dev(x["prefix_len"]), to_dev(x["k_tree"]), to_dev(x["v_tree"]), tree,
+                                 scale=scale)
+    return out.cpu().numpy(), lse.cpu().numpy()
+
+
+def _rand_inputs(rng, dtype, B, Hq, Hkv, T, D, Lmax, prefix):
+    enc = (lambda a: wl.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    n = lambda *s: enc(rng.standard_normal(s, dtype=np.float32))
+    return dict(q=n(B, Hq, T, D), k_cache=n(B, Hkv, Lmax, D), v_cache=n(B, Hkv, Lmax, D),
+                prefix_len=np.array(prefix, dtype=np.int32), k_tree=n(B, Hkv, T, D), v_tree=n(B, Hkv, T, D))
+
+
+CASES = [
+    # dtype, B, Hq, Hkv, tree, D, Lmax, prefix
+    ("f32", 1, 4, 4, ("cartesian", (2, 3)), 64, 128, [128]),
+    ("f32", 2, 4, 2, ("random", 17), 64, 100, [0, 100]),            # empty prefix, Lmax not a tile multiple
+    ("bf16", 1, 8, 1, ("random", 1), 128, 130, [130]),              # root only
+    ("bf16", 3, 6, 2, ("random", 70), 128, 300, [1, 150, 300]),     # two mask words
+    ("bf16", 2, 2, 2, ("random", 130), 64, 64, [64, 7]),            # three mask words
+    ("bf16", 1, 32, 32, ("sparse", (8, 4, 2, 1), 64, 64), 128, 1024, [1024]),
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=[f"{c[0]}-B{c[1]}-H{c[2]}/{c[3]}-{c[4][0]}-L{c[6]}" for c in CASES])
+def test_attention_matches_oracle(case):
+    st = lib()
+    dtype, B, Hq, Hkv, tspec, D, Lmax, prefix = case
+    rng = np.random.default_rng(zlib.crc32(str(case).encode()))
+    if tspec[0] == "random":
+        parent, rank = wl.random_tree(rng, tspec[1], max_children=4)
+    else:
+        parent, rank = wl.make_tree(tspec)
+    tree = st.spec_tree_build(parent, rank)
+    x = _rand_inputs(rng, dtype, B, Hq, Hkv, len(parent), D, Lmax, prefix)
+    out, lse = _run(st, x, tree, dtype)
+    O, L = oracle.tree_attention(**x, tree=oracle.tree_encode(parent, rank), dtype=dtype)
+    assert_close(out, O, dtype, "out")
+    assert_close(lse, L, dtype, "lse")
+
+
+@pytest.mark.parametrize("cfg,sample", [(1, None), (2, None), (4, 24), (5, 6)])
+def test_attention_workloads(cfg, sample):
+    """Full-size workloads; for the big ones the oracle computes a sample of (sequence, head) pairs."""
+    st = lib()
+    w = wl.WORKLOADS[cfg]
+    parent, rank = wl.make_tree(w.tree)
+    tree = st.spec_tree_build(parent, rank)
+    x = wl.attention_inputs(w, len(parent))
+    out, lse = _run(st, x, tree, w.dtype)
+    heads = None
+    if sample:
+        rng = np.random.default_rng(cfg)
+        pairs = [(b, h) for b in range(w.B) for h in range(w.Hq)]
+        heads = [pairs[i] for i in rng.choice(len(pairs), size=sample, replace=False)]
+    O, L = oracle.tree_attention(**x, tree=oracle.tree_encode(parent, rank), dtype=w.dtype, heads=heads)
+    sel = ~np.isnan(L)
+    assert sel.any()
+    assert_close(out[sel], O[sel], w.dtype, "out")
+    assert_close(lse[sel], L[sel], w.dtype, "lse")
+
+
+def test_attention_dense_256_variant():
+    st = lib()
+    w = wl.WORKLOADS[5]
+    p, r = wl.cartesian_tree((4, 4, 4, 4))
+    parent, rank = wl.bfs_prefix_tree(p, r, 256)
+    tree = st.spec_tree_build(parent, rank)
+    x = wl.attention_inputs(w, 256)
+    out, lse = _run(st, x, tree, w.dtype)
+    O, L = oracle.tree_attention(**x, tree=oracle.tree_encode(parent, rank), dtype=w.dtype, heads=[(0, 0), (0, 31)])
+    sel = ~np.isnan(L)
+    assert_close(out[sel], O[sel], w.dtype, "out")
+
+
+def test_attention_is_deterministic_and_respects_scale():
+    st = lib()
+    rng = np.random.default_rng(5)
+    parent, rank = wl.cartesian_tree((3, 2))
+    tree = st.spec_tree_build(parent, rank)
+    x = _rand_inputs(rng, "f32", 2, 4, 2, len(parent), 64, 90, [90, 33])
+    a, _ = _run(st, x, tree, "f32", scale=0.05)
+    b, _ = _run(st, x, tree, "f32", scale=0.05)
+    assert np.array_equal(a, b)
+    O, _ = oracle.tree_attention(**x, tree=oracle.tree_encode(parent, rank), dtype="f32", scale=0.05)
+    assert_close(a, O, "f32", "out")

@@ -1,0 +1,134 @@
+"""Draft heads: CUDA path vs the oracle (GPU).
+
+Tokens must match exactly, except at near ties of the top-k: a token that
+differs must score, in the oracle's own logits row, within 1e-6 (fp32 inputs)
+or 1e-3 x |logit| (bf16 inputs) of the oracle's pick for that rank; such ties
+are counted.  The oracle is re-run teacher-forced on the GPU's tokens so later
+depths stay comparable.  Logits and log-probabilities within the tolerances.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import spec_workloads as wl
+from gpu_util import assert_close, lib, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(st, x, tree):
+    return st.hydra_draft(to_dev(x["h"]), to_dev(x["E"]), [to_dev(a) for a in x["W1"]],
+                          None if x["b1"] is None else [to_dev(a) for a in x["b1"]],
+                          [to_dev(a) for a in x["W2"]], list(x["cond"]), list(x["topk"]), to_dev(x["root_tok"]), tree)
+
+
+def _compare(st, x, parent, rank, dtype):
+    tree = st.spec_tree_build(parent, rank)
+    tok, logit, logprob = _run(st, x, tree)
+    tok, logit, logprob = tok.cpu().numpy(), logit.cpu().numpy(), logprob.cpu().numpy()
+    to = oracle.tree_encode(parent, rank)
+    ref = oracle.hydra_draft(x["h"], x["E"], x["W1"], x["b1"], x["W2"], x["cond"], x["topk"], x["root_tok"], to,
+                             dtype, teacher_tok=tok, keep_logits=True)
+    B, T = tok.shape
+    near = 0
+    for b in range(B):
+        for c in range(1, T):
+            if tok[b, c] == ref["node_tok"][b, c]:
+                continue
+            # a different token is only acceptable at a near tie: in the oracle's own row
+            # it must score within the tie tolerance of the oracle's pick for that rank
+            row = ref["logits"][(b, int(parent[c]))] if (b, int(parent[c])) in ref["logits"] else None
+            assert row is not None, (b, c)
+            tol = 1e-6 if dtype == "f32" else 1e-3 * abs(ref["node_logit"][b, c]) + 1e-6
+            diff = abs(row[tok[b, c]] - row[ref["node_tok"][b, c]])
+            assert diff <= tol, (b, c, tok[b, c], ref["node_tok"][b, c], diff, tol)
+            near += 1
+    assert tok[:, 0].tolist() == list(x["root_tok"])
+    assert_close(logit, ref["node_logit"], dtype, "node_logit")
+    assert_close(logprob, ref["node_logprob"], dtype, "node_logprob")
+    return near
+
+
+def test_draft_tiny_fp32_workload():
+    st = lib()
+    w = wl.WORKLOADS[1]
+    parent, rank = wl.make_tree(w.tree)
+    _compare(st, wl.draft_inputs(w), parent, rank, "f32")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [
+    # d, V, B, branching, cond, topk
+    (64, 500, 2, (3, 2, 2), (0, 1, 1), (3, 2, 2)),
+    (128, 4099, 3, (4, 1), (1, 1), (5, 1)),           # vocab not a tile multiple, top-k above the ranks used
+    (32, 64, 1, (8, 4), (1, 0), (8, 16)),             # Medusa head at depth 2, top-16
+])
+def test_draft_small_shapes(dtype, shape):
+    st = lib()
+    d, V, B, branching, cond, topk = shape
+    w = wl.Workload("t", dtype, B=B, seed=11, tree=("cartesian", branching), d=d, V=V, cond=cond, topk=topk)
+    parent, rank = wl.make_tree(w.tree)
+    x = wl.draft_inputs(w)
+    # larger weights than the workloads' 0.02 so the logits spread and ties are rare
+    rng = np.random.default_rng(3)
+    enc = (lambda a: wl.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    x["W2"] = [enc(rng.standard_normal(np.shape(a), dtype=np.float32) * np.float32(0.25)) for a in x["W2"]]
+    _compare(st, x, parent, rank, dtype)
+
+
+def test_draft_on_sparse_tree_with_missing_ranks():
+    # pruned tree: some parents keep children of ranks {0, 2}, so top-k > children
+    st = lib()
+    w = wl.Workload("t", "bf16", B=2, seed=12, tree=("sparse", (8, 4, 2, 1), 64, 64), d=128, V=3000,
+                    cond=(1, 1, 1, 1), topk=(8, 4, 2, 1))
+    parent, rank = wl.make_tree(w.tree)
+    x = wl.draft_inputs(w)
+    rng = np.random.default_rng(4)
+    x["W2"] = [wl.f32_to_bf16_bits(rng.standard_normal(np.shape(a), dtype=np.float32) * np.float32(0.25)) for a in x["W2"]]
+    _compare(st, x, parent, rank, "bf16")
+
+
+def test_draft_hydra_heads_workload():
+    """The Hydra-heads workload at full size: B=4, d=4096, V=32000, 4 heads, 64-node tree."""
+    st = lib()
+    w = wl.WORKLOADS[3]
+    parent, rank = wl.make_tree(w.tree)
+    near = _compare(st, wl.draft_inputs(w), parent, rank, "bf16")
+    print(f"hydra heads workload: {near} near ties")
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+def test_zero_init_heads_reproduce_lm_head_on_gpu(dtype):
+    # Medusa Heads page: zeroed feed-forward + copied lm_head -> each head predicts lm_head's top token.
+    st = lib()
+    d, V, K = 256, 1000, 3
+    rng = np.random.default_rng(6)
+    lm = rng.standard_normal((V, d), dtype=np.float32) * np.float32(0.02)
+    h = rng.standard_normal((1, d), dtype=np.float32)
+    enc = (lambda a: wl.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    lm, h = enc(lm), enc(h)
+    zw = enc(np.zeros((d, d), dtype=np.float32))
+    zb = enc(np.zeros(d, dtype=np.float32))
+    parent, rank = wl.chain_tree(K + 1)
+    x = dict(h=h, E=lm, W1=[zw] * K, b1=[zb] * K, W2=[lm] * K, cond=np.zeros(K, np.int32), topk=np.ones(K, np.int32),
+             root_tok=np.array([0], dtype=np.int32))
+    tree = st.spec_tree_build(parent, rank)
+    tok, logit, _ = _run(st, x, tree)
+    dec = oracle.bf16_bits_to_f64 if dtype == "bf16" else (lambda a: a.astype(np.float64))
+    ref = dec(lm) @ dec(h)[0]
+    assert tok.cpu().numpy()[0, 1:].tolist() == [int(np.argmax(ref))] * K
+    assert_close(logit.cpu().numpy()[0, 1:], [ref.max()] * K, dtype, "logit")
+
+
+def test_medusa_sibling_sets_repeat_on_gpu():
+    st = lib()
+    w = wl.Workload("t", "f32", B=2, seed=13, tree=("cartesian", (3, 4)), d=64, V=300, cond=(0, 0), topk=(3, 4))
+    parent, rank = wl.make_tree(w.tree)
+    tree = st.spec_tree_build(parent, rank)
+    tok, _, _ = _run(st, wl.draft_inputs(w), tree)
+    tok = tok.cpu().numpy()
+    to = oracle.tree_encode(parent, rank)
+    for b in range(2):
+        sets = [tuple(tok[b, to["children"][u]]) for u in to["children"][0]]
+        assert all(s == sets[0] for s in sets)

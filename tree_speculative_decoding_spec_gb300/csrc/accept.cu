@@ -1,0 +1,435 @@
+// tree_accept: longest accepted path over the candidate tree, and the extra token.
+//
+// Greedy -- Hydra Guide, "Parallel Verification and Greedy Acceptance
+// Algorithm": follow the target's argmax down the tree while a child carries
+// it; emit the argmax at the node where the walk stops.
+// Rejection -- Speculative Decoding (thegustafson.com), "The acceptance
+// criterion", "The correctness guarantee", "A worked example": accept the edge
+// into c with token x iff u_c < p(x)/q(x); at the deepest accepted node draw
+// the extra token from norm(max(p - q, 0)) if the node has children (all of
+// them rejected), else from p (the bonus token).
+//
+// Two launches per call:
+//   rows   grid (vocab slices x B*T rows), one pass over each logits row slice:
+//          greedy: the slice's best and second-best values (argmax, ties to the
+//          lower id); rejection: (max, sum exp) of logits/temperature for p and,
+//          on rows of nodes with children, for q.
+//   walk   one CTA per sequence: merge the slices, decide every edge, resolve
+//          accepted(c) = accepted(parent) && pass(c) depth by depth, pick the
+//          deepest accepted node (lowest index on ties) and, for rejection,
+//          draw the extra token by inverse CDF over the vocabulary.
+#include <algorithm>
+
+#include "common.cuh"
+#include "philox.cuh"
+
+namespace spec {
+namespace accept {
+
+constexpr int kRowThreads = 256;
+constexpr int kWalkThreads = 1024;
+
+struct Plan {
+    int slices, slice;
+    size_t off_part, total;
+};
+
+Plan make_plan(const spec_tree* t, int B, int V) {
+    Plan p{};
+    const int64_t rows = static_cast<int64_t>(B) * t->T;
+    const int64_t target = 2ll * device_sm_count();
+    const int max_slices = std::max(1, V / 2048);
+    p.slices = static_cast<int>(std::min<int64_t>(std::max<int64_t>((target + rows - 1) / rows, 1), max_slices));
+    p.slice = static_cast<int>(round_up((V + p.slices - 1) / p.slices, 4));
+    p.slices = (V + p.slice - 1) / p.slice;
+    p.off_part = kWsHeader;
+    p.total = kWsHeader + round_up(sizeof(float4) * static_cast<size_t>(rows) * p.slices, 256);
+    return p;
+}
+
+// ---------------------------------------------------------------- rows (greedy)
+
+// better = larger value, then lower index
+__device__ __forceinline__ void top2_push(float& v1, int& i1, float& v2, float v, int i) {
+    if (v > v1 || (v == v1 && i < i1)) { v2 = v1; v1 = v; i1 = i; }
+    else if (v > v2) { v2 = v; }
+}
+__device__ __forceinline__ void top2_merge(float& v1, int& i1, float& v2, float w1, int j1, float w2) {
+    if (w1 > v1 || (w1 == v1 && j1 < i1)) { v2 = fmaxf(v1, w2); v1 = w1; i1 = j1; }
+    else { v2 = fmaxf(v2, w1); }
+}
+
+__global__ void __launch_bounds__(kRowThreads) k_rows_greedy(const float* __restrict__ logits, int V, int slice,
+                                                             int slices, float4* __restrict__ part) {
+    const int sl = blockIdx.x;
+    const size_t row = blockIdx.y;
+    const float* x = logits + row * V;
+    const int v0 = sl * slice, v1 = min(V, v0 + slice);
+    float b1 = -INFINITY, b2 = -INFINITY;
+    int i1 = 0x7fffffff;
+    if ((V & 3) == 0) {
+        for (int e = v0 + 4 * threadIdx.x; e < v1; e += 4 * kRowThreads) {
+            const float4 q = __ldcs(reinterpret_cast<const float4*>(x + e));
+            top2_push(b1, i1, b2, q.x, e);
+            top2_push(b1, i1, b2, q.y, e + 1);
+            top2_push(b1, i1, b2, q.z, e + 2);
+            top2_push(b1, i1, b2, q.w, e + 3);
+        }
+    } else {
+        for (int e = v0 + threadIdx.x; e < v1; e += kRowThreads) top2_push(b1, i1, b2, x[e], e);
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        const float w1 = __shfl_xor_sync(0xffffffffu, b1, o);
+        const int j1 = __shfl_xor_sync(0xffffffffu, i1, o);
+        const float w2 = __shfl_xor_sync(0xffffffffu, b2, o);
+        top2_merge(b1, i1, b2, w1, j1, w2);
+    }
+    __shared__ float4 red[kRowThreads / 32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float4(b1, __int_as_float(i1), b2, 0.f);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kRowThreads / 32; ++w) top2_merge(b1, i1, b2, red[w].x, __float_as_int(red[w].y), red[w].z);
+        part[row * slices + sl] = make_float4(b1, __int_as_float(i1), b2, 0.f);
+    }
+}
+
+// ---------------------------------------------------------------- rows (rejection)
+
+__device__ __forceinline__ void lse_push(float& m, float& s, float v) {
+    if (v > m) { s = s * expf(m - v) + 1.f; m = v; }
+    else s += expf(v - m);
+}
+
+__global__ void __launch_bounds__(kRowThreads) k_rows_lse(const float* __restrict__ lp, const float* __restrict__ lq,
+                                                          const int32_t* __restrict__ child_off, int Tn, int V,
+                                                          int slice, int slices, float inv_temp,
+                                                          float4* __restrict__ part) {
+    const int sl = blockIdx.x;
+    const size_t row = blockIdx.y;
+    const int u = static_cast<int>(row % Tn);
+    const bool internal = child_off[u + 1] > child_off[u];
+    const int v0 = sl * slice, v1 = min(V, v0 + slice);
+    float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
+    const float* xp = lp + row * V;
+    const float* xq = lq + row * V;
+    if ((V & 3) == 0) {
+        for (int e = v0 + 4 * threadIdx.x; e < v1; e += 4 * kRowThreads) {
+            const float4 a = __ldcs(reinterpret_cast<const float4*>(xp + e));
+            lse_push(mp, sp, a.x * inv_temp); lse_push(mp, sp, a.y * inv_temp);
+            lse_push(mp, sp, a.z * inv_temp); lse_push(mp, sp, a.w * inv_temp);
+            if (internal) {
+                const float4 c = __ldcs(reinterpret_cast<const float4*>(xq + e));
+                lse_push(mq, sq, c.x * inv_temp); lse_push(mq, sq, c.y * inv_temp);
+                lse_push(mq, sq, c.z * inv_temp); lse_push(mq, sq, c.w * inv_temp);
+            }
+        }
+    } else {
+        for (int e = v0 + threadIdx.x; e < v1; e += kRowThreads) {
+            lse_push(mp, sp, xp[e] * inv_temp);
+            if (internal) lse_push(mq, sq, xq[e] * inv_temp);
+        }
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+        lse_merge(mp, sp, __shfl_xor_sync(0xffffffffu, mp, o), __shfl_xor_sync(0xffffffffu, sp, o));
+        lse_merge(mq, sq, __shfl_xor_sync(0xffffffffu, mq, o), __shfl_xor_sync(0xffffffffu, sq, o));
+    }
+    __shared__ float4 red[kRowThreads / 32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float4(mp, sp, mq, sq);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kRowThreads / 32; ++w) {
+            lse_merge(mp, sp, red[w].x, red[w].y);
+            lse_merge(mq, sq, red[w].z, red[w].w);
+        }
+        part[row * slices + sl] = make_float4(mp, sp, mq, sq);
+    }
+}
+
+// ---------------------------------------------------------------- walk helpers
+
+// Block-wide reductions for 1024 threads (32 warps) through shared memory.
+__device__ __forceinline__ int block_max_int(int v, int* scratch) {
+    for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    __syncthreads();
+    int r = scratch[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = max(r, scratch[w]);
+    return r;
+}
+__device__ __forceinline__ int block_min_int(int v, int* scratch) {
+    return -block_max_int(-v, scratch);
+}
+__device__ __forceinline__ float block_min_f(float v, float* scratch) {
+    v = warp_min(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = scratch[0];
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = fminf(r, scratch[w]);
+    return r;
+}
+__device__ __forceinline__ float block_sum_f(float v, float* scratch) {
+    v = warp_sum(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = 0.f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r += scratch[w];
+    return r;
+}
+
+// accepted(c) = accepted(parent(c)) && pass(c), resolved depth by depth; then the
+// deepest accepted node (lowest index on equal depth) and the root-first path.
+__device__ int resolve_path(const int32_t* __restrict__ parent, const int32_t* __restrict__ depth, int Tn, int max_depth,
+                            unsigned char* acc, const unsigned char* pass, int* iscratch) {
+    for (int u = threadIdx.x; u < Tn; u += blockDim.x) acc[u] = (u == 0);
+    __syncthreads();
+    for (int lev = 1; lev <= max_depth; ++lev) {
+        for (int u = threadIdx.x; u < Tn; u += blockDim.x)
+            if (depth[u] == lev) acc[u] = acc[parent[u]] && pass[u];
+        __syncthreads();
+    }
+    int key = -1;
+    for (int u = threadIdx.x; u < Tn; u += blockDim.x)
+        if (acc[u]) key = max(key, depth[u] * 2048 + (2047 - u));
+    key = block_max_int(key, iscratch);
+    return 2047 - (key % 2048);
+}
+
+__device__ void write_path(const int32_t* __restrict__ parent, const int32_t* __restrict__ depth, int ustar, int b,
+                           int max_depth, int32_t* __restrict__ accept_len, int32_t* __restrict__ accept_path) {
+    if (threadIdx.x != 0) return;
+    const int m = depth[ustar];
+    accept_len[b] = m;
+    int32_t* path = accept_path + static_cast<size_t>(b) * (max_depth + 1);
+    for (int k = m + 1; k <= max_depth; ++k) path[k] = -1;
+    int u = ustar;
+    for (int k = m; k >= 0; --k) { path[k] = u; u = parent[u]; }
+}
+
+// ---------------------------------------------------------------- walk (greedy)
+
+__global__ void __launch_bounds__(kWalkThreads) k_walk_greedy(const float4* __restrict__ part, int slices,
+                                                              const int32_t* __restrict__ node_tok,
+                                                              const int32_t* __restrict__ parent,
+                                                              const int32_t* __restrict__ depth, int Tn, int max_depth,
+                                                              int32_t* __restrict__ accept_len,
+                                                              int32_t* __restrict__ accept_path,
+                                                              int32_t* __restrict__ next_token, float* __restrict__ margin) {
+    const int b = blockIdx.x;
+    __shared__ int amax[SPEC_MAX_T];
+    __shared__ float gap[SPEC_MAX_T];
+    __shared__ unsigned char pass[SPEC_MAX_T], acc[SPEC_MAX_T];
+    __shared__ int iscr[32];
+    __shared__ float fscr[32];
+    for (int u = threadIdx.x; u < Tn; u += blockDim.x) {
+        const float4* pr = part + (static_cast<size_t>(b) * Tn + u) * slices;
+        float v1 = pr[0].x, v2 = pr[0].z;
+        int i1 = __float_as_int(pr[0].y);
+        for (int s = 1; s < slices; ++s) top2_merge(v1, i1, v2, pr[s].x, __float_as_int(pr[s].y), pr[s].z);
+        amax[u] = i1;
+        gap[u] = v1 - v2;
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < Tn; c += blockDim.x)
+        pass[c] = (c > 0) && node_tok[static_cast<size_t>(b) * Tn + c] == amax[parent[c]];
+    __syncthreads();
+    const int ustar = resolve_path(parent, depth, Tn, max_depth, acc, pass, iscr);
+    float mg = INFINITY;
+    for (int u = threadIdx.x; u < Tn; u += blockDim.x)
+        if (acc[u]) mg = fminf(mg, gap[u]);
+    mg = block_min_f(mg, fscr);
+    write_path(parent, depth, ustar, b, max_depth, accept_len, accept_path);
+    if (threadIdx.x == 0) {
+        next_token[b] = amax[ustar];
+        if (margin) margin[b] = mg;
+    }
+}
+
+// ---------------------------------------------------------------- walk (rejection)
+
+__global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __restrict__ part, int slices,
+                                                              const float* __restrict__ lp, const float* __restrict__ lq,
+                                                              const int32_t* __restrict__ node_tok,
+                                                              const int32_t* __restrict__ parent,
+                                                              const int32_t* __restrict__ depth,
+                                                              const int32_t* __restrict__ child_off, int Tn,
+                                                              int max_depth, int V, float inv_temp, uint64_t seed,
+                                                              uint64_t offset, int32_t* __restrict__ accept_len,
+                                                              int32_t* __restrict__ accept_path,
+                                                              int32_t* __restrict__ next_token, float* __restrict__ margin,
+                                                              void* ws) {
+    const int b = blockIdx.x;
+    __shared__ float lse_p[SPEC_MAX_T], lse_q[SPEC_MAX_T];
+    __shared__ unsigned char pass[SPEC_MAX_T], acc[SPEC_MAX_T];
+    __shared__ float dmar[SPEC_MAX_T];
+    __shared__ int iscr[32];
+    __shared__ float fscr[32];
+    __shared__ float seg_excl[kWalkThreads];
+    for (int u = threadIdx.x; u < Tn; u += blockDim.x) {
+        const float4* pr = part + (static_cast<size_t>(b) * Tn + u) * slices;
+        float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
+        for (int s = 0; s < slices; ++s) { lse_merge(mp, sp, pr[s].x, pr[s].y); lse_merge(mq, sq, pr[s].z, pr[s].w); }
+        lse_p[u] = mp + logf(sp);
+        lse_q[u] = (child_off[u + 1] > child_off[u]) ? mq + logf(sq) : NAN;
+    }
+    __syncthreads();
+    for (int c = threadIdx.x; c < Tn; c += blockDim.x) {
+        pass[c] = 0;
+        dmar[c] = INFINITY;
+        if (c == 0) continue;
+        const int par = parent[c];
+        const int x = node_tok[static_cast<size_t>(b) * Tn + c];
+        if (x < 0 || x >= V) {   // a token outside the vocabulary is never accepted
+            flag_status(ws, SPEC_EINVAL);
+            continue;
+        }
+        const size_t prow = (static_cast<size_t>(b) * Tn + par) * V;
+        const float logp = lp[prow + x] * inv_temp - lse_p[par];
+        const float logq = lq[prow + x] * inv_temp - lse_q[par];
+        const float ratio = expf(logp - logq);
+        const float u = uniform24(spec_draw(seed, offset, static_cast<uint32_t>(c), static_cast<uint32_t>(b)).w[0]);
+        pass[c] = u < ratio;
+        if (ratio < 1.f) dmar[c] = fabsf(u - ratio);
+    }
+    __syncthreads();
+    const int ustar = resolve_path(parent, depth, Tn, max_depth, acc, pass, iscr);
+    float mg = INFINITY;
+    for (int c = threadIdx.x; c < Tn; c += blockDim.x)
+        if (c > 0 && acc[parent[c]]) mg = fminf(mg, dmar[c]);
+    mg = block_min_f(mg, fscr);
+    write_path(parent, depth, ustar, b, max_depth, accept_len, accept_path);
+
+    // ---- the extra token: inverse CDF over the vocabulary, ascending token order
+    const bool leaf = child_off[ustar + 1] == child_off[ustar];
+    const size_t srow = (static_cast<size_t>(b) * Tn + ustar) * V;
+    const float lsp = lse_p[ustar], lsq = lse_q[ustar];
+    const float* rp = lp + srow;
+    const float* rq = lq + srow;
+    // weight of token x: p (leaf, or residual all zero) or max(p - q, 0)
+    auto weight = [&](int x, bool resid) -> float {
+        const float pv = expf(rp[x] * inv_temp - lsp);
+        if (!resid) return pv;
+        return fmaxf(pv - expf(rq[x] * inv_temp - lsq), 0.f);
+    };
+    const int seg = (V + kWalkThreads - 1) / kWalkThreads;
+    const int x0 = min(V, threadIdx.x * seg), x1 = min(V, x0 + seg);
+    bool resid = !leaf;
+    float ssum = 0.f;
+    for (int x = x0; x < x1; ++x) ssum += weight(x, resid);
+    if (resid) {
+        const float total_r = block_sum_f(ssum, fscr);
+        if (total_r == 0.f) {   // alpha = 1: no residual mass, fall back to p
+            resid = false;
+            ssum = 0.f;
+            for (int x = x0; x < x1; ++x) ssum += weight(x, resid);
+        }
+    }
+    // exclusive scan of the per-thread segment sums (thread order = token order)
+    seg_excl[threadIdx.x] = ssum;
+    __syncthreads();
+    for (int off = 1; off < kWalkThreads; off <<= 1) {
+        const float add = threadIdx.x >= off ? seg_excl[threadIdx.x - off] : 0.f;
+        __syncthreads();
+        seg_excl[threadIdx.x] += add;
+        __syncthreads();
+    }
+    const float total = seg_excl[kWalkThreads - 1];
+    const float excl = seg_excl[threadIdx.x] - ssum;
+    const float u1 = uniform24(spec_draw(seed, offset, 0u, static_cast<uint32_t>(b)).w[1]);
+    const float target = u1 * total;
+    const float need = target - excl;
+    const bool here = ssum > 0.f && ssum > need;
+    const int first = block_min_int(here ? static_cast<int>(threadIdx.x) : kWalkThreads, iscr);
+    __shared__ int pick;
+    __shared__ float smar;
+    if (first == kWalkThreads) {
+        // target at or beyond the total (rounding): take the last token of positive weight
+        const int last = block_max_int(ssum > 0.f ? static_cast<int>(threadIdx.x) : -1, iscr);
+        if (static_cast<int>(threadIdx.x) == last) {
+            int xs = x0;
+            for (int x = x0; x < x1; ++x) if (weight(x, resid) > 0.f) xs = x;
+            pick = xs;
+            smar = 0.f;
+        }
+    } else if (static_cast<int>(threadIdx.x) == first) {
+        float run = 0.f;
+        int xs = x1 - 1;
+        float lo = 0.f, hi = 0.f;
+        for (int x = x0; x < x1; ++x) {
+            const float w = weight(x, resid);
+            lo = run;
+            run += w;
+            if (run > need) { xs = x; hi = run; break; }
+        }
+        pick = xs;
+        smar = fminf(hi - need, need - lo) / total;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        next_token[b] = pick;
+        if (margin) margin[b] = fminf(mg, fabsf(smar));
+    }
+}
+
+spec_status check_args(int mode, const spec_tree* t, int B, int V, float temperature) {
+    spec_status st = check_tree(t);
+    if (st != SPEC_OK) return st;
+    if (mode != 0 && mode != 1) return fail(SPEC_EINVAL, "mode = %d must be 0 (greedy) or 1 (rejection)", mode);
+    if (B < 1 || B > 65535) return fail(SPEC_EINVAL, "B = %d out of 1..65535", B);
+    if (V < 2 || V > (1 << 24)) return fail(SPEC_EINVAL, "V = %d out of 2..2^24", V);
+    if (mode == 1 && !(temperature > 0.f && temperature < 1e30f)) return fail(SPEC_EINVAL, "temperature must be positive");
+    if (static_cast<int64_t>(B) * t->T > 65535) return fail(SPEC_EINVAL, "B * T = %lld rows exceed 65535", (long long)B * t->T);
+    return SPEC_OK;
+}
+
+}  // namespace accept
+}  // namespace spec
+
+using namespace spec;
+
+extern "C" size_t tree_accept_workspace_size(int32_t mode, const spec_tree* tree, int32_t B, int32_t V) {
+    clear_error();
+    if (accept::check_args(mode, tree, B, V, 1.0f) != SPEC_OK) return 0;
+    return accept::make_plan(tree, B, V).total;
+}
+
+extern "C" spec_status tree_accept(int32_t mode, const float* logits_p, const float* logits_q, const int32_t* node_tok,
+                                   const spec_tree* tree, int32_t B, int32_t V, float temperature, uint64_t seed,
+                                   uint64_t offset, int32_t* accept_len, int32_t* accept_path, int32_t* next_token,
+                                   float* margin, void* ws, size_t ws_bytes, spec_stream_t s_) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(s_);
+    clear_error();
+    spec_status st = accept::check_args(mode, tree, B, V, temperature);
+    if (st != SPEC_OK) return st;
+    if (!logits_p || !node_tok || !accept_len || !accept_path || !next_token)
+        return fail(SPEC_EINVAL, "logits_p, node_tok and the outputs must not be NULL");
+    if (mode == 1 && !logits_q) return fail(SPEC_EINVAL, "rejection needs logits_q");
+    if (!aligned16(logits_p) || (logits_q && !aligned16(logits_q))) return fail(SPEC_EALIGN, "logits must be 16-byte aligned");
+    if (!aligned4(node_tok) || !aligned4(accept_len) || !aligned4(accept_path) || !aligned4(next_token) ||
+        (margin && !aligned4(margin)))
+        return fail(SPEC_EALIGN, "token buffers must be 4-byte aligned");
+    const accept::Plan p = accept::make_plan(tree, B, V);
+    if (!ws || ws_bytes < p.total) return fail(SPEC_EWORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, p.total);
+    if (!aligned16(ws)) return fail(SPEC_EALIGN, "workspace must be 16-byte aligned");
+    float4* part = reinterpret_cast<float4*>(static_cast<unsigned char*>(ws) + p.off_part);
+    const dim3 grid(p.slices, B * tree->T);
+    SPEC_CUDA_TRY(reset_device_status(ws, s));
+    if (mode == 0) {
+        SPEC_CUDA_TRY(launch("accept_rows_greedy", accept::k_rows_greedy, grid, dim3(accept::kRowThreads), 0, s, logits_p, V,
+                             p.slice, p.slices, part));
+        SPEC_CUDA_TRY(launch("accept_walk_greedy", accept::k_walk_greedy, dim3(B), dim3(accept::kWalkThreads), 0, s, part,
+                             p.slices, node_tok, tree->parent, tree->depth, tree->T, tree->max_depth, accept_len,
+                             accept_path, next_token, margin));
+    } else {
+        const float inv_temp = 1.0f / temperature;
+        SPEC_CUDA_TRY(launch("accept_rows_lse", accept::k_rows_lse, grid, dim3(accept::kRowThreads), 0, s, logits_p, logits_q,
+                             tree->child_off, tree->T, V, p.slice, p.slices, inv_temp, part));
+        SPEC_CUDA_TRY(launch("accept_walk_reject", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), 0, s, part,
+                             p.slices, logits_p, logits_q, node_tok, tree->parent, tree->depth, tree->child_off,
+                             tree->T, tree->max_depth, V, inv_temp, seed, offset, accept_len, accept_path, next_token,
+                             margin, ws));
+    }
+    return SPEC_OK;
+}

@@ -1,0 +1,330 @@
+// tree_attention: the T tree tokens attend over the cached prefix plus their
+// own ancestors.
+//
+// Hydra Guide, "Tree Attention Matrix with Topology-Aware Causal Masking": the
+// prefix is always visible; among the tree tokens node i sees exactly anc*(i)
+// (itself and its ancestors).  The ancestor sets arrive as one bit row per node
+// (spec_tree.anc) and are applied to the scores in registers.
+//
+// Split-KV layout: the key sequence of one (sequence, KV head) is cut into
+// `n_pre` prefix chunks plus one tail chunk holding the T tree keys.  One CTA
+// takes a block of query rows (all query heads of the KV group x tree nodes)
+// against one chunk with an online softmax and writes (max, sum, unnormalised
+// output) to the workspace; a combine kernel merges the chunks of each row.
+#include <algorithm>
+
+#include "attention_tc.cuh"
+#include "common.cuh"
+
+namespace spec {
+namespace attn {
+
+constexpr int BR = 64;   // query rows per CTA
+constexpr int BC = 64;   // keys per tile
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ---------------------------------------------------------------- CUDA-core split-KV kernel
+
+template <typename T, int D>
+__global__ void __launch_bounds__(256) k_attn_fma(const T* __restrict__ q, const T* __restrict__ kc,
+                                                  const T* __restrict__ vc, const int32_t* __restrict__ prefix_len,
+                                                  const T* __restrict__ kt, const T* __restrict__ vt,
+                                                  const uint64_t* __restrict__ anc, int Tn, int words, int Hq, int Hkv,
+                                                  int Lmax, float scale_log2, int chunk, int n_pre, int n_rowblocks,
+                                                  float* __restrict__ part) {
+    constexpr int LD = D + 4;
+    constexpr int LP = BC + 4;
+    constexpr int DT = D / 16;   // output dims per thread
+    extern __shared__ float4 smem4[];
+    float* Qs = reinterpret_cast<float*>(smem4);
+    float* Ks = Qs + BR * LD;
+    float* Vs = Ks + BC * LD;
+    float* Ps = Vs + BC * LD;
+
+    const int g = Hq / Hkv;
+    const int R = Tn * g;
+    const int c = blockIdx.x;
+    const int kvh = blockIdx.y / n_rowblocks, rb = blockIdx.y % n_rowblocks;
+    const int b = blockIdx.z;
+    const int L = min(max(prefix_len[b], 0), Lmax);
+    const bool tail = (c == n_pre);
+    const int k_begin = tail ? 0 : c * chunk;
+    const int k_end = tail ? Tn : min(L, k_begin + chunk);
+    if (k_begin >= k_end) return;
+    const int t = threadIdx.x;
+    const int rg = t >> 4, kg = t & 15;
+    const int r0 = rb * BR;
+
+    for (int idx = t; idx < BR * (D / 4); idx += 256) {
+        const int rl = idx / (D / 4), c4 = idx % (D / 4);
+        const int r = r0 + rl;
+        float v[4] = {0.f, 0.f, 0.f, 0.f};
+        if (r < R) {
+            const int hl = r / Tn, i = r % Tn;
+            const int h = kvh * g + hl;
+            load4(q + ((static_cast<size_t>(b) * Hq + h) * Tn + i) * D + c4 * 4, v);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) v[e] *= scale_log2;
+        }
+        *reinterpret_cast<float4*>(&Qs[rl * LD + c4 * 4]) = make_float4(v[0], v[1], v[2], v[3]);
+    }
+    int node[4];
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) node[ii] = (r0 + 4 * rg + ii) % Tn;
+
+    float m_run[4], l_run[4], o[4][DT];
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+        m_run[ii] = -INFINITY;
+        l_run[ii] = 0.f;
+#pragma unroll
+        for (int e = 0; e < DT; ++e) o[ii][e] = 0.f;
+    }
+    const size_t kv_off = tail ? (static_cast<size_t>(b) * Hkv + kvh) * Tn * D
+                               : (static_cast<size_t>(b) * Hkv + kvh) * static_cast<size_t>(Lmax) * D;
+    const T* Kb = (tail ? kt : kc) + kv_off;
+    const T* Vb = (tail ? vt : vc) + kv_off;
+
+    for (int j0 = k_begin; j0 < k_end; j0 += BC) {
+        __syncthreads();
+        for (int idx = t; idx < BC * (D / 4); idx += 256) {
+            const int jl = idx / (D / 4), c4 = idx % (D / 4);
+            const int j = j0 + jl;
+            float kv[4] = {0.f, 0.f, 0.f, 0.f}, vv[4] = {0.f, 0.f, 0.f, 0.f};
+            if (j < k_end) {
+                load4(Kb + static_cast<size_t>(j) * D + c4 * 4, kv);
+                load4(Vb + static_cast<size_t>(j) * D + c4 * 4, vv);
+            }
+            *reinterpret_cast<float4*>(&Ks[jl * LD + c4 * 4]) = make_float4(kv[0], kv[1], kv[2], kv[3]);
+            *reinterpret_cast<float4*>(&Vs[jl * LD + c4 * 4]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+        }
+        __syncthreads();
+
+        float s[4][4];
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) s[ii][jj] = 0.f;
+#pragma unroll 4
+        for (int dd = 0; dd < D; dd += 4) {
+            float4 qa[4], kb[4];
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) qa[ii] = *reinterpret_cast<const float4*>(&Qs[(4 * rg + ii) * LD + dd]);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) kb[jj] = *reinterpret_cast<const float4*>(&Ks[(kg + 16 * jj) * LD + dd]);
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii)
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj)
+                    s[ii][jj] += qa[ii].x * kb[jj].x + qa[ii].y * kb[jj].y + qa[ii].z * kb[jj].z + qa[ii].w * kb[jj].w;
+        }
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+            const int key = j0 + kg + 16 * jj;
+            const bool in = key < k_end;
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+                bool ok = in;
+                if (tail && ok) ok = (anc[static_cast<size_t>(node[ii]) * words + (key >> 6)] >> (key & 63)) & 1ull;
+                if (!ok) s[ii][jj] = -INFINITY;
+            }
+        }
+#pragma unroll
+        for (int ii = 0; ii < 4; ++ii) {
+            float mt = fmaxf(fmaxf(s[ii][0], s[ii][1]), fmaxf(s[ii][2], s[ii][3]));
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, off));
+            const float m_new = fmaxf(m_run[ii], mt);
+            float alpha = 1.f, lt = 0.f;
+            float p[4];
+            if (m_new == -INFINITY) {
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) p[jj] = 0.f;
+            } else {
+                alpha = exp2f(m_run[ii] - m_new);
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) { p[jj] = exp2f(s[ii][jj] - m_new); lt += p[jj]; }
+            }
+#pragma unroll
+            for (int off = 8; off > 0; off >>= 1) lt += __shfl_xor_sync(0xffffffffu, lt, off);
+            l_run[ii] = l_run[ii] * alpha + lt;
+            m_run[ii] = m_new;
+#pragma unroll
+            for (int e = 0; e < DT; ++e) o[ii][e] *= alpha;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) Ps[(4 * rg + ii) * LP + kg + 16 * jj] = p[jj];
+        }
+        __syncwarp();
+#pragma unroll 4
+        for (int j = 0; j < BC; ++j) {
+            float pj[4];
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) pj[ii] = Ps[(4 * rg + ii) * LP + j];
+#pragma unroll
+            for (int half = 0; half < DT / 4; ++half) {
+                const float4 v = *reinterpret_cast<const float4*>(&Vs[j * LD + half * 64 + kg * 4]);
+#pragma unroll
+                for (int ii = 0; ii < 4; ++ii) {
+                    o[ii][half * 4 + 0] += pj[ii] * v.x;
+                    o[ii][half * 4 + 1] += pj[ii] * v.y;
+                    o[ii][half * 4 + 2] += pj[ii] * v.z;
+                    o[ii][half * 4 + 3] += pj[ii] * v.w;
+                }
+            }
+        }
+    }
+    const int n_chunks = n_pre + 1;
+#pragma unroll
+    for (int ii = 0; ii < 4; ++ii) {
+        const int r = r0 + 4 * rg + ii;
+        if (r >= R) continue;
+        const int hl = r / Tn, i = r % Tn;
+        const int h = kvh * g + hl;
+        const size_t row = (static_cast<size_t>(b) * Hq + h) * Tn + i;
+        float* base = part + (row * n_chunks + c) * (D + 4);
+        if (kg == 0) { base[0] = m_run[ii]; base[1] = l_run[ii]; }
+#pragma unroll
+        for (int half = 0; half < DT / 4; ++half)
+            *reinterpret_cast<float4*>(&base[4 + half * 64 + kg * 4]) =
+                make_float4(o[ii][half * 4 + 0], o[ii][half * 4 + 1], o[ii][half * 4 + 2], o[ii][half * 4 + 3]);
+    }
+}
+
+// ---------------------------------------------------------------- combine
+
+__global__ void k_attn_combine(const float* __restrict__ part, const int32_t* __restrict__ prefix_len, int Tn, int Hq,
+                               int D, int Lmax, int chunk, int n_pre, float* __restrict__ out, float* __restrict__ lse) {
+    const int row = blockIdx.x;
+    const int b = row / (Hq * Tn);
+    const int L = min(max(prefix_len[b], 0), Lmax);
+    const int nvalid = (L + chunk - 1) / chunk;
+    const int n_chunks = n_pre + 1;
+    const float* base = part + static_cast<size_t>(row) * n_chunks * (D + 4);
+    float M = base[static_cast<size_t>(n_pre) * (D + 4)];
+    for (int c = 0; c < nvalid; ++c) M = fmaxf(M, base[static_cast<size_t>(c) * (D + 4)]);
+    float l = 0.f;
+    const int d = threadIdx.x;
+    float o = 0.f;
+    for (int c = 0; c <= nvalid; ++c) {
+        const int cc = (c == nvalid) ? n_pre : c;
+        const float* pc = base + static_cast<size_t>(cc) * (D + 4);
+        const float w = exp2f(pc[0] - M);
+        l += w * pc[1];
+        if (d < D) o += w * pc[4 + d];
+    }
+    if (d < D) out[static_cast<size_t>(row) * D + d] = o / l;
+    if (lse && d == 0) lse[row] = (M + log2f(l)) * kLn2;
+}
+
+// ---------------------------------------------------------------- planning
+
+struct Plan {
+    bool tc;
+    int n_rowblocks, chunk, n_pre;
+    size_t part_bytes, total;
+    tc::AttnTcPlan tcp;
+};
+
+Plan make_plan(const spec_tree* t, int B, int Hq, int Hkv, int Lmax, int D, spec_dtype dt) {
+    Plan p{};
+    const int g = Hq / Hkv;
+    const int R = t->T * g;
+    p.tc = (dt == SPEC_BF16) && tc::attn_tc_supported(R, D);
+    if (p.tc) {
+        p.tcp = tc::attn_tc_plan(B, Hq, Hkv, t->T, Lmax, D, device_sm_count());
+        p.part_bytes = p.tcp.part_bytes;
+    } else {
+        p.n_rowblocks = (R + BR - 1) / BR;
+        const int64_t base = static_cast<int64_t>(B) * Hkv * p.n_rowblocks;
+        const int64_t target = 2ll * device_sm_count();
+        const int max_chunks = (Lmax + BC - 1) / BC;
+        const int want = static_cast<int>(std::min<int64_t>(std::max<int64_t>((target + base - 1) / base, 1), max_chunks));
+        p.chunk = static_cast<int>(round_up((Lmax + want - 1) / want, BC));
+        p.n_pre = (Lmax + p.chunk - 1) / p.chunk;
+        p.part_bytes = sizeof(float) * static_cast<size_t>(B) * Hq * t->T * (p.n_pre + 1) * (D + 4);
+    }
+    p.total = kWsHeader + round_up(p.part_bytes, 256);
+    return p;
+}
+
+spec_status check_args(const spec_tree* t, int B, int Hq, int Hkv, int Lmax, int D, spec_dtype dt) {
+    spec_status st = check_tree(t);
+    if (st != SPEC_OK) return st;
+    if (dt != SPEC_F32 && dt != SPEC_BF16) return fail(SPEC_EINVAL, "dtype %d unknown", (int)dt);
+    if (B < 1 || B > 65535) return fail(SPEC_EINVAL, "B = %d out of 1..65535", B);
+    if (Hkv < 1 || Hq < Hkv || Hq % Hkv || Hq > 1024) return fail(SPEC_EINVAL, "Hq = %d must be a multiple of Hkv = %d", Hq, Hkv);
+    if (D != 64 && D != 128) return fail(SPEC_EUNSUPPORTED, "D = %d: only 64 and 128 are built", D);
+    if (Lmax < 1 || Lmax > (1 << 22)) return fail(SPEC_EINVAL, "Lmax = %d out of 1..2^22", Lmax);
+    if (static_cast<int64_t>(t->T) * (Hq / Hkv) > 65535ll * BR) return fail(SPEC_EINVAL, "too many query rows per KV head");
+    return SPEC_OK;
+}
+
+template <typename T>
+spec_status run_fma(const T* q, const T* kc, const T* vc, const int32_t* prefix_len, const T* kt, const T* vt,
+                    const spec_tree* t, int B, int Hq, int Hkv, int Lmax, int D, float scale, float* out, float* lse,
+                    void* ws, const Plan& p, cudaStream_t s) {
+    float* part = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kWsHeader);
+    const dim3 grid(p.n_pre + 1, Hkv * p.n_rowblocks, B);
+    const float sl2 = scale * kLog2e;
+    if (D == 128) {
+        const size_t smem = sizeof(float) * (BR * 132 + 2 * BC * 132 + BR * (BC + 4));
+        SPEC_CUDA_TRY(cudaFuncSetAttribute(k_attn_fma<T, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        SPEC_CUDA_TRY(launch("attn_fma", k_attn_fma<T, 128>, grid, dim3(256), smem, s, q, kc, vc, prefix_len, kt, vt,
+                             t->anc, t->T, t->words, Hq, Hkv, Lmax, sl2, p.chunk, p.n_pre, p.n_rowblocks, part));
+    } else {
+        const size_t smem = sizeof(float) * (BR * 68 + 2 * BC * 68 + BR * (BC + 4));
+        SPEC_CUDA_TRY(cudaFuncSetAttribute(k_attn_fma<T, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+        SPEC_CUDA_TRY(launch("attn_fma", k_attn_fma<T, 64>, grid, dim3(256), smem, s, q, kc, vc, prefix_len, kt, vt,
+                             t->anc, t->T, t->words, Hq, Hkv, Lmax, sl2, p.chunk, p.n_pre, p.n_rowblocks, part));
+    }
+    SPEC_CUDA_TRY(launch("attn_combine", k_attn_combine, dim3(B * Hq * t->T), dim3(D), 0, s, part, prefix_len, t->T,
+                         Hq, D, Lmax, p.chunk, p.n_pre, out, lse));
+    return SPEC_OK;
+}
+
+}  // namespace attn
+}  // namespace spec
+
+using namespace spec;
+
+extern "C" size_t tree_attention_workspace_size(const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv,
+                                                int32_t Lmax, int32_t D, spec_dtype dt) {
+    clear_error();
+    if (attn::check_args(tree, B, Hq, Hkv, Lmax, D, dt) != SPEC_OK) return 0;
+    return attn::make_plan(tree, B, Hq, Hkv, Lmax, D, dt).total;
+}
+
+extern "C" spec_status tree_attention(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* prefix_len, const void* k_tree, const void* v_tree,
+                                      const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
+                                      int32_t D, float scale, spec_dtype dt, float* out, float* lse, void* ws,
+                                      size_t ws_bytes, spec_stream_t s_) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(s_);
+    clear_error();
+    spec_status st = attn::check_args(tree, B, Hq, Hkv, Lmax, D, dt);
+    if (st != SPEC_OK) return st;
+    if (!q || !k_cache || !v_cache || !prefix_len || !k_tree || !v_tree || !out)
+        return fail(SPEC_EINVAL, "q, caches, prefix_len, tree K/V and out must not be NULL");
+    if (!(scale > 0.f) || !(scale < 1e30f)) return fail(SPEC_EINVAL, "scale must be positive and finite");
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_tree) || !aligned16(v_tree) ||
+        !aligned16(out) || !aligned4(prefix_len) || (lse && !aligned4(lse)))
+        return fail(SPEC_EALIGN, "tensors must be 16-byte aligned (prefix_len and lse 4-byte)");
+    const attn::Plan p = attn::make_plan(tree, B, Hq, Hkv, Lmax, D, dt);
+    if (!ws || ws_bytes < p.total) return fail(SPEC_EWORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, p.total);
+    if (!aligned16(ws)) return fail(SPEC_EALIGN, "workspace must be 16-byte aligned");
+    SPEC_CUDA_TRY(reset_device_status(ws, s));
+    if (dt == SPEC_BF16) {
+        using T = __nv_bfloat16;
+        if (p.tc)
+            return tc::attn_tc_run(p.tcp, static_cast<const T*>(q), static_cast<const T*>(k_cache),
+                                   static_cast<const T*>(v_cache), prefix_len, static_cast<const T*>(k_tree),
+                                   static_cast<const T*>(v_tree), tree, B, Hq, Hkv, Lmax, D, scale, out, lse, ws, s);
+        return attn::run_fma<T>(static_cast<const T*>(q), static_cast<const T*>(k_cache), static_cast<const T*>(v_cache),
+                                prefix_len, static_cast<const T*>(k_tree), static_cast<const T*>(v_tree), tree, B, Hq,
+                                Hkv, Lmax, D, scale, out, lse, ws, p, s);
+    }
+    return attn::run_fma<float>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
+                                static_cast<const float*>(v_cache), prefix_len, static_cast<const float*>(k_tree),
+                                static_cast<const float*>(v_tree), tree, B, Hq, Hkv, Lmax, D, scale, out, lse, ws, p, s);
+}

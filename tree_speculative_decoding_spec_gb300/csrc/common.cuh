@@ -1,0 +1,111 @@
+// Shared host/device helpers of the spec_tree library: error reporting,
+// argument checks, the traced launch wrapper, element conversions.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdint>
+#include <cstdio>
+#include <utility>
+
+#include "spec_tree.h"
+
+namespace spec {
+
+// ---------------------------------------------------------------- errors (host)
+
+void set_error(const char* fmt, ...);
+void clear_error();
+
+// Record a message and return the status, for `return fail(SPEC_EINVAL, "...")`.
+spec_status fail(spec_status st, const char* fmt, ...);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count();
+
+// Checks of a spec_tree passed by a caller (host fields and device pointers).
+spec_status check_tree(const spec_tree* t);
+
+// Workspace header: the first 16 bytes of every workspace hold the device status word.
+constexpr size_t kWsHeader = 256;
+inline size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Reset the device status word of a workspace (queued on the stream).
+cudaError_t reset_device_status(void* ws, cudaStream_t s);
+
+// ---------------------------------------------------------------- traced launches
+
+void trace_before(cudaStream_t s);
+void trace_after(cudaStream_t s, const char* name);
+void count_launch();
+
+// Launch `kernel` on stream `s`, bracketed by trace events when tracing is on.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch(const char* name, void (*kernel)(KArgs...), dim3 grid, dim3 block,
+                          size_t smem, cudaStream_t s, Args&&... args) {
+    trace_before(s);
+    kernel<<<grid, block, smem, s>>>(std::forward<Args>(args)...);
+    cudaError_t e = cudaGetLastError();
+    trace_after(s, name);
+    count_launch();
+    return e;
+}
+
+#define SPEC_CUDA_TRY(expr)                                                              \
+    do {                                                                                 \
+        cudaError_t _e = (expr);                                                         \
+        if (_e != cudaSuccess)                                                           \
+            return ::spec::fail(SPEC_ECUDA, "%s: %s", #expr, cudaGetErrorString(_e));    \
+    } while (0)
+
+// ---------------------------------------------------------------- device helpers
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Load 4 consecutive elements (16 bytes of fp32 or 8 bytes of bf16) as floats.
+__device__ __forceinline__ void load4(const float* p, float (&v)[4]) {
+    float4 t = *reinterpret_cast<const float4*>(p);
+    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
+}
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float (&v)[4]) {
+    uint2 t = *reinterpret_cast<const uint2*>(p);
+    v[0] = __uint_as_float(t.x << 16); v[1] = __uint_as_float(t.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(t.y << 16); v[3] = __uint_as_float(t.y & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_min(float v) {
+    for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+__device__ __forceinline__ float warp_sum(float v) {
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Record a device-detected failure in a workspace's status word (largest code wins).
+__device__ __forceinline__ void flag_status(void* ws, int code) { atomicMax(static_cast<int*>(ws), code); }
+
+// Merge two (max, sum of exp(x - max)) pairs.
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+    if (m2 == -INFINITY) return;
+    if (m == -INFINITY) { m = m2; s = s2; return; }
+    if (m2 > m) { s = s * expf(m - m2) + s2; m = m2; }
+    else { s = s + s2 * expf(m2 - m); }
+}
+
+}  // namespace spec

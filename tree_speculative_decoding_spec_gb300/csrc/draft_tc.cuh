@@ -1,0 +1,32 @@
+// Tensor-core (tcgen05) path of the draft heads, bf16 weights.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+
+namespace spec {
+namespace draft {
+struct Cand;
+}
+namespace tc {
+
+struct DraftTcPlan {
+    int rows_pad = 0;              // rows padded to the MMA N granule
+    int nslices = 0;               // vocabulary slices (one per 128-row W2 tile)
+    size_t mlp_partial_bytes = 0;  // split-K partial sums of the MLP
+};
+
+bool draft_tc_supported(int d, int V);
+DraftTcPlan draft_tc_plan(int rows, int d, int d_in_max, int V, int kmax);
+
+// One head: MLP (split-K, fused SiLU/residual epilogue) then the projection with
+// per-slice top-k and (max, sum exp) partials.  xin holds the gathered rows
+// (row stride d_in_pad); z receives the bf16 MLP output.
+spec_status draft_head_tc(const DraftTcPlan& p, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
+                          const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* xin, int d_in,
+                          int d_in_pad, __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax,
+                          float* scratch, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s);
+
+}  // namespace tc
+}  // namespace spec
