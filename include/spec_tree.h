@@ -176,6 +176,31 @@ spec_status tree_attention(const void* q, const void* k_cache, const void* v_cac
                            int32_t D, float scale, spec_dtype dt, float* out, float* lse,
                            void* ws, size_t ws_bytes, spec_stream_t s);
 
+/*
+ * tree_attention without a caller-provided workspace.  The pages have no
+ * counterpart to this call: it exists for callers that cannot allocate device
+ * memory, such as a plugin running inside a host engine that has already
+ * handed out the device memory and forbids further cudaMalloc calls, or a
+ * caller whose own interface has no way to pass a workspace pointer through.
+ *
+ * Arguments, results and errors are those of tree_attention without ws and
+ * ws_bytes.  The scratch is a 32 MiB array inside this library's device image
+ * (every GPU that loads the library holds it until the process exits); shapes
+ * whose tree_attention_workspace_size exceeds 32 MiB are rejected with
+ * SPEC_EWORKSPACE before anything is queued.  The call allocates nothing.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  All calls share the one array and it keeps the
+ * last call's contents (each call clears what must start at zero): calls
+ * whose work overlaps on the GPU -- on different streams, or from different
+ * host threads -- race on it and must not be issued.
+ */
+spec_status tree_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* prefix_len, const void* k_tree, const void* v_tree,
+                                   const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
+                                   int32_t D, float scale, spec_dtype dt, float* out, float* lse, spec_stream_t s);
+
 /* Workspace bytes tree_accept needs (0 on invalid arguments). */
 size_t tree_accept_workspace_size(int32_t mode, const spec_tree* tree, int32_t B, int32_t V);
 

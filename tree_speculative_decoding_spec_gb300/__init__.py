@@ -9,7 +9,7 @@ binding loads the library and fails loudly when it has not been built.
 __all__ = [
     "spec_tree_build", "spec_tree_device_bytes",
     "hydra_draft", "hydra_draft_workspace_size",
-    "tree_attention", "tree_attention_workspace_size",
+    "tree_attention", "tree_attention_workspace_size", "tree_attention_noalloc",
     "tree_accept", "tree_accept_workspace_size",
     "spec_philox_uniform", "spec_read_device_status", "spec_last_error",
     "spec_trace_begin", "spec_trace_end", "spec_launch_count",

@@ -62,6 +62,7 @@ def _load():
         "hydra_draft": (i32, [vp, vp, i32, vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]),
         "tree_attention_workspace_size": (sz, [tp, i32, i32, i32, i32, i32, i32]),
         "tree_attention": (i32, [vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]),
+        "tree_attention_noalloc": (i32, [vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp]),
         "tree_accept_workspace_size": (sz, [i32, tp, i32, i32]),
         "tree_accept": (i32, [i32, vp, vp, vp, tp, i32, i32, f32, u64, u64, vp, vp, vp, vp, vp, sz, vp]),
         "spec_philox_uniform": (i32, [u64, u64, i32, i32, vp, vp, vp]),
@@ -273,6 +274,40 @@ def tree_attention(q, k_cache, v_cache, prefix_len, k_tree, v_tree, tree, scale=
                                                      _ptr(k_tree), _ptr(v_tree), tree.ref(), B, Hq, Hkv, Lmax, D,
                                                      float(scale), dt, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
                                                      _stream(stream)))
+    return out, lse
+
+
+def tree_attention_noalloc(q, k_cache, v_cache, prefix_len, k_tree, v_tree, tree, scale=None, out=None, lse=None,
+                           want_lse=True, stream=None):
+    """tree_attention for callers that cannot allocate device scratch: the library's
+    built-in 32 MiB buffer serves as workspace (one call at a time per process).
+    Outputs are allocated here only when the caller passes none."""
+    _need(q, "q", ndim=4)
+    dev = q.device
+    dt = _dtype_code(q)
+    B, Hq, T, D = q.shape
+    _need(k_cache, "k_cache", dtype=q.dtype, ndim=4, device=dev)
+    _need(v_cache, "v_cache", dtype=q.dtype, ndim=4, device=dev)
+    Hkv, Lmax = k_cache.shape[1], k_cache.shape[2]
+    if tuple(k_cache.shape) != (B, Hkv, Lmax, D) or tuple(v_cache.shape) != (B, Hkv, Lmax, D):
+        raise ValueError("caches must be [B, Hkv, Lmax, D]")
+    _need(k_tree, "k_tree", dtype=q.dtype, ndim=4, device=dev)
+    _need(v_tree, "v_tree", dtype=q.dtype, ndim=4, device=dev)
+    if tuple(k_tree.shape) != (B, Hkv, T, D) or tuple(v_tree.shape) != (B, Hkv, T, D):
+        raise ValueError("tree keys/values must be [B, Hkv, T, D]")
+    if T != tree.T:
+        raise ValueError(f"q has {T} nodes, the tree {tree.T}")
+    _need(prefix_len, "prefix_len", dtype=torch.int32, ndim=1, device=dev)
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    if out is None:
+        out = torch.empty(B, Hq, T, D, dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        _check("tree_attention_noalloc", _lib.tree_attention_noalloc(
+            _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(prefix_len), _ptr(k_tree), _ptr(v_tree), tree.ref(),
+            B, Hq, Hkv, Lmax, D, float(scale), dt, _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
 
 

@@ -12,6 +12,7 @@
 // against one chunk with an online softmax and writes (max, sum, unnormalised
 // output) to the workspace; a combine kernel merges the chunks of each row.
 #include <algorithm>
+#include <mutex>
 
 #include "attention_tc.cuh"
 #include "common.cuh"
@@ -327,4 +328,64 @@ extern "C" spec_status tree_attention(const void* q, const void* k_cache, const 
     return attn::run_fma<float>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
                                 static_cast<const float*>(v_cache), prefix_len, static_cast<const float*>(k_tree),
                                 static_cast<const float*>(v_tree), tree, B, Hq, Hkv, Lmax, D, scale, out, lse, ws, p, s);
+}
+
+// ---------------------------------------------------------------- tree_attention without caller scratch
+//
+// Some callers cannot allocate device memory: a plugin running inside a host
+// engine that has already handed out the device memory and forbids further
+// cudaMalloc calls, or a caller whose own interface has no way to carry a
+// workspace pointer through.  tree_attention_noalloc serves them with scratch
+// held in the file-scope array below instead of a caller-provided workspace.
+// The array is part of this library's device image, so every GPU that loads
+// the library holds it until the process exits.
+
+namespace spec {
+namespace attn {
+
+constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once per
+// device (host code sees only a host-side stand-in under the array's name).
+static spec_status noalloc_scratch(void** out) {
+    static std::mutex mu;
+    static void* addr[64] = {};
+    int dev = -1;
+    SPEC_CUDA_TRY(cudaGetDevice(&dev));
+    if (dev < 0 || dev >= 64) return fail(SPEC_EUNSUPPORTED, "device ordinal %d out of range", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void* p = nullptr;
+        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess || !p)
+            return fail(SPEC_ECUDA, "cudaGetSymbolAddress of the built-in scratch failed: %s", cudaGetErrorString(e));
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return SPEC_OK;
+}
+
+}  // namespace attn
+}  // namespace spec
+
+extern "C" spec_status tree_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
+                                              const int32_t* prefix_len, const void* k_tree, const void* v_tree,
+                                              const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
+                                              int32_t D, float scale, spec_dtype dt, float* out, float* lse,
+                                              spec_stream_t s) {
+    clear_error();
+    spec_status st = attn::check_args(tree, B, Hq, Hkv, Lmax, D, dt);
+    if (st != SPEC_OK) return st;
+    const size_t need = attn::make_plan(tree, B, Hq, Hkv, Lmax, D, dt).total;
+    if (need > attn::kNoAllocScratchBytes)
+        return fail(SPEC_EWORKSPACE,
+                    "tree_attention_noalloc: these shapes need %zu bytes of scratch, more than the %zu-byte built-in "
+                    "buffer; call tree_attention with a workspace instead",
+                    need, attn::kNoAllocScratchBytes);
+    void* ws = nullptr;
+    st = attn::noalloc_scratch(&ws);
+    if (st != SPEC_OK) return st;
+    return tree_attention(q, k_cache, v_cache, prefix_len, k_tree, v_tree, tree, B, Hq, Hkv, Lmax, D, scale, dt, out,
+                          lse, ws, attn::kNoAllocScratchBytes, s);
 }
