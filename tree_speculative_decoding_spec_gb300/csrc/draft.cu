@@ -114,11 +114,6 @@ __global__ void __launch_bounds__(256) k_gemm_fma(const T* __restrict__ W, const
 
 // ---------------------------------------------------------------- top-k over logits rows (fp32 path)
 
-// A candidate (value, token): "better" = larger value, then lower token.
-struct Cand {
-    float v;
-    int i;
-};
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) { return va > vb || (va == vb && ia < ib); }
 
 // Insert (v, i) into a descending list of length k (registers, fully unrolled).

@@ -1,21 +1,408 @@
-// Tensor-core (tcgen05) path of the draft heads.
+// Tensor-core (tcgen05) path of the draft heads, bf16 weights.
+//
+// Both GEMMs of a head are "skinny": a few to a few hundred activation rows
+// against a weight matrix streamed once from HBM.  They run swap-AB: weight
+// rows fill the MMA's M = 128 side, activation rows its N side (padded to 16),
+// so one CTA owns a 128-row weight tile and TMEM holds its 128 x N fp32 result.
+//
+// Per CTA: thread 0 issues TMA loads of 128 x 64 weight and N x 64 activation
+// tiles (128-byte swizzle) into a ring of shared-memory stages; thread 32
+// issues tcgen05.mma (K = 16 per instruction) as stages land and releases each
+// stage through tcgen05.commit; after the last stage all four warps read TMEM.
+// Every wait is bounded (2 s); on expiry the kernel records SPEC_ETIMEOUT in the
+// workspace status word, drains its own loads and frees TMEM.
+//
+// Epilogues:
+//   MLP (W1, split over K): fp32 partial sums per split, reduced by
+//       k_mlp_finish with bias, SiLU, the residual h and bf16 rounding.
+//   projection (W2): per activation row, the top-k (value desc, token asc)
+//       and (max, sum exp) of the tile's 128 logits; logits never reach HBM.
+#include <mutex>
+
 #include "draft_tc.cuh"
+#include "tc.cuh"
 
 namespace spec {
 namespace tc {
 
-bool draft_tc_supported(int, int) { return false; }
+constexpr int kBM = 128;        // MMA M: weight rows per CTA
+constexpr int kBK = 64;         // K per stage: one 128-byte swizzled row of bf16
+constexpr int kThreads = 128;
+constexpr int kStageA = kBM * kBK * 2;
+constexpr int kSmemBudget = 100 * 1024;   // keeps two CTAs per SM
 
-DraftTcPlan draft_tc_plan(int rows, int, int, int, int) {
+struct UmmaParams {
+    int M;          // weight rows
+    int k_iters;    // K stages per split
+    int total_iters;
+    int n_pad;      // MMA N
+    int n_valid;    // valid activation rows in this launch
+    int stages;
+    uint32_t tmem_cols;
+    // MLP epilogue
+    float* partial;     // [splits][n_pad][M]
+    // projection epilogue
+    int topk;
+    int V;
+    int nslices;
+    int row0;           // first activation row of this launch (output row offset)
+    draft::Cand* part_c;
+    float2* part_l;
+    int kmax;
+    void* ws;           // status word
+};
+
+__device__ __forceinline__ bool cbetter(float va, int ia, float vb, int ib) {
+    return va > vb || (va == vb && ia < ib);
+}
+
+template <int KMAX>
+__device__ __forceinline__ void push_topk(float (&lv)[KMAX], int (&li)[KMAX], int k, float v, int i) {
+    if (!cbetter(v, i, lv[k - 1], li[k - 1])) return;
+#pragma unroll
+    for (int s = KMAX - 1; s > 0; --s) {
+        if (s < k && cbetter(v, i, lv[s - 1], li[s - 1])) { lv[s] = lv[s - 1]; li[s] = li[s - 1]; }
+        else if (s < k && cbetter(v, i, lv[s], li[s])) { lv[s] = v; li[s] = i; }
+    }
+    if (cbetter(v, i, lv[0], li[0])) { lv[0] = v; li[0] = i; }
+}
+
+__device__ __forceinline__ void lse_add(float& m, float& s, float v) {
+    if (v == -INFINITY) return;
+    if (v > m) { s = s * expf(m - v) + 1.f; m = v; }
+    else s += expf(v - m);
+}
+
+template <int EPI, int KMAX>
+__global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CUtensorMap tmA,
+                                                      const __grid_constant__ CUtensorMap tmB, const UmmaParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const int stage_b = p.n_pad * kBK * 2;
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + p.stages * kStageA;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sB + p.stages * stage_b);
+    uint64_t* empty = full + p.stages;
+    uint64_t* accum = empty + p.stages;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(accum + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * kBM;
+    const int it0 = blockIdx.y * p.k_iters;
+    const int n_it = max(0, min(p.k_iters, p.total_iters - it0));
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < p.stages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(accum, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, p.tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    int issued = 0;   // producer: stages loaded
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < n_it; ++i) {
+            const int s = i % p.stages;
+            if (i >= p.stages && !mbar_wait(&empty[s], ((i / p.stages) - 1) & 1)) {
+                flag_status(p.ws, SPEC_ETIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            if (*abort_flag) break;
+            mbar_arrive_expect_tx(&full[s], kStageA + stage_b);
+            const int kx = (it0 + i) * kBK;
+            tma_load_2d(sA + s * kStageA, &tmA, &full[s], kx, m0);
+            tma_load_2d(sB + s * stage_b, &tmB, &full[s], kx, 0);
+            issued = i + 1;
+        }
+    } else if (threadIdx.x == 32) {
+        const uint32_t idesc = idesc_bf16_f32(kBM, p.n_pad);
+        for (int i = 0; i < n_it; ++i) {
+            const int s = i % p.stages;
+            if (!mbar_wait(&full[s], (i / p.stages) & 1)) {
+                flag_status(p.ws, SPEC_ETIMEOUT);
+                *abort_flag = 1;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + s * kStageA), b0 = smem_u32(sB + s * stage_b);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+                mma_bf16(tmem, sdesc_k128(a0 + kk * 32), sdesc_k128(b0 + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
+            mma_commit(&empty[s]);
+        }
+        mma_commit(accum);
+    }
+
+    const bool have = mbar_wait(accum, 0);
+    if (!have && threadIdx.x == 64) flag_status(p.ws, SPEC_ETIMEOUT);
+    tc_fence_after();
+    __syncthreads();
+    const bool run_epi = have && !*abort_flag && n_it > 0;
+
+    if (run_epi && EPI == 0) {
+        const int m = m0 + warp * 32 + lane;
+        for (int c0 = 0; c0 < p.n_pad; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, r);
+            tmem_ld_wait();
+            if (m < p.M) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    const int n = c0 + j;
+                    if (n < p.n_valid)
+                        p.partial[(static_cast<size_t>(blockIdx.y) * p.n_pad + n) * p.M + m] = __uint_as_float(r[j]);
+                }
+            }
+        }
+    }
+    if (run_epi && EPI == 1) {
+        // stage buffers are free now: reuse them for the transposed tile and the candidate lists
+        float* tile = reinterpret_cast<float*>(smem);                      // [32 columns][4 quarters][33]
+        draft::Cand* cl = reinterpret_cast<draft::Cand*>(smem + 32 * 132 * 4);   // [128 threads][KMAX]
+        float2* ml = reinterpret_cast<float2*>(cl + kThreads * KMAX);      // [128]
+        const int j = threadIdx.x >> 2, q = threadIdx.x & 3;               // scan: column j, rows 32q .. 32q+31
+        const int k = p.topk;
+        for (int c0 = 0; c0 < p.n_pad; c0 += 32) {
+            uint32_t r[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) tile[jj * 132 + warp * 33 + lane] = __uint_as_float(r[jj]);
+            __syncthreads();
+            float lv[KMAX];
+            int li[KMAX];
+#pragma unroll
+            for (int s = 0; s < KMAX; ++s) { lv[s] = -INFINITY; li[s] = 0x7fffffff; }
+            float mx = -INFINITY, sm = 0.f;
+            const int n = c0 + j;
+            if (n < p.n_valid) {
+                for (int i = 0; i < 32; ++i) {
+                    const int v = m0 + 32 * q + i;
+                    if (v >= p.V) break;
+                    const float x = tile[j * 132 + q * 33 + i];
+                    push_topk<KMAX>(lv, li, k, x, v);
+                    lse_add(mx, sm, x);
+                }
+            }
+#pragma unroll
+            for (int s = 0; s < KMAX; ++s) cl[threadIdx.x * KMAX + s] = draft::Cand{lv[s], li[s]};
+            ml[threadIdx.x] = make_float2(mx, sm);
+            __syncthreads();
+            if (q == 0 && n < p.n_valid) {
+                int head[4] = {0, 0, 0, 0};
+                const size_t out = (static_cast<size_t>(p.row0 + n) * p.nslices + blockIdx.x);
+                for (int s = 0; s < k; ++s) {
+                    int best = -1;
+                    float bv = -INFINITY;
+                    int bi = 0x7fffffff;
+#pragma unroll
+                    for (int qq = 0; qq < 4; ++qq) {
+                        if (head[qq] >= k) continue;
+                        const draft::Cand c = cl[(threadIdx.x + qq) * KMAX + head[qq]];
+                        if (best < 0 || cbetter(c.v, c.i, bv, bi)) { best = qq; bv = c.v; bi = c.i; }
+                    }
+                    head[best] += 1;
+                    p.part_c[out * p.kmax + s] = draft::Cand{bv, bi};
+                }
+                float M = -INFINITY, S = 0.f;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const float2 e = ml[threadIdx.x + qq];
+                    if (e.x == -INFINITY) continue;
+                    if (M == -INFINITY) { M = e.x; S = e.y; }
+                    else if (e.x > M) { S = S * expf(M - e.x) + e.y; M = e.x; }
+                    else S += e.y * expf(e.x - M);
+                }
+                p.part_l[out] = make_float2(M, S);
+            }
+            __syncthreads();
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (threadIdx.x == 0 && *abort_flag) {
+        // a wait ran out: let this CTA's own loads land before the shared memory is released
+        for (int i = max(0, issued - p.stages); i < issued; ++i)
+            mbar_wait(&full[i % p.stages], (i / p.stages) & 1, 100000000ull);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, p.tmem_cols);
+    }
+}
+
+// z[row0 + n][m] = h[b][m] + SiLU(sum_s partial[s][n][m] + b1[m]), rounded to bf16,
+// for the `rows` activation rows of one group (b = the sequence of that row).
+__global__ void k_mlp_finish(const float* __restrict__ partial, int splits, int n_pad, int rows, int row0, int d,
+                             const __nv_bfloat16* __restrict__ b1, const __nv_bfloat16* __restrict__ h, int cond,
+                             int n_int, __nv_bfloat16* __restrict__ z) {
+    const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= static_cast<size_t>(rows) * d) return;
+    const int n = static_cast<int>(idx / d), m = static_cast<int>(idx % d);
+    float a = b1 ? __bfloat162float(b1[m]) : 0.f;
+    for (int s = 0; s < splits; ++s) a += partial[(static_cast<size_t>(s) * n_pad + n) * d + m];
+    const int row = row0 + n;
+    const int b = cond ? row / n_int : row;
+    const float zz = __bfloat162float(h[static_cast<size_t>(b) * d + m]) + a / (1.0f + expf(-a));
+    z[static_cast<size_t>(row) * d + m] = __float2bfloat16_rn(zz);
+}
+
+// ---------------------------------------------------------------- host
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+int n_pad_of(int rows) { return std::max(16, static_cast<int>(round_up(rows, 16))); }
+
+uint32_t tmem_cols_of(int n_pad) {
+    uint32_t c = 32;
+    while (c < static_cast<uint32_t>(n_pad)) c <<= 1;
+    return c;
+}
+
+int stages_of(int n_pad) {
+    const int per = kStageA + n_pad * kBK * 2;
+    return std::max(2, std::min(8, kSmemBudget / per));
+}
+
+size_t smem_of(int n_pad, int stages) {
+    return 1024 + static_cast<size_t>(stages) * (kStageA + n_pad * kBK * 2) + (2 * stages + 1) * 8 + 16;
+}
+
+constexpr int kMaxN = 256;
+
+}  // namespace
+
+cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols, uint64_t ld,
+                              uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {ld * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+// The merge kernel keeps one list head per 128-token slice, at most 1024 slices.
+bool draft_tc_supported(int d, int V) {
+    return d >= 8 && d % 8 == 0 && V >= 1 && (V + kBM - 1) / kBM <= 1024 && encode_fn() != nullptr;
+}
+
+static int mlp_splits(int d, int d_in) {
+    const int m_tiles = (d + kBM - 1) / kBM;
+    const int total = (d_in + kBK - 1) / kBK;
+    const int want = std::max(1, (2 * device_sm_count() + m_tiles - 1) / m_tiles);
+    const int per = (total + want - 1) / want;
+    return (total + per - 1) / per;
+}
+
+DraftTcPlan draft_tc_plan(int rows, int d, int d_in_max, int V, int kmax) {
     DraftTcPlan p;
-    p.rows_pad = rows;
+    p.rows_pad = n_pad_of(rows);
+    p.nslices = (V + kBM - 1) / kBM;
+    const int splits = std::max(mlp_splits(d, d), mlp_splits(d, d_in_max));
+    p.mlp_partial_bytes = sizeof(float) * static_cast<size_t>(splits) * std::min(p.rows_pad, kMaxN) * d;
+    (void)kmax;
     return p;
 }
 
-spec_status draft_head_tc(const DraftTcPlan&, const __nv_bfloat16*, const __nv_bfloat16*, const __nv_bfloat16*,
-                          const __nv_bfloat16*, const __nv_bfloat16*, int, int, __nv_bfloat16*, int, int, int, int, int,
-                          int, int, float*, draft::Cand*, float2*, void*, cudaStream_t) {
-    return fail(SPEC_EUNSUPPORTED, "tensor-core draft path not built");
+template <int EPI, int KMAX>
+static spec_status launch_umma(const CUtensorMap& ta, const CUtensorMap& tb, dim3 grid, const UmmaParams& p,
+                               cudaStream_t s, const char* name) {
+    const size_t smem = smem_of(p.n_pad, p.stages);
+    SPEC_CUDA_TRY(cudaFuncSetAttribute(k_umma<EPI, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
+    SPEC_CUDA_TRY(launch(name, k_umma<EPI, KMAX>, grid, dim3(kThreads), smem, s, ta, tb, p));
+    return SPEC_OK;
+}
+
+spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
+                          const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* xin, int d_in,
+                          int d_in_pad, __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax,
+                          float* scratch, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s) {
+    const int splits = mlp_splits(d, d_in);
+    const int total_mlp = (d_in + kBK - 1) / kBK;
+    const int per_split = (total_mlp + splits - 1) / splits;
+    // ---- MLP, activation rows in groups of at most 256 (the MMA's largest N)
+    for (int g0 = 0; g0 < R; g0 += kMaxN) {
+        const int rows = std::min(kMaxN, R - g0);
+        const int n_pad = n_pad_of(rows);
+        CUtensorMap ta, tb;
+        SPEC_CUDA_TRY(make_tmap_bf16_2d(&ta, W1, d, d_in, d_in, kBM));
+        SPEC_CUDA_TRY(make_tmap_bf16_2d(&tb, xin + static_cast<size_t>(g0) * d_in_pad, rows, d_in, d_in_pad, n_pad));
+        UmmaParams p{};
+        p.M = d;
+        p.k_iters = per_split;
+        p.total_iters = total_mlp;
+        p.n_pad = n_pad;
+        p.n_valid = rows;
+        p.stages = stages_of(n_pad);
+        p.tmem_cols = tmem_cols_of(n_pad);
+        p.partial = scratch;
+        p.ws = ws;
+        spec_status st = launch_umma<0, 8>(ta, tb, dim3((d + kBM - 1) / kBM, splits), p, s, "draft_mlp_tc");
+        if (st != SPEC_OK) return st;
+        const size_t total = static_cast<size_t>(rows) * d;
+        SPEC_CUDA_TRY(launch("draft_mlp_finish", k_mlp_finish, dim3(static_cast<unsigned>((total + 255) / 256)), dim3(256),
+                             0, s, scratch, splits, n_pad, rows, g0, d, b1, h, cond, n_int, z));
+    }
+    // ---- projection with the top-k epilogue
+    for (int g0 = 0; g0 < R; g0 += kMaxN) {
+        const int rows = std::min(kMaxN, R - g0);
+        const int n_pad = n_pad_of(rows);
+        CUtensorMap ta, tb;
+        SPEC_CUDA_TRY(make_tmap_bf16_2d(&ta, W2, V, d, d, kBM));
+        SPEC_CUDA_TRY(make_tmap_bf16_2d(&tb, z + static_cast<size_t>(g0) * d, rows, d, d, n_pad));
+        UmmaParams p{};
+        p.M = V;
+        p.total_iters = (d + kBK - 1) / kBK;
+        p.k_iters = p.total_iters;
+        p.n_pad = n_pad;
+        p.n_valid = rows;
+        p.stages = stages_of(n_pad);
+        p.tmem_cols = tmem_cols_of(n_pad);
+        p.topk = k;
+        p.V = V;
+        p.nslices = plan.nslices;
+        p.row0 = g0;
+        p.part_c = pc;
+        p.part_l = pl;
+        p.kmax = kmax;
+        p.ws = ws;
+        const dim3 grid(plan.nslices, 1);
+        spec_status st = kmax == 8 ? launch_umma<1, 8>(ta, tb, grid, p, s, "draft_proj_tc")
+                                   : launch_umma<1, 16>(ta, tb, grid, p, s, "draft_proj_tc");
+        if (st != SPEC_OK) return st;
+    }
+    return SPEC_OK;
 }
 
 }  // namespace tc

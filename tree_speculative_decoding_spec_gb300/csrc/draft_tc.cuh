@@ -7,7 +7,11 @@
 
 namespace spec {
 namespace draft {
-struct Cand;
+// A top-k candidate (logit, token); "better" = larger logit, then lower token.
+struct Cand {
+    float v;
+    int i;
+};
 }
 namespace tc {
 
