@@ -78,6 +78,8 @@ static std::atomic<int64_t> g_launches{0};
 
 void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+bool trace_active() { return g_trace.on; }
+
 void trace_before(cudaStream_t s) {
     if (!g_trace.on || g_trace.used >= g_trace.capacity) return;
     cudaEventRecord(g_trace.ev[2 * g_trace.used], s);

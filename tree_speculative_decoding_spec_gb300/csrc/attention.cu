@@ -317,10 +317,16 @@ extern "C" spec_status tree_attention(const void* q, const void* k_cache, const 
     SPEC_CUDA_TRY(reset_device_status(ws, s));
     if (dt == SPEC_BF16) {
         using T = __nv_bfloat16;
-        if (p.tc)
-            return tc::attn_tc_run(p.tcp, static_cast<const T*>(q), static_cast<const T*>(k_cache),
-                                   static_cast<const T*>(v_cache), prefix_len, static_cast<const T*>(k_tree),
-                                   static_cast<const T*>(v_tree), tree, B, Hq, Hkv, Lmax, D, scale, out, lse, ws, s);
+        if (p.tc) {
+            float* part = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kWsHeader);
+            st = tc::attn_tc_run(p.tcp, static_cast<const T*>(q), static_cast<const T*>(k_cache),
+                                 static_cast<const T*>(v_cache), prefix_len, static_cast<const T*>(k_tree),
+                                 static_cast<const T*>(v_tree), tree, B, Hq, Hkv, Lmax, scale, part, ws, s);
+            if (st != SPEC_OK) return st;
+            SPEC_CUDA_TRY(launch("attn_combine", attn::k_attn_combine, dim3(B * Hq * tree->T), dim3(D), 0, s, part,
+                                 prefix_len, tree->T, Hq, D, Lmax, p.tcp.chunk, p.tcp.n_pre, out, lse));
+            return SPEC_OK;
+        }
         return attn::run_fma<T>(static_cast<const T*>(q), static_cast<const T*>(k_cache), static_cast<const T*>(v_cache),
                                 prefix_len, static_cast<const T*>(k_tree), static_cast<const T*>(v_tree), tree, B, Hq,
                                 Hkv, Lmax, D, scale, out, lse, ws, p, s);

@@ -1,17 +1,386 @@
 // Tensor-core (tcgen05) path of tree attention.
+//
+// Hydra Guide, "Tree Attention Matrix with Topology-Aware Causal Masking":
+// every tree node sees the cached prefix and its own ancestors; the ancestor
+// sets arrive as one bit row per node and are applied to the scores in
+// registers.
+//
+// One CTA = one (key split, KV head x 128-query-row block, sequence).  The
+// query rows of a KV head are its g query heads x T nodes, which are
+// contiguous in q [B, Hq, T, D], so one 2-D TMA box fetches them.  Six warps:
+//   warp 4    TMA: the 128 x 128 Q tile once, then a 3-stage ring of
+//             64-key K and V tiles (128-byte swizzle)
+//   warp 5    MMA: S_j = Q K_j^T into one of two TMEM score buffers
+//             (M 128, N 64, K 128), and O += P_j V_j (M 128, N 128, K 64,
+//             V read as an MN-major operand) into the TMEM output
+//   warps 0-3 one thread per query row: read S_j from TMEM, mask (prefix
+//             length, ancestor bits), online softmax in base 2 with lazy
+//             rescaling (O in TMEM is rescaled only when the row maximum
+//             grows by more than 2^8), write bf16 P_j into a swizzled shared
+//             tile for the next MMA; at the end read O and write the split's
+//             (max, sum, O) partial.
+// Waits are bounded (2 s); on expiry SPEC_ETIMEOUT goes to the status word,
+// the CTA drains its own loads and frees TMEM.
+#include <algorithm>
+
 #include "attention_tc.cuh"
+#include "tc.cuh"
 
 namespace spec {
 namespace tc {
 
-bool attn_tc_supported(int, int) { return false; }
+constexpr int kARows = 128;        // query rows per CTA (MMA M)
+constexpr int kAKeys = 64;         // keys per tile
+constexpr int kAD = 128;           // head dim
+constexpr int kAStages = 3;
+constexpr int kAThreads = 192;
+constexpr int kQBytes = 2 * kARows * 128;         // two 64-column halves of 128 rows
+constexpr int kKVHalf = kAKeys * 128;             // one 64-column half of a 64-key tile
+constexpr int kStageBytes = 4 * kKVHalf;          // K and V, two halves each
+constexpr int kPBytes = kARows * 128;             // 128 rows x 64 bf16
+constexpr size_t kASmem = 1024 + kQBytes + kAStages * kStageBytes + 2 * kPBytes + 256;
+constexpr uint32_t kATmemCols = 256;              // S0 [0,64) S1 [64,128) O [128,256)
 
-AttnTcPlan attn_tc_plan(int, int, int, int, int, int, int) { return AttnTcPlan{}; }
+struct AttnTcParams {
+    int T, g, Hq, Hkv, Lmax, words;
+    int chunk, n_pre, n_rb;
+    float scale_log2;
+    const int32_t* prefix_len;
+    const uint64_t* anc;
+    float* part;
+    void* ws;
+};
 
-spec_status attn_tc_run(const AttnTcPlan&, const __nv_bfloat16*, const __nv_bfloat16*, const __nv_bfloat16*,
-                        const int32_t*, const __nv_bfloat16*, const __nv_bfloat16*, const spec_tree*, int, int, int,
-                        int, int, float, float*, float*, void*, cudaStream_t) {
-    return fail(SPEC_EUNSUPPORTED, "tensor-core attention path not built");
+__global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant__ CUtensorMap tmQ,
+                                                          const __grid_constant__ CUtensorMap tmKc,
+                                                          const __grid_constant__ CUtensorMap tmVc,
+                                                          const __grid_constant__ CUtensorMap tmKt,
+                                                          const __grid_constant__ CUtensorMap tmVt,
+                                                          const AttnTcParams p) {
+    const int c = blockIdx.x;
+    const int kvh = blockIdx.y / p.n_rb, rb = blockIdx.y % p.n_rb;
+    const int b = blockIdx.z;
+    const int L = min(max(p.prefix_len[b], 0), p.Lmax);
+    const bool tail = (c == p.n_pre);
+    const int k_begin = tail ? 0 : c * p.chunk;
+    const int k_end = tail ? p.T : min(L, k_begin + p.chunk);
+    if (k_begin >= k_end) return;   // whole CTA: nothing allocated yet
+    const int n_tiles = (k_end - k_begin + kAKeys - 1) / kAKeys;
+
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sQ = smem;
+    uint8_t* sKV = sQ + kQBytes;                       // stage s: K half0, K half1, V half0, V half1
+    uint8_t* sP = sKV + kAStages * kStageBytes;        // two P buffers
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kPBytes);
+    uint64_t* q_full = bars;
+    uint64_t* kv_full = bars + 1;
+    uint64_t* kv_empty = kv_full + kAStages;
+    uint64_t* s_full = kv_empty + kAStages;
+    uint64_t* p_full = s_full + 2;
+    uint64_t* pv_done = p_full + 2;
+    uint64_t* o_final = pv_done + 2;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < kAStages; ++s) {
+            mbar_init(&kv_full[s], 1);
+            mbar_init(&kv_empty[s], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&s_full[i], 1);
+            mbar_init(&p_full[i], kARows);
+            mbar_init(&pv_done[i], 1);
+        }
+        mbar_init(o_final, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(tail ? &tmKt : &tmKc);
+        prefetch_tmap(tail ? &tmVt : &tmVc);
+    }
+    if (warp == 0) tmem_alloc(tmem_slot, kATmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const CUtensorMap* tmK = tail ? &tmKt : &tmKc;
+    const CUtensorMap* tmV = tail ? &tmVt : &tmVc;
+    const int kv_row0 = tail ? (b * p.Hkv + kvh) * p.T : (b * p.Hkv + kvh) * p.Lmax;
+    const int q_row0 = (b * p.Hq + kvh * p.g) * p.T + rb * kARows;
+    int issued = 0;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            mbar_arrive_expect_tx(q_full, kQBytes);
+            tma_load_2d(sQ, &tmQ, q_full, 0, q_row0);
+            tma_load_2d(sQ + kARows * 128, &tmQ, q_full, 64, q_row0);
+            for (int j = 0; j < n_tiles; ++j) {
+                const int s = j % kAStages;
+                if (j >= kAStages && !mbar_wait_or_abort(&kv_empty[s], ((j / kAStages) - 1) & 1, abort_flag)) {
+                    flag_status(p.ws, SPEC_ETIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                uint8_t* st = sKV + s * kStageBytes;
+                const int row = kv_row0 + k_begin + j * kAKeys;
+                mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
+                tma_load_2d(st, tmK, &kv_full[s], 0, row);
+                tma_load_2d(st + kKVHalf, tmK, &kv_full[s], 64, row);
+                tma_load_2d(st + 2 * kKVHalf, tmV, &kv_full[s], 0, row);
+                tma_load_2d(st + 3 * kKVHalf, tmV, &kv_full[s], 64, row);
+                issued = j + 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        if (lane == 0) {
+            const uint32_t idesc_s = idesc_bf16_f32(kARows, kAKeys);
+            const uint32_t idesc_o = idesc_bf16_f32_bmn(kARows, kAD);
+            const uint32_t q0 = smem_u32(sQ);
+            bool ok = mbar_wait_or_abort(q_full, 0, abort_flag);
+            // S_j = Q K_j^T: K = 128 in 8 steps of 16 (two 64-column halves)
+            auto issue_s = [&](int j) -> bool {
+                const int s = j % kAStages;
+                if (!mbar_wait_or_abort(&kv_full[s], (j / kAStages) & 1, abort_flag)) return false;
+                tc_fence_after();
+                const uint32_t k0 = smem_u32(sKV + s * kStageBytes);
+                const uint32_t dst = tmem + (j & 1) * kAKeys;
+#pragma unroll
+                for (int ks = 0; ks < kAD / 16; ++ks) {
+                    const uint32_t off = (ks & 3) * 32;
+                    mma_bf16(dst, sdesc_k128(q0 + (ks >> 2) * (kARows * 128) + off),
+                             sdesc_k128(k0 + (ks >> 2) * kKVHalf + off), idesc_s, ks > 0 ? 1u : 0u);
+                }
+                mma_commit(&s_full[j & 1]);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int j = 0; ok && j < n_tiles; ++j) {
+                if (j + 1 < n_tiles && !issue_s(j + 1)) { ok = false; break; }
+                if (!mbar_wait_or_abort(&p_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+                tc_fence_after();
+                // O += P_j V_j: K = 64 keys in 4 steps of 16; V is MN-major (d contiguous):
+                // 64-wide d halves 8 KB apart, 8-key atoms 1 KB apart
+                const uint32_t pa = smem_u32(sP + (j & 1) * kPBytes);
+                const uint32_t v0 = smem_u32(sKV + (j % kAStages) * kStageBytes + 2 * kKVHalf);
+#pragma unroll
+                for (int ks = 0; ks < kAKeys / 16; ++ks)
+                    mma_bf16(tmem + 2 * kAKeys, sdesc_k128(pa + ks * 32), sdesc_mn128(v0 + ks * 2048, kKVHalf, 1024),
+                             idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+                mma_commit(&pv_done[j & 1]);
+                mma_commit(&kv_empty[j % kAStages]);
+            }
+            if (!ok) {
+                flag_status(p.ws, SPEC_ETIMEOUT);
+                *abort_flag = 1;
+            }
+            mma_commit(o_final);
+        }
+        __syncwarp();
+    } else {
+        const int r = threadIdx.x;                        // query row of this block = TMEM lane
+        const int rg = rb * kARows + r;                   // row within the KV head's g*T rows
+        const int node = rg % p.T;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+        const uint32_t o_col = 2 * kAKeys;
+        const uint64_t* anc_row = p.anc + static_cast<size_t>(node) * p.words;
+        float m_used = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&s_full[j & 1], (j >> 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+            uint32_t sa[32], sb[32];
+            tmem_ld32(lane_base + (j & 1) * kAKeys, sa);
+            tmem_ld32(lane_base + (j & 1) * kAKeys + 32, sb);
+            tmem_ld_wait();
+            const int key0 = k_begin + j * kAKeys;
+            const int nvalid = min(kAKeys, k_end - key0);
+            uint64_t bits = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+            if (tail) bits &= anc_row[key0 >> 6];
+            float sv[64];
+            float tmax = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+                sv[e] = ((bits >> e) & 1ull) ? __uint_as_float(sa[e]) * p.scale_log2 : -INFINITY;
+                sv[32 + e] = ((bits >> (32 + e)) & 1ull) ? __uint_as_float(sb[e]) * p.scale_log2 : -INFINITY;
+                tmax = fmaxf(tmax, fmaxf(sv[e], sv[32 + e]));
+            }
+            // lazy rescale: keep the old reference maximum unless the row max grew by > 2^8
+            float m_new = m_used, alpha = 1.f;
+            bool rescale = false;
+            if (tmax > m_used + 8.f) {
+                if (m_used != -INFINITY) {
+                    rescale = true;
+                    alpha = exp2f(m_used - tmax);
+                }
+                m_new = tmax;
+            }
+            if (j >= 1) {   // O and this P buffer are stable once PV_{j-1} is done
+                ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag));
+                if (!ok) break;
+                tc_fence_after();
+            }
+            if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                for (int cc = 0; cc < kAD / 32; ++cc) {
+                    uint32_t o[32];
+                    tmem_ld32(lane_base + o_col + cc * 32, o);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st32(lane_base + o_col + cc * 32, o);
+                }
+                tmem_st_wait();
+                l *= alpha;
+            }
+            m_used = m_new;
+            // P = 2^(s - m_used) in bf16, 128-byte swizzled row (16-byte chunk q at q ^ (r % 8));
+            // the row sum uses the rounded values the MMA will see
+            uint8_t* prow = sP + (j & 1) * kPBytes + r * 128;
+            float psum = 0.f;
+#pragma unroll
+            for (int qc = 0; qc < 8; ++qc) {
+                uint32_t packed[4];
+#pragma unroll
+                for (int h2 = 0; h2 < 4; ++h2) {
+                    const int e0 = qc * 8 + 2 * h2;
+                    const float a0 = m_used == -INFINITY ? 0.f : exp2f(sv[e0] - m_used);
+                    const float a1 = m_used == -INFINITY ? 0.f : exp2f(sv[e0 + 1] - m_used);
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(a0, a1);
+                    psum += __low2float(pr) + __high2float(pr);
+                    packed[h2] = *reinterpret_cast<const uint32_t*>(&pr);
+                }
+                *reinterpret_cast<uint4*>(prow + ((qc ^ (r & 7)) * 16)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+            }
+            l += psum;
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&p_full[j & 1]);
+        }
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait_or_abort(o_final, 0, abort_flag));
+        if (!ok) {
+            flag_status(p.ws, SPEC_ETIMEOUT);
+            *abort_flag = 1;
+        } else {
+            tc_fence_after();
+            const bool valid = rg < p.T * p.g;
+            float* dst = nullptr;
+            if (valid) {
+                const int hl = rg / p.T, i = rg % p.T;
+                const size_t row = (static_cast<size_t>(b) * p.Hq + kvh * p.g + hl) * p.T + i;
+                dst = p.part + (row * (p.n_pre + 1) + c) * (kAD + 4);
+                dst[0] = m_used;
+                dst[1] = l;
+            }
+#pragma unroll 1
+            for (int cc = 0; cc < kAD / 32; ++cc) {
+                uint32_t o[32];
+                tmem_ld32(lane_base + o_col + cc * 32, o);
+                tmem_ld_wait();
+                if (valid) {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        *reinterpret_cast<float4*>(dst + 4 + cc * 32 + 4 * e) =
+                            make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
+                                        __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (*abort_flag) {
+        // a wait ran out: let this CTA's own loads and MMAs land before releasing memory
+        if (warp == 4 && lane == 0) {
+            for (int j = max(0, issued - kAStages); j < issued; ++j)
+                mbar_wait(&kv_full[j % kAStages], (j / kAStages) & 1, 100000000ull);
+            mbar_wait(q_full, 0, 100000000ull);
+        }
+        if (warp == 5 && lane == 0) mbar_wait(o_final, 0, 100000000ull);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kATmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host
+
+bool attn_tc_supported(int rows_per_kv_head, int D) {
+    if (D != kAD || rows_per_kv_head < 64) return false;
+    CUtensorMap probe;
+    alignas(256) static const uint16_t dummy[kAD * 64] = {};
+    // tensor-map encoding must be available (driver entry point); the probe map is never used
+    return make_tmap_bf16_2d(&probe, dummy, 64, kAD, kAD, 64) == cudaSuccess;
+}
+
+// Splits of the prefix: one CTA per (split, KV head x row block, sequence) plus one
+// tree-key split each.  Pick the split count that minimises an estimated
+// makespan (waves of one CTA per SM x tiles per CTA, with ~2 tiles of fixed cost
+// per CTA); ties go to fewer splits (less combine traffic).
+AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_count) {
+    AttnTcPlan p;
+    const int g = Hq / Hkv;
+    p.n_rb = (T * g + kARows - 1) / kARows;
+    const int64_t base = static_cast<int64_t>(B) * Hkv * p.n_rb;
+    const int tiles = (Lmax + kAKeys - 1) / kAKeys;
+    const int tail_tiles = (T + kAKeys - 1) / kAKeys;
+    int64_t best_cost = INT64_MAX;
+    int best = 1;
+    for (int n = 1; n <= std::min(tiles, 64); ++n) {
+        const int per = (tiles + n - 1) / n;
+        const int64_t ctas = base * n;
+        const int64_t waves = (ctas + sm_count - 1) / sm_count;
+        const int64_t tail_waves = (base + sm_count - 1) / sm_count;
+        const int64_t cost = waves * (per + 2) + tail_waves * (tail_tiles + 2);
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = n;
+        }
+    }
+    p.chunk = static_cast<int>(round_up((Lmax + best - 1) / best, kAKeys));
+    p.n_pre = (Lmax + p.chunk - 1) / p.chunk;
+    p.part_bytes = sizeof(float) * static_cast<size_t>(B) * Hq * T * (p.n_pre + 1) * (D + 4);
+    return p;
+}
+
+spec_status attn_tc_run(const AttnTcPlan& pl, const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
+                        const int32_t* prefix_len, const __nv_bfloat16* kt, const __nv_bfloat16* vt,
+                        const spec_tree* tree, int B, int Hq, int Hkv, int Lmax, float scale, float* part, void* ws,
+                        cudaStream_t s) {
+    const int T = tree->T;
+    CUtensorMap tq, tkc, tvc, tkt, tvt;
+    SPEC_CUDA_TRY(make_tmap_bf16_2d(&tq, q, static_cast<uint64_t>(B) * Hq * T, kAD, kAD, kARows));
+    SPEC_CUDA_TRY(make_tmap_bf16_2d(&tkc, kc, static_cast<uint64_t>(B) * Hkv * Lmax, kAD, kAD, kAKeys));
+    SPEC_CUDA_TRY(make_tmap_bf16_2d(&tvc, vc, static_cast<uint64_t>(B) * Hkv * Lmax, kAD, kAD, kAKeys));
+    SPEC_CUDA_TRY(make_tmap_bf16_2d(&tkt, kt, static_cast<uint64_t>(B) * Hkv * T, kAD, kAD, kAKeys));
+    SPEC_CUDA_TRY(make_tmap_bf16_2d(&tvt, vt, static_cast<uint64_t>(B) * Hkv * T, kAD, kAD, kAKeys));
+    AttnTcParams p{};
+    p.T = T;
+    p.g = Hq / Hkv;
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.Lmax = Lmax;
+    p.words = tree->words;
+    p.chunk = pl.chunk;
+    p.n_pre = pl.n_pre;
+    p.n_rb = pl.n_rb;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.prefix_len = prefix_len;
+    p.anc = tree->anc;
+    p.part = part;
+    p.ws = ws;
+    SPEC_CUDA_TRY(cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem));
+    SPEC_CUDA_TRY(launch("attn_tc", k_attn_tc, dim3(pl.n_pre + 1, Hkv * pl.n_rb, B), dim3(kAThreads), kASmem, s, tq, tkc,
+                         tvc, tkt, tvt, p));
+    return SPEC_OK;
 }
 
 }  // namespace tc

@@ -1,4 +1,4 @@
-// Tensor-core (tcgen05) path of tree attention, bf16 inputs.
+// Tensor-core (tcgen05) path of tree attention, bf16 inputs, head dim 128.
 #pragma once
 
 #include <cuda_bf16.h>
@@ -9,15 +9,23 @@ namespace spec {
 namespace tc {
 
 struct AttnTcPlan {
+    int n_rb = 0;       // 128-row query blocks per KV head
+    int chunk = 0;      // prefix keys per split (multiple of 64)
+    int n_pre = 0;      // prefix splits; split n_pre holds the tree keys
     size_t part_bytes = 0;
 };
 
+// Used when there are at least 64 query rows per KV head (tree nodes x query
+// heads per KV head) and the head dimension is 128.
 bool attn_tc_supported(int rows_per_kv_head, int D);
 AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_count);
+
+// Queue the split-KV kernel; it writes per-(row, split) partials in the layout
+// the combine kernel of attention.cu reads ([B*Hq*T][n_pre+1][D+4] floats).
 spec_status attn_tc_run(const AttnTcPlan& p, const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
                         const int32_t* prefix_len, const __nv_bfloat16* kt, const __nv_bfloat16* vt,
-                        const spec_tree* tree, int B, int Hq, int Hkv, int Lmax, int D, float scale, float* out,
-                        float* lse, void* ws, cudaStream_t s);
+                        const spec_tree* tree, int B, int Hq, int Hkv, int Lmax, float scale, float* part, void* ws,
+                        cudaStream_t s);
 
 }  // namespace tc
 }  // namespace spec

@@ -56,6 +56,33 @@ inline cudaError_t launch(const char* name, void (*kernel)(KArgs...), dim3 grid,
     return e;
 }
 
+bool trace_active();
+
+// Launch with cudaLaunchKernelEx; `pdl` allows programmatic dependent launch
+// (the kernel may start while the previous kernel on the stream drains; it must
+// call griddep_wait() before touching that kernel's results).  Tracing turns
+// the overlap off so each kernel's events bracket it alone.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_ex(const char* name, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    const bool use_pdl = pdl && !trace_active();
+    cfg.attrs = use_pdl ? attr : nullptr;
+    cfg.numAttrs = use_pdl ? 1 : 0;
+    trace_before(s);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    trace_after(s, name);
+    count_launch();
+    return e;
+}
+
 #define SPEC_CUDA_TRY(expr)                                                              \
     do {                                                                                 \
         cudaError_t _e = (expr);                                                         \
@@ -96,6 +123,11 @@ __device__ __forceinline__ float warp_sum(float v) {
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
+
+// Programmatic dependent launch: wait for the preceding kernel's results /
+// allow the next kernel to start launching.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // Record a device-detected failure in a workspace's status word (largest code wins).
 __device__ __forceinline__ void flag_status(void* ws, int code) { atomicMax(static_cast<int*>(ws), code); }

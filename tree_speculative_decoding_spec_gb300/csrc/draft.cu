@@ -6,17 +6,19 @@
 // Construction": later heads also read the base embedding of the parent's
 // token, and every node's children are the top-k of the head run on it.
 //
-// One head (depth k+1):
-//   gather   u_in rows = [h_b || E[tok(u)]] (or h_b) for every parent row
-//   mlp      z = h_b + SiLU(W1 u_in + b1), rounded to the input dtype
-//   proj     logits = W2 z and, per row and vocabulary slice, the slice's
-//            top-k and (max, sum exp); the tensor-core path takes these
-//            straight from its accumulators (logits never reach memory), the
-//            CUDA-core path (fp32) stores the logits and scans them
-//   select   merge the partials of each row, write the children's tokens,
-//            logits and cumulative log-probabilities.
-// Rows are (sequence, parent node) pairs; a Medusa head (cond = 0) has one row
-// per sequence, shared by every parent of that depth.
+// Rows are (sequence, parent node) pairs of one depth; a Medusa head
+// (cond = 0) has one row per sequence, shared by every parent of that depth.
+// One head (filling depth k+1) on the bf16 path is three launches:
+//   mlp      z = h + SiLU(W1 u_in + b1) (tcgen05, split over K; the last split
+//            of each weight tile adds bias, SiLU and the residual, rounds to bf16)
+//   proj     logits = W2 z (tcgen05); per row and 128-token slice, the slice's
+//            top-k and (max, sum exp) straight from TMEM (logits never reach HBM)
+//   select   merge the slices of each row, write the children's tokens, logits
+//            and cumulative log-probabilities, and the next depth's input rows
+//            u_in = [h_b || E[tok(child)]]
+// and the launches are chained with programmatic dependent launch, so each
+// kernel's weight loads start while the previous kernel drains.  The fp32 path
+// (CUDA cores) stores logits and scans them per slice instead of `proj`.
 #include <algorithm>
 #include <type_traits>
 
@@ -25,27 +27,6 @@
 
 namespace spec {
 namespace draft {
-
-// ---------------------------------------------------------------- gather
-
-template <typename T>
-__global__ void k_gather(const T* __restrict__ h, const T* __restrict__ emb, const int32_t* __restrict__ node_tok,
-                         const int32_t* __restrict__ internal, int int_off, int n_int, int Tn, int d, int cond,
-                         int R, int d_in_pad, T* __restrict__ xin) {
-    const int r = blockIdx.x;
-    if (r >= R) return;
-    const int b = cond ? r / n_int : r;
-    const int u = cond ? internal[int_off + r % n_int] : 0;
-    const int vec = 16 / sizeof(T);
-    const uint4* hs = reinterpret_cast<const uint4*>(h + static_cast<size_t>(b) * d);
-    uint4* dst = reinterpret_cast<uint4*>(xin + static_cast<size_t>(r) * d_in_pad);
-    for (int i = threadIdx.x; i < d / vec; i += blockDim.x) dst[i] = hs[i];
-    if (cond) {
-        const int tok = node_tok[static_cast<size_t>(b) * Tn + u];
-        const uint4* es = reinterpret_cast<const uint4*>(emb + static_cast<size_t>(tok) * d);
-        for (int i = threadIdx.x; i < d / vec; i += blockDim.x) dst[d / vec + i] = es[i];
-    }
-}
 
 // ---------------------------------------------------------------- CUDA-core GEMM (fp32 path, small shapes)
 //
@@ -189,101 +170,175 @@ __global__ void __launch_bounds__(256) k_topk_slices(const float* __restrict__ l
     }
 }
 
+
 // ---------------------------------------------------------------- select: merge slices, fill children
 
-template <int KMAX>
+// Copy the next depth's input row [h_b || E[tok]] (2d elements) with the whole CTA.
+template <typename T>
+__device__ __forceinline__ void write_next_row(T* __restrict__ dst, const T* __restrict__ hb, const T* __restrict__ er,
+                                               int d) {
+    const int vec = 16 / sizeof(T);
+    const uint4* hs = reinterpret_cast<const uint4*>(hb);
+    const uint4* es = reinterpret_cast<const uint4*>(er);
+    uint4* o = reinterpret_cast<uint4*>(dst);
+    for (int i = threadIdx.x; i < d / vec; i += blockDim.x) {
+        o[i] = hs[i];
+        o[d / vec + i] = es[i];
+    }
+}
+
+// One CTA per row: top-k over the row's sorted per-slice candidate lists and
+// the row's log-sum-exp, then the children of the row's parent node(s).
+// Tournament: each thread folds its slices into one sorted list (shared
+// memory), each warp merges its 32 lists by k rounds of shuffles, warp 0
+// merges the 8 warp lists.
+template <int KMAX, typename T>
 __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c, const float2* __restrict__ part_l,
                                                 int nslices, int k, int cond, int n_int, int int_off,
                                                 const int32_t* __restrict__ internal, const int32_t* __restrict__ child_off,
                                                 const int32_t* __restrict__ child_idx, const int32_t* __restrict__ rank,
-                                                int Tn, int V, int32_t* __restrict__ node_tok, float* __restrict__ node_logit,
-                                                float* __restrict__ node_logprob, void* ws) {
+                                                const int32_t* __restrict__ row_of, int Tn, int V,
+                                                int32_t* __restrict__ node_tok, float* __restrict__ node_logit,
+                                                float* __restrict__ node_logprob, void* ws, int next_n_int,
+                                                const T* __restrict__ h, const T* __restrict__ emb, int d,
+                                                T* __restrict__ xin) {
+    griddep_wait();
     const int r = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ Cand lists[256][KMAX];
+    __shared__ Cand wl[8][KMAX];
     __shared__ float topv[KMAX];
     __shared__ int topi[KMAX];
+    __shared__ float2 wlse[8];
     __shared__ float lse_s;
-    // (max, sum) over slices
-    {
-        float M = -INFINITY, S = 0.f;
-        for (int s = threadIdx.x; s < nslices; s += blockDim.x) {
-            const float2 p = part_l[static_cast<size_t>(r) * nslices + s];
-            lse_merge(M, S, p.x, p.y);
+
+    // 1. fold this thread's slices into one sorted list
+    float M = -INFINITY, S = 0.f;
+    int n = 0;
+    for (int s = tid; s < nslices; s += blockDim.x) {
+        const Cand* src = part_c + (static_cast<size_t>(r) * nslices + s) * KMAX;
+        if (n == 0) {
+            for (int e = 0; e < k; ++e) lists[tid][e] = src[e];
+            n = k;
+        } else {
+            for (int e = 0; e < k; ++e) {
+                const Cand c = src[e];
+                if (!better(c.v, c.i, lists[tid][k - 1].v, lists[tid][k - 1].i)) break;
+                int pos = k - 1;
+                while (pos > 0 && better(c.v, c.i, lists[tid][pos - 1].v, lists[tid][pos - 1].i)) {
+                    lists[tid][pos] = lists[tid][pos - 1];
+                    --pos;
+                }
+                lists[tid][pos] = c;
+            }
         }
-        __shared__ float2 red[256];
-        red[threadIdx.x] = make_float2(M, S);
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float MM = -INFINITY, SS = 0.f;
-            for (int t = 0; t < blockDim.x; ++t) lse_merge(MM, SS, red[t].x, red[t].y);
-            lse_s = MM + logf(SS);
-        }
+        const float2 p = part_l[static_cast<size_t>(r) * nslices + s];
+        lse_merge(M, S, p.x, p.y);
     }
-    // top-k over nslices sorted lists of length k: k rounds of a block arg-best over list heads
-    __shared__ int head[1024];
-    for (int s = threadIdx.x; s < nslices; s += blockDim.x) head[s] = 0;
-    __syncthreads();
+    if (n == 0)
+        for (int e = 0; e < k; ++e) lists[tid][e] = Cand{-INFINITY, 0x7fffffff};
+    for (int o = 16; o > 0; o >>= 1) lse_merge(M, S, __shfl_xor_sync(0xffffffffu, M, o), __shfl_xor_sync(0xffffffffu, S, o));
+    if (lane == 0) wlse[warp] = make_float2(M, S);
+    __syncwarp();
+
+    // 2. warp tournament over the warp's 32 lists
+    int head = 0;
     for (int round = 0; round < k; ++round) {
-        float v = -INFINITY;
-        int i = 0x7fffffff, who = -1;
-        for (int s = threadIdx.x; s < nslices; s += blockDim.x) {
-            const int hd = head[s];
-            if (hd >= k) continue;
-            const Cand c = part_c[(static_cast<size_t>(r) * nslices + s) * KMAX + hd];
-            if (who < 0 || better(c.v, c.i, v, i)) { v = c.v; i = c.i; who = s; }
-        }
+        const Cand mine = head < k ? lists[tid][head] : Cand{-INFINITY, 0x7fffffff};
+        float v = mine.v;
+        int i = mine.i, who = lane;
         for (int o = 16; o > 0; o >>= 1) {
             const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
             const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
             const int w2 = __shfl_xor_sync(0xffffffffu, who, o);
-            if (w2 >= 0 && (who < 0 || better(v2, i2, v, i))) { v = v2; i = i2; who = w2; }
+            if (better(v2, i2, v, i) || (v2 == v && i2 == i && w2 < who)) { v = v2; i = i2; who = w2; }
         }
-        __shared__ float bv[8];
-        __shared__ int bi[8], bw[8];
-        if ((threadIdx.x & 31) == 0) { bv[threadIdx.x >> 5] = v; bi[threadIdx.x >> 5] = i; bw[threadIdx.x >> 5] = who; }
-        __syncthreads();
-        if (threadIdx.x == 0) {
-            float vb = bv[0];
-            int ib = bi[0], wb = bw[0];
-            for (int w = 1; w < (int)(blockDim.x >> 5); ++w)
-                if (bw[w] >= 0 && (wb < 0 || better(bv[w], bi[w], vb, ib))) { vb = bv[w]; ib = bi[w]; wb = bw[w]; }
-            // fewer than k finite logits (NaN/inf weights) leave placeholders: keep tokens in range
-            if (ib < 0 || ib >= V) { flag_status(ws, SPEC_EINVAL); ib = 0; }
-            topv[round] = vb;
-            topi[round] = ib;
-            if (wb >= 0) head[wb] += 1;
-        }
-        __syncthreads();
+        if (lane == who) ++head;
+        if (lane == 0) wl[warp][round] = Cand{v, i};
     }
-    // children of this row's parent node(s)
+    __syncthreads();
+
+    // 3. warp 0 merges the 8 warp lists
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        int h8 = 0;
+        for (int round = 0; round < k; ++round) {
+            const Cand mine = (lane < nw && h8 < k) ? wl[lane][h8] : Cand{-INFINITY, 0x7fffffff};
+            float v = mine.v;
+            int i = mine.i, who = lane;
+            for (int o = 16; o > 0; o >>= 1) {
+                const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
+                const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+                const int w2 = __shfl_xor_sync(0xffffffffu, who, o);
+                if (better(v2, i2, v, i) || (v2 == v && i2 == i && w2 < who)) { v = v2; i = i2; who = w2; }
+            }
+            if (lane == who) ++h8;
+            if (lane == 0) {
+                // fewer than k finite logits (NaN/inf weights) leave placeholders: keep tokens in range
+                if (i < 0 || i >= V) { flag_status(ws, SPEC_EINVAL); i = 0; }
+                topv[round] = v;
+                topi[round] = i;
+            }
+        }
+        if (lane == 0) {
+            float MM = -INFINITY, SS = 0.f;
+            for (int w = 0; w < nw; ++w) lse_merge(MM, SS, wlse[w].x, wlse[w].y);
+            lse_s = MM + logf(SS);
+        }
+    }
+    __syncthreads();
+    griddep_launch();
+
+    // 4. children of this row's parent node(s); next depth's input rows
     const int b = cond ? r / n_int : r;
     const int j0 = cond ? r % n_int : 0, j1 = cond ? j0 + 1 : n_int;
     for (int j = j0; j < j1; ++j) {
         const int u = internal[int_off + j];
         const float base = node_logprob ? node_logprob[static_cast<size_t>(b) * Tn + u] : 0.f;
-        for (int a = child_off[u] + threadIdx.x; a < child_off[u + 1]; a += blockDim.x) {
+        for (int a = child_off[u] + tid; a < child_off[u + 1]; a += blockDim.x) {
             const int c = child_idx[a];
             const int rr = rank[c];
             node_tok[static_cast<size_t>(b) * Tn + c] = topi[rr];
             node_logit[static_cast<size_t>(b) * Tn + c] = topv[rr];
             if (node_logprob) node_logprob[static_cast<size_t>(b) * Tn + c] = base + (topv[rr] - lse_s);
         }
+        if (next_n_int > 0) {
+            for (int a = child_off[u]; a < child_off[u + 1]; ++a) {
+                const int c = child_idx[a];
+                const int ro = row_of[c];
+                if (ro < 0) continue;
+                const size_t row = static_cast<size_t>(b) * next_n_int + ro;
+                write_next_row(xin + row * 2 * d, h + static_cast<size_t>(b) * d,
+                               emb + static_cast<size_t>(topi[rank[c]]) * d, d);
+            }
+        }
     }
 }
 
 // Node 0 of every sequence: its token is the root token (clamped to the
-// vocabulary, with SPEC_EINVAL in the status word, so later reads stay in bounds).
+// vocabulary, with SPEC_EINVAL in the status word, so later reads stay in
+// bounds); writes head 0's input rows when head 0 is conditioned, and zeroes
+// the split-K tickets of the tensor-core MLP.  One CTA per sequence.
+template <typename T>
 __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn, int V, int32_t* __restrict__ node_tok,
-                            float* __restrict__ node_logit, float* __restrict__ node_logprob, void* ws) {
-    const int b = blockIdx.x * blockDim.x + threadIdx.x;
-    if (b >= B) return;
+                            float* __restrict__ node_logit, float* __restrict__ node_logprob, void* ws, int cond0,
+                            const T* __restrict__ h, const T* __restrict__ emb, int d, T* __restrict__ xin,
+                            int* __restrict__ tickets, int n_tickets) {
+    const int b = blockIdx.x;
     int tok = root_tok[b];
     if (tok < 0 || tok >= V) {
-        flag_status(ws, SPEC_EINVAL);
+        if (threadIdx.x == 0) flag_status(ws, SPEC_EINVAL);
         tok = min(max(tok, 0), V - 1);
     }
-    node_tok[static_cast<size_t>(b) * Tn] = tok;
-    node_logit[static_cast<size_t>(b) * Tn] = 0.f;
-    if (node_logprob) node_logprob[static_cast<size_t>(b) * Tn] = 0.f;
+    if (threadIdx.x == 0) {
+        node_tok[static_cast<size_t>(b) * Tn] = tok;
+        node_logit[static_cast<size_t>(b) * Tn] = 0.f;
+        if (node_logprob) node_logprob[static_cast<size_t>(b) * Tn] = 0.f;
+    }
+    if (b == 0)
+        for (int i = threadIdx.x; i < n_tickets; i += blockDim.x) tickets[i] = 0;
+    if (cond0) write_next_row(xin + static_cast<size_t>(b) * 2 * d, h + static_cast<size_t>(b) * d,
+                              emb + static_cast<size_t>(tok) * d, d);
 }
 
 // ---------------------------------------------------------------- planning
@@ -291,11 +346,11 @@ __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn,
 struct Plan {
     int K;
     int max_rows;        // largest row count over heads
-    int d_in_max;        // largest u_in width
-    int kmax;            // largest top-k
-    int nslices_fma;     // vocab slices for the fp32 path
-    int slice_fma;
-    size_t off_xin, off_z, off_logits, off_pc, off_pl, total;
+    int kmax;            // list length of the top-k partials (8 or 16)
+    int nslices;         // vocabulary slices per row
+    int slice_fma;       // fp32 path: tokens per slice
+    size_t off_xin, off_z, off_scratch, off_pc, off_pl, off_tickets, total;
+    int n_tickets;
     bool tc;             // bf16 tensor-core path
     tc::DraftTcPlan tcp;
 };
@@ -307,10 +362,11 @@ inline int rows_of(const spec_tree* t, int k, int cond, int B) {
 Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* cond, const int32_t* topk, spec_dtype dt) {
     Plan p{};
     p.K = K;
+    int max_cond_rows = 0;
     for (int k = 0; k < K; ++k) {
         if (t->n_internal_at_depth[k] == 0) continue;
         p.max_rows = std::max(p.max_rows, rows_of(t, k, cond[k], B));
-        p.d_in_max = std::max(p.d_in_max, d * (cond[k] ? 2 : 1));
+        if (cond[k]) max_cond_rows = std::max(max_cond_rows, rows_of(t, k, 1, B));
         p.kmax = std::max(p.kmax, topk[k]);
     }
     p.kmax = p.kmax <= 8 ? 8 : 16;
@@ -319,21 +375,26 @@ Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* co
     auto take = [&](size_t bytes) { size_t at = off; off = round_up(off + bytes, 256); return at; };
     const size_t es = dt == SPEC_BF16 ? 2 : 4;
     if (p.tc) {
-        p.tcp = tc::draft_tc_plan(p.max_rows, d, p.d_in_max, V, p.kmax);
-        p.off_xin = take(es * static_cast<size_t>(p.tcp.rows_pad) * p.d_in_max);
+        p.tcp = tc::draft_tc_plan(p.max_rows, d, V);
+        p.nslices = p.tcp.nslices;
+        p.off_xin = take(es * static_cast<size_t>(std::max(max_cond_rows, 1)) * 2 * d);
         p.off_z = take(es * static_cast<size_t>(p.tcp.rows_pad) * d);
-        p.off_logits = take(p.tcp.mlp_partial_bytes);
-        p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.tcp.rows_pad) * p.tcp.nslices * p.kmax);
-        p.off_pl = take(sizeof(float2) * static_cast<size_t>(p.tcp.rows_pad) * p.tcp.nslices);
+        p.off_scratch = take(p.tcp.mlp_partial_bytes);
+        p.n_tickets = p.tcp.n_tickets;
+        p.off_tickets = take(sizeof(int) * static_cast<size_t>(p.n_tickets));
+        p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.max_rows) * p.nslices * p.kmax);
+        p.off_pl = take(sizeof(float2) * static_cast<size_t>(p.max_rows) * p.nslices);
     } else {
-        // at most 1024 slices per row (the select kernel keeps one list head per slice)
+        // at most 1024 slices per row
         p.slice_fma = std::max(4096, static_cast<int>(round_up((V + 1023) / 1024, 256)));
-        p.nslices_fma = (V + p.slice_fma - 1) / p.slice_fma;
-        p.off_xin = take(es * static_cast<size_t>(p.max_rows) * p.d_in_max);
+        p.nslices = (V + p.slice_fma - 1) / p.slice_fma;
+        p.off_xin = take(es * static_cast<size_t>(std::max(max_cond_rows, 1)) * 2 * d);
         p.off_z = take(es * static_cast<size_t>(p.max_rows) * d);
-        p.off_logits = take(sizeof(float) * static_cast<size_t>(p.max_rows) * V);
-        p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.max_rows) * p.nslices_fma * p.kmax);
-        p.off_pl = take(sizeof(float2) * static_cast<size_t>(p.max_rows) * p.nslices_fma);
+        p.off_scratch = take(sizeof(float) * static_cast<size_t>(p.max_rows) * V);
+        p.n_tickets = 0;
+        p.off_tickets = take(16);
+        p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.max_rows) * p.nslices * p.kmax);
+        p.off_pl = take(sizeof(float2) * static_cast<size_t>(p.max_rows) * p.nslices);
     }
     p.total = off;
     return p;
@@ -343,7 +404,7 @@ spec_status check_args(const spec_tree* t, int B, int d, int V, int K, const int
     spec_status st = check_tree(t);
     if (st != SPEC_OK) return st;
     if (dt != SPEC_F32 && dt != SPEC_BF16) return fail(SPEC_EINVAL, "dtype %d unknown", (int)dt);
-    if (B < 1 || B > (1 << 16)) return fail(SPEC_EINVAL, "B = %d out of range", B);
+    if (B < 1 || B > 65535) return fail(SPEC_EINVAL, "B = %d out of 1..65535", B);
     if (d < 8 || d > 16384 || d % 8) return fail(SPEC_EINVAL, "d = %d must be a multiple of 8 in 8..16384", d);
     if (V < 2 || V > (1 << 24)) return fail(SPEC_EINVAL, "V = %d out of 2..2^24", V);
     if (K < 1 || K > SPEC_MAX_DEPTH) return fail(SPEC_EINVAL, "K = %d out of 1..%d", K, SPEC_MAX_DEPTH);
@@ -355,9 +416,21 @@ spec_status check_args(const spec_tree* t, int B, int d, int V, int K, const int
             return fail(SPEC_EINVAL, "topk[%d] = %d out of 1..min(%d, V)", k, topk[k], SPEC_MAX_TOPK);
         if (k + 1 <= t->max_depth && t->max_rank_at_depth[k + 1] >= topk[k])
             return fail(SPEC_EINVAL, "a depth-%d node has rank %d >= topk[%d] = %d", k + 1, t->max_rank_at_depth[k + 1], k, topk[k]);
-        if (static_cast<int64_t>(rows_of(t, k, cond[k], B)) > (1 << 20))
-            return fail(SPEC_EINVAL, "head %d has too many rows", k);
+        if (static_cast<int64_t>(rows_of(t, k, cond[k], B)) > 65535)
+            return fail(SPEC_EINVAL, "head %d has %lld rows, more than 65535", k, (long long)rows_of(t, k, cond[k], B));
     }
+    return SPEC_OK;
+}
+
+template <int KMAX, typename T>
+spec_status launch_select(bool pdl, const Plan& p, const spec_tree* t, int R, int k, int topk, int cond, int n_int,
+                          int int_off, int next_n_int, int V, const Cand* pc, const float2* pl, int32_t* node_tok,
+                          float* node_logit, float* node_logprob, void* ws, const T* h, const T* emb, int d, T* xin,
+                          cudaStream_t s) {
+    SPEC_CUDA_TRY(launch_ex("draft_select", k_select<KMAX, T>, dim3(R), dim3(256), 0, s, pdl, pc, pl, p.nslices, topk, cond,
+                            n_int, int_off, t->internal, t->child_off, t->child_idx, t->rank, t->row_of, t->T, V,
+                            node_tok, node_logit, node_logprob, ws, next_n_int, h, emb, d, xin));
+    (void)k;
     return SPEC_OK;
 }
 
@@ -369,58 +442,57 @@ spec_status run(const T* h, const T* emb, int K, const void* const* W1, const vo
     unsigned char* w = static_cast<unsigned char*>(ws);
     T* xin = reinterpret_cast<T*>(w + p.off_xin);
     T* z = reinterpret_cast<T*>(w + p.off_z);
-    float* logits = reinterpret_cast<float*>(w + p.off_logits);
+    float* scratch = reinterpret_cast<float*>(w + p.off_scratch);
+    int* tickets = reinterpret_cast<int*>(w + p.off_tickets);
     Cand* pc = reinterpret_cast<Cand*>(w + p.off_pc);
     float2* pl = reinterpret_cast<float2*>(w + p.off_pl);
+    const bool first_cond = t->n_internal_at_depth[0] > 0 && cond[0];
     SPEC_CUDA_TRY(reset_device_status(ws, s));
-    SPEC_CUDA_TRY(launch("draft_init_root", k_init_root, dim3((B + 127) / 128), dim3(128), 0, s, root_tok, B, t->T, V,
-                         node_tok, node_logit, node_logprob, ws));
-    for (int k = 0; k < K; ++k) {
+    SPEC_CUDA_TRY(launch("draft_init_root", k_init_root<T>, dim3(B), dim3(128), 0, s, root_tok, B, t->T, V, node_tok,
+                         node_logit, node_logprob, ws, first_cond ? 1 : 0, h, emb, d, xin, tickets, p.n_tickets));
+    int int_off = 0;
+    for (int k = 0; k < K; int_off += t->n_internal_at_depth[k], ++k) {
         const int n_int = t->n_internal_at_depth[k];
         if (n_int == 0) continue;   // no node of depth k has children: nothing to draft at depth k+1
-        int int_off = 0;
-        for (int j = 0; j < k; ++j) int_off += t->n_internal_at_depth[j];
         const int R = rows_of(t, k, cond[k], B);
         const int d_in = d * (cond[k] ? 2 : 1);
+        const T* X = cond[k] ? xin : h;   // conditioned rows were written by the previous select (or init)
+        const int ldx = cond[k] ? 2 * d : d;
+        const int next_n_int = (k + 1 < K && k + 1 <= SPEC_MAX_DEPTH && t->n_internal_at_depth[k + 1] > 0 && cond[k + 1])
+                                   ? t->n_internal_at_depth[k + 1] : 0;
         const T* W1k = static_cast<const T*>(W1[k]);
         const T* b1k = b1 ? static_cast<const T*>(b1[k]) : nullptr;
         const T* W2k = static_cast<const T*>(W2[k]);
-        const int d_in_pad = p.tc ? p.d_in_max : d_in;
-        SPEC_CUDA_TRY(launch("draft_gather", k_gather<T>, dim3(R), dim3(128), 0, s, h, emb, node_tok, t->internal,
-                             int_off, n_int, t->T, d, cond[k], R, d_in_pad, xin));
         if constexpr (std::is_same<T, __nv_bfloat16>::value) {
             if (p.tc) {
-                spec_status st = tc::draft_head_tc(p.tcp, W1k, b1k, W2k, h, xin, d_in, d_in_pad, z, R, d, V, cond[k],
-                                                   n_int, topk[k], p.kmax, logits, pc, pl, ws, s);
+                spec_status st = tc::draft_head_tc(p.tcp, W1k, b1k, W2k, h, X, d_in, ldx, z, R, d, V, cond[k], n_int,
+                                                   topk[k], p.kmax, scratch, tickets, pc, pl, ws, s);
                 if (st != SPEC_OK) return st;
-                if (p.kmax == 8)
-                    SPEC_CUDA_TRY(launch("draft_select", k_select<8>, dim3(R), dim3(256), 0, s, pc, pl, p.tcp.nslices, topk[k],
-                                         cond[k], n_int, int_off, t->internal, t->child_off, t->child_idx, t->rank,
-                                         t->T, V, node_tok, node_logit, node_logprob, ws));
-                else
-                    SPEC_CUDA_TRY(launch("draft_select", k_select<16>, dim3(R), dim3(256), 0, s, pc, pl, p.tcp.nslices, topk[k],
-                                         cond[k], n_int, int_off, t->internal, t->child_off, t->child_idx, t->rank,
-                                         t->T, V, node_tok, node_logit, node_logprob, ws));
+                st = p.kmax == 8 ? launch_select<8, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
+                                                       pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, s)
+                                 : launch_select<16, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
+                                                        pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, s);
+                if (st != SPEC_OK) return st;
                 continue;
             }
         }
         SPEC_CUDA_TRY(launch("draft_mlp_fma", k_gemm_fma<T, 0>, dim3((d + GBM - 1) / GBM, (R + GBN - 1) / GBN), dim3(256), 0, s,
-                             W1k, xin, d, R, d_in, d_in_pad, b1k, h, cond[k], n_int, z, nullptr));
+                             W1k, X, d, R, d_in, ldx, b1k, h, cond[k], n_int, z, nullptr));
         SPEC_CUDA_TRY(launch("draft_proj_fma", k_gemm_fma<T, 1>, dim3((V + GBM - 1) / GBM, (R + GBN - 1) / GBN), dim3(256), 0, s,
-                             W2k, z, V, R, d, d, nullptr, nullptr, 0, 1, nullptr, logits));
+                             W2k, z, V, R, d, d, nullptr, nullptr, 0, 1, nullptr, scratch));
+        spec_status st;
         if (p.kmax == 8) {
-            SPEC_CUDA_TRY(launch("draft_topk_slices", k_topk_slices<8>, dim3(p.nslices_fma, R), dim3(256), 0, s, logits, V,
-                                 topk[k], p.slice_fma, pc, pl, p.nslices_fma));
-            SPEC_CUDA_TRY(launch("draft_select", k_select<8>, dim3(R), dim3(256), 0, s, pc, pl, p.nslices_fma, topk[k], cond[k],
-                                 n_int, int_off, t->internal, t->child_off, t->child_idx, t->rank, t->T, V, node_tok,
-                                 node_logit, node_logprob, ws));
+            SPEC_CUDA_TRY(launch("draft_topk_slices", k_topk_slices<8>, dim3(p.nslices, R), dim3(256), 0, s, scratch, V,
+                                 topk[k], p.slice_fma, pc, pl, p.nslices));
+            st = launch_select<8, T>(false, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V, pc, pl, node_tok,
+                                     node_logit, node_logprob, ws, h, emb, d, xin, s);
         } else {
-            SPEC_CUDA_TRY(launch("draft_topk_slices", k_topk_slices<16>, dim3(p.nslices_fma, R), dim3(256), 0, s, logits, V,
-                                 topk[k], p.slice_fma, pc, pl, p.nslices_fma));
-            SPEC_CUDA_TRY(launch("draft_select", k_select<16>, dim3(R), dim3(256), 0, s, pc, pl, p.nslices_fma, topk[k], cond[k],
-                                 n_int, int_off, t->internal, t->child_off, t->child_idx, t->rank, t->T, V, node_tok,
-                                 node_logit, node_logprob, ws));
+            SPEC_CUDA_TRY(launch("draft_topk_slices", k_topk_slices<16>, dim3(p.nslices, R), dim3(256), 0, s, scratch, V,
+                                 topk[k], p.slice_fma, pc, pl, p.nslices));
+            st = launch_select<16, T>(false, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V, pc, pl, node_tok,
+                                      node_logit, node_logprob, ws, h, emb, d, xin, s);
         }
+        if (st != SPEC_OK) return st;
     }
     return SPEC_OK;
 }

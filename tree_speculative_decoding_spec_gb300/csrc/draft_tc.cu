@@ -13,8 +13,9 @@
 // workspace status word, drains its own loads and frees TMEM.
 //
 // Epilogues:
-//   MLP (W1, split over K): fp32 partial sums per split, reduced by
-//       k_mlp_finish with bias, SiLU, the residual h and bf16 rounding.
+//   MLP (W1, split over K): fp32 partial sums per split; the last split to
+//       finish a weight tile (atomic ticket) sums them and applies bias, SiLU,
+//       the residual h and bf16 rounding.
 //   projection (W2): per activation row, the top-k (value desc, token asc)
 //       and (max, sum exp) of the tile's 128 logits; logits never reach HBM.
 #include <mutex>
@@ -50,6 +51,13 @@ struct UmmaParams {
     float2* part_l;
     int kmax;
     void* ws;           // status word
+    // MLP finish (last split of each weight tile): z = h + SiLU(sum + b1)
+    int* tickets;       // [weight tiles], zero on entry, reset by the last split
+    const __nv_bfloat16* bias;
+    const __nv_bfloat16* h;
+    __nv_bfloat16* z;
+    int cond;
+    int n_int;
 };
 
 __device__ __forceinline__ bool cbetter(float va, int ia, float vb, int ib) {
@@ -109,46 +117,67 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
+    // The next kernel on the stream may start launching now: it only reads its
+    // own weights until its griddep_wait().
+    griddep_launch();
+
     int issued = 0;   // producer: stages loaded
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < n_it; ++i) {
-            const int s = i % p.stages;
-            if (i >= p.stages && !mbar_wait(&empty[s], ((i / p.stages) - 1) & 1)) {
-                flag_status(p.ws, SPEC_ETIMEOUT);
-                *abort_flag = 1;
-                break;
+    if (warp == 0) {
+        if (lane == 0) {
+            // Weight tiles do not depend on the previous kernel: fill the ring first,
+            // then wait for the previous kernel's results before loading activations.
+            const int pre = min(n_it, p.stages);
+            for (int i = 0; i < pre; ++i) {
+                mbar_arrive_expect_tx(&full[i], kStageA + stage_b);
+                tma_load_2d(sA + i * kStageA, &tmA, &full[i], (it0 + i) * kBK, m0);
             }
-            if (*abort_flag) break;
-            mbar_arrive_expect_tx(&full[s], kStageA + stage_b);
-            const int kx = (it0 + i) * kBK;
-            tma_load_2d(sA + s * kStageA, &tmA, &full[s], kx, m0);
-            tma_load_2d(sB + s * stage_b, &tmB, &full[s], kx, 0);
-            issued = i + 1;
+            griddep_wait();
+            for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * stage_b, &tmB, &full[i], (it0 + i) * kBK, 0);
+            issued = pre;
+            for (int i = pre; i < n_it; ++i) {
+                const int s = i % p.stages;
+                if (!mbar_wait(&empty[s], ((i / p.stages) - 1) & 1)) {
+                    flag_status(p.ws, SPEC_ETIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                if (*abort_flag) break;
+                mbar_arrive_expect_tx(&full[s], kStageA + stage_b);
+                const int kx = (it0 + i) * kBK;
+                tma_load_2d(sA + s * kStageA, &tmA, &full[s], kx, m0);
+                tma_load_2d(sB + s * stage_b, &tmB, &full[s], kx, 0);
+                issued = i + 1;
+            }
         }
-    } else if (threadIdx.x == 32) {
-        const uint32_t idesc = idesc_bf16_f32(kBM, p.n_pad);
-        for (int i = 0; i < n_it; ++i) {
-            const int s = i % p.stages;
-            if (!mbar_wait(&full[s], (i / p.stages) & 1)) {
-                flag_status(p.ws, SPEC_ETIMEOUT);
-                *abort_flag = 1;
-                break;
-            }
-            tc_fence_after();
-            const uint32_t a0 = smem_u32(sA + s * kStageA), b0 = smem_u32(sB + s * stage_b);
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t idesc = idesc_bf16_f32(kBM, p.n_pad);
+            for (int i = 0; i < n_it; ++i) {
+                const int s = i % p.stages;
+                if (!mbar_wait(&full[s], (i / p.stages) & 1)) {
+                    flag_status(p.ws, SPEC_ETIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t a0 = smem_u32(sA + s * kStageA), b0 = smem_u32(sB + s * stage_b);
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk)
-                mma_bf16(tmem, sdesc_k128(a0 + kk * 32), sdesc_k128(b0 + kk * 32), idesc, (i > 0 || kk > 0) ? 1u : 0u);
-            mma_commit(&empty[s]);
+                for (int kk = 0; kk < kBK / 16; ++kk)
+                    mma_bf16(tmem, sdesc_k128(a0 + kk * 32), sdesc_k128(b0 + kk * 32), idesc,
+                             (i > 0 || kk > 0) ? 1u : 0u);
+                mma_commit(&empty[s]);
+            }
+            mma_commit(accum);
         }
-        mma_commit(accum);
+        __syncwarp();
     }
 
     const bool have = mbar_wait(accum, 0);
-    if (!have && threadIdx.x == 64) flag_status(p.ws, SPEC_ETIMEOUT);
+    if (!have) flag_status(p.ws, SPEC_ETIMEOUT);
     tc_fence_after();
-    __syncthreads();
-    const bool run_epi = have && !*abort_flag && n_it > 0;
+    const int all_have = __syncthreads_and(have ? 1 : 0);   // one decision for the whole CTA
+    const bool run_epi = all_have && !*abort_flag && n_it > 0;
 
     if (run_epi && EPI == 0) {
         const int m = m0 + warp * 32 + lane;
@@ -164,6 +193,43 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
                         p.partial[(static_cast<size_t>(blockIdx.y) * p.n_pad + n) * p.M + m] = __uint_as_float(r[j]);
                 }
             }
+        }
+        // the last split to finish this weight tile sums all splits and writes z
+        __shared__ int last;
+        __threadfence();
+        __syncthreads();
+        if (threadIdx.x == 0) last = atomicAdd(&p.tickets[blockIdx.x], 1) == static_cast<int>(gridDim.y) - 1;
+        __syncthreads();
+        if (last) {
+            __threadfence();
+            // 4 consecutive outputs per thread and pass: 32 threads cover the tile's 128
+            // weight rows of one activation row, so a pass handles 4 activation rows;
+            // all split loads of a pass are independent
+            const int mq = m0 + (threadIdx.x & 31) * 4;
+            const int nsub = threadIdx.x >> 5;
+            const int splits = static_cast<int>(gridDim.y);
+            for (int n = nsub; n < p.n_valid; n += 4) {
+                if (mq >= p.M) break;
+                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+                for (int sp = 0; sp < splits; ++sp) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                        &p.partial[(static_cast<size_t>(sp) * p.n_pad + n) * p.M + mq]));
+                    a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
+                }
+                const int row = p.row0 + n;
+                const int b = p.cond ? row / p.n_int : row;
+                const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int mm = mq + e;
+                    if (mm >= p.M) break;
+                    const float x = av[e] + (p.bias ? __bfloat162float(p.bias[mm]) : 0.f);
+                    const float zz = __bfloat162float(p.h[static_cast<size_t>(b) * p.M + mm]) + x / (1.0f + expf(-x));
+                    p.z[static_cast<size_t>(row) * p.M + mm] = __float2bfloat16_rn(zz);
+                }
+            }
+            if (threadIdx.x == 0) p.tickets[blockIdx.x] = 0;   // ready for the next launch
         }
     }
     if (run_epi && EPI == 1) {
@@ -244,22 +310,6 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
     }
 }
 
-// z[row0 + n][m] = h[b][m] + SiLU(sum_s partial[s][n][m] + b1[m]), rounded to bf16,
-// for the `rows` activation rows of one group (b = the sequence of that row).
-__global__ void k_mlp_finish(const float* __restrict__ partial, int splits, int n_pad, int rows, int row0, int d,
-                             const __nv_bfloat16* __restrict__ b1, const __nv_bfloat16* __restrict__ h, int cond,
-                             int n_int, __nv_bfloat16* __restrict__ z) {
-    const size_t idx = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (idx >= static_cast<size_t>(rows) * d) return;
-    const int n = static_cast<int>(idx / d), m = static_cast<int>(idx % d);
-    float a = b1 ? __bfloat162float(b1[m]) : 0.f;
-    for (int s = 0; s < splits; ++s) a += partial[(static_cast<size_t>(s) * n_pad + n) * d + m];
-    const int row = row0 + n;
-    const int b = cond ? row / n_int : row;
-    const float zz = __bfloat162float(h[static_cast<size_t>(b) * d + m]) + a / (1.0f + expf(-a));
-    z[static_cast<size_t>(row) * d + m] = __float2bfloat16_rn(zz);
-}
-
 // ---------------------------------------------------------------- host
 
 namespace {
@@ -325,13 +375,13 @@ static int mlp_splits(int d, int d_in) {
     return (total + per - 1) / per;
 }
 
-DraftTcPlan draft_tc_plan(int rows, int d, int d_in_max, int V, int kmax) {
+DraftTcPlan draft_tc_plan(int rows, int d, int V) {
     DraftTcPlan p;
     p.rows_pad = n_pad_of(rows);
     p.nslices = (V + kBM - 1) / kBM;
-    const int splits = std::max(mlp_splits(d, d), mlp_splits(d, d_in_max));
+    p.n_tickets = (d + kBM - 1) / kBM;
+    const int splits = std::max(mlp_splits(d, d), mlp_splits(d, 2 * d));
     p.mlp_partial_bytes = sizeof(float) * static_cast<size_t>(splits) * std::min(p.rows_pad, kMaxN) * d;
-    (void)kmax;
     return p;
 }
 
@@ -340,14 +390,14 @@ static spec_status launch_umma(const CUtensorMap& ta, const CUtensorMap& tb, dim
                                cudaStream_t s, const char* name) {
     const size_t smem = smem_of(p.n_pad, p.stages);
     SPEC_CUDA_TRY(cudaFuncSetAttribute(k_umma<EPI, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    SPEC_CUDA_TRY(launch(name, k_umma<EPI, KMAX>, grid, dim3(kThreads), smem, s, ta, tb, p));
+    SPEC_CUDA_TRY(launch_ex(name, k_umma<EPI, KMAX>, grid, dim3(kThreads), smem, s, true, ta, tb, p));
     return SPEC_OK;
 }
 
 spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
-                          const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* xin, int d_in,
-                          int d_in_pad, __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax,
-                          float* scratch, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s) {
+                          const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* X, int d_in, int ldx,
+                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax, float* scratch,
+                          int* tickets, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s) {
     const int splits = mlp_splits(d, d_in);
     const int total_mlp = (d_in + kBK - 1) / kBK;
     const int per_split = (total_mlp + splits - 1) / splits;
@@ -357,7 +407,7 @@ spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, cons
         const int n_pad = n_pad_of(rows);
         CUtensorMap ta, tb;
         SPEC_CUDA_TRY(make_tmap_bf16_2d(&ta, W1, d, d_in, d_in, kBM));
-        SPEC_CUDA_TRY(make_tmap_bf16_2d(&tb, xin + static_cast<size_t>(g0) * d_in_pad, rows, d_in, d_in_pad, n_pad));
+        SPEC_CUDA_TRY(make_tmap_bf16_2d(&tb, X + static_cast<size_t>(g0) * ldx, rows, d_in, ldx, n_pad));
         UmmaParams p{};
         p.M = d;
         p.k_iters = per_split;
@@ -368,11 +418,15 @@ spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, cons
         p.tmem_cols = tmem_cols_of(n_pad);
         p.partial = scratch;
         p.ws = ws;
+        p.row0 = g0;
+        p.tickets = tickets;
+        p.bias = b1;
+        p.h = h;
+        p.z = z;
+        p.cond = cond;
+        p.n_int = n_int;
         spec_status st = launch_umma<0, 8>(ta, tb, dim3((d + kBM - 1) / kBM, splits), p, s, "draft_mlp_tc");
         if (st != SPEC_OK) return st;
-        const size_t total = static_cast<size_t>(rows) * d;
-        SPEC_CUDA_TRY(launch("draft_mlp_finish", k_mlp_finish, dim3(static_cast<unsigned>((total + 255) / 256)), dim3(256),
-                             0, s, scratch, splits, n_pad, rows, g0, d, b1, h, cond, n_int, z));
     }
     // ---- projection with the top-k epilogue
     for (int g0 = 0; g0 < R; g0 += kMaxN) {

@@ -12,25 +12,29 @@ struct Cand {
     float v;
     int i;
 };
-}
+}  // namespace draft
 namespace tc {
 
 struct DraftTcPlan {
     int rows_pad = 0;              // rows padded to the MMA N granule
     int nslices = 0;               // vocabulary slices (one per 128-row W2 tile)
+    int n_tickets = 0;             // split-K tickets of the MLP (one per 128-row W1 tile)
     size_t mlp_partial_bytes = 0;  // split-K partial sums of the MLP
 };
 
 bool draft_tc_supported(int d, int V);
-DraftTcPlan draft_tc_plan(int rows, int d, int d_in_max, int V, int kmax);
+DraftTcPlan draft_tc_plan(int rows, int d, int V);
 
-// One head: MLP (split-K, fused SiLU/residual epilogue) then the projection with
-// per-slice top-k and (max, sum exp) partials.  xin holds the gathered rows
-// (row stride d_in_pad); z receives the bf16 MLP output.
+// One head: the MLP (split over K; the last split of each weight tile applies
+// bias, SiLU, residual and bf16 rounding) then the projection with per-slice
+// top-k and (max, sum exp) partials.  X holds the head's input rows (row stride
+// ldx: the gathered [h || E[tok]] rows, or h itself for an unconditioned head);
+// z receives the bf16 MLP output.  Kernels are launched with programmatic
+// dependent launch.
 spec_status draft_head_tc(const DraftTcPlan& p, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
-                          const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* xin, int d_in,
-                          int d_in_pad, __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax,
-                          float* scratch, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s);
+                          const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* X, int d_in, int ldx,
+                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax, float* scratch,
+                          int* tickets, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s);
 
 }  // namespace tc
 }  // namespace spec
