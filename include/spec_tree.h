@@ -255,6 +255,15 @@ const char* spec_last_error(void);
 spec_status spec_read_device_status(const void* ws, int32_t* status, spec_stream_t s);
 
 /*
+ * Self-test of the device failure path: queues one kernel that waits on a
+ * shared-memory barrier nothing completes, with the bounded wait the
+ * tensor-core kernels use; after limit_ns (capped at 1 s) it gives up and
+ * records SPEC_ETIMEOUT in the first word of ws (read it back with
+ * spec_read_device_status).  ws: device, >= 16 bytes, 16-byte aligned.
+ */
+spec_status spec_selftest_timeout(void* ws, uint64_t limit_ns, spec_stream_t s);
+
+/*
  * Kernel tracing.  While enabled, every kernel this library launches is
  * bracketed by a pair of CUDA events on its launch stream (at most `capacity`
  * launches are recorded).  spec_trace_end waits for them, totals the time per

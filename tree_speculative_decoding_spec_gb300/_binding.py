@@ -68,6 +68,7 @@ def _load():
         "spec_philox_uniform": (i32, [u64, u64, i32, i32, vp, vp, vp]),
         "spec_last_error": (ctypes.c_char_p, []),
         "spec_read_device_status": (i32, [vp, _i32p, vp]),
+        "spec_selftest_timeout": (i32, [vp, u64, vp]),
         "spec_trace_begin": (i32, [i32]),
         "spec_trace_end": (i32, [ctypes.POINTER(spec_trace_entry), i32]),
         "spec_launch_count": (ctypes.c_int64, []),
@@ -367,6 +368,13 @@ def spec_read_device_status(ws, stream=None):
     v = ctypes.c_int32(0)
     _check("spec_read_device_status", _lib.spec_read_device_status(_ptr(ws), ctypes.byref(v), _stream(stream)))
     return v.value
+
+
+def spec_selftest_timeout(ws, limit_ns=1_000_000, stream=None):
+    """Run the bounded-wait self-test kernel on `ws` (a CUDA uint8 tensor >= 16 bytes)."""
+    _need(ws, "ws")
+    with torch.cuda.device(ws.device):
+        _check("spec_selftest_timeout", _lib.spec_selftest_timeout(_ptr(ws), int(limit_ns), _stream(stream)))
 
 
 def spec_last_error():

@@ -301,3 +301,31 @@ extern "C" spec_status spec_philox_uniform(uint64_t seed, uint64_t offset, int32
                          u_accept, u_sample));
     return SPEC_OK;
 }
+
+// ---------------------------------------------------------------- bounded-wait self-test
+
+#include "tc.cuh"
+
+namespace spec {
+// One thread waits on a shared-memory barrier that nothing completes; the
+// bounded wait used by the tensor-core kernels gives up after limit_ns and
+// records SPEC_ETIMEOUT in the workspace status word.
+__global__ void k_selftest_timeout(void* ws, uint64_t limit_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x != 0) return;
+    tc::mbar_init(&bar, 1);
+    tc::fence_mbar_init();
+    if (!tc::mbar_wait(&bar, 0, limit_ns)) flag_status(ws, SPEC_ETIMEOUT);
+}
+}  // namespace spec
+
+extern "C" spec_status spec_selftest_timeout(void* ws, uint64_t limit_ns, spec_stream_t s_) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(s_);
+    clear_error();
+    if (!ws) return fail(SPEC_EINVAL, "ws must not be NULL");
+    if (!aligned16(ws)) return fail(SPEC_EALIGN, "ws must be 16-byte aligned");
+    if (limit_ns > 1000000000ull) limit_ns = 1000000000ull;
+    SPEC_CUDA_TRY(reset_device_status(ws, s));
+    SPEC_CUDA_TRY(launch("selftest_timeout", k_selftest_timeout, dim3(1), dim3(32), 0, s, ws, limit_ns));
+    return SPEC_OK;
+}

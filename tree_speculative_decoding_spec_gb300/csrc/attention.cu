@@ -194,28 +194,45 @@ __global__ void __launch_bounds__(256) k_attn_fma(const T* __restrict__ q, const
 
 // ---------------------------------------------------------------- combine
 
-__global__ void k_attn_combine(const float* __restrict__ part, const int32_t* __restrict__ prefix_len, int Tn, int Hq,
-                               int D, int Lmax, int chunk, int n_pre, float* __restrict__ out, float* __restrict__ lse) {
-    const int row = blockIdx.x;
+// One warp per (sequence, query head, node) row, 8 rows per CTA: merge the
+// row's split partials (max m_c in base 2, sum l_c, unnormalised O_c):
+// O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c, lse = (M + log2 l) ln 2.
+// Slots read: the non-empty prefix splits, plus the tree slot n_pre unless the
+// tree keys were folded into the last prefix split (tensor-core layout).
+__global__ void __launch_bounds__(256) k_attn_combine(const float* __restrict__ part, const int32_t* __restrict__ prefix_len,
+                                                      int Tn, int Hq, int D, int Lmax, int chunk, int n_pre, int folded,
+                                                      int nrows, float* __restrict__ out, float* __restrict__ lse) {
+    const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= nrows) return;
+    const int lane = threadIdx.x & 31;
     const int b = row / (Hq * Tn);
     const int L = min(max(prefix_len[b], 0), Lmax);
     const int nvalid = (L + chunk - 1) / chunk;
-    const int n_chunks = n_pre + 1;
-    const float* base = part + static_cast<size_t>(row) * n_chunks * (D + 4);
-    float M = base[static_cast<size_t>(n_pre) * (D + 4)];
-    for (int c = 0; c < nvalid; ++c) M = fmaxf(M, base[static_cast<size_t>(c) * (D + 4)]);
+    const int nread = folded ? max(nvalid, 1) : nvalid + 1;
+    const float* base = part + static_cast<size_t>(row) * (n_pre + 1) * (D + 4);
+    auto slot = [&](int i) { return (!folded && i == nvalid) ? n_pre : i; };
+    float M = -INFINITY;
+    for (int i = lane; i < nread; i += 32) M = fmaxf(M, base[static_cast<size_t>(slot(i)) * (D + 4)]);
+    M = warp_max(M);
+    const bool has = 4 * lane < D;
     float l = 0.f;
-    const int d = threadIdx.x;
-    float o = 0.f;
-    for (int c = 0; c <= nvalid; ++c) {
-        const int cc = (c == nvalid) ? n_pre : c;
-        const float* pc = base + static_cast<size_t>(cc) * (D + 4);
-        const float w = exp2f(pc[0] - M);
+    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < nread; ++i) {
+        const float* pc = base + static_cast<size_t>(slot(i)) * (D + 4);
+        const float m = pc[0];
+        const float w = m == -INFINITY ? 0.f : exp2f(m - M);
         l += w * pc[1];
-        if (d < D) o += w * pc[4 + d];
+        if (has && w != 0.f) {
+            const float4 v = *reinterpret_cast<const float4*>(pc + 4 + 4 * lane);
+            o.x += w * v.x; o.y += w * v.y; o.z += w * v.z; o.w += w * v.w;
+        }
     }
-    if (d < D) out[static_cast<size_t>(row) * D + d] = o / l;
-    if (lse && d == 0) lse[row] = (M + log2f(l)) * kLn2;
+    if (has) {
+        const float inv = 1.f / l;
+        *reinterpret_cast<float4*>(out + static_cast<size_t>(row) * D + 4 * lane) =
+            make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+    }
+    if (lse && lane == 0) lse[row] = (M + log2f(l)) * kLn2;
 }
 
 // ---------------------------------------------------------------- planning
@@ -279,8 +296,9 @@ spec_status run_fma(const T* q, const T* kc, const T* vc, const int32_t* prefix_
         SPEC_CUDA_TRY(launch("attn_fma", k_attn_fma<T, 64>, grid, dim3(256), smem, s, q, kc, vc, prefix_len, kt, vt,
                              t->anc, t->T, t->words, Hq, Hkv, Lmax, sl2, p.chunk, p.n_pre, p.n_rowblocks, part));
     }
-    SPEC_CUDA_TRY(launch("attn_combine", k_attn_combine, dim3(B * Hq * t->T), dim3(D), 0, s, part, prefix_len, t->T,
-                         Hq, D, Lmax, p.chunk, p.n_pre, out, lse));
+    const int nrows = B * Hq * t->T;
+    SPEC_CUDA_TRY(launch("attn_combine", k_attn_combine, dim3((nrows + 7) / 8), dim3(256), 0, s, part, prefix_len, t->T,
+                         Hq, D, Lmax, p.chunk, p.n_pre, 0, nrows, out, lse));
     return SPEC_OK;
 }
 
@@ -323,8 +341,9 @@ extern "C" spec_status tree_attention(const void* q, const void* k_cache, const 
                                  static_cast<const T*>(v_cache), prefix_len, static_cast<const T*>(k_tree),
                                  static_cast<const T*>(v_tree), tree, B, Hq, Hkv, Lmax, scale, part, ws, s);
             if (st != SPEC_OK) return st;
-            SPEC_CUDA_TRY(launch("attn_combine", attn::k_attn_combine, dim3(B * Hq * tree->T), dim3(D), 0, s, part,
-                                 prefix_len, tree->T, Hq, D, Lmax, p.tcp.chunk, p.tcp.n_pre, out, lse));
+            const int nrows = B * Hq * tree->T;
+            SPEC_CUDA_TRY(launch("attn_combine", attn::k_attn_combine, dim3((nrows + 7) / 8), dim3(256), 0, s, part,
+                                 prefix_len, tree->T, Hq, D, Lmax, p.tcp.chunk, p.tcp.n_pre, 1, nrows, out, lse));
             return SPEC_OK;
         }
         return attn::run_fma<T>(static_cast<const T*>(q), static_cast<const T*>(k_cache), static_cast<const T*>(v_cache),

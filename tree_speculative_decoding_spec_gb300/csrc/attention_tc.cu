@@ -5,22 +5,24 @@
 // sets arrive as one bit row per node and are applied to the scores in
 // registers.
 //
-// One CTA = one (key split, KV head x 128-query-row block, sequence).  The
-// query rows of a KV head are its g query heads x T nodes, which are
-// contiguous in q [B, Hq, T, D], so one 2-D TMA box fetches them.  Six warps:
-//   warp 4    TMA: the 128 x 128 Q tile once, then a 3-stage ring of
-//             64-key K and V tiles (128-byte swizzle)
-//   warp 5    MMA: S_j = Q K_j^T into one of two TMEM score buffers
-//             (M 128, N 64, K 128), and O += P_j V_j (M 128, N 128, K 64,
-//             V read as an MN-major operand) into the TMEM output
-//   warps 0-3 one thread per query row: read S_j from TMEM, mask (prefix
-//             length, ancestor bits), online softmax in base 2 with lazy
-//             rescaling (O in TMEM is rescaled only when the row maximum
-//             grows by more than 2^8), write bf16 P_j into a swizzled shared
-//             tile for the next MMA; at the end read O and write the split's
-//             (max, sum, O) partial.
-// Waits are bounded (2 s); on expiry SPEC_ETIMEOUT goes to the status word,
-// the CTA drains its own loads and frees TMEM.
+// One CTA = one (prefix split, KV head x 128-query-row block, sequence); the
+// CTA holding the last non-empty prefix split of a sequence also takes the
+// tree keys.  The query rows of a KV head are its g query heads x T nodes,
+// contiguous in q [B, Hq, T, D], so one 2-D TMA box fetches them.  Ten warps:
+//   warp 8    TMA: the 128 x 128 Q tile once, then a 3-stage ring of 64-key
+//             K and V tiles (128-byte swizzle), prefix tiles then tree tiles
+//   warp 9    MMA: S_j = Q K_j^T into TMEM score buffer j % 2 (M 128, N 64,
+//             K 128) and O_{j%2} += P_j V_j (M 128, N 128, K 64, V read as an
+//             MN-major operand)
+//   warps 0-3 / 4-7: two softmax groups; group j % 2 owns tile j.  One thread
+//             per query row reads S_j from TMEM, masks (prefix length,
+//             ancestor bits), keeps its group's running maximum and sum in
+//             base 2 (O is rescaled in TMEM only when the maximum grows by
+//             more than 2^8) and writes bf16 P_j to a swizzled shared tile.
+//             At the end group 0 merges the two groups' (max, sum, O) and
+//             writes the split's partial.
+// Waits are bounded (2 s); on expiry SPEC_ETIMEOUT goes to the status word and
+// the CTA drains its own loads and MMAs before freeing TMEM.
 #include <algorithm>
 
 #include "attention_tc.cuh"
@@ -33,13 +35,13 @@ constexpr int kARows = 128;        // query rows per CTA (MMA M)
 constexpr int kAKeys = 64;         // keys per tile
 constexpr int kAD = 128;           // head dim
 constexpr int kAStages = 3;
-constexpr int kAThreads = 192;
+constexpr int kAThreads = 320;
 constexpr int kQBytes = 2 * kARows * 128;         // two 64-column halves of 128 rows
 constexpr int kKVHalf = kAKeys * 128;             // one 64-column half of a 64-key tile
 constexpr int kStageBytes = 4 * kKVHalf;          // K and V, two halves each
 constexpr int kPBytes = kARows * 128;             // 128 rows x 64 bf16
-constexpr size_t kASmem = 1024 + kQBytes + kAStages * kStageBytes + 2 * kPBytes + 256;
-constexpr uint32_t kATmemCols = 256;              // S0 [0,64) S1 [64,128) O [128,256)
+constexpr size_t kASmem = 1024 + kQBytes + kAStages * kStageBytes + 2 * kPBytes + 2048;
+constexpr uint32_t kATmemCols = 512;              // S0 [0,64) S1 [64,128) O0 [128,256) O1 [256,384)
 
 struct AttnTcParams {
     int T, g, Hq, Hkv, Lmax, words;
@@ -51,6 +53,15 @@ struct AttnTcParams {
     void* ws;
 };
 
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Named barrier for the 256 softmax threads (warps 0-7).
+__device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
 __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant__ CUtensorMap tmQ,
                                                           const __grid_constant__ CUtensorMap tmKc,
                                                           const __grid_constant__ CUtensorMap tmVc,
@@ -61,27 +72,31 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     const int kvh = blockIdx.y / p.n_rb, rb = blockIdx.y % p.n_rb;
     const int b = blockIdx.z;
     const int L = min(max(p.prefix_len[b], 0), p.Lmax);
-    const bool tail = (c == p.n_pre);
-    const int k_begin = tail ? 0 : c * p.chunk;
-    const int k_end = tail ? p.T : min(L, k_begin + p.chunk);
-    if (k_begin >= k_end) return;   // whole CTA: nothing allocated yet
-    const int n_tiles = (k_end - k_begin + kAKeys - 1) / kAKeys;
+    const int pre_begin = c * p.chunk;
+    const int pre_end = min(L, pre_begin + p.chunk);
+    const int n_pt = pre_end > pre_begin ? (pre_end - pre_begin + kAKeys - 1) / kAKeys : 0;
+    const int n_pref = (L + p.chunk - 1) / p.chunk;          // non-empty prefix splits
+    const bool has_tree = (c == max(n_pref - 1, 0));          // this split also takes the tree keys
+    const int n_tt = has_tree ? (p.T + kAKeys - 1) / kAKeys : 0;
+    const int n_tiles = n_pt + n_tt;
+    if (n_tiles == 0) return;   // whole CTA: nothing allocated yet
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
     uint8_t* sKV = sQ + kQBytes;                       // stage s: K half0, K half1, V half0, V half1
-    uint8_t* sP = sKV + kAStages * kStageBytes;        // two P buffers
+    uint8_t* sP = sKV + kAStages * kStageBytes;        // P buffers of group 0 and group 1
     uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kPBytes);
     uint64_t* q_full = bars;
     uint64_t* kv_full = bars + 1;
     uint64_t* kv_empty = kv_full + kAStages;
-    uint64_t* s_full = kv_empty + kAStages;
-    uint64_t* p_full = s_full + 2;
-    uint64_t* pv_done = p_full + 2;
+    uint64_t* s_full = kv_empty + kAStages;            // [group]
+    uint64_t* p_full = s_full + 2;                     // [group]
+    uint64_t* pv_done = p_full + 2;                    // [group]
     uint64_t* o_final = pv_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float2* merge = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(bars) + 256);   // [128] group 1's (m, l)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
@@ -99,21 +114,24 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmQ);
-        prefetch_tmap(tail ? &tmKt : &tmKc);
-        prefetch_tmap(tail ? &tmVt : &tmVc);
+        prefetch_tmap(&tmKc);
+        prefetch_tmap(&tmVc);
+        if (n_tt) {
+            prefetch_tmap(&tmKt);
+            prefetch_tmap(&tmVt);
+        }
     }
     if (warp == 0) tmem_alloc(tmem_slot, kATmemCols);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const CUtensorMap* tmK = tail ? &tmKt : &tmKc;
-    const CUtensorMap* tmV = tail ? &tmVt : &tmVc;
-    const int kv_row0 = tail ? (b * p.Hkv + kvh) * p.T : (b * p.Hkv + kvh) * p.Lmax;
+    const int kvc_row0 = (b * p.Hkv + kvh) * p.Lmax + pre_begin;   // first prefix key of this split
+    const int kvt_row0 = (b * p.Hkv + kvh) * p.T;                  // first tree key
     const int q_row0 = (b * p.Hq + kvh * p.g) * p.T + rb * kARows;
     int issued = 0;
 
-    if (warp == 4) {
+    if (warp == 8) {
         if (lane == 0) {
             mbar_arrive_expect_tx(q_full, kQBytes);
             tma_load_2d(sQ, &tmQ, q_full, 0, q_row0);
@@ -125,18 +143,21 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                     *abort_flag = 1;
                     break;
                 }
+                const bool tree_tile = j >= n_pt;
+                const CUtensorMap* tk = tree_tile ? &tmKt : &tmKc;
+                const CUtensorMap* tv = tree_tile ? &tmVt : &tmVc;
+                const int row = tree_tile ? kvt_row0 + (j - n_pt) * kAKeys : kvc_row0 + j * kAKeys;
                 uint8_t* st = sKV + s * kStageBytes;
-                const int row = kv_row0 + k_begin + j * kAKeys;
                 mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
-                tma_load_2d(st, tmK, &kv_full[s], 0, row);
-                tma_load_2d(st + kKVHalf, tmK, &kv_full[s], 64, row);
-                tma_load_2d(st + 2 * kKVHalf, tmV, &kv_full[s], 0, row);
-                tma_load_2d(st + 3 * kKVHalf, tmV, &kv_full[s], 64, row);
+                tma_load_2d(st, tk, &kv_full[s], 0, row);
+                tma_load_2d(st + kKVHalf, tk, &kv_full[s], 64, row);
+                tma_load_2d(st + 2 * kKVHalf, tv, &kv_full[s], 0, row);
+                tma_load_2d(st + 3 * kKVHalf, tv, &kv_full[s], 64, row);
                 issued = j + 1;
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kARows, kAKeys);
             const uint32_t idesc_o = idesc_bf16_f32_bmn(kARows, kAD);
@@ -158,21 +179,25 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                 mma_commit(&s_full[j & 1]);
                 return true;
             };
+            // S for the first tile of each group, then per tile: PV_j, S_{j+2}
             if (ok) ok = issue_s(0);
+            if (ok && n_tiles > 1) ok = issue_s(1);
             for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles && !issue_s(j + 1)) { ok = false; break; }
                 if (!mbar_wait_or_abort(&p_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                // O += P_j V_j: K = 64 keys in 4 steps of 16; V is MN-major (d contiguous):
+                // O_{j%2} += P_j V_j: K = 64 keys in 4 steps of 16; V is MN-major (d contiguous):
                 // 64-wide d halves 8 KB apart, 8-key atoms 1 KB apart
                 const uint32_t pa = smem_u32(sP + (j & 1) * kPBytes);
                 const uint32_t v0 = smem_u32(sKV + (j % kAStages) * kStageBytes + 2 * kKVHalf);
+                const uint32_t o = tmem + 2 * kAKeys + (j & 1) * kAD;
 #pragma unroll
                 for (int ks = 0; ks < kAKeys / 16; ++ks)
-                    mma_bf16(tmem + 2 * kAKeys, sdesc_k128(pa + ks * 32), sdesc_mn128(v0 + ks * 2048, kKVHalf, 1024),
-                             idesc_o, (j > 0 || ks > 0) ? 1u : 0u);
+                    mma_bf16(o, sdesc_k128(pa + ks * 32), sdesc_mn128(v0 + ks * 2048, kKVHalf, 1024), idesc_o,
+                             (j >= 2 || ks > 0) ? 1u : 0u);
                 mma_commit(&pv_done[j & 1]);
                 mma_commit(&kv_empty[j % kAStages]);
+                // the score buffer of this group is free once its P_j is written (p_full_j passed)
+                if (j + 2 < n_tiles && !issue_s(j + 2)) { ok = false; break; }
             }
             if (!ok) {
                 flag_status(p.ws, SPEC_ETIMEOUT);
@@ -182,46 +207,59 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
         }
         __syncwarp();
     } else {
-        const int r = threadIdx.x;                        // query row of this block = TMEM lane
-        const int rg = rb * kARows + r;                   // row within the KV head's g*T rows
+        const int grp = warp >> 2;                         // softmax group: tiles j with j % 2 == grp
+        const int r = (warp & 3) * 32 + lane;              // query row of this block = TMEM lane
+        const int rg = rb * kARows + r;                    // row within the KV head's g*T rows
         const int node = rg % p.T;
-        const uint32_t lane_base = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-        const uint32_t o_col = 2 * kAKeys;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
+        const uint32_t s_col = grp * kAKeys;
+        const uint32_t o_col = 2 * kAKeys + grp * kAD;
         const uint64_t* anc_row = p.anc + static_cast<size_t>(node) * p.words;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
-        for (int j = 0; j < n_tiles; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&s_full[j & 1], (j >> 1) & 1, abort_flag));
+        for (int j = grp; j < n_tiles; j += 2) {
+            ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&s_full[grp], (j >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
             uint32_t sa[32], sb[32];
-            tmem_ld32(lane_base + (j & 1) * kAKeys, sa);
-            tmem_ld32(lane_base + (j & 1) * kAKeys + 32, sb);
+            tmem_ld32(lane_base + s_col, sa);
+            tmem_ld32(lane_base + s_col + 32, sb);
             tmem_ld_wait();
-            const int key0 = k_begin + j * kAKeys;
-            const int nvalid = min(kAKeys, k_end - key0);
-            uint64_t bits = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
-            if (tail) bits &= anc_row[key0 >> 6];
+            uint64_t bits;
+            if (j >= n_pt) {   // tree keys: only the node's ancestors (and itself)
+                const int t = j - n_pt;
+                const int nvalid = min(kAKeys, p.T - t * kAKeys);
+                bits = (nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull)) & anc_row[t];
+            } else {           // prefix keys below prefix_len
+                const int nvalid = min(kAKeys, pre_end - (pre_begin + j * kAKeys));
+                bits = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+            }
             float sv[64];
-            float tmax = -INFINITY;
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
                 sv[e] = ((bits >> e) & 1ull) ? __uint_as_float(sa[e]) * p.scale_log2 : -INFINITY;
                 sv[32 + e] = ((bits >> (32 + e)) & 1ull) ? __uint_as_float(sb[e]) * p.scale_log2 : -INFINITY;
-                tmax = fmaxf(tmax, fmaxf(sv[e], sv[32 + e]));
             }
+            float mx[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) mx[e] = fmaxf(fmaxf(sv[e], sv[e + 16]), fmaxf(sv[e + 32], sv[e + 48]));
+#pragma unroll
+            for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+                for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
+            const float tmax = mx[0];
             // lazy rescale: keep the old reference maximum unless the row max grew by > 2^8
             float m_new = m_used, alpha = 1.f;
             bool rescale = false;
             if (tmax > m_used + 8.f) {
                 if (m_used != -INFINITY) {
                     rescale = true;
-                    alpha = exp2f(m_used - tmax);
+                    alpha = ex2(m_used - tmax);
                 }
                 m_new = tmax;
             }
-            if (j >= 1) {   // O and this P buffer are stable once PV_{j-1} is done
-                ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&pv_done[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag));
+            if (j >= 2) {   // PV_{j-2} (same O, same P buffer) must be done
+                ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&pv_done[grp], ((j - 2) >> 1) & 1, abort_flag));
                 if (!ok) break;
                 tc_fence_after();
             }
@@ -241,53 +279,68 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             m_used = m_new;
             // P = 2^(s - m_used) in bf16, 128-byte swizzled row (16-byte chunk q at q ^ (r % 8));
             // the row sum uses the rounded values the MMA will see
-            uint8_t* prow = sP + (j & 1) * kPBytes + r * 128;
-            float psum = 0.f;
+            uint8_t* prow = sP + grp * kPBytes + r * 128;
+            const float mref = m_used == -INFINITY ? 0.f : m_used;
+            float ps[8];
 #pragma unroll
             for (int qc = 0; qc < 8; ++qc) {
                 uint32_t packed[4];
+                float acc = 0.f;
 #pragma unroll
                 for (int h2 = 0; h2 < 4; ++h2) {
                     const int e0 = qc * 8 + 2 * h2;
-                    const float a0 = m_used == -INFINITY ? 0.f : exp2f(sv[e0] - m_used);
-                    const float a1 = m_used == -INFINITY ? 0.f : exp2f(sv[e0 + 1] - m_used);
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(a0, a1);
-                    psum += __low2float(pr) + __high2float(pr);
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(ex2(sv[e0] - mref), ex2(sv[e0 + 1] - mref));
+                    acc += __low2float(pr) + __high2float(pr);
                     packed[h2] = *reinterpret_cast<const uint32_t*>(&pr);
                 }
+                ps[qc] = acc;
                 *reinterpret_cast<uint4*>(prow + ((qc ^ (r & 7)) * 16)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
             }
-            l += psum;
+            l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(&p_full[j & 1]);
+            mbar_arrive(&p_full[grp]);
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_or_abort(o_final, 0, abort_flag));
         if (!ok) {
             flag_status(p.ws, SPEC_ETIMEOUT);
             *abort_flag = 1;
-        } else {
+        }
+        if (grp == 1) merge[r] = make_float2(m_used, l);
+        softmax_sync();
+        if (grp == 0 && !*abort_flag) {
             tc_fence_after();
+            // merge the two groups: (m, l, O) = rescaled sums of (m0, l0, O0) and (m1, l1, O1)
+            const float2 g1 = merge[r];
+            const float m = fmaxf(m_used, g1.x);
+            const float a0 = m_used == -INFINITY ? 0.f : ex2(m_used - m);
+            const float a1 = g1.x == -INFINITY ? 0.f : ex2(g1.x - m);
             const bool valid = rg < p.T * p.g;
             float* dst = nullptr;
             if (valid) {
                 const int hl = rg / p.T, i = rg % p.T;
                 const size_t row = (static_cast<size_t>(b) * p.Hq + kvh * p.g + hl) * p.T + i;
                 dst = p.part + (row * (p.n_pre + 1) + c) * (kAD + 4);
-                dst[0] = m_used;
-                dst[1] = l;
+                dst[0] = m;
+                dst[1] = a0 * l + a1 * g1.y;
             }
 #pragma unroll 1
             for (int cc = 0; cc < kAD / 32; ++cc) {
-                uint32_t o[32];
-                tmem_ld32(lane_base + o_col + cc * 32, o);
+                uint32_t o0[32], o1[32];
+                tmem_ld32(lane_base + 2 * kAKeys + cc * 32, o0);
+                tmem_ld32(lane_base + 2 * kAKeys + kAD + cc * 32, o1);
                 tmem_ld_wait();
                 if (valid) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        *reinterpret_cast<float4*>(dst + 4 + cc * 32 + 4 * e) =
-                            make_float4(__uint_as_float(o[4 * e]), __uint_as_float(o[4 * e + 1]),
-                                        __uint_as_float(o[4 * e + 2]), __uint_as_float(o[4 * e + 3]));
+                    for (int e = 0; e < 8; ++e) {
+                        float v[4];
+#pragma unroll
+                        for (int t = 0; t < 4; ++t) {
+                            const float x0 = a0 * __uint_as_float(o0[4 * e + t]);
+                            v[t] = a1 != 0.f ? x0 + a1 * __uint_as_float(o1[4 * e + t]) : x0;   // group 1 may own no tile
+                        }
+                        *reinterpret_cast<float4*>(dst + 4 + cc * 32 + 4 * e) = make_float4(v[0], v[1], v[2], v[3]);
+                    }
                 }
             }
         }
@@ -297,12 +350,12 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     __syncthreads();
     if (*abort_flag) {
         // a wait ran out: let this CTA's own loads and MMAs land before releasing memory
-        if (warp == 4 && lane == 0) {
+        if (warp == 8 && lane == 0) {
             for (int j = max(0, issued - kAStages); j < issued; ++j)
                 mbar_wait(&kv_full[j % kAStages], (j / kAStages) & 1, 100000000ull);
             mbar_wait(q_full, 0, 100000000ull);
         }
-        if (warp == 5 && lane == 0) mbar_wait(o_final, 0, 100000000ull);
+        if (warp == 9 && lane == 0) mbar_wait(o_final, 0, 100000000ull);
     }
     __syncthreads();
     if (warp == 0) {
@@ -321,25 +374,24 @@ bool attn_tc_supported(int rows_per_kv_head, int D) {
     return make_tmap_bf16_2d(&probe, dummy, 64, kAD, kAD, 64) == cudaSuccess;
 }
 
-// Splits of the prefix: one CTA per (split, KV head x row block, sequence) plus one
-// tree-key split each.  Pick the split count that minimises an estimated
-// makespan (waves of one CTA per SM x tiles per CTA, with ~2 tiles of fixed cost
-// per CTA); ties go to fewer splits (less combine traffic).
+// Prefix splits: one CTA per (split, KV head x row block, sequence); the last
+// non-empty split of each sequence also takes the tree keys.  Pick the split
+// count minimising an estimated makespan -- waves of one CTA per SM times the
+// longest CTA (its prefix tiles, the tree tiles, ~2 tiles of fixed cost) --
+// ties to fewer splits (less combine traffic).
 AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_count) {
     AttnTcPlan p;
     const int g = Hq / Hkv;
     p.n_rb = (T * g + kARows - 1) / kARows;
     const int64_t base = static_cast<int64_t>(B) * Hkv * p.n_rb;
     const int tiles = (Lmax + kAKeys - 1) / kAKeys;
-    const int tail_tiles = (T + kAKeys - 1) / kAKeys;
+    const int tree_tiles = (T + kAKeys - 1) / kAKeys;
     int64_t best_cost = INT64_MAX;
     int best = 1;
     for (int n = 1; n <= std::min(tiles, 64); ++n) {
         const int per = (tiles + n - 1) / n;
-        const int64_t ctas = base * n;
-        const int64_t waves = (ctas + sm_count - 1) / sm_count;
-        const int64_t tail_waves = (base + sm_count - 1) / sm_count;
-        const int64_t cost = waves * (per + 2) + tail_waves * (tail_tiles + 2);
+        const int64_t waves = (base * n + sm_count - 1) / sm_count;
+        const int64_t cost = waves * (per + tree_tiles + 2);
         if (cost < best_cost) {
             best_cost = cost;
             best = n;
@@ -347,6 +399,7 @@ AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_c
     }
     p.chunk = static_cast<int>(round_up((Lmax + best - 1) / best, kAKeys));
     p.n_pre = (Lmax + p.chunk - 1) / p.chunk;
+    // partial layout shared with the CUDA-core path: n_pre + 1 slots per row (the last unused here)
     p.part_bytes = sizeof(float) * static_cast<size_t>(B) * Hq * T * (p.n_pre + 1) * (D + 4);
     return p;
 }
@@ -378,7 +431,7 @@ spec_status attn_tc_run(const AttnTcPlan& pl, const __nv_bfloat16* q, const __nv
     p.part = part;
     p.ws = ws;
     SPEC_CUDA_TRY(cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem));
-    SPEC_CUDA_TRY(launch("attn_tc", k_attn_tc, dim3(pl.n_pre + 1, Hkv * pl.n_rb, B), dim3(kAThreads), kASmem, s, tq, tkc,
+    SPEC_CUDA_TRY(launch("attn_tc", k_attn_tc, dim3(pl.n_pre, Hkv * pl.n_rb, B), dim3(kAThreads), kASmem, s, tq, tkc,
                          tvc, tkt, tvt, p));
     return SPEC_OK;
 }

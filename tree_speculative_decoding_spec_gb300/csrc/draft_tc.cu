@@ -27,10 +27,32 @@ namespace spec {
 namespace tc {
 
 constexpr int kBM = 128;        // MMA M: weight rows per CTA
-constexpr int kBK = 64;         // K per stage: one 128-byte swizzled row of bf16
+// Build-time shape knobs (defaults are the tuned choice):
+//   SPEC_DRAFT_KB        64-column K blocks per pipeline stage
+//   SPEC_DRAFT_SMEM_KB   shared-memory budget per CTA in KB (100 keeps two CTAs per SM)
+//   SPEC_DRAFT_L2PROMO   L2 promotion of the weight loads: 0 none, 1 128 B, 2 256 B
+//   SPEC_DRAFT_ROTATE    1: each CTA starts its K loop at a different stage (by
+//                        weight tile), so the CTAs do not all read the same
+//                        activation lines from L2 at the same moment
+#ifndef SPEC_DRAFT_KB
+#define SPEC_DRAFT_KB 2
+#endif
+#ifndef SPEC_DRAFT_SMEM_KB
+#define SPEC_DRAFT_SMEM_KB 100
+#endif
+#ifndef SPEC_DRAFT_ROTATE
+#define SPEC_DRAFT_ROTATE 1
+#endif
+#ifndef SPEC_DRAFT_L2PROMO
+#define SPEC_DRAFT_L2PROMO 2
+#endif
+constexpr int kBK = 64;         // K per TMA box: one 128-byte swizzled row of bf16
+constexpr int kKB = SPEC_DRAFT_KB;
+constexpr int kBKS = kBK * kKB; // K per stage
 constexpr int kThreads = 128;
-constexpr int kStageA = kBM * kBK * 2;
-constexpr int kSmemBudget = 100 * 1024;   // keeps two CTAs per SM
+constexpr int kStageA = kBM * kBKS * 2;
+constexpr int kBoxA = kBM * kBK * 2;      // one K block of the weight tile
+constexpr int kSmemBudget = SPEC_DRAFT_SMEM_KB * 1024;
 
 struct UmmaParams {
     int M;          // weight rows
@@ -86,7 +108,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
                                                       const __grid_constant__ CUtensorMap tmB, const UmmaParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    const int stage_b = p.n_pad * kBK * 2;
+    const int stage_b = p.n_pad * kBKS * 2;
+    const int box_b = p.n_pad * kBK * 2;
     uint8_t* sA = smem;
     uint8_t* sB = smem + p.stages * kStageA;
     uint64_t* full = reinterpret_cast<uint64_t*>(sB + p.stages * stage_b);
@@ -98,6 +121,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * kBM;
     const int it0 = blockIdx.y * p.k_iters;
+    // stage i of this CTA covers K stage it0 + (i + rot) mod n_it
+    const int rot = SPEC_DRAFT_ROTATE ? static_cast<int>(blockIdx.x % max(1, min(p.k_iters, p.total_iters - it0))) : 0;
     const int n_it = max(0, min(p.k_iters, p.total_iters - it0));
 
     if (threadIdx.x == 0) {
@@ -129,10 +154,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
             const int pre = min(n_it, p.stages);
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(&full[i], kStageA + stage_b);
-                tma_load_2d(sA + i * kStageA, &tmA, &full[i], (it0 + i) * kBK, m0);
+                for (int kb = 0; kb < kKB; ++kb)
+                    tma_load_2d(sA + i * kStageA + kb * kBoxA, &tmA, &full[i], (it0 + (i + rot) % n_it) * kBKS + kb * kBK, m0);
             }
             griddep_wait();
-            for (int i = 0; i < pre; ++i) tma_load_2d(sB + i * stage_b, &tmB, &full[i], (it0 + i) * kBK, 0);
+            for (int i = 0; i < pre; ++i)
+                for (int kb = 0; kb < kKB; ++kb)
+                    tma_load_2d(sB + i * stage_b + kb * box_b, &tmB, &full[i], (it0 + (i + rot) % n_it) * kBKS + kb * kBK, 0);
             issued = pre;
             for (int i = pre; i < n_it; ++i) {
                 const int s = i % p.stages;
@@ -143,9 +171,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
                 }
                 if (*abort_flag) break;
                 mbar_arrive_expect_tx(&full[s], kStageA + stage_b);
-                const int kx = (it0 + i) * kBK;
-                tma_load_2d(sA + s * kStageA, &tmA, &full[s], kx, m0);
-                tma_load_2d(sB + s * stage_b, &tmB, &full[s], kx, 0);
+                const int kx = (it0 + (i + rot) % n_it) * kBKS;
+                for (int kb = 0; kb < kKB; ++kb) {
+                    tma_load_2d(sA + s * kStageA + kb * kBoxA, &tmA, &full[s], kx + kb * kBK, m0);
+                    tma_load_2d(sB + s * stage_b + kb * box_b, &tmB, &full[s], kx + kb * kBK, 0);
+                }
                 issued = i + 1;
             }
         }
@@ -163,9 +193,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
                 tc_fence_after();
                 const uint32_t a0 = smem_u32(sA + s * kStageA), b0 = smem_u32(sB + s * stage_b);
 #pragma unroll
-                for (int kk = 0; kk < kBK / 16; ++kk)
-                    mma_bf16(tmem, sdesc_k128(a0 + kk * 32), sdesc_k128(b0 + kk * 32), idesc,
-                             (i > 0 || kk > 0) ? 1u : 0u);
+                for (int kb = 0; kb < kKB; ++kb)
+#pragma unroll
+                    for (int kk = 0; kk < kBK / 16; ++kk)
+                        mma_bf16(tmem, sdesc_k128(a0 + kb * kBoxA + kk * 32), sdesc_k128(b0 + kb * box_b + kk * 32),
+                                 idesc, (i > 0 || kb > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&empty[s]);
             }
             mma_commit(accum);
@@ -336,12 +368,12 @@ uint32_t tmem_cols_of(int n_pad) {
 }
 
 int stages_of(int n_pad) {
-    const int per = kStageA + n_pad * kBK * 2;
+    const int per = kStageA + n_pad * kBKS * 2;
     return std::max(2, std::min(8, kSmemBudget / per));
 }
 
 size_t smem_of(int n_pad, int stages) {
-    return 1024 + static_cast<size_t>(stages) * (kStageA + n_pad * kBK * 2) + (2 * stages + 1) * 8 + 16;
+    return 1024 + static_cast<size_t>(stages) * (kStageA + n_pad * kBKS * 2) + (2 * stages + 1) * 8 + 16;
 }
 
 constexpr int kMaxN = 256;
@@ -357,7 +389,10 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows,
     const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          SPEC_DRAFT_L2PROMO == 0 ? CU_TENSOR_MAP_L2_PROMOTION_NONE
+                          : SPEC_DRAFT_L2PROMO == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
+                                                    : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
@@ -369,7 +404,7 @@ bool draft_tc_supported(int d, int V) {
 
 static int mlp_splits(int d, int d_in) {
     const int m_tiles = (d + kBM - 1) / kBM;
-    const int total = (d_in + kBK - 1) / kBK;
+    const int total = (d_in + kBKS - 1) / kBKS;
     const int want = std::max(1, (2 * device_sm_count() + m_tiles - 1) / m_tiles);
     const int per = (total + want - 1) / want;
     return (total + per - 1) / per;
@@ -399,7 +434,7 @@ spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, cons
                           __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax, float* scratch,
                           int* tickets, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s) {
     const int splits = mlp_splits(d, d_in);
-    const int total_mlp = (d_in + kBK - 1) / kBK;
+    const int total_mlp = (d_in + kBKS - 1) / kBKS;
     const int per_split = (total_mlp + splits - 1) / splits;
     // ---- MLP, activation rows in groups of at most 256 (the MMA's largest N)
     for (int g0 = 0; g0 < R; g0 += kMaxN) {
@@ -437,7 +472,7 @@ spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, cons
         SPEC_CUDA_TRY(make_tmap_bf16_2d(&tb, z + static_cast<size_t>(g0) * d, rows, d, d, n_pad));
         UmmaParams p{};
         p.M = V;
-        p.total_iters = (d + kBK - 1) / kBK;
+        p.total_iters = (d + kBKS - 1) / kBKS;
         p.k_iters = p.total_iters;
         p.n_pad = n_pad;
         p.n_valid = rows;
