@@ -202,6 +202,9 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                                                 float* __restrict__ node_logprob, void* ws, int next_n_int,
                                                 const T* __restrict__ h, const T* __restrict__ emb, int d,
                                                 T* __restrict__ xin) {
+    // the next head's MLP may launch now: it streams its weights and waits for
+    // this kernel's outputs (tokens, input rows) with its own griddep_wait()
+    griddep_launch();
     griddep_wait();
     const int r = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -287,7 +290,6 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
         }
     }
     __syncthreads();
-    griddep_launch();
 
     // 4. children of this row's parent node(s); next depth's input rows
     const int b = cond ? r / n_int : r;
@@ -325,6 +327,7 @@ __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn,
                             const T* __restrict__ h, const T* __restrict__ emb, int d, T* __restrict__ xin,
                             int* __restrict__ tickets, int n_tickets) {
     const int b = blockIdx.x;
+    griddep_launch();   // head 0's MLP may start streaming its weights
     int tok = root_tok[b];
     if (tok < 0 || tok >= V) {
         if (threadIdx.x == 0) flag_status(ws, SPEC_EINVAL);
