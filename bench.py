@@ -482,6 +482,132 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+COMPONENTS = {
+    # name: (workload id, part, tree override)
+    "attention-vicuna7b": (2, "attention", None),
+    "attention-70b-gqa": (4, "attention", None),
+    "attention-32k": (5, "attention", None),
+    "attention-32k-t256": (5, "attention", ("dense_prefix", (4, 4, 4, 4), 256)),
+    "draft-hydra-b4": (3, "draft", None),
+    "accept-greedy-vicuna7b": (2, "accept", None),
+    "accept-rejection-32k": (5, "accept", None),
+}
+
+
+def run_component(args):
+    """Time one entry point on one of the parity workloads (a separate line, not the headline step)."""
+    import torch
+    _, local, _ = dist_info()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    import spec_workloads as wl
+    import tree_speculative_decoding_spec_gb300 as st
+
+    wid, part, tree_spec = COMPONENTS[args.workload]
+    w = wl.WORKLOADS[wid]
+    parent, rank_arr = wl.make_tree(tree_spec or w.tree)
+    T = len(parent)
+    tree = st.spec_tree_build(parent, rank_arr, device=dev)
+
+    def dev_t(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+        return torch.from_numpy(a).to(dev)
+
+    s = 2 if w.dtype == "bf16" else 4
+    flops = 0.0
+    if part == "attention":
+        ax = wl.attention_inputs(w, T)
+        q, kc, vc, plen, kt, vt = (dev_t(ax[k]) for k in ("q", "k_cache", "v_cache", "prefix_len", "k_tree", "v_tree"))
+        out = torch.empty(w.B, w.Hq, T, w.D, dtype=torch.float32, device=dev)
+        lse = torch.empty(w.B, w.Hq, T, dtype=torch.float32, device=dev)
+        ws = torch.empty(st.tree_attention_workspace_size(tree, w.B, w.Hq, w.Hkv, w.Lmax, w.D, 1 if s == 2 else 0),
+                         dtype=torch.uint8, device=dev)
+        call = lambda: st.tree_attention(q, kc, vc, plen, kt, vt, tree, out=out, lse=lse, ws=ws)
+        L = [int(x) for x in ax["prefix_len"]]
+        abytes = (sum(L) * w.Hkv * w.D * 2 * s + w.B * w.Hq * T * w.D * s + w.B * w.Hkv * T * w.D * 2 * s
+                  + w.B * w.Hq * T * (w.D + 1) * 4)
+        flops = 4.0 * w.D * w.Hq * T * sum(l + T for l in L)
+    elif part == "draft":
+        dx = wl.draft_inputs(w)
+        h, E, root = dev_t(dx["h"]), dev_t(dx["E"]), dev_t(dx["root_tok"])
+        W1 = [dev_t(a) for a in dx["W1"]]
+        b1 = [dev_t(a) for a in dx["b1"]]
+        W2 = [dev_t(a) for a in dx["W2"]]
+        cond, topk = list(w.cond), list(w.topk)
+        nt = torch.empty(w.B, T, dtype=torch.int32, device=dev)
+        nl = torch.empty(w.B, T, dtype=torch.float32, device=dev)
+        nlp = torch.empty(w.B, T, dtype=torch.float32, device=dev)
+        ws = torch.empty(st.hydra_draft_workspace_size(tree, w.B, w.d, w.V, cond, topk, 1), dtype=torch.uint8, device=dev)
+        call = lambda: st.hydra_draft(h, E, W1, b1, W2, cond, topk, root, tree, node_tok=nt, node_logit=nl,
+                                      node_logprob=nlp, ws=ws)
+        abytes, d, V = 0.0, w.d, w.V
+        for k in range(len(cond)):
+            n_int = tree.struct.n_internal_at_depth[k]
+            if not n_int:
+                continue
+            rows = w.B * n_int if cond[k] else w.B
+            d_in = d * (2 if cond[k] else 1)
+            abytes += (d * d_in + d + V * d) * s + rows * (d_in + d) * s
+            flops += 2.0 * rows * (d_in * d + d * V)
+    else:
+        B = w.B
+        if w.accept == "greedy":
+            gx = wl.greedy_inputs(w, parent)
+            lp, tok = dev_t(gx["logits_p"]), dev_t(gx["node_tok"])
+            lq = None
+            mode, abytes = 0, B * T * w.V * 4
+        else:
+            rx = wl.rejection_inputs(w, parent, rank_arr)
+            lp, lq, tok = dev_t(rx["logits_p"]), dev_t(rx["logits_q"]), dev_t(rx["node_tok"])
+            mode = 1
+            n_int = sum(tree.struct.n_internal_at_depth[k] for k in range(tree.max_depth + 1))
+            abytes = B * T * w.V * 4 + B * n_int * w.V * 4
+        outs = [torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, tree.max_depth + 1, dtype=torch.int32, device=dev),
+                torch.empty(B, dtype=torch.int32, device=dev), torch.empty(B, dtype=torch.float32, device=dev)]
+        ws = torch.empty(st.tree_accept_workspace_size(mode, tree, B, w.V), dtype=torch.uint8, device=dev)
+        call = lambda: st.tree_accept(mode, lp, lq, tok, tree, temperature=w.temperature, seed=w.philox_seed,
+                                      accept_len=outs[0], accept_path=outs[1], next_token=outs[2], margin=outs[3], ws=ws)
+
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def timed(n):
+        evs = []
+        for _ in range(n):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            call()
+            b.record(stream)
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in evs]
+
+    timed(max(args.warmup, 3))
+    ms = timed(args.steps)
+    st.spec_trace_begin(100000)
+    timed(args.steps)
+    kernels = st.spec_trace_end(64)
+    us = 1000.0 * statistics.median(ms)
+    hbm, tf_burst, _, src = peaks()
+    line = {
+        "workload": args.workload, "config_id": wid, "impl": "ours", "metric": "calls/s", "value": 1e6 / us,
+        "us_per_call": us, "dtype": w.dtype, "steps": args.steps, "tree_nodes": T,
+        "algorithmic_bytes": abytes, "flops": flops,
+        "hbm_GBps": abytes / us / 1e3, "hbm_frac": abytes / us / 1e3 / hbm,
+        "tensor_TFLOPs": flops / us / 1e6 if flops else None,
+        "tensor_frac": (flops / us / 1e6) / tf_burst if flops else None,
+        "roofline_us": max(abytes / hbm / 1e3, flops / tf_burst / 1e6),
+        "peak_source": src,
+        "kernels": {k: {"launches": n, "us_per_launch": 1000.0 * t / n} for k, (n, t) in kernels.items()},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -490,11 +616,15 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--workload", choices=["step"] + sorted(COMPONENTS), default="step",
+                    help="step (default): the headline verification step; otherwise one entry point on one workload")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload != "step":
+        run_component(args)
     else:
         run_ours(args)
 

@@ -28,6 +28,7 @@ namespace accept {
 
 constexpr int kRowThreads = 256;
 constexpr int kWalkThreads = 1024;
+constexpr int kLseIter = 16;   // 4-wide loads per thread and operand: a slice holds <= 256*4*16 tokens
 
 struct Plan {
     int slices, slice;
@@ -40,6 +41,8 @@ Plan make_plan(const spec_tree* t, int B, int V) {
     const int64_t target = 2ll * device_sm_count();
     const int max_slices = std::max(1, V / 2048);
     p.slices = static_cast<int>(std::min<int64_t>(std::max<int64_t>((target + rows - 1) / rows, 1), max_slices));
+    // the rejection row kernel keeps a thread's values in registers: <= 16384 tokens per slice
+    p.slices = std::max(p.slices, (V + kRowThreads * 4 * kLseIter - 1) / (kRowThreads * 4 * kLseIter));
     p.slice = static_cast<int>(round_up((V + p.slices - 1) / p.slices, 4));
     p.slices = (V + p.slice - 1) / p.slice;
     p.off_part = kWsHeader;
@@ -95,9 +98,35 @@ __global__ void __launch_bounds__(kRowThreads) k_rows_greedy(const float* __rest
 
 // ---------------------------------------------------------------- rows (rejection)
 
-__device__ __forceinline__ void lse_push(float& m, float& s, float v) {
-    if (v > m) { s = s * expf(m - v) + 1.f; m = v; }
-    else s += expf(v - m);
+// (max, sum exp(x - max)) of x = logits * inv_temp over this thread's share of
+// [v0, v1): the values are held in registers, so one HBM pass and no branches.
+__device__ __forceinline__ float2 thread_lse(const float* __restrict__ row, int v0, int v1, float inv_temp, bool vec4) {
+    float x[4 * kLseIter];
+    float m = -INFINITY;
+    if (vec4) {
+#pragma unroll
+        for (int it = 0; it < kLseIter; ++it) {
+            const int e = v0 + 4 * (static_cast<int>(threadIdx.x) + kRowThreads * it);
+            float4 q = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (e < v1) q = __ldcs(reinterpret_cast<const float4*>(row + e));
+            x[4 * it] = q.x * inv_temp; x[4 * it + 1] = q.y * inv_temp;
+            x[4 * it + 2] = q.z * inv_temp; x[4 * it + 3] = q.w * inv_temp;
+            m = fmaxf(m, fmaxf(fmaxf(x[4 * it], x[4 * it + 1]), fmaxf(x[4 * it + 2], x[4 * it + 3])));
+        }
+    } else {
+#pragma unroll
+        for (int it = 0; it < 4 * kLseIter; ++it) {
+            const int e = v0 + static_cast<int>(threadIdx.x) + kRowThreads * it;
+            x[it] = e < v1 ? row[e] * inv_temp : -INFINITY;
+            m = fmaxf(m, x[it]);
+        }
+    }
+    float s = 0.f;
+    if (m != -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < 4 * kLseIter; ++i) s += expf(x[i] - m);
+    }
+    return make_float2(m, s);
 }
 
 __global__ void __launch_bounds__(kRowThreads) k_rows_lse(const float* __restrict__ lp, const float* __restrict__ lq,
@@ -109,25 +138,13 @@ __global__ void __launch_bounds__(kRowThreads) k_rows_lse(const float* __restric
     const int u = static_cast<int>(row % Tn);
     const bool internal = child_off[u + 1] > child_off[u];
     const int v0 = sl * slice, v1 = min(V, v0 + slice);
-    float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
-    const float* xp = lp + row * V;
-    const float* xq = lq + row * V;
-    if ((V & 3) == 0) {
-        for (int e = v0 + 4 * threadIdx.x; e < v1; e += 4 * kRowThreads) {
-            const float4 a = __ldcs(reinterpret_cast<const float4*>(xp + e));
-            lse_push(mp, sp, a.x * inv_temp); lse_push(mp, sp, a.y * inv_temp);
-            lse_push(mp, sp, a.z * inv_temp); lse_push(mp, sp, a.w * inv_temp);
-            if (internal) {
-                const float4 c = __ldcs(reinterpret_cast<const float4*>(xq + e));
-                lse_push(mq, sq, c.x * inv_temp); lse_push(mq, sq, c.y * inv_temp);
-                lse_push(mq, sq, c.z * inv_temp); lse_push(mq, sq, c.w * inv_temp);
-            }
-        }
-    } else {
-        for (int e = v0 + threadIdx.x; e < v1; e += kRowThreads) {
-            lse_push(mp, sp, xp[e] * inv_temp);
-            if (internal) lse_push(mq, sq, xq[e] * inv_temp);
-        }
+    const bool vec4 = (V & 3) == 0;
+    const float2 P = thread_lse(lp + row * V, v0, v1, inv_temp, vec4);
+    float mp = P.x, sp = P.y, mq = -INFINITY, sq = 0.f;
+    if (internal) {
+        const float2 Q = thread_lse(lq + row * V, v0, v1, inv_temp, vec4);
+        mq = Q.x;
+        sq = Q.y;
     }
     for (int o = 16; o > 0; o >>= 1) {
         lse_merge(mp, sp, __shfl_xor_sync(0xffffffffu, mp, o), __shfl_xor_sync(0xffffffffu, sp, o));
@@ -266,7 +283,6 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
     __shared__ float dmar[SPEC_MAX_T];
     __shared__ int iscr[32];
     __shared__ float fscr[32];
-    __shared__ float seg_excl[kWalkThreads];
     for (int u = threadIdx.x; u < Tn; u += blockDim.x) {
         const float4* pr = part + (static_cast<size_t>(b) * Tn + u) * slices;
         float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
@@ -313,58 +329,100 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
         if (!resid) return pv;
         return fmaxf(pv - expf(rq[x] * inv_temp - lsq), 0.f);
     };
-    const int seg = (V + kWalkThreads - 1) / kWalkThreads;
-    const int x0 = min(V, threadIdx.x * seg), x1 = min(V, x0 + seg);
+    // Draw: warp w owns the contiguous token range [w*Rw, (w+1)*Rw); each warp sums its range
+    // with coalesced loads, warp 0 scans the 32 range sums, the warp holding the target
+    // scans its range 32 tokens at a time (ascending token order throughout).
+    __shared__ float wsum[32], wexcl[32];
+    __shared__ float s_total, s_target;
+    __shared__ int s_wstar, pick;
+    __shared__ float smar;
+    const int wid = threadIdx.x >> 5, ln = threadIdx.x & 31;
+    const int Rw = ((V + 31) / 32 + 31) / 32 * 32;
+    const int w0 = min(V, wid * Rw), w1 = min(V, w0 + Rw);
     bool resid = !leaf;
-    float ssum = 0.f;
-    for (int x = x0; x < x1; ++x) ssum += weight(x, resid);
+    auto range_sum = [&](bool rs) {
+        float acc = 0.f;
+        for (int x = w0 + ln; x < w1; x += 32) acc += weight(x, rs);
+        return warp_sum(acc);
+    };
+    float my = range_sum(resid);
+    if (ln == 0) wsum[wid] = my;
+    __syncthreads();
     if (resid) {
-        const float total_r = block_sum_f(ssum, fscr);
-        if (total_r == 0.f) {   // alpha = 1: no residual mass, fall back to p
+        float tot = 0.f;
+        for (int i = 0; i < 32; ++i) tot += wsum[i];
+        if (tot == 0.f) {   // alpha = 1: no residual mass, fall back to p
             resid = false;
-            ssum = 0.f;
-            for (int x = x0; x < x1; ++x) ssum += weight(x, resid);
+            __syncthreads();
+            my = range_sum(false);
+            if (ln == 0) wsum[wid] = my;
+            __syncthreads();
         }
     }
-    // exclusive scan of the per-thread segment sums (thread order = token order)
-    seg_excl[threadIdx.x] = ssum;
-    __syncthreads();
-    for (int off = 1; off < kWalkThreads; off <<= 1) {
-        const float add = threadIdx.x >= off ? seg_excl[threadIdx.x - off] : 0.f;
-        __syncthreads();
-        seg_excl[threadIdx.x] += add;
-        __syncthreads();
-    }
-    const float total = seg_excl[kWalkThreads - 1];
-    const float excl = seg_excl[threadIdx.x] - ssum;
     const float u1 = uniform24(spec_draw(seed, offset, 0u, static_cast<uint32_t>(b)).w[1]);
-    const float target = u1 * total;
-    const float need = target - excl;
-    const bool here = ssum > 0.f && ssum > need;
-    const int first = block_min_int(here ? static_cast<int>(threadIdx.x) : kWalkThreads, iscr);
-    __shared__ int pick;
-    __shared__ float smar;
-    if (first == kWalkThreads) {
+    if (wid == 0) {
+        const float v = wsum[ln];
+        float inc = v;
+        for (int o = 1; o < 32; o <<= 1) {
+            const float t = __shfl_up_sync(0xffffffffu, inc, o);
+            if (ln >= o) inc += t;
+        }
+        wexcl[ln] = inc - v;
+        const float total = __shfl_sync(0xffffffffu, inc, 31);
+        const float target = u1 * total;
+        const unsigned hit = __ballot_sync(0xffffffffu, v > 0.f && v > target - (inc - v));
+        if (ln == 0) {
+            s_total = total;
+            s_target = target;
+            s_wstar = hit ? __ffs(hit) - 1 : -1;
+        }
+    }
+    __syncthreads();
+    const int wstar = s_wstar;
+    if (wstar < 0) {
         // target at or beyond the total (rounding): take the last token of positive weight
-        const int last = block_max_int(ssum > 0.f ? static_cast<int>(threadIdx.x) : -1, iscr);
-        if (static_cast<int>(threadIdx.x) == last) {
-            int xs = x0;
-            for (int x = x0; x < x1; ++x) if (weight(x, resid) > 0.f) xs = x;
-            pick = xs;
+        int lastx = -1;
+        for (int x = threadIdx.x; x < V; x += blockDim.x)
+            if (weight(x, resid) > 0.f) lastx = x;
+        lastx = block_max_int(lastx, iscr);
+        if (threadIdx.x == 0) {
+            pick = max(lastx, 0);
             smar = 0.f;
         }
-    } else if (static_cast<int>(threadIdx.x) == first) {
-        float run = 0.f;
-        int xs = x1 - 1;
-        float lo = 0.f, hi = 0.f;
-        for (int x = x0; x < x1; ++x) {
-            const float w = weight(x, resid);
-            lo = run;
-            run += w;
-            if (run > need) { xs = x; hi = run; break; }
+    } else if (wid == wstar) {
+        const float need = s_target - wexcl[wstar];
+        float run = 0.f, lo = 0.f, hi = 0.f;
+        int found = -1, lastpos = -1;
+        for (int base = w0; base < w1; base += 32) {
+            const int x = base + ln;
+            const float wv = x < w1 ? weight(x, resid) : 0.f;
+            float inc = wv;
+            for (int o = 1; o < 32; o <<= 1) {
+                const float t = __shfl_up_sync(0xffffffffu, inc, o);
+                if (ln >= o) inc += t;
+            }
+            const float cum = run + inc;
+            const unsigned hit = __ballot_sync(0xffffffffu, wv > 0.f && cum > need);
+            const unsigned pos = __ballot_sync(0xffffffffu, wv > 0.f);
+            if (pos) lastpos = base + 31 - __clz(pos);
+            if (hit) {
+                const int l = __ffs(hit) - 1;
+                found = base + l;
+                hi = __shfl_sync(0xffffffffu, cum, l);
+                lo = hi - __shfl_sync(0xffffffffu, wv, l);
+                break;
+            }
+            run += __shfl_sync(0xffffffffu, inc, 31);
         }
-        pick = xs;
-        smar = fminf(hi - need, need - lo) / total;
+        if (ln == 0) {
+            if (found < 0) {   // rounding left the target past this range's last positive token
+                pick = lastpos;
+                smar = 0.f;
+            } else {
+                pick = found;
+                smar = fminf(hi - need, need - lo) / s_total;
+            }
+        }
     }
     __syncthreads();
     if (threadIdx.x == 0) {

@@ -225,20 +225,26 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             tmem_ld32(lane_base + s_col, sa);
             tmem_ld32(lane_base + s_col + 32, sb);
             tmem_ld_wait();
-            uint64_t bits;
-            if (j >= n_pt) {   // tree keys: only the node's ancestors (and itself)
-                const int t = j - n_pt;
-                const int nvalid = min(kAKeys, p.T - t * kAKeys);
-                bits = (nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull)) & anc_row[t];
-            } else {           // prefix keys below prefix_len
-                const int nvalid = min(kAKeys, pre_end - (pre_begin + j * kAKeys));
-                bits = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
-            }
+            // raw scores (the scale is applied inside the exponent: scale > 0 keeps the order);
+            // masking only on tree tiles and on a partial last prefix tile (tile-uniform branch)
             float sv[64];
+            const bool tree_tile = j >= n_pt;
+            const int nvalid = tree_tile ? min(kAKeys, p.T - (j - n_pt) * kAKeys)
+                                         : min(kAKeys, pre_end - (pre_begin + j * kAKeys));
+            if (!tree_tile && nvalid == kAKeys) {
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-                sv[e] = ((bits >> e) & 1ull) ? __uint_as_float(sa[e]) * p.scale_log2 : -INFINITY;
-                sv[32 + e] = ((bits >> (32 + e)) & 1ull) ? __uint_as_float(sb[e]) * p.scale_log2 : -INFINITY;
+                for (int e = 0; e < 32; ++e) {
+                    sv[e] = __uint_as_float(sa[e]);
+                    sv[32 + e] = __uint_as_float(sb[e]);
+                }
+            } else {
+                uint64_t bits = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
+                if (tree_tile) bits &= anc_row[j - n_pt];   // only the node's ancestors (and itself)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    sv[e] = ((bits >> e) & 1ull) ? __uint_as_float(sa[e]) : -INFINITY;
+                    sv[32 + e] = ((bits >> (32 + e)) & 1ull) ? __uint_as_float(sb[e]) : -INFINITY;
+                }
             }
             float mx[16];
 #pragma unroll
@@ -247,7 +253,7 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             for (int w2 = 8; w2 > 0; w2 >>= 1)
 #pragma unroll
                 for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
-            const float tmax = mx[0];
+            const float tmax = mx[0] * p.scale_log2;   // base-2 units
             // lazy rescale: keep the old reference maximum unless the row max grew by > 2^8
             float m_new = m_used, alpha = 1.f;
             bool rescale = false;
@@ -277,10 +283,10 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                 l *= alpha;
             }
             m_used = m_new;
-            // P = 2^(s - m_used) in bf16, 128-byte swizzled row (16-byte chunk q at q ^ (r % 8));
-            // the row sum uses the rounded values the MMA will see
+            // P = 2^(scale * s - m_used) in bf16 (one FFMA + ex2 per score), 128-byte swizzled
+            // row (16-byte chunk q at q ^ (r % 8)); the row sum in fp32 over 8 partial sums
             uint8_t* prow = sP + grp * kPBytes + r * 128;
-            const float mref = m_used == -INFINITY ? 0.f : m_used;
+            const float nmref = m_used == -INFINITY ? 0.f : -m_used;
             float ps[8];
 #pragma unroll
             for (int qc = 0; qc < 8; ++qc) {
@@ -289,8 +295,10 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
 #pragma unroll
                 for (int h2 = 0; h2 < 4; ++h2) {
                     const int e0 = qc * 8 + 2 * h2;
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(ex2(sv[e0] - mref), ex2(sv[e0 + 1] - mref));
-                    acc += __low2float(pr) + __high2float(pr);
+                    const float a0 = ex2(fmaf(sv[e0], p.scale_log2, nmref));
+                    const float a1 = ex2(fmaf(sv[e0 + 1], p.scale_log2, nmref));
+                    acc += a0 + a1;
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(a0, a1);
                     packed[h2] = *reinterpret_cast<const uint32_t*>(&pr);
                 }
                 ps[qc] = acc;

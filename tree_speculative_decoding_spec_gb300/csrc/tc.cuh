@@ -190,13 +190,28 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
     return idesc_bf16_f32(M, N) | (1u << 16);
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` while the phase is pending.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait that also gives up as soon as another thread of the CTA raised
+// *abort_flag; pending threads suspend (20 us hint) instead of spinning on issue slots.
 __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                                   uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && (*abort_flag || globaltimer_ns() - t0 > limit_ns)) return false;
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+        if ((i & 15u) == 15u && (*abort_flag || globaltimer_ns() - t0 > limit_ns)) return false;
     }
 }
 
