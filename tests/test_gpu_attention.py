@@ -34,6 +34,8 @@ CASES = [
     ("bf16", 3, 6, 2, ("random", 70), 128, 300, [1, 150, 300]),     # two mask words
     ("bf16", 2, 2, 2, ("random", 130), 64, 64, [64, 7]),            # three mask words
     ("bf16", 1, 32, 32, ("sparse", (8, 4, 2, 1), 64, 64), 128, 1024, [1024]),
+    ("bf16", 2, 4, 2, ("random", 200), 128, 700, [333, 700]),       # two tree tiles, four mask words
+    ("bf16", 1, 2, 1, ("random", 130), 128, 257, [257]),            # second tree tile: one mask word
 ]
 
 
@@ -99,3 +101,29 @@ def test_attention_is_deterministic_and_respects_scale():
     assert np.array_equal(a, b)
     O, _ = oracle.tree_attention(**x, tree=oracle.tree_encode(parent, rank), dtype="f32", scale=0.05)
     assert_close(a, O, "f32", "out")
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,T", [("bf16", 4, 2, 100), ("f32", 4, 2, 20), ("bf16", 8, 8, 3)])
+def test_attention_ignores_cache_past_prefix(dtype, Hq, Hkv, T):
+    """Cache slots at or past prefix_len[b] hold NaN: no output may depend on them."""
+    st = lib()
+    rng = np.random.default_rng(11 + T)
+    parent, rank = wl.random_tree(rng, T, max_children=3)
+    tree = st.spec_tree_build(parent, rank)
+    Lmax, prefix = 520, [1, 200, 519]
+    x = _rand_inputs(rng, dtype, len(prefix), Hq, Hkv, T, 128, Lmax, prefix)
+    nan = wl.f32_to_bf16_bits(np.float32(np.nan)) if dtype == "bf16" else np.float32(np.nan)
+    for b, L in enumerate(prefix):
+        x["k_cache"][b, :, L:] = nan
+        x["v_cache"][b, :, L:] = nan
+    out, lse = _run(st, x, tree, dtype)
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+    clean = dict(x)
+    clean["k_cache"] = x["k_cache"].copy()
+    clean["v_cache"] = x["v_cache"].copy()
+    for b, L in enumerate(prefix):
+        clean["k_cache"][b, :, L:] = 0
+        clean["v_cache"][b, :, L:] = 0
+    O, Lse = oracle.tree_attention(**clean, tree=oracle.tree_encode(parent, rank), dtype=dtype)
+    assert_close(out, O, dtype, "out")
+    assert_close(lse, Lse, dtype, "lse")

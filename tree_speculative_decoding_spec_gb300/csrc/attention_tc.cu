@@ -9,18 +9,24 @@
 // CTA holding the last non-empty prefix split of a sequence also takes the
 // tree keys.  The query rows of a KV head are its g query heads x T nodes,
 // contiguous in q [B, Hq, T, D], so one 2-D TMA box fetches them.  Ten warps:
-//   warp 8    TMA: the 128 x 128 Q tile once, then a 3-stage ring of 64-key
+//   warp 8    TMA: the 128 x 128 Q tile once, then a 3-stage ring of 128-key
 //             K and V tiles (128-byte swizzle), prefix tiles then tree tiles
-//   warp 9    MMA: S_j = Q K_j^T into TMEM score buffer j % 2 (M 128, N 64,
-//             K 128) and O_{j%2} += P_j V_j (M 128, N 128, K 64, V read as an
-//             MN-major operand)
+//   warp 9    MMA: S_j = Q K_j^T into TMEM score buffer j % 2 (M 128, N 128,
+//             K 128, both operands in shared memory) and O_{j%2} += P_j V_j
+//             (M 128, N 128, K 128) with P_j read from TMEM and V as an
+//             MN-major shared-memory operand
 //   warps 0-3 / 4-7: two softmax groups; group j % 2 owns tile j.  One thread
 //             per query row reads S_j from TMEM, masks (prefix length,
 //             ancestor bits), keeps its group's running maximum and sum in
 //             base 2 (O is rescaled in TMEM only when the maximum grows by
-//             more than 2^8) and writes bf16 P_j to a swizzled shared tile.
-//             At the end group 0 merges the two groups' (max, sum, O) and
-//             writes the split's partial.
+//             more than 2^8) and writes P_j as bf16 pairs over the first 64
+//             columns of its own score buffer.  At the end group 0 merges the
+//             two groups' (max, sum, O) and writes the split's partial.
+// The tensor pipe runs its MMAs in issue order, so S_{j+2} may overwrite the
+// buffer PV_j reads, and the completion of S_j implies that of PV_{j-2}.
+// Cache rows past the prefix length inside the last prefix tile are zeroed in
+// shared memory before PV reads them (their scores are masked, and a stale
+// non-finite value times a zero weight would still poison O).
 // Waits are bounded (2 s); on expiry SPEC_ETIMEOUT goes to the status word and
 // the CTA drains its own loads and MMAs before freeing TMEM.
 #include <algorithm>
@@ -32,16 +38,17 @@ namespace spec {
 namespace tc {
 
 constexpr int kARows = 128;        // query rows per CTA (MMA M)
-constexpr int kAKeys = 64;         // keys per tile
+constexpr int kAKeys = 128;        // keys per tile
 constexpr int kAD = 128;           // head dim
 constexpr int kAStages = 3;
 constexpr int kAThreads = 320;
 constexpr int kQBytes = 2 * kARows * 128;         // two 64-column halves of 128 rows
-constexpr int kKVHalf = kAKeys * 128;             // one 64-column half of a 64-key tile
+constexpr int kKVHalf = kAKeys * 128;             // one 64-column half of a 128-key tile
 constexpr int kStageBytes = 4 * kKVHalf;          // K and V, two halves each
-constexpr int kPBytes = kARows * 128;             // 128 rows x 64 bf16
-constexpr size_t kASmem = 1024 + kQBytes + kAStages * kStageBytes + 2 * kPBytes + 2048;
-constexpr uint32_t kATmemCols = 512;              // S0 [0,64) S1 [64,128) O0 [128,256) O1 [256,384)
+constexpr size_t kASmem = 1024 + kQBytes + kAStages * kStageBytes + 2048;
+constexpr uint32_t kATmemCols = 512;              // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
+constexpr uint32_t kAO = 2 * kAKeys;              // first O column
+static_assert(kASmem <= 232448, "shared memory of one CTA");
 
 struct AttnTcParams {
     int T, g, Hq, Hkv, Lmax, words;
@@ -85,15 +92,13 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sQ = smem;
     uint8_t* sKV = sQ + kQBytes;                       // stage s: K half0, K half1, V half0, V half1
-    uint8_t* sP = sKV + kAStages * kStageBytes;        // P buffers of group 0 and group 1
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sP + 2 * kPBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + kAStages * kStageBytes);
     uint64_t* q_full = bars;
     uint64_t* kv_full = bars + 1;
     uint64_t* kv_empty = kv_full + kAStages;
     uint64_t* s_full = kv_empty + kAStages;            // [group]
     uint64_t* p_full = s_full + 2;                     // [group]
-    uint64_t* pv_done = p_full + 2;                    // [group]
-    uint64_t* o_final = pv_done + 2;
+    uint64_t* o_final = p_full + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float2* merge = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(bars) + 256);   // [128] group 1's (m, l)
@@ -108,7 +113,6 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], kARows);
-            mbar_init(&pv_done[i], 1);
         }
         mbar_init(o_final, 1);
         *abort_flag = 0;
@@ -185,18 +189,18 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (!mbar_wait_or_abort(&p_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
-                // O_{j%2} += P_j V_j: K = 64 keys in 4 steps of 16; V is MN-major (d contiguous):
-                // 64-wide d halves 8 KB apart, 8-key atoms 1 KB apart
-                const uint32_t pa = smem_u32(sP + (j & 1) * kPBytes);
+                // O_{j%2} += P_j V_j: K = 128 keys in 8 steps of 16.  P_j: bf16 pairs in the first
+                // 64 columns of score buffer j % 2 (8 columns per step).  V is MN-major (d
+                // contiguous): 64-wide d halves kKVHalf apart, 8-key atoms 1 KB apart.
+                const uint32_t pa = tmem + (j & 1) * kAKeys;
                 const uint32_t v0 = smem_u32(sKV + (j % kAStages) * kStageBytes + 2 * kKVHalf);
-                const uint32_t o = tmem + 2 * kAKeys + (j & 1) * kAD;
+                const uint32_t o = tmem + kAO + (j & 1) * kAD;
 #pragma unroll
                 for (int ks = 0; ks < kAKeys / 16; ++ks)
-                    mma_bf16(o, sdesc_k128(pa + ks * 32), sdesc_mn128(v0 + ks * 2048, kKVHalf, 1024), idesc_o,
-                             (j >= 2 || ks > 0) ? 1u : 0u);
-                mma_commit(&pv_done[j & 1]);
+                    mma_bf16_ts(o, pa + ks * 8, sdesc_mn128(v0 + ks * 2048, kKVHalf, 1024), idesc_o,
+                                (j >= 2 || ks > 0) ? 1u : 0u);
                 mma_commit(&kv_empty[j % kAStages]);
-                // the score buffer of this group is free once its P_j is written (p_full_j passed)
+                // in issue order after PV_j, so S_{j+2} may overwrite P_j
                 if (j + 2 < n_tiles && !issue_s(j + 2)) { ok = false; break; }
             }
             if (!ok) {
@@ -213,48 +217,61 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
         const int node = rg % p.T;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16);
         const uint32_t s_col = grp * kAKeys;
-        const uint32_t o_col = 2 * kAKeys + grp * kAD;
+        const uint32_t o_col = kAO + grp * kAD;
         const uint64_t* anc_row = p.anc + static_cast<size_t>(node) * p.words;
         float m_used = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = grp; j < n_tiles; j += 2) {
+            // S_j complete also means PV_{j-2} (same O, same buffer) is complete
             ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&s_full[grp], (j >> 1) & 1, abort_flag));
             if (!ok) break;
             tc_fence_after();
-            uint32_t sa[32], sb[32];
-            tmem_ld32(lane_base + s_col, sa);
-            tmem_ld32(lane_base + s_col + 32, sb);
+            uint32_t s0[32], s1[32], s2[32], s3[32];
+            tmem_ld32(lane_base + s_col, s0);
+            tmem_ld32(lane_base + s_col + 32, s1);
+            tmem_ld32(lane_base + s_col + 64, s2);
+            tmem_ld32(lane_base + s_col + 96, s3);
             tmem_ld_wait();
+            auto sraw = [&](int e) -> uint32_t {
+                return e < 32 ? s0[e] : e < 64 ? s1[e - 32] : e < 96 ? s2[e - 64] : s3[e - 96];
+            };
             // raw scores (the scale is applied inside the exponent: scale > 0 keeps the order);
             // masking only on tree tiles and on a partial last prefix tile (tile-uniform branch)
-            float sv[64];
+            float sv[kAKeys];
             const bool tree_tile = j >= n_pt;
             const int nvalid = tree_tile ? min(kAKeys, p.T - (j - n_pt) * kAKeys)
                                          : min(kAKeys, pre_end - (pre_begin + j * kAKeys));
             if (!tree_tile && nvalid == kAKeys) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    sv[e] = __uint_as_float(sa[e]);
-                    sv[32 + e] = __uint_as_float(sb[e]);
-                }
+                for (int e = 0; e < kAKeys; ++e) sv[e] = __uint_as_float(sraw(e));
             } else {
-                uint64_t bits = nvalid >= 64 ? ~0ull : ((1ull << nvalid) - 1ull);
-                if (tree_tile) bits &= anc_row[j - n_pt];   // only the node's ancestors (and itself)
+                uint64_t bits[2];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    sv[e] = ((bits >> e) & 1ull) ? __uint_as_float(sa[e]) : -INFINITY;
-                    sv[32 + e] = ((bits >> (32 + e)) & 1ull) ? __uint_as_float(sb[e]) : -INFINITY;
+                for (int w = 0; w < 2; ++w) {
+                    const int nv = min(max(nvalid - 64 * w, 0), 64);
+                    bits[w] = nv >= 64 ? ~0ull : ((1ull << nv) - 1ull);
                 }
+                if (tree_tile) {   // only the node's ancestors (and itself)
+                    const int w0 = 2 * (j - n_pt);
+                    bits[0] &= anc_row[w0];
+                    bits[1] &= (w0 + 1 < p.words) ? anc_row[w0 + 1] : 0ull;
+                }
+#pragma unroll
+                for (int e = 0; e < kAKeys; ++e)
+                    sv[e] = ((bits[e >> 6] >> (e & 63)) & 1ull) ? __uint_as_float(sraw(e)) : -INFINITY;
             }
             float mx[16];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) mx[e] = fmaxf(fmaxf(sv[e], sv[e + 16]), fmaxf(sv[e + 32], sv[e + 48]));
+            for (int e = 0; e < 16; ++e)
+                mx[e] = fmaxf(fmaxf(fmaxf(sv[e], sv[e + 16]), fmaxf(sv[e + 32], sv[e + 48])),
+                              fmaxf(fmaxf(sv[e + 64], sv[e + 80]), fmaxf(sv[e + 96], sv[e + 112])));
 #pragma unroll
             for (int w2 = 8; w2 > 0; w2 >>= 1)
 #pragma unroll
                 for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
             const float tmax = mx[0] * p.scale_log2;   // base-2 units
-            // lazy rescale: keep the old reference maximum unless the row max grew by > 2^8
+            // lazy rescale: keep the old reference maximum unless the row max grew by > 2^8; the
+            // TMEM accesses are warp-collective, so a warp rescales together (alpha = 1 for the rest)
             float m_new = m_used, alpha = 1.f;
             bool rescale = false;
             if (tmax > m_used + 8.f) {
@@ -264,48 +281,52 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                 }
                 m_new = tmax;
             }
-            if (j >= 2) {   // PV_{j-2} (same O, same P buffer) must be done
-                ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&pv_done[grp], ((j - 2) >> 1) & 1, abort_flag));
-                if (!ok) break;
-                tc_fence_after();
-            }
             if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
-                for (int cc = 0; cc < kAD / 32; ++cc) {
-                    uint32_t o[32];
-                    tmem_ld32(lane_base + o_col + cc * 32, o);
+                for (int cc = 0; cc < kAD / 16; ++cc) {
+                    uint32_t o[16];
+                    tmem_ld16(lane_base + o_col + cc * 16, o);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-                    tmem_st32(lane_base + o_col + cc * 32, o);
+                    for (int e = 0; e < 16; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                    tmem_st16(lane_base + o_col + cc * 16, o);
                 }
-                tmem_st_wait();
                 l *= alpha;
             }
             m_used = m_new;
-            // P = 2^(scale * s - m_used) in bf16 (one FFMA + ex2 per score), 128-byte swizzled
-            // row (16-byte chunk q at q ^ (r % 8)); the row sum in fp32 over 8 partial sums
-            uint8_t* prow = sP + grp * kPBytes + r * 128;
+            // P = 2^(scale * s - m_used) in bf16 (one FFMA + ex2 per score), written over the
+            // first 64 columns of this group's score buffer; row sum in fp32 over 4 partials
             const float nmref = m_used == -INFINITY ? 0.f : -m_used;
-            float ps[8];
+            float ps[4];
 #pragma unroll
-            for (int qc = 0; qc < 8; ++qc) {
-                uint32_t packed[4];
+            for (int qc = 0; qc < 4; ++qc) {
+                uint32_t packed[16];
                 float acc = 0.f;
 #pragma unroll
-                for (int h2 = 0; h2 < 4; ++h2) {
-                    const int e0 = qc * 8 + 2 * h2;
+                for (int h2 = 0; h2 < 16; ++h2) {
+                    const int e0 = qc * 32 + 2 * h2;
                     const float a0 = ex2(fmaf(sv[e0], p.scale_log2, nmref));
                     const float a1 = ex2(fmaf(sv[e0 + 1], p.scale_log2, nmref));
                     acc += a0 + a1;
-                    const __nv_bfloat162 pr = __floats2bfloat162_rn(a0, a1);
+                    const __nv_bfloat162 pr = __floats2bfloat162_rn(a0, a1);   // .x (lower key) low
                     packed[h2] = *reinterpret_cast<const uint32_t*>(&pr);
                 }
                 ps[qc] = acc;
-                *reinterpret_cast<uint4*>(prow + ((qc ^ (r & 7)) * 16)) = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                tmem_st16(lane_base + s_col + qc * 16, packed);
             }
-            l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            fence_proxy_async_smem();
+            l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+            if (!tree_tile && nvalid < kAKeys) {
+                // zero the V rows past the prefix (both 64-column halves) before PV_j reads them
+                uint8_t* sv_tile = sKV + (j % kAStages) * kStageBytes + 2 * kKVHalf;
+                const int r_in = (warp & 3) * 32 + lane;
+                for (int i = r_in; i < (kAKeys - nvalid) * 16; i += kARows) {
+                    const int row = nvalid + (i >> 4);
+                    *reinterpret_cast<uint4*>(sv_tile + ((i >> 3) & 1) * kKVHalf + row * 128 + (i & 7) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+            }
+            tmem_st_wait();
             tc_fence_before();
             mbar_arrive(&p_full[grp]);
         }
@@ -335,8 +356,8 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
 #pragma unroll 1
             for (int cc = 0; cc < kAD / 32; ++cc) {
                 uint32_t o0[32], o1[32];
-                tmem_ld32(lane_base + 2 * kAKeys + cc * 32, o0);
-                tmem_ld32(lane_base + 2 * kAKeys + kAD + cc * 32, o1);
+                tmem_ld32(lane_base + kAO + cc * 32, o0);
+                tmem_ld32(lane_base + kAO + kAD + cc * 32, o1);
                 tmem_ld_wait();
                 if (valid) {
 #pragma unroll

@@ -10,7 +10,7 @@ namespace tc {
 
 struct AttnTcPlan {
     int n_rb = 0;       // 128-row query blocks per KV head
-    int chunk = 0;      // prefix keys per split (multiple of 64)
+    int chunk = 0;      // prefix keys per split (multiple of 128)
     int n_pre = 0;      // prefix splits; split n_pre holds the tree keys
     size_t part_bytes = 0;
 };
