@@ -97,14 +97,15 @@ __global__ void __launch_bounds__(256) k_gemm_fma(const T* __restrict__ W, const
 
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) { return va > vb || (va == vb && ia < ib); }
 
-// Insert (v, i) into a descending list of length k (registers, fully unrolled).
+// Insert (v, i) into a descending list of KMAX candidates (registers, every
+// index static); callers keep KMAX >= k and use the first k.
 template <int KMAX>
-__device__ __forceinline__ void insert_topk(float (&lv)[KMAX], int (&li)[KMAX], int k, float v, int i) {
-    if (!better(v, i, lv[k - 1], li[k - 1])) return;
+__device__ __forceinline__ void insert_topk(float (&lv)[KMAX], int (&li)[KMAX], float v, int i) {
+    if (!better(v, i, lv[KMAX - 1], li[KMAX - 1])) return;
 #pragma unroll
     for (int s = KMAX - 1; s > 0; --s) {
-        if (s < k && better(v, i, lv[s - 1], li[s - 1])) { lv[s] = lv[s - 1]; li[s] = li[s - 1]; }
-        else if (s < k && better(v, i, lv[s], li[s])) { lv[s] = v; li[s] = i; }
+        if (better(v, i, lv[s - 1], li[s - 1])) { lv[s] = lv[s - 1]; li[s] = li[s - 1]; }
+        else if (better(v, i, lv[s], li[s])) { lv[s] = v; li[s] = i; }
     }
     if (better(v, i, lv[0], li[0])) { lv[0] = v; li[0] = i; }
 }
@@ -125,13 +126,14 @@ __global__ void __launch_bounds__(256) k_topk_slices(const float* __restrict__ l
     float m = -INFINITY, ssum = 0.f;
     for (int x = v0 + threadIdx.x; x < v1; x += blockDim.x) {
         const float v = row[x];
-        insert_topk<KMAX>(lv, li, k, v, x);
+        insert_topk<KMAX>(lv, li, v, x);
         if (v > m) { ssum = ssum * expf(m - v) + 1.f; m = v; }
         else ssum += expf(v - m);
     }
     __shared__ Cand sc[256 * KMAX];
     __shared__ float2 sl2[256];
-    for (int s = 0; s < k; ++s) sc[threadIdx.x * KMAX + s] = Cand{lv[s], li[s]};
+#pragma unroll
+    for (int s = 0; s < KMAX; ++s) sc[threadIdx.x * KMAX + s] = Cand{lv[s], li[s]};
     sl2[threadIdx.x] = make_float2(m, ssum);
     __syncthreads();
     if (threadIdx.x == 0) {

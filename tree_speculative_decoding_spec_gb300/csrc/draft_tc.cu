@@ -86,23 +86,6 @@ __device__ __forceinline__ bool cbetter(float va, int ia, float vb, int ib) {
     return va > vb || (va == vb && ia < ib);
 }
 
-template <int KMAX>
-__device__ __forceinline__ void push_topk(float (&lv)[KMAX], int (&li)[KMAX], int k, float v, int i) {
-    if (!cbetter(v, i, lv[k - 1], li[k - 1])) return;
-#pragma unroll
-    for (int s = KMAX - 1; s > 0; --s) {
-        if (s < k && cbetter(v, i, lv[s - 1], li[s - 1])) { lv[s] = lv[s - 1]; li[s] = li[s - 1]; }
-        else if (s < k && cbetter(v, i, lv[s], li[s])) { lv[s] = v; li[s] = i; }
-    }
-    if (cbetter(v, i, lv[0], li[0])) { lv[0] = v; li[0] = i; }
-}
-
-__device__ __forceinline__ void lse_add(float& m, float& s, float v) {
-    if (v == -INFINITY) return;
-    if (v > m) { s = s * expf(m - v) + 1.f; m = v; }
-    else s += expf(v - m);
-}
-
 template <int EPI, int KMAX>
 __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CUtensorMap tmA,
                                                       const __grid_constant__ CUtensorMap tmB, const UmmaParams p) {
@@ -265,11 +248,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
         }
     }
     if (run_epi && EPI == 1) {
-        // stage buffers are free now: reuse them for the transposed tile and the candidate lists
+        // stage buffers are free now: reuse them for the transposed tile
         float* tile = reinterpret_cast<float*>(smem);                      // [32 columns][4 quarters][33]
-        draft::Cand* cl = reinterpret_cast<draft::Cand*>(smem + 32 * 132 * 4);   // [128 threads][KMAX]
-        float2* ml = reinterpret_cast<float2*>(cl + kThreads * KMAX);      // [128]
-        const int j = threadIdx.x >> 2, q = threadIdx.x & 3;               // scan: column j, rows 32q .. 32q+31
+        const int j = threadIdx.x >> 2, q = threadIdx.x & 3;               // column j, rows 32q .. 32q+31
         const int k = p.topk;
         for (int c0 = 0; c0 < p.n_pad; c0 += 32) {
             uint32_t r[32];
@@ -278,51 +259,75 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
 #pragma unroll
             for (int jj = 0; jj < 32; ++jj) tile[jj * 132 + warp * 33 + lane] = __uint_as_float(r[jj]);
             __syncthreads();
-            float lv[KMAX];
-            int li[KMAX];
-#pragma unroll
-            for (int s = 0; s < KMAX; ++s) { lv[s] = -INFINITY; li[s] = 0x7fffffff; }
-            float mx = -INFINITY, sm = 0.f;
             const int n = c0 + j;
+            const int v0 = m0 + 32 * q;   // first vocabulary row of this thread's quarter
+            // the 4 threads of a column are adjacent lanes and take every branch below together:
+            // their shuffles use the group's own mask
+            const unsigned gmask = 0xFu << (lane & ~3);
             if (n < p.n_valid) {
-                for (int i = 0; i < 32; ++i) {
-                    const int v = m0 + 32 * q + i;
-                    if (v >= p.V) break;
-                    const float x = tile[j * 132 + q * 33 + i];
-                    push_topk<KMAX>(lv, li, k, x, v);
-                    lse_add(mx, sm, x);
+                float xs[32];
+#pragma unroll
+                for (int i = 0; i < 32; ++i) xs[i] = v0 + i < p.V ? tile[j * 132 + q * 33 + i] : -INFINITY;
+                // quarter (max, sum of exp), merged over the column's 4 threads
+                float mq[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) mq[e] = fmaxf(fmaxf(xs[e], xs[e + 8]), fmaxf(xs[e + 16], xs[e + 24]));
+                float mx = fmaxf(fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3])), fmaxf(fmaxf(mq[4], mq[5]), fmaxf(mq[6], mq[7])));
+                const float mref = mx == -INFINITY ? 0.f : mx;
+                float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ps[i & 3] += expf(xs[i] - mref);
+                float sm = (ps[0] + ps[1]) + (ps[2] + ps[3]);
+#pragma unroll
+                for (int o = 1; o <= 2; o <<= 1) {
+                    const float m2 = __shfl_xor_sync(gmask, mx, o, 4);
+                    const float s2 = __shfl_xor_sync(gmask, sm, o, 4);
+                    const float M = fmaxf(mx, m2);
+                    if (M != -INFINITY) sm = sm * expf(mx - M) + s2 * expf(m2 - M);
+                    mx = M;
                 }
-            }
+                const size_t out = static_cast<size_t>(p.row0 + n) * p.nslices + blockIdx.x;
+                if (q == 0) p.part_l[out] = make_float2(mx, mx == -INFINITY ? 0.f : sm);
+                // top-k by tournament: k rounds of (tree argmax over the thread's 32 logits,
+                // then over the 4 threads), the winner knocked out; lower index wins ties.
+                // NaN never wins; a round whose best is -inf ends the list (the slots left
+                // keep the (-inf, INT_MAX) placeholder).
 #pragma unroll
-            for (int s = 0; s < KMAX; ++s) cl[threadIdx.x * KMAX + s] = draft::Cand{lv[s], li[s]};
-            ml[threadIdx.x] = make_float2(mx, sm);
-            __syncthreads();
-            if (q == 0 && n < p.n_valid) {
-                int head[4] = {0, 0, 0, 0};
-                const size_t out = (static_cast<size_t>(p.row0 + n) * p.nslices + blockIdx.x);
-                for (int s = 0; s < k; ++s) {
-                    int best = -1;
-                    float bv = -INFINITY;
-                    int bi = 0x7fffffff;
+                for (int i = 0; i < 32; ++i) xs[i] = xs[i] == xs[i] ? xs[i] : -INFINITY;
+                int rr = 0;
+#pragma unroll 1
+                for (; rr < k; ++rr) {
+                    float tv[16];
+                    int ti[16];
 #pragma unroll
-                    for (int qq = 0; qq < 4; ++qq) {
-                        if (head[qq] >= k) continue;
-                        const draft::Cand c = cl[(threadIdx.x + qq) * KMAX + head[qq]];
-                        if (best < 0 || cbetter(c.v, c.i, bv, bi)) { best = qq; bv = c.v; bi = c.i; }
+                    for (int e = 0; e < 16; ++e) {
+                        const bool right = xs[2 * e + 1] > xs[2 * e];
+                        tv[e] = right ? xs[2 * e + 1] : xs[2 * e];
+                        ti[e] = right ? 2 * e + 1 : 2 * e;
                     }
-                    head[best] += 1;
-                    p.part_c[out * p.kmax + s] = draft::Cand{bv, bi};
-                }
-                float M = -INFINITY, S = 0.f;
 #pragma unroll
-                for (int qq = 0; qq < 4; ++qq) {
-                    const float2 e = ml[threadIdx.x + qq];
-                    if (e.x == -INFINITY) continue;
-                    if (M == -INFINITY) { M = e.x; S = e.y; }
-                    else if (e.x > M) { S = S * expf(M - e.x) + e.y; M = e.x; }
-                    else S += e.y * expf(e.x - M);
+                    for (int w2 = 8; w2 > 0; w2 >>= 1)
+#pragma unroll
+                        for (int e = 0; e < w2; ++e) {
+                            const bool right = tv[2 * e + 1] > tv[2 * e];
+                            tv[e] = right ? tv[2 * e + 1] : tv[2 * e];
+                            ti[e] = right ? ti[2 * e + 1] : ti[2 * e];
+                        }
+                    float bv = tv[0];
+                    int bi = bv == -INFINITY ? 0x7fffffff : v0 + ti[0];
+#pragma unroll
+                    for (int o = 1; o <= 2; o <<= 1) {
+                        const float v2 = __shfl_xor_sync(gmask, bv, o, 4);
+                        const int i2 = __shfl_xor_sync(gmask, bi, o, 4);
+                        if (cbetter(v2, i2, bv, bi)) { bv = v2; bi = i2; }
+                    }
+                    if (bv == -INFINITY) break;   // uniform over the 4-lane group
+                    if (q == 0) p.part_c[out * p.kmax + rr] = draft::Cand{bv, bi};
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) xs[i] = v0 + i == bi ? -INFINITY : xs[i];
                 }
-                p.part_l[out] = make_float2(M, S);
+                if (q == 0)
+                    for (; rr < k; ++rr) p.part_c[out * p.kmax + rr] = draft::Cand{-INFINITY, 0x7fffffff};
             }
             __syncthreads();
         }
