@@ -407,10 +407,12 @@ bool draft_tc_supported(int d, int V) {
     return d >= 8 && d % 8 == 0 && V >= 1 && (V + kBM - 1) / kBM <= 1024 && encode_fn() != nullptr;
 }
 
-static int mlp_splits(int d, int d_in) {
+// Split-K factor of the MLP: as many splits as fit in one wave of resident
+// CTAs (`resident` per SM), so no CTA waits for a second wave.
+static int mlp_splits(int d, int d_in, int resident) {
     const int m_tiles = (d + kBM - 1) / kBM;
     const int total = (d_in + kBKS - 1) / kBKS;
-    const int want = std::max(1, (2 * device_sm_count() + m_tiles - 1) / m_tiles);
+    const int want = std::max(1, resident * device_sm_count() / m_tiles);
     const int per = (total + want - 1) / want;
     return (total + per - 1) / per;
 }
@@ -420,7 +422,8 @@ DraftTcPlan draft_tc_plan(int rows, int d, int V) {
     p.rows_pad = n_pad_of(rows);
     p.nslices = (V + kBM - 1) / kBM;
     p.n_tickets = (d + kBM - 1) / kBM;
-    const int splits = std::max(mlp_splits(d, d), mlp_splits(d, 2 * d));
+    // resident <= 2 for every activation width (each CTA holds two 32 KB weight stages at least)
+    const int splits = std::max(mlp_splits(d, d, 2), mlp_splits(d, 2 * d, 2));
     p.mlp_partial_bytes = sizeof(float) * static_cast<size_t>(splits) * std::min(p.rows_pad, kMaxN) * d;
     return p;
 }
@@ -438,13 +441,16 @@ spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, cons
                           const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* X, int d_in, int ldx,
                           __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax, float* scratch,
                           int* tickets, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s) {
-    const int splits = mlp_splits(d, d_in);
     const int total_mlp = (d_in + kBKS - 1) / kBKS;
-    const int per_split = (total_mlp + splits - 1) / splits;
     // ---- MLP, activation rows in groups of at most 256 (the MMA's largest N)
     for (int g0 = 0; g0 < R; g0 += kMaxN) {
         const int rows = std::min(kMaxN, R - g0);
         const int n_pad = n_pad_of(rows);
+        // CTAs per SM by shared memory (228 KB per SM, 1 KB reserved per CTA); at most 2
+        const int resident = static_cast<int>(std::max<size_t>(
+            1, std::min<size_t>(2, 233472 / (smem_of(n_pad, stages_of(n_pad)) + 1024))));
+        const int splits = mlp_splits(d, d_in, resident);
+        const int per_split = (total_mlp + splits - 1) / splits;
         CUtensorMap ta, tb;
         SPEC_CUDA_TRY(make_tmap_bf16_2d(&ta, W1, d, d_in, d_in, kBM));
         SPEC_CUDA_TRY(make_tmap_bf16_2d(&tb, X + static_cast<size_t>(g0) * ldx, rows, d_in, ldx, n_pad));
