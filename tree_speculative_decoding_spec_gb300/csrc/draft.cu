@@ -307,13 +307,47 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
             if (node_logprob) node_logprob[static_cast<size_t>(b) * Tn + c] = base + (topv[rr] - lse_s);
         }
         if (next_n_int > 0) {
-            for (int a = child_off[u]; a < child_off[u + 1]; ++a) {
-                const int c = child_idx[a];
-                const int ro = row_of[c];
-                if (ro < 0) continue;
-                const size_t row = static_cast<size_t>(b) * next_n_int + ro;
-                write_next_row(xin + row * 2 * d, h + static_cast<size_t>(b) * d,
-                               emb + static_cast<size_t>(topi[rank[c]]) * d, d);
+            // next depth's input rows [h_b || E[token]] of all children at once: one 16-byte
+            // chunk per thread and step, so the embedding rows' cold loads overlap
+            // (a node has at most k <= KMAX children: their rows and tokens go to shared memory first)
+            __shared__ int c_row[KMAX], c_tok[KMAX];
+            const int a0 = child_off[u], nc = min(child_off[u + 1] - a0, KMAX);
+            __syncthreads();
+            if (tid < nc) {
+                const int c = child_idx[a0 + tid];
+                c_row[tid] = row_of[c];
+                c_tok[tid] = topi[rank[c]];
+            }
+            __syncthreads();
+            const int per = d / (16 / static_cast<int>(sizeof(T)));   // 16-byte chunks per half row
+            const uint4* hs = reinterpret_cast<const uint4*>(h + static_cast<size_t>(b) * d);
+            // every load of a chunk column (h_b once, one embedding row per child) is issued
+            // before any store, so one CTA keeps all children's rows in flight
+            for (int w0 = tid; w0 < per; w0 += 2 * blockDim.x) {
+                const int w1 = w0 + blockDim.x;   // second chunk column of this thread (if any)
+                const bool two = w1 < per;
+                const uint4 hv0 = hs[w0];
+                const uint4 hv1 = two ? hs[w1] : hv0;
+                uint4 ev0[KMAX], ev1[KMAX];
+#pragma unroll
+                for (int a = 0; a < KMAX; ++a)
+                    if (a < nc) {
+                        const uint4* er = reinterpret_cast<const uint4*>(emb + static_cast<size_t>(c_tok[a]) * d);
+                        ev0[a] = er[w0];
+                        if (two) ev1[a] = er[w1];
+                    }
+#pragma unroll
+                for (int a = 0; a < KMAX; ++a) {
+                    if (a < nc && c_row[a] >= 0) {
+                        uint4* o = reinterpret_cast<uint4*>(xin + (static_cast<size_t>(b) * next_n_int + c_row[a]) * 2 * d);
+                        o[w0] = hv0;
+                        o[per + w0] = ev0[a];
+                        if (two) {
+                            o[w1] = hv1;
+                            o[per + w1] = ev1[a];
+                        }
+                    }
+                }
             }
         }
     }
