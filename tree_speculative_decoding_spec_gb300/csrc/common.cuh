@@ -83,6 +83,31 @@ inline cudaError_t launch_ex(const char* name, void (*kernel)(KArgs...), dim3 gr
     return e;
 }
 
+// launch_ex with a thread-block cluster shape (cluster.x * y * z CTAs, at most 8).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_cluster(const char* name, void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                  cudaStream_t s, bool pdl, dim3 cluster, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = cluster.x;
+    attr[0].val.clusterDim.y = cluster.y;
+    attr[0].val.clusterDim.z = cluster.z;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl && !trace_active() ? 2 : 1;
+    trace_before(s);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    trace_after(s, name);
+    count_launch();
+    return e;
+}
+
 #define SPEC_CUDA_TRY(expr)                                                              \
     do {                                                                                 \
         cudaError_t _e = (expr);                                                         \

@@ -355,13 +355,12 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
 
 // Node 0 of every sequence: its token is the root token (clamped to the
 // vocabulary, with SPEC_EINVAL in the status word, so later reads stay in
-// bounds); writes head 0's input rows when head 0 is conditioned, and zeroes
-// the split-K tickets of the tensor-core MLP.  One CTA per sequence.
+// bounds); writes head 0's input rows when head 0 is conditioned.  One CTA
+// per sequence.
 template <typename T>
 __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn, int V, int32_t* __restrict__ node_tok,
                             float* __restrict__ node_logit, float* __restrict__ node_logprob, void* ws, int cond0,
-                            const T* __restrict__ h, const T* __restrict__ emb, int d, T* __restrict__ xin,
-                            int* __restrict__ tickets, int n_tickets) {
+                            const T* __restrict__ h, const T* __restrict__ emb, int d, T* __restrict__ xin) {
     const int b = blockIdx.x;
     griddep_launch();   // head 0's MLP may start streaming its weights
     int tok = root_tok[b];
@@ -374,8 +373,6 @@ __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn,
         node_logit[static_cast<size_t>(b) * Tn] = 0.f;
         if (node_logprob) node_logprob[static_cast<size_t>(b) * Tn] = 0.f;
     }
-    if (b == 0)
-        for (int i = threadIdx.x; i < n_tickets; i += blockDim.x) tickets[i] = 0;
     if (cond0) write_next_row(xin + static_cast<size_t>(b) * 2 * d, h + static_cast<size_t>(b) * d,
                               emb + static_cast<size_t>(tok) * d, d);
 }
@@ -388,8 +385,7 @@ struct Plan {
     int kmax;            // list length of the top-k partials (8 or 16)
     int nslices;         // vocabulary slices per row
     int slice_fma;       // fp32 path: tokens per slice
-    size_t off_xin, off_z, off_scratch, off_pc, off_pl, off_tickets, total;
-    int n_tickets;
+    size_t off_xin, off_z, off_scratch, off_pc, off_pl, total;
     bool tc;             // bf16 tensor-core path
     tc::DraftTcPlan tcp;
 };
@@ -418,9 +414,7 @@ Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* co
         p.nslices = p.tcp.nslices;
         p.off_xin = take(es * static_cast<size_t>(std::max(max_cond_rows, 1)) * 2 * d);
         p.off_z = take(es * static_cast<size_t>(p.tcp.rows_pad) * d);
-        p.off_scratch = take(p.tcp.mlp_partial_bytes);
-        p.n_tickets = p.tcp.n_tickets;
-        p.off_tickets = take(sizeof(int) * static_cast<size_t>(p.n_tickets));
+        p.off_scratch = 0;   // unused: the MLP reduces its split-K partials on chip
         p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.max_rows) * p.nslices * p.kmax);
         p.off_pl = take(sizeof(float2) * static_cast<size_t>(p.max_rows) * p.nslices);
     } else {
@@ -430,8 +424,6 @@ Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* co
         p.off_xin = take(es * static_cast<size_t>(std::max(max_cond_rows, 1)) * 2 * d);
         p.off_z = take(es * static_cast<size_t>(p.max_rows) * d);
         p.off_scratch = take(sizeof(float) * static_cast<size_t>(p.max_rows) * V);
-        p.n_tickets = 0;
-        p.off_tickets = take(16);
         p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.max_rows) * p.nslices * p.kmax);
         p.off_pl = take(sizeof(float2) * static_cast<size_t>(p.max_rows) * p.nslices);
     }
@@ -482,13 +474,12 @@ spec_status run(const T* h, const T* emb, int K, const void* const* W1, const vo
     T* xin = reinterpret_cast<T*>(w + p.off_xin);
     T* z = reinterpret_cast<T*>(w + p.off_z);
     float* scratch = reinterpret_cast<float*>(w + p.off_scratch);
-    int* tickets = reinterpret_cast<int*>(w + p.off_tickets);
     Cand* pc = reinterpret_cast<Cand*>(w + p.off_pc);
     float2* pl = reinterpret_cast<float2*>(w + p.off_pl);
     const bool first_cond = t->n_internal_at_depth[0] > 0 && cond[0];
     SPEC_CUDA_TRY(reset_device_status(ws, s));
     SPEC_CUDA_TRY(launch("draft_init_root", k_init_root<T>, dim3(B), dim3(128), 0, s, root_tok, B, t->T, V, node_tok,
-                         node_logit, node_logprob, ws, first_cond ? 1 : 0, h, emb, d, xin, tickets, p.n_tickets));
+                         node_logit, node_logprob, ws, first_cond ? 1 : 0, h, emb, d, xin));
     int int_off = 0;
     for (int k = 0; k < K; int_off += t->n_internal_at_depth[k], ++k) {
         const int n_int = t->n_internal_at_depth[k];
@@ -505,7 +496,7 @@ spec_status run(const T* h, const T* emb, int K, const void* const* W1, const vo
         if constexpr (std::is_same<T, __nv_bfloat16>::value) {
             if (p.tc) {
                 spec_status st = tc::draft_head_tc(p.tcp, W1k, b1k, W2k, h, X, d_in, ldx, z, R, d, V, cond[k], n_int,
-                                                   topk[k], p.kmax, scratch, tickets, pc, pl, ws, s);
+                                                   topk[k], p.kmax, pc, pl, ws, s);
                 if (st != SPEC_OK) return st;
                 st = p.kmax == 8 ? launch_select<8, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
                                                        pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, s)

@@ -13,9 +13,10 @@
 // workspace status word, drains its own loads and frees TMEM.
 //
 // Epilogues:
-//   MLP (W1, split over K): fp32 partial sums per split; the last split to
-//       finish a weight tile (atomic ticket) sums them and applies bias, SiLU,
-//       the residual h and bf16 rounding.
+//   MLP (W1, split over K): the splits of a weight tile form one thread-block
+//       cluster; each keeps its fp32 partial tile in shared memory and the
+//       cluster reduces it over distributed shared memory, applying bias,
+//       SiLU, the residual h and bf16 rounding.
 //   projection (W2): per activation row, the top-k (value desc, token asc)
 //       and (max, sum exp) of the tile's 128 logits; logits never reach HBM.
 #include <mutex>
@@ -27,6 +28,7 @@ namespace spec {
 namespace tc {
 
 constexpr int kBM = 128;        // MMA M: weight rows per CTA
+constexpr int kMaxSplits = 8;   // MLP split-K: one cluster (portable size) per weight tile
 // Build-time shape knobs (defaults are the tuned choice):
 //   SPEC_DRAFT_KB        64-column K blocks per pipeline stage
 //   SPEC_DRAFT_SMEM_KB   shared-memory budget per CTA in KB (100 keeps two CTAs per SM)
@@ -62,8 +64,6 @@ struct UmmaParams {
     int n_valid;    // valid activation rows in this launch
     int stages;
     uint32_t tmem_cols;
-    // MLP epilogue
-    float* partial;     // [splits][n_pad][M]
     // projection epilogue
     int topk;
     int V;
@@ -73,8 +73,7 @@ struct UmmaParams {
     float2* part_l;
     int kmax;
     void* ws;           // status word
-    // MLP finish (last split of each weight tile): z = h + SiLU(sum + b1)
-    int* tickets;       // [weight tiles], zero on entry, reset by the last split
+    // MLP finish (cluster of a weight tile's splits): z = h + SiLU(sum + b1)
     const __nv_bfloat16* bias;
     const __nv_bfloat16* h;
     __nv_bfloat16* z;
@@ -194,58 +193,50 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
     const int all_have = __syncthreads_and(have ? 1 : 0);   // one decision for the whole CTA
     const bool run_epi = all_have && !*abort_flag && n_it > 0;
 
-    if (run_epi && EPI == 0) {
-        const int m = m0 + warp * 32 + lane;
-        for (int c0 = 0; c0 < p.n_pad; c0 += 32) {
-            uint32_t r[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, r);
-            tmem_ld_wait();
-            if (m < p.M) {
+    if (EPI == 0) {
+        // Split-K reduction inside the cluster of this weight tile's splits (cluster rank
+        // = split): each CTA puts its fp32 partial tile [n][128 weight rows] in its own
+        // shared memory (the stage buffers are free), then CTA q reduces activation rows
+        // n = q, q + splits, ... over the cluster's shared memory and writes
+        // z = h + SiLU(sum + b1) in bf16.  Every CTA reaches both cluster barriers, also
+        // after a timeout; a CTA whose accumulator is not valid clears its flag and no
+        // row is written.
+        float* red = reinterpret_cast<float*>(smem);
+        int* ok_flag = reinterpret_cast<int*>(red + p.n_valid * kBM);
+        if (run_epi) {
+            for (int c0 = 0; c0 < p.n_pad; c0 += 32) {
+                uint32_t r[32];
+                tmem_ld32(tmem + (static_cast<uint32_t>(warp * 32) << 16) + c0, r);
+                tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int n = c0 + j;
-                    if (n < p.n_valid)
-                        p.partial[(static_cast<size_t>(blockIdx.y) * p.n_pad + n) * p.M + m] = __uint_as_float(r[j]);
-                }
+                for (int j = 0; j < 32; ++j)
+                    if (c0 + j < p.n_valid) red[(c0 + j) * kBM + threadIdx.x] = __uint_as_float(r[j]);
             }
         }
-        // the last split to finish this weight tile sums all splits and writes z
-        __shared__ int last;
-        __threadfence();
-        __syncthreads();
-        if (threadIdx.x == 0) last = atomicAdd(&p.tickets[blockIdx.x], 1) == static_cast<int>(gridDim.y) - 1;
-        __syncthreads();
-        if (last) {
-            __threadfence();
-            // 4 consecutive outputs per thread and pass: 32 threads cover the tile's 128
-            // weight rows of one activation row, so a pass handles 4 activation rows;
-            // all split loads of a pass are independent
-            const int mq = m0 + (threadIdx.x & 31) * 4;
-            const int nsub = threadIdx.x >> 5;
-            const int splits = static_cast<int>(gridDim.y);
-            for (int n = nsub; n < p.n_valid; n += 4) {
-                if (mq >= p.M) break;
-                float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-                for (int sp = 0; sp < splits; ++sp) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                        &p.partial[(static_cast<size_t>(sp) * p.n_pad + n) * p.M + mq]));
-                    a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
-                }
+        if (threadIdx.x == 0) *ok_flag = run_epi ? 1 : 0;
+        cluster_sync();
+        const int nsplit = static_cast<int>(gridDim.y);
+        const uint32_t rank = cluster_ctarank();
+        bool all_ok = true;
+        for (int sp = 0; sp < nsplit; ++sp) all_ok &= dsmem_ld_s32(dsmem_map(smem_u32(ok_flag), sp)) != 0;
+        const int m = m0 + threadIdx.x;
+        if (all_ok && m < p.M) {
+            const float bias = p.bias ? __bfloat162float(p.bias[m]) : 0.f;
+            for (int n = static_cast<int>(rank); n < p.n_valid; n += nsplit) {
+                const uint32_t a = smem_u32(red + n * kBM + threadIdx.x);
+                float v[kMaxSplits];
+#pragma unroll
+                for (int sp = 0; sp < kMaxSplits; ++sp) v[sp] = sp < nsplit ? dsmem_ld_f32(dsmem_map(a, sp)) : 0.f;
+                float x = bias;
+#pragma unroll
+                for (int sp = 0; sp < kMaxSplits; ++sp) x += v[sp];
                 const int row = p.row0 + n;
                 const int b = p.cond ? row / p.n_int : row;
-                const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int mm = mq + e;
-                    if (mm >= p.M) break;
-                    const float x = av[e] + (p.bias ? __bfloat162float(p.bias[mm]) : 0.f);
-                    const float zz = __bfloat162float(p.h[static_cast<size_t>(b) * p.M + mm]) + x / (1.0f + expf(-x));
-                    p.z[static_cast<size_t>(row) * p.M + mm] = __float2bfloat16_rn(zz);
-                }
+                const float zz = __bfloat162float(p.h[static_cast<size_t>(b) * p.M + m]) + x / (1.0f + expf(-x));
+                p.z[static_cast<size_t>(row) * p.M + m] = __float2bfloat16_rn(zz);
             }
-            if (threadIdx.x == 0) p.tickets[blockIdx.x] = 0;   // ready for the next launch
         }
+        cluster_sync();   // the peers have read this CTA's partials
     }
     if (run_epi && EPI == 1) {
         // stage buffers are free now: reuse them for the transposed tile
@@ -412,7 +403,7 @@ bool draft_tc_supported(int d, int V) {
 static int mlp_splits(int d, int d_in, int resident) {
     const int m_tiles = (d + kBM - 1) / kBM;
     const int total = (d_in + kBKS - 1) / kBKS;
-    const int want = std::max(1, resident * device_sm_count() / m_tiles);
+    const int want = std::min(kMaxSplits, std::max(1, resident * device_sm_count() / m_tiles));
     const int per = (total + want - 1) / want;
     return (total + per - 1) / per;
 }
@@ -421,10 +412,7 @@ DraftTcPlan draft_tc_plan(int rows, int d, int V) {
     DraftTcPlan p;
     p.rows_pad = n_pad_of(rows);
     p.nslices = (V + kBM - 1) / kBM;
-    p.n_tickets = (d + kBM - 1) / kBM;
-    // resident <= 2 for every activation width (each CTA holds two 32 KB weight stages at least)
-    const int splits = std::max(mlp_splits(d, d, 2), mlp_splits(d, 2 * d, 2));
-    p.mlp_partial_bytes = sizeof(float) * static_cast<size_t>(splits) * std::min(p.rows_pad, kMaxN) * d;
+    (void)d;
     return p;
 }
 
@@ -433,14 +421,18 @@ static spec_status launch_umma(const CUtensorMap& ta, const CUtensorMap& tb, dim
                                cudaStream_t s, const char* name) {
     const size_t smem = smem_of(p.n_pad, p.stages);
     SPEC_CUDA_TRY(cudaFuncSetAttribute(k_umma<EPI, KMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
-    SPEC_CUDA_TRY(launch_ex(name, k_umma<EPI, KMAX>, grid, dim3(kThreads), smem, s, true, ta, tb, p));
+    if (EPI == 0)   // the splits of one weight tile (grid.y of them) share a cluster
+        SPEC_CUDA_TRY(launch_cluster(name, k_umma<EPI, KMAX>, grid, dim3(kThreads), smem, s, true, dim3(1, grid.y, 1),
+                                     ta, tb, p));
+    else
+        SPEC_CUDA_TRY(launch_ex(name, k_umma<EPI, KMAX>, grid, dim3(kThreads), smem, s, true, ta, tb, p));
     return SPEC_OK;
 }
 
 spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
                           const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* X, int d_in, int ldx,
-                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax, float* scratch,
-                          int* tickets, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s) {
+                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax,
+                          draft::Cand* pc, float2* pl, void* ws, cudaStream_t s) {
     const int total_mlp = (d_in + kBKS - 1) / kBKS;
     // ---- MLP, activation rows in groups of at most 256 (the MMA's largest N)
     for (int g0 = 0; g0 < R; g0 += kMaxN) {
@@ -462,10 +454,8 @@ spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, cons
         p.n_valid = rows;
         p.stages = stages_of(n_pad);
         p.tmem_cols = tmem_cols_of(n_pad);
-        p.partial = scratch;
         p.ws = ws;
         p.row0 = g0;
-        p.tickets = tickets;
         p.bias = b1;
         p.h = h;
         p.z = z;

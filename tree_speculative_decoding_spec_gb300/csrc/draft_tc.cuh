@@ -18,8 +18,6 @@ namespace tc {
 struct DraftTcPlan {
     int rows_pad = 0;              // rows padded to the MMA N granule
     int nslices = 0;               // vocabulary slices (one per 128-row W2 tile)
-    int n_tickets = 0;             // split-K tickets of the MLP (one per 128-row W1 tile)
-    size_t mlp_partial_bytes = 0;  // split-K partial sums of the MLP
 };
 
 bool draft_tc_supported(int d, int V);
@@ -33,8 +31,8 @@ DraftTcPlan draft_tc_plan(int rows, int d, int V);
 // dependent launch.
 spec_status draft_head_tc(const DraftTcPlan& p, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
                           const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* X, int d_in, int ldx,
-                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax, float* scratch,
-                          int* tickets, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s);
+                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax,
+                          draft::Cand* pc, float2* pl, void* ws, cudaStream_t s);
 
 }  // namespace tc
 }  // namespace spec

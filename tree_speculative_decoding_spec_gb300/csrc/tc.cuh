@@ -49,14 +49,29 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that may suspend the thread for up to `hint_ns` while the phase is pending.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase of parity `parity` has completed, for at most `limit_ns`
-// nanoseconds.  Returns false when the limit ran out.
+// nanoseconds.  Returns false when the limit ran out.  A pending thread
+// suspends (20 us hint, woken when the phase completes) instead of spinning, so
+// long waits leave the issue slots to the CTAs that share the SM.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 0;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 255u && globaltimer_ns() - t0 > limit_ns) return false;
+        if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+        if ((i & 15u) == 15u && globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
@@ -74,6 +89,39 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// ---------------------------------------------------------------- clusters
+
+// Barrier over every thread of every CTA of the cluster; writes to shared
+// memory before it are visible to the cluster's CTAs after it.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_map(uint32_t smem_addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float dsmem_ld_f32(uint32_t cluster_addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(cluster_addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ int dsmem_ld_s32(uint32_t cluster_addr) {
+    int v;
+    asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
+    return v;
 }
 
 // ---------------------------------------------------------------- TMEM
@@ -222,19 +270,6 @@ __device__ __forceinline__ uint64_t sdesc_mn128(uint32_t smem_addr, uint32_t lbo
 // Instruction descriptor with an MN-major B operand (A K-major), bf16 in, fp32 out.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32_bmn(int M, int N) {
     return idesc_bf16_f32(M, N) | (1u << 16);
-}
-
-// try_wait that may suspend the thread for up to `hint_ns` while the phase is pending.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
 }
 
 // Bounded wait that also gives up as soon as another thread of the CTA raised
