@@ -204,10 +204,12 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                                                 float* __restrict__ node_logprob, void* ws, int next_n_int,
                                                 const T* __restrict__ h, const T* __restrict__ emb, int d,
                                                 T* __restrict__ xin) {
-    // the next head's MLP may launch now: it streams its weights and waits for
-    // this kernel's outputs (tokens, input rows) with its own griddep_wait()
-    griddep_launch();
+    // Once the projection before this kernel is complete, the next head's MLP may
+    // launch: it streams its weights and waits for this kernel's outputs (tokens,
+    // input rows) with its own griddep_wait().  Triggering only after the wait keeps
+    // that MLP's CTAs off the SMs while the projection still streams.
     griddep_wait();
+    griddep_launch();
     const int r = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __shared__ Cand lists[256][KMAX];
