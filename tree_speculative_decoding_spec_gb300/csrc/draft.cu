@@ -309,9 +309,8 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
             if (node_logprob) node_logprob[static_cast<size_t>(b) * Tn + c] = base + (topv[rr] - lse_s);
         }
         if (next_n_int > 0) {
-            // next depth's input rows [h_b || E[token]] of all children at once: one 16-byte
-            // chunk per thread and step, so the embedding rows' cold loads overlap
-            // (a node has at most k <= KMAX children: their rows and tokens go to shared memory first)
+            // next depth's input rows [h_b || E[token]] of all children at once (a node has
+            // at most k <= KMAX children: their rows and tokens go to shared memory first)
             __shared__ int c_row[KMAX], c_tok[KMAX];
             const int a0 = child_off[u], nc = min(child_off[u + 1] - a0, KMAX);
             __syncthreads();
@@ -322,14 +321,11 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
             }
             __syncthreads();
             const int per = d / (16 / static_cast<int>(sizeof(T)));   // 16-byte chunks per half row
-            const uint4* hs = reinterpret_cast<const uint4*>(h + static_cast<size_t>(b) * d);
-            // every load of a chunk column (h_b once, one embedding row per child) is issued
-            // before any store, so one CTA keeps all children's rows in flight
+            // the embedding halves only (the h_b halves were written by the step's first
+            // kernel); every load of a chunk column is issued before any store
             for (int w0 = tid; w0 < per; w0 += 2 * blockDim.x) {
                 const int w1 = w0 + blockDim.x;   // second chunk column of this thread (if any)
                 const bool two = w1 < per;
-                const uint4 hv0 = hs[w0];
-                const uint4 hv1 = two ? hs[w1] : hv0;
                 uint4 ev0[KMAX], ev1[KMAX];
 #pragma unroll
                 for (int a = 0; a < KMAX; ++a)
@@ -342,12 +338,8 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                 for (int a = 0; a < KMAX; ++a) {
                     if (a < nc && c_row[a] >= 0) {
                         uint4* o = reinterpret_cast<uint4*>(xin + (static_cast<size_t>(b) * next_n_int + c_row[a]) * 2 * d);
-                        o[w0] = hv0;
                         o[per + w0] = ev0[a];
-                        if (two) {
-                            o[w1] = hv1;
-                            o[per + w1] = ev1[a];
-                        }
+                        if (two) o[per + w1] = ev1[a];
                     }
                 }
             }
@@ -355,16 +347,41 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
     }
 }
 
-// Node 0 of every sequence: its token is the root token (clamped to the
-// vocabulary, with SPEC_EINVAL in the status word, so later reads stay in
-// bounds); writes head 0's input rows when head 0 is conditioned.  One CTA
-// per sequence.
+// The h_b halves of the conditioned heads' input rows [h_b || E[tok]] at
+// depths >= 1 depend on no drafted token, so the step's first kernel writes
+// them all; each select then writes only the embedding halves of the next
+// depth.  Depth slot i lists n_int[i] rows per sequence, starting at row
+// first[i] of the per-sequence numbering and at element off[i] of the
+// input-row region (rows of 2d elements, sequence-major).
+struct HRows {
+    int per_seq;
+    int n;
+    int first[SPEC_MAX_DEPTH];
+    int n_int[SPEC_MAX_DEPTH];
+    size_t off[SPEC_MAX_DEPTH];
+};
+
+// CTA (b, 0): node 0 of sequence b -- its token is the root token (clamped to
+// the vocabulary, with SPEC_EINVAL in the status word, so later reads stay in
+// bounds) -- and head 0's whole input row when head 0 is conditioned.  CTA
+// (b, 1 + r): the h_b half of row r of sequence b in HRows.
 template <typename T>
 __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn, int V, int32_t* __restrict__ node_tok,
                             float* __restrict__ node_logit, float* __restrict__ node_logprob, void* ws, int cond0,
-                            const T* __restrict__ h, const T* __restrict__ emb, int d, T* __restrict__ xin) {
+                            const T* __restrict__ h, const T* __restrict__ emb, int d, T* __restrict__ xin0,
+                            T* __restrict__ xbase, const HRows hr) {
     const int b = blockIdx.x;
     griddep_launch();   // head 0's MLP may start streaming its weights
+    if (blockIdx.y > 0) {
+        const int r = static_cast<int>(blockIdx.y) - 1;
+        int i = 0;
+        while (i + 1 < hr.n && r >= hr.first[i + 1]) ++i;
+        const size_t row = static_cast<size_t>(b) * hr.n_int[i] + (r - hr.first[i]);
+        const uint4* hs = reinterpret_cast<const uint4*>(h + static_cast<size_t>(b) * d);
+        uint4* o = reinterpret_cast<uint4*>(xbase + hr.off[i] + row * 2 * d);
+        for (int w = threadIdx.x; w < d / (16 / static_cast<int>(sizeof(T))); w += blockDim.x) o[w] = hs[w];
+        return;
+    }
     int tok = root_tok[b];
     if (tok < 0 || tok >= V) {
         if (threadIdx.x == 0) flag_status(ws, SPEC_EINVAL);
@@ -375,7 +392,7 @@ __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn,
         node_logit[static_cast<size_t>(b) * Tn] = 0.f;
         if (node_logprob) node_logprob[static_cast<size_t>(b) * Tn] = 0.f;
     }
-    if (cond0) write_next_row(xin + static_cast<size_t>(b) * 2 * d, h + static_cast<size_t>(b) * d,
+    if (cond0) write_next_row(xin0 + static_cast<size_t>(b) * 2 * d, h + static_cast<size_t>(b) * d,
                               emb + static_cast<size_t>(tok) * d, d);
 }
 
@@ -388,6 +405,8 @@ struct Plan {
     int nslices;         // vocabulary slices per row
     int slice_fma;       // fp32 path: tokens per slice
     size_t off_xin, off_z, off_scratch, off_pc, off_pl, total;
+    size_t xin_at[SPEC_MAX_DEPTH + 1];   // element offset of depth k's input rows (conditioned heads)
+    HRows hr;
     bool tc;             // bf16 tensor-core path
     tc::DraftTcPlan tcp;
 };
@@ -396,14 +415,35 @@ inline int rows_of(const spec_tree* t, int k, int cond, int B) {
     return cond ? B * t->n_internal_at_depth[k] : B;
 }
 
+// Lay out every conditioned depth's input rows (B x n_int rows of 2d elements
+// each) one after the other; fills xin_at and the HRows table (depths >= 1).
+// Returns the total row count (at least 1).
+size_t xin_rows(Plan& p, const spec_tree* t, int K, const int32_t* cond, int B) {
+    size_t rows = 0;
+    p.hr = HRows{};
+    for (int k = 0; k < K && k <= SPEC_MAX_DEPTH; ++k) {
+        p.xin_at[k] = 0;
+        const int n_int = t->n_internal_at_depth[k];
+        if (!cond[k] || n_int == 0) continue;
+        p.xin_at[k] = rows;   // in rows for now
+        if (k >= 1 && p.hr.n < SPEC_MAX_DEPTH) {
+            p.hr.first[p.hr.n] = p.hr.per_seq;
+            p.hr.n_int[p.hr.n] = n_int;
+            p.hr.off[p.hr.n] = rows;
+            p.hr.per_seq += n_int;
+            ++p.hr.n;
+        }
+        rows += static_cast<size_t>(B) * n_int;
+    }
+    return std::max<size_t>(rows, 1);
+}
+
 Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* cond, const int32_t* topk, spec_dtype dt) {
     Plan p{};
     p.K = K;
-    int max_cond_rows = 0;
     for (int k = 0; k < K; ++k) {
         if (t->n_internal_at_depth[k] == 0) continue;
         p.max_rows = std::max(p.max_rows, rows_of(t, k, cond[k], B));
-        if (cond[k]) max_cond_rows = std::max(max_cond_rows, rows_of(t, k, 1, B));
         p.kmax = std::max(p.kmax, topk[k]);
     }
     p.kmax = p.kmax <= 8 ? 8 : 16;
@@ -414,7 +454,7 @@ Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* co
     if (p.tc) {
         p.tcp = tc::draft_tc_plan(p.max_rows, d, V);
         p.nslices = p.tcp.nslices;
-        p.off_xin = take(es * static_cast<size_t>(std::max(max_cond_rows, 1)) * 2 * d);
+        p.off_xin = take(es * xin_rows(p, t, K, cond, B) * 2 * d);
         p.off_z = take(es * static_cast<size_t>(p.tcp.rows_pad) * d);
         p.off_scratch = 0;   // unused: the MLP reduces its split-K partials on chip
         p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.max_rows) * p.nslices * p.kmax);
@@ -423,12 +463,14 @@ Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* co
         // at most 1024 slices per row
         p.slice_fma = std::max(4096, static_cast<int>(round_up((V + 1023) / 1024, 256)));
         p.nslices = (V + p.slice_fma - 1) / p.slice_fma;
-        p.off_xin = take(es * static_cast<size_t>(std::max(max_cond_rows, 1)) * 2 * d);
+        p.off_xin = take(es * xin_rows(p, t, K, cond, B) * 2 * d);
         p.off_z = take(es * static_cast<size_t>(p.max_rows) * d);
         p.off_scratch = take(sizeof(float) * static_cast<size_t>(p.max_rows) * V);
         p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.max_rows) * p.nslices * p.kmax);
         p.off_pl = take(sizeof(float2) * static_cast<size_t>(p.max_rows) * p.nslices);
     }
+    for (int k = 0; k <= SPEC_MAX_DEPTH; ++k) p.xin_at[k] *= 2 * static_cast<size_t>(d);
+    for (int i = 0; i < p.hr.n; ++i) p.hr.off[i] *= 2 * static_cast<size_t>(d);
     p.total = off;
     return p;
 }
@@ -473,22 +515,25 @@ spec_status run(const T* h, const T* emb, int K, const void* const* W1, const vo
                 int V, int32_t* node_tok, float* node_logit, float* node_logprob, void* ws, const Plan& p,
                 cudaStream_t s) {
     unsigned char* w = static_cast<unsigned char*>(ws);
-    T* xin = reinterpret_cast<T*>(w + p.off_xin);
+    T* xbase = reinterpret_cast<T*>(w + p.off_xin);
     T* z = reinterpret_cast<T*>(w + p.off_z);
     float* scratch = reinterpret_cast<float*>(w + p.off_scratch);
     Cand* pc = reinterpret_cast<Cand*>(w + p.off_pc);
     float2* pl = reinterpret_cast<float2*>(w + p.off_pl);
     const bool first_cond = t->n_internal_at_depth[0] > 0 && cond[0];
     SPEC_CUDA_TRY(reset_device_status(ws, s));
-    SPEC_CUDA_TRY(launch("draft_init_root", k_init_root<T>, dim3(B), dim3(128), 0, s, root_tok, B, t->T, V, node_tok,
-                         node_logit, node_logprob, ws, first_cond ? 1 : 0, h, emb, d, xin));
+    SPEC_CUDA_TRY(launch("draft_init_root", k_init_root<T>, dim3(B, 1 + p.hr.per_seq), dim3(128), 0, s, root_tok, B,
+                         t->T, V, node_tok, node_logit, node_logprob, ws, first_cond ? 1 : 0, h, emb, d,
+                         xbase + p.xin_at[0], xbase, p.hr));
     int int_off = 0;
     for (int k = 0; k < K; int_off += t->n_internal_at_depth[k], ++k) {
         const int n_int = t->n_internal_at_depth[k];
         if (n_int == 0) continue;   // no node of depth k has children: nothing to draft at depth k+1
         const int R = rows_of(t, k, cond[k], B);
         const int d_in = d * (cond[k] ? 2 : 1);
-        const T* X = cond[k] ? xin : h;   // conditioned rows were written by the previous select (or init)
+        // conditioned rows: h_b halves by the step's first kernel, embedding halves by the previous select
+        const T* X = cond[k] ? xbase + p.xin_at[k] : h;
+        T* xin = k + 1 <= SPEC_MAX_DEPTH ? xbase + p.xin_at[k + 1] : xbase;   // next depth's rows
         const int ldx = cond[k] ? 2 * d : d;
         const int next_n_int = (k + 1 < K && k + 1 <= SPEC_MAX_DEPTH && t->n_internal_at_depth[k + 1] > 0 && cond[k + 1])
                                    ? t->n_internal_at_depth[k + 1] : 0;
@@ -498,7 +543,7 @@ spec_status run(const T* h, const T* emb, int K, const void* const* W1, const vo
         if constexpr (std::is_same<T, __nv_bfloat16>::value) {
             if (p.tc) {
                 spec_status st = tc::draft_head_tc(p.tcp, W1k, b1k, W2k, h, X, d_in, ldx, z, R, d, V, cond[k], n_int,
-                                                   topk[k], p.kmax, pc, pl, ws, s);
+                                                   topk[k], p.kmax, cond[k] ? d : d_in, pc, pl, ws, s);
                 if (st != SPEC_OK) return st;
                 st = p.kmax == 8 ? launch_select<8, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
                                                        pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, s)

@@ -79,6 +79,10 @@ struct UmmaParams {
     __nv_bfloat16* z;
     int cond;
     int n_int;
+    // MLP: input columns >= dep_k0 come from the previous kernel; a CTA whose K range
+    // lies below it (and is not CTA (0, 0), which always waits so that this kernel
+    // completes after the previous one) starts without waiting for it
+    int dep_k0;
 };
 
 __device__ __forceinline__ bool cbetter(float va, int ia, float vb, int ib) {
@@ -139,7 +143,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
                 for (int kb = 0; kb < kKB; ++kb)
                     tma_load_2d(sA + i * kStageA + kb * kBoxA, &tmA, &full[i], (it0 + (i + rot) % n_it) * kBKS + kb * kBK, m0);
             }
-            griddep_wait();
+            const bool independent = EPI == 0 && (it0 + n_it) * kBKS <= p.dep_k0 && (blockIdx.x | blockIdx.y) != 0;
+            if (!independent) griddep_wait();
             for (int i = 0; i < pre; ++i)
                 for (int kb = 0; kb < kKB; ++kb)
                     tma_load_2d(sB + i * stage_b + kb * box_b, &tmB, &full[i], (it0 + (i + rot) % n_it) * kBKS + kb * kBK, 0);
@@ -431,7 +436,7 @@ static spec_status launch_umma(const CUtensorMap& ta, const CUtensorMap& tb, dim
 
 spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
                           const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* X, int d_in, int ldx,
-                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax,
+                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax, int dep_k0,
                           draft::Cand* pc, float2* pl, void* ws, cudaStream_t s) {
     const int total_mlp = (d_in + kBKS - 1) / kBKS;
     // ---- MLP, activation rows in groups of at most 256 (the MMA's largest N)
@@ -461,6 +466,7 @@ spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, cons
         p.z = z;
         p.cond = cond;
         p.n_int = n_int;
+        p.dep_k0 = dep_k0;
         spec_status st = launch_umma<0, 8>(ta, tb, dim3((d + kBM - 1) / kBM, splits), p, s, "draft_mlp_tc");
         if (st != SPEC_OK) return st;
     }

@@ -31,7 +31,7 @@ DraftTcPlan draft_tc_plan(int rows, int d, int V);
 // dependent launch.
 spec_status draft_head_tc(const DraftTcPlan& p, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
                           const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* X, int d_in, int ldx,
-                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax,
+                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax, int dep_k0,
                           draft::Cand* pc, float2* pl, void* ws, cudaStream_t s);
 
 }  // namespace tc
