@@ -110,6 +110,32 @@ __device__ __forceinline__ void insert_topk(float (&lv)[KMAX], int (&li)[KMAX], 
     if (better(v, i, lv[0], li[0])) { lv[0] = v; li[0] = i; }
 }
 
+// a and b: best-first lists of N candidates (N a power of two).  Leaves in a
+// the best N of both, best-first: the element-wise better of a[e] and
+// b[N-1-e] is a bitonic sequence holding exactly those N, which log2(N)
+// half-cleaner stages sort.  Every index is static (registers only).
+template <int N>
+__device__ __forceinline__ void merge_top(float (&av)[N], int (&ai)[N], const float (&bv)[N], const int (&bi)[N]) {
+#pragma unroll
+    for (int e = 0; e < N; ++e)
+        if (better(bv[N - 1 - e], bi[N - 1 - e], av[e], ai[e])) {
+            av[e] = bv[N - 1 - e];
+            ai[e] = bi[N - 1 - e];
+        }
+#pragma unroll
+    for (int j = N / 2; j > 0; j >>= 1)
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+            if ((e & j) == 0 && better(av[e + j], ai[e + j], av[e], ai[e])) {
+                const float tv = av[e];
+                const int ti = ai[e];
+                av[e] = av[e + j];
+                ai[e] = ai[e + j];
+                av[e + j] = tv;
+                ai[e + j] = ti;
+            }
+}
+
 // Per (row, vocab slice): the slice's top-k and (max, sum exp) -> partials.
 // Used by the fp32 path on stored logits; the tensor-core path produces the
 // same partials from its accumulators.
@@ -191,9 +217,10 @@ __device__ __forceinline__ void write_next_row(T* __restrict__ dst, const T* __r
 
 // One CTA per row: top-k over the row's sorted per-slice candidate lists and
 // the row's log-sum-exp, then the children of the row's parent node(s).
-// Tournament: each thread folds its slices into one sorted list (shared
-// memory), each warp merges its 32 lists by k rounds of shuffles, warp 0
-// merges the 8 warp lists.
+// Merging: each thread holds its slice's sorted list in registers (more
+// slices than threads are folded in by bitonic merges); k rounds then take the
+// best list head of the CTA -- a warp butterfly and one barrier per round --
+// and pop it from its owner's list.
 template <int KMAX, typename T>
 __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c, const float2* __restrict__ part_l,
                                                 int nslices, int k, int cond, int n_int, int int_off,
@@ -212,86 +239,81 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
     griddep_launch();
     const int r = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    __shared__ Cand lists[256][KMAX];
-    __shared__ Cand wl[8][KMAX];
     __shared__ float topv[KMAX];
     __shared__ int topi[KMAX];
     __shared__ float2 wlse[8];
     __shared__ float lse_s;
 
-    // 1. fold this thread's slices into one sorted list
+    // 1. each thread takes the list of slice tid (first k valid, placeholders after)
+    // and its (max, sum exp); slices beyond blockDim are folded in by bitonic merges
+    float lv[KMAX];
+    int li[KMAX];
     float M = -INFINITY, S = 0.f;
-    int n = 0;
-    for (int s = tid; s < nslices; s += blockDim.x) {
-        const Cand* src = part_c + (static_cast<size_t>(r) * nslices + s) * KMAX;
-        if (n == 0) {
-            for (int e = 0; e < k; ++e) lists[tid][e] = src[e];
-            n = k;
-        } else {
-            for (int e = 0; e < k; ++e) {
-                const Cand c = src[e];
-                if (!better(c.v, c.i, lists[tid][k - 1].v, lists[tid][k - 1].i)) break;
-                int pos = k - 1;
-                while (pos > 0 && better(c.v, c.i, lists[tid][pos - 1].v, lists[tid][pos - 1].i)) {
-                    lists[tid][pos] = lists[tid][pos - 1];
-                    --pos;
-                }
-                lists[tid][pos] = c;
-            }
+    auto load_list = [&](int sl, float (&v)[KMAX], int (&ix)[KMAX]) {
+        const Cand* src = part_c + (static_cast<size_t>(r) * nslices + sl) * KMAX;
+#pragma unroll
+        for (int e = 0; e < KMAX; ++e) {
+            const Cand c = (sl < nslices && e < k) ? src[e] : Cand{-INFINITY, 0x7fffffff};
+            v[e] = c.v;
+            ix[e] = c.i;
         }
-        const float2 p = part_l[static_cast<size_t>(r) * nslices + s];
-        lse_merge(M, S, p.x, p.y);
+        if (sl < nslices) {
+            const float2 p = part_l[static_cast<size_t>(r) * nslices + sl];
+            lse_merge(M, S, p.x, p.y);
+        }
+    };
+    load_list(tid, lv, li);
+#pragma unroll 1
+    for (int sl = tid + blockDim.x; sl < nslices; sl += blockDim.x) {
+        float bv[KMAX];
+        int bi[KMAX];
+        load_list(sl, bv, bi);
+        merge_top<KMAX>(lv, li, bv, bi);
     }
-    if (n == 0)
-        for (int e = 0; e < k; ++e) lists[tid][e] = Cand{-INFINITY, 0x7fffffff};
     for (int o = 16; o > 0; o >>= 1) lse_merge(M, S, __shfl_xor_sync(0xffffffffu, M, o), __shfl_xor_sync(0xffffffffu, S, o));
     if (lane == 0) wlse[warp] = make_float2(M, S);
-    __syncwarp();
 
-    // 2. warp tournament over the warp's 32 lists
-    int head = 0;
-    for (int round = 0; round < k; ++round) {
-        const Cand mine = head < k ? lists[tid][head] : Cand{-INFINITY, 0x7fffffff};
-        float v = mine.v;
-        int i = mine.i, who = lane;
+    // 2. k rounds over the list heads: the warp's best head by an xor butterfly, the
+    // CTA's best over the warps' (double-buffered shared slots, one barrier per
+    // round), and the owner of the winning candidate shifts its list.  Candidates are
+    // unique (the slices are disjoint), so the index identifies the owner.
+    __shared__ Cand slot[2][8];
+    const int nw = blockDim.x >> 5;
+#pragma unroll 1
+    for (int rr = 0; rr < k; ++rr) {
+        float v = lv[0];
+        int i = li[0];
+#pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
             const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
-            const int w2 = __shfl_xor_sync(0xffffffffu, who, o);
-            if (better(v2, i2, v, i) || (v2 == v && i2 == i && w2 < who)) { v = v2; i = i2; who = w2; }
+            if (better(v2, i2, v, i)) { v = v2; i = i2; }
         }
-        if (lane == who) ++head;
-        if (lane == 0) wl[warp][round] = Cand{v, i};
+        if (lane == 0) slot[rr & 1][warp] = Cand{v, i};
+        __syncthreads();
+        Cand best = slot[rr & 1][0];
+        for (int w = 1; w < nw; ++w) {
+            const Cand c = slot[rr & 1][w];
+            if (better(c.v, c.i, best.v, best.i)) best = c;
+        }
+        if (li[0] == best.i && best.v == lv[0]) {   // this thread's head won: pop it
+#pragma unroll
+            for (int e = 0; e + 1 < KMAX; ++e) { lv[e] = lv[e + 1]; li[e] = li[e + 1]; }
+            lv[KMAX - 1] = -INFINITY;
+            li[KMAX - 1] = 0x7fffffff;
+        }
+        if (tid == 0) {
+            int ix = best.i;
+            // fewer than k finite logits (NaN/inf weights) leave placeholders: keep tokens in range
+            if (ix < 0 || ix >= V) { flag_status(ws, SPEC_EINVAL); ix = 0; }
+            topv[rr] = best.v;
+            topi[rr] = ix;
+        }
     }
-    __syncthreads();
-
-    // 3. warp 0 merges the 8 warp lists
-    if (warp == 0) {
-        const int nw = blockDim.x >> 5;
-        int h8 = 0;
-        for (int round = 0; round < k; ++round) {
-            const Cand mine = (lane < nw && h8 < k) ? wl[lane][h8] : Cand{-INFINITY, 0x7fffffff};
-            float v = mine.v;
-            int i = mine.i, who = lane;
-            for (int o = 16; o > 0; o >>= 1) {
-                const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-                const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
-                const int w2 = __shfl_xor_sync(0xffffffffu, who, o);
-                if (better(v2, i2, v, i) || (v2 == v && i2 == i && w2 < who)) { v = v2; i = i2; who = w2; }
-            }
-            if (lane == who) ++h8;
-            if (lane == 0) {
-                // fewer than k finite logits (NaN/inf weights) leave placeholders: keep tokens in range
-                if (i < 0 || i >= V) { flag_status(ws, SPEC_EINVAL); i = 0; }
-                topv[round] = v;
-                topi[round] = i;
-            }
-        }
-        if (lane == 0) {
-            float MM = -INFINITY, SS = 0.f;
-            for (int w = 0; w < nw; ++w) lse_merge(MM, SS, wlse[w].x, wlse[w].y);
-            lse_s = MM + logf(SS);
-        }
+    if (tid == 0) {
+        float MM = -INFINITY, SS = 0.f;
+        for (int w = 0; w < nw; ++w) lse_merge(MM, SS, wlse[w].x, wlse[w].y);
+        lse_s = MM + logf(SS);
     }
     __syncthreads();
 
