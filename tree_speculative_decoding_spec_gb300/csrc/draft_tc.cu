@@ -33,6 +33,7 @@ constexpr int kMaxSplits = 8;   // MLP split-K: one cluster (portable size) per 
 //   SPEC_DRAFT_KB        64-column K blocks per pipeline stage
 //   SPEC_DRAFT_SMEM_KB   shared-memory budget per CTA in KB (100 keeps two CTAs per SM)
 //   SPEC_DRAFT_L2PROMO   L2 promotion of the weight loads: 0 none, 1 128 B, 2 256 B
+//   SPEC_DRAFT_EVICT_FIRST  1: weight loads carry the L2 evict-first policy
 //   SPEC_DRAFT_ROTATE    1: each CTA starts its K loop at a different stage (by
 //                        weight tile), so the CTAs do not all read the same
 //                        activation lines from L2 at the same moment
@@ -45,11 +46,15 @@ constexpr int kMaxSplits = 8;   // MLP split-K: one cluster (portable size) per 
 #ifndef SPEC_DRAFT_ROTATE
 #define SPEC_DRAFT_ROTATE 1
 #endif
+#ifndef SPEC_DRAFT_EVICT_FIRST
+#define SPEC_DRAFT_EVICT_FIRST 1
+#endif
 #ifndef SPEC_DRAFT_L2PROMO
 #define SPEC_DRAFT_L2PROMO 2
 #endif
 constexpr int kBK = 64;         // K per TMA box: one 128-byte swizzled row of bf16
 constexpr int kKB = SPEC_DRAFT_KB;
+constexpr bool kWeightsEvictFirst = SPEC_DRAFT_EVICT_FIRST != 0;
 constexpr int kBKS = kBK * kKB; // K per stage
 constexpr int kThreads = 128;
 constexpr int kStageA = kBM * kBKS * 2;
@@ -137,11 +142,17 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
         if (lane == 0) {
             // Weight tiles do not depend on the previous kernel: fill the ring first,
             // then wait for the previous kernel's results before loading activations.
+            // Weights are read once per call: evict-first in L2.
+            const uint64_t wpol = kWeightsEvictFirst ? l2_policy_evict_first() : 0;
+            auto load_w = [&](void* dst, uint64_t* bar, int x) {
+                if constexpr (kWeightsEvictFirst) tma_load_2d_hint(dst, &tmA, bar, x, m0, wpol);
+                else tma_load_2d(dst, &tmA, bar, x, m0);
+            };
             const int pre = min(n_it, p.stages);
             for (int i = 0; i < pre; ++i) {
                 mbar_arrive_expect_tx(&full[i], kStageA + stage_b);
                 for (int kb = 0; kb < kKB; ++kb)
-                    tma_load_2d(sA + i * kStageA + kb * kBoxA, &tmA, &full[i], (it0 + (i + rot) % n_it) * kBKS + kb * kBK, m0);
+                    load_w(sA + i * kStageA + kb * kBoxA, &full[i], (it0 + (i + rot) % n_it) * kBKS + kb * kBK);
             }
             const bool independent = EPI == 0 && (it0 + n_it) * kBKS <= p.dep_k0 && (blockIdx.x | blockIdx.y) != 0;
             if (!independent) griddep_wait();
@@ -160,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
                 mbar_arrive_expect_tx(&full[s], kStageA + stage_b);
                 const int kx = (it0 + (i + rot) % n_it) * kBKS;
                 for (int kb = 0; kb < kKB; ++kb) {
-                    tma_load_2d(sA + s * kStageA + kb * kBoxA, &tmA, &full[s], kx + kb * kBK, m0);
+                    load_w(sA + s * kStageA + kb * kBoxA, &full[s], kx + kb * kBK);
                     tma_load_2d(sB + s * stage_b + kb * box_b, &tmB, &full[s], kx + kb * kBK, 0);
                 }
                 issued = i + 1;
