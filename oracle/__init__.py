@@ -14,7 +14,8 @@ cites the passage it follows:
   sections on embedding conditioning, candidate tree construction, the tree
   attention matrix and greedy acceptance;
 * "Speculative Decoding" (thegustafson.com), the sections on the acceptance
-  criterion, the correctness guarantee and the worked example;
+  criterion (including what happens to the caches after it), the correctness
+  guarantee and the worked example;
 * "Medusa Heads" (ultralytics glossary), the sections on how the heads predict
   and on tree attention and acceptance;
 * Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3"
@@ -31,6 +32,7 @@ from .tree import tree_encode, tree_mask
 from .heads import silu, hydra_draft
 from .attention import tree_attention
 from .accept import greedy_accept, rejection_accept
+from .kv_commit import kv_commit
 from .philox import philox4, philox4x32_10, philox_uniform_pair, uniform_from_u32
 
 __all__ = [
@@ -38,6 +40,6 @@ __all__ = [
     "tree_encode", "tree_mask",
     "silu", "hydra_draft",
     "tree_attention",
-    "greedy_accept", "rejection_accept",
+    "greedy_accept", "rejection_accept", "kv_commit",
     "philox4", "philox4x32_10", "philox_uniform_pair", "uniform_from_u32",
 ]
