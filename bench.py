@@ -508,6 +508,8 @@ COMPONENTS = {
     "draft-hydra-b4": (3, "draft", None),
     "accept-greedy-vicuna7b": (2, "accept", None),
     "accept-rejection-32k": (5, "accept", None),
+    "kv-commit-vicuna7b": (2, "commit", None),
+    "kv-commit-70b-b8": (4, "commit", None),
 }
 
 
@@ -570,6 +572,20 @@ def run_component(args):
             d_in = d * (2 if cond[k] else 1)
             abytes += (d * d_in + d + V * d) * s + rows * (d_in + d) * s
             flops += 2.0 * rows * (d_in * d + d * V)
+    elif part == "commit":
+        # paths from the library's own greedy acceptance on planted target logits (once, untimed)
+        ax = wl.attention_inputs(w, T)
+        kc, vc, kt, vt = (dev_t(ax[k]) for k in ("k_cache", "v_cache", "k_tree", "v_tree"))
+        plen0 = dev_t(np.minimum(ax["prefix_len"], w.Lmax - tree.max_depth - 1).astype(np.int32))
+        plen = plen0.clone()
+        gw = wl.Workload("paths", "f32", B=w.B, seed=w.seed, tree=w.tree, V=4096, accept_lengths=(1, 2, 3, 4))
+        gx = wl.greedy_inputs(gw, parent)
+        alen, apath, _, _ = st.tree_accept(0, dev_t(gx["logits_p"]), None, dev_t(gx["node_tok"]), tree)
+        ws = torch.empty(st.tree_kv_commit_workspace_size(), dtype=torch.uint8, device=dev)
+        rows = int(alen.sum().item()) + w.B                   # committed rows per head, over the batch
+        abytes = 2.0 * 2 * rows * w.Hkv * w.D * s             # K and V, read from the tree and written to the cache
+        pre = lambda: plen.copy_(plen0)                       # every call commits onto the same prefix
+        call = lambda: st.tree_kv_commit(kt, vt, kc, vc, plen, alen, apath, tree, ws=ws)
     else:
         B = w.B
         if w.accept == "greedy":
@@ -591,10 +607,13 @@ def run_component(args):
 
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream()
+    if part != "commit":
+        pre = lambda: None
 
     def timed(n):
         evs = []
         for _ in range(n):
+            pre()
             flush()
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)

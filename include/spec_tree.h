@@ -248,6 +248,41 @@ spec_status tree_accept(int32_t mode, const float* logits_p, const float* logits
 spec_status spec_philox_uniform(uint64_t seed, uint64_t offset, int32_t B, int32_t T,
                                 float* u_accept, float* u_sample, spec_stream_t s);
 
+/* Workspace bytes tree_kv_commit needs (its status word only). */
+size_t tree_kv_commit_workspace_size(void);
+
+/*
+ * KV commit of the accepted path -- Speculative Decoding (thegustafson.com),
+ * section "The acceptance criterion" (the suffix past the rejection point is
+ * discarded from the caches; the next round starts from the last accepted
+ * token), and Hydra Guide, section "3. Tree KV-Cache Page Sizing" (discarded
+ * candidates are rolled back without deallocation).
+ *
+ * For every sequence b with m = accept_len[b] and L = prefix_len[b]: the K and
+ * V rows of the m + 1 nodes accept_path[b, 0..m] (root first) of every KV head
+ * are copied from the tree buffers to cache rows L .. L + m, and prefix_len[b]
+ * becomes L + m + 1.  No other cache row changes: the rejected nodes are never
+ * copied.  The extra token tree_accept emits is not committed (it is the root
+ * of the next round's tree).
+ *
+ *   k_tree, v_tree    device [B, Hkv, T, D] (dt): the tree nodes' keys/values
+ *   k_cache, v_cache  device [B, Hkv, Lmax, D] (dt), updated in place
+ *   prefix_len        device [B], updated in place
+ *   accept_len        device [B]; accept_path device [B, max_depth + 1]: the
+ *                     outputs of tree_accept for the same tree
+ *   ws                >= tree_kv_commit_workspace_size() bytes, 16-byte aligned
+ * Tree, cache and tree buffers 16-byte aligned; D * element size a multiple of
+ * 16 bytes.  Host-checked arguments fail with a status before anything is
+ * queued.  A sequence whose path is not root-first along tree edges, whose m is
+ * outside 0..max_depth, or whose commit would pass Lmax is left unchanged and
+ * SPEC_EINVAL goes to the status word (spec_read_device_status).  Caller owns
+ * every buffer; the call queues work on s and does not synchronise.
+ */
+spec_status tree_kv_commit(const void* k_tree, const void* v_tree, void* k_cache, void* v_cache,
+                           int32_t* prefix_len, const int32_t* accept_len, const int32_t* accept_path,
+                           const spec_tree* tree, int32_t B, int32_t Hkv, int32_t Lmax, int32_t D,
+                           spec_dtype dt, void* ws, size_t ws_bytes, spec_stream_t s);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char* spec_last_error(void);
 

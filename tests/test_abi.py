@@ -181,6 +181,27 @@ def test_entry_points_reject_before_launch(lib):
     assert st == 1
 
 
+def test_kv_commit_rejects_before_launch(lib):
+    # every call here fails a host check, so nothing is queued (no device access)
+    import spec_workloads as wl
+    parent, _ = wl.cartesian_tree((2, 3))
+    t = _fake_tree(lib, [int(x) for x in parent])
+    L = lib._lib
+    vp = ctypes.c_void_p
+    assert L.tree_kv_commit_workspace_size() == 256
+
+    def call(k_tree=FAKE, k_cache=FAKE, D=64, dt=1, ws_bytes=256, B=1, tree=t):
+        return L.tree_kv_commit(vp(k_tree), vp(FAKE), vp(k_cache), vp(FAKE), vp(FAKE), vp(FAKE), vp(FAKE),
+                                ctypes.byref(tree), B, 4, 128, D, dt, vp(FAKE), ws_bytes, None)
+    assert call(k_tree=0) == 1                 # NULL buffer
+    assert call(k_cache=FAKE + 4) == 3         # misaligned cache
+    assert call(D=4) == 1                      # 8-byte rows (bf16): not 16-byte chunks
+    assert call(ws_bytes=16) == 4              # workspace below its size
+    assert call(dt=7) == 5                     # dtype
+    assert call(B=0) == 1
+    assert call(tree=lib.spec_tree()) == 1     # a tree that was never built
+
+
 def test_binding_refuses_to_run_without_library(tmp_path, monkeypatch):
     # the product path fails loudly when the compiled library is absent
     import importlib

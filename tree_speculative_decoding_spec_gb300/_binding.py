@@ -65,6 +65,8 @@ def _load():
         "tree_attention_noalloc": (i32, [vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp]),
         "tree_accept_workspace_size": (sz, [i32, tp, i32, i32]),
         "tree_accept": (i32, [i32, vp, vp, vp, tp, i32, i32, f32, u64, u64, vp, vp, vp, vp, vp, sz, vp]),
+        "tree_kv_commit_workspace_size": (sz, []),
+        "tree_kv_commit": (i32, [vp, vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, vp, sz, vp]),
         "spec_philox_uniform": (i32, [u64, u64, i32, i32, vp, vp, vp]),
         "spec_last_error": (ctypes.c_char_p, []),
         "spec_read_device_status": (i32, [vp, _i32p, vp]),
@@ -350,6 +352,40 @@ def tree_accept(mode, logits_p, logits_q, node_tok, tree, temperature=1.0, seed=
                                                int(offset), _ptr(accept_len), _ptr(accept_path), _ptr(next_token),
                                                _ptr(margin), _ptr(ws), ws.numel(), _stream(stream)))
     return accept_len, accept_path, next_token, margin
+
+
+def tree_kv_commit_workspace_size():
+    return int(_lib.tree_kv_commit_workspace_size())
+
+
+def tree_kv_commit(k_tree, v_tree, k_cache, v_cache, prefix_len, accept_len, accept_path, tree, ws=None,
+                   stream=None):
+    """Append the accepted path's K/V rows to the caches and advance prefix_len, in place."""
+    _need(k_tree, "k_tree", ndim=4)
+    dev = k_tree.device
+    B, Hkv, T, D = k_tree.shape
+    if T != tree.T:
+        raise ValueError(f"k_tree has {T} nodes, the tree {tree.T}")
+    for name, t in (("v_tree", v_tree), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _need(t, name, dtype=k_tree.dtype, ndim=4, device=dev)
+    if tuple(v_tree.shape) != (B, Hkv, T, D):
+        raise ValueError("v_tree must match k_tree")
+    Lmax = k_cache.shape[2]
+    if tuple(k_cache.shape) != (B, Hkv, Lmax, D) or tuple(v_cache.shape) != (B, Hkv, Lmax, D):
+        raise ValueError("caches must be [B, Hkv, Lmax, D] with the tree's B, Hkv and D")
+    _need(prefix_len, "prefix_len", dtype=torch.int32, ndim=1, device=dev)
+    _need(accept_len, "accept_len", dtype=torch.int32, ndim=1, device=dev)
+    _need(accept_path, "accept_path", dtype=torch.int32, ndim=2, device=dev)
+    if prefix_len.shape[0] != B or accept_len.shape[0] != B or tuple(accept_path.shape) != (B, tree.max_depth + 1):
+        raise ValueError("prefix_len, accept_len [B] and accept_path [B, max_depth + 1] must match")
+    dt = _dtype_code(k_tree)
+    ws = _workspace(int(_lib.tree_kv_commit_workspace_size()), dev, ws)
+    with torch.cuda.device(dev):
+        _check("tree_kv_commit", _lib.tree_kv_commit(_ptr(k_tree), _ptr(v_tree), _ptr(k_cache), _ptr(v_cache),
+                                                     _ptr(prefix_len), _ptr(accept_len), _ptr(accept_path),
+                                                     tree.ref(), B, Hkv, Lmax, D, dt, _ptr(ws), ws.numel(),
+                                                     _stream(stream)))
+    return ws
 
 
 def spec_philox_uniform(seed, offset, B, T, device=None, stream=None):
