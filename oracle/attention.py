@@ -75,3 +75,35 @@ def tree_attention(q, k_cache, v_cache, prefix_len, k_tree, v_tree, tree, dtype,
             O[b, h] = (P @ np.concatenate([Vp, Vt], axis=0)) / denom
             lse[b, h] = (m + np.log(denom))[:, 0]
     return O, lse
+
+
+def gather_pages(pool, block_table, block_size, prefix_len):
+    """Contiguous caches [B, Hkv, n_blocks * block_size, D] from a paged pool.
+
+    Hydra Guide, "Hydra Production Engineering Checklist", item 3 (KV-Cache
+    Tree Branch Management): the cache lives in pre-allocated static blocks.
+    Taken here: pool [num_blocks, Hkv, block_size, D]; block_table[b, j] is the
+    pool block holding positions j*block_size .. (j+1)*block_size - 1 of
+    sequence b.  Entries past the last block prefix_len[b] needs are not read
+    (their rows come out as zeros).
+    """
+    pool = np.asarray(pool)
+    block_table = np.asarray(block_table, dtype=np.int64)
+    B, n_blocks = block_table.shape
+    _, Hkv, bs, D = pool.shape
+    if bs != block_size:
+        raise ValueError("pool block size differs from block_size")
+    out = np.zeros((B, Hkv, n_blocks * bs, D), dtype=pool.dtype)
+    for b in range(B):
+        used = -(-int(prefix_len[b]) // bs)
+        for j in range(used):
+            out[b, :, j * bs:(j + 1) * bs] = pool[block_table[b, j]]
+    return out
+
+
+def tree_attention_paged(q, k_pool, v_pool, block_table, block_size, prefix_len, k_tree, v_tree, tree, dtype,
+                         scale=None, heads=None):
+    """tree_attention over a paged cache: the pages gathered into contiguous rows, then the same definition."""
+    k_cache = gather_pages(k_pool, block_table, block_size, prefix_len)
+    v_cache = gather_pages(v_pool, block_table, block_size, prefix_len)
+    return tree_attention(q, k_cache, v_cache, prefix_len, k_tree, v_tree, tree, dtype, scale=scale, heads=heads)
