@@ -508,6 +508,7 @@ COMPONENTS = {
     "draft-hydra-b4": (3, "draft", None),
     "accept-greedy-vicuna7b": (2, "accept", None),
     "accept-rejection-32k": (5, "accept", None),
+    "attention-paged-70b-b8": (4, "attention_paged", None),
     "kv-commit-vicuna7b": (2, "commit", None),
     "kv-commit-70b-b8": (4, "commit", None),
 }
@@ -547,6 +548,30 @@ def run_component(args):
                          dtype=torch.uint8, device=dev)
         call = lambda: st.tree_attention(q, kc, vc, plen, kt, vt, tree, out=out, lse=lse, ws=ws)
         L = [int(x) for x in ax["prefix_len"]]
+        abytes = (sum(L) * w.Hkv * w.D * 2 * s + w.B * w.Hq * T * w.D * s + w.B * w.Hkv * T * w.D * 2 * s
+                  + w.B * w.Hq * T * (w.D + 1) * 4)
+        flops = 4.0 * w.D * w.Hq * T * sum(l + T for l in L)
+    elif part == "attention_paged":
+        # the same layer over a paged pool: 128-key blocks scattered to a shuffled slot order
+        ax = wl.attention_inputs(w, T)
+        bs = 128
+        n_blocks = w.Lmax // bs
+        L = [int(x) for x in ax["prefix_len"]]
+        slots = np.random.default_rng(w.seed).permutation(w.B * n_blocks)
+        table = slots.reshape(w.B, n_blocks).astype(np.int32)
+        kpool = np.empty((w.B * n_blocks, w.Hkv, bs, w.D), dtype=ax["k_cache"].dtype)
+        vpool = np.empty_like(kpool)
+        for b in range(w.B):
+            for j in range(n_blocks):
+                kpool[table[b, j]] = ax["k_cache"][b, :, j * bs:(j + 1) * bs]
+                vpool[table[b, j]] = ax["v_cache"][b, :, j * bs:(j + 1) * bs]
+        q, plen, kt, vt = (dev_t(ax[k]) for k in ("q", "prefix_len", "k_tree", "v_tree"))
+        kp, vp, tb = dev_t(kpool), dev_t(vpool), dev_t(table)
+        out = torch.empty(w.B, w.Hq, T, w.D, dtype=torch.float32, device=dev)
+        lse = torch.empty(w.B, w.Hq, T, dtype=torch.float32, device=dev)
+        ws = torch.empty(st.tree_attention_paged_workspace_size(tree, w.B, w.Hq, w.Hkv, n_blocks, bs, w.D,
+                                                                1 if s == 2 else 0), dtype=torch.uint8, device=dev)
+        call = lambda: st.tree_attention_paged(q, kp, vp, tb, plen, kt, vt, tree, out=out, lse=lse, ws=ws)
         abytes = (sum(L) * w.Hkv * w.D * 2 * s + w.B * w.Hq * T * w.D * s + w.B * w.Hkv * T * w.D * 2 * s
                   + w.B * w.Hq * T * (w.D + 1) * 4)
         flops = 4.0 * w.D * w.Hq * T * sum(l + T for l in L)

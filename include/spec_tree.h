@@ -162,7 +162,9 @@ size_t tree_attention_workspace_size(const spec_tree* tree, int32_t B, int32_t H
  *     out   = softmax(scale * q . keys) . values,  lse = log(sum exp(scale * q . keys))
  *
  *   q                 device [B, Hq, T, D]
- *   k_cache, v_cache  device [B, Hkv, Lmax, D]; rows >= prefix_len[b] are not read
+ *   k_cache, v_cache  device [B, Hkv, Lmax, D]; rows >= prefix_len[b] do not affect the
+ *                     result (the tensor-core path reads, then discards, those inside
+ *                     the last 128-key tile of a sequence: they must be readable memory)
  *   prefix_len        device [B], each in 0 .. Lmax (values outside are clamped to it)
  *   k_tree, v_tree    device [B, Hkv, T, D]: keys/values of the tree tokens
  *   scale             > 0 (usually 1/sqrt(D))
@@ -200,6 +202,34 @@ spec_status tree_attention_noalloc(const void* q, const void* k_cache, const voi
                                    const int32_t* prefix_len, const void* k_tree, const void* v_tree,
                                    const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
                                    int32_t D, float scale, spec_dtype dt, float* out, float* lse, spec_stream_t s);
+
+/* Workspace bytes tree_attention_paged needs (0 on invalid arguments). */
+size_t tree_attention_paged_workspace_size(const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv,
+                                           int32_t max_blocks, int32_t block_size, int32_t D, spec_dtype dt);
+
+/*
+ * Tree attention over a paged KV cache -- Hydra Guide, "Hydra Production
+ * Engineering Checklist", item 3 (KV-Cache Tree Branch Management: the tree
+ * attention KV cache lives in pre-allocated static blocks).  The same result
+ * as tree_attention with k_cache[b, :, j] = k_pool[block_table[b, j / block_size],
+ * :, j % block_size] (likewise V).
+ *
+ *   k_pool, v_pool  device [num_blocks, Hkv, block_size, D]
+ *   block_table     device [B, max_blocks] int32: pool block of positions
+ *                   j*block_size .. (j+1)*block_size - 1 of sequence b; only the
+ *                   first ceil(prefix_len[b] / block_size) entries are read
+ *   prefix_len      device [B], each in 0 .. max_blocks * block_size (clamped)
+ *   block_size      a positive multiple of 64; max_blocks * block_size <= 2^22
+ *   the rest as tree_attention.
+ * A table entry outside 0 .. num_blocks-1 is reported as SPEC_EINVAL in the
+ * status word and its keys read as zeros (no memory outside the pool is read).
+ */
+spec_status tree_attention_paged(const void* q, const void* k_pool, const void* v_pool, int32_t num_blocks,
+                                 const int32_t* block_table, int32_t max_blocks, int32_t block_size,
+                                 const int32_t* prefix_len, const void* k_tree, const void* v_tree,
+                                 const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                 float scale, spec_dtype dt, float* out, float* lse, void* ws,
+                                 size_t ws_bytes, spec_stream_t s);
 
 /* Workspace bytes tree_accept needs (0 on invalid arguments). */
 size_t tree_accept_workspace_size(int32_t mode, const spec_tree* tree, int32_t B, int32_t V);

@@ -63,6 +63,9 @@ def _load():
         "tree_attention_workspace_size": (sz, [tp, i32, i32, i32, i32, i32, i32]),
         "tree_attention": (i32, [vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]),
         "tree_attention_noalloc": (i32, [vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp]),
+        "tree_attention_paged_workspace_size": (sz, [tp, i32, i32, i32, i32, i32, i32, i32]),
+        "tree_attention_paged": (i32, [vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, tp, i32, i32, i32, i32, f32, i32,
+                                       vp, vp, vp, sz, vp]),
         "tree_accept_workspace_size": (sz, [i32, tp, i32, i32]),
         "tree_accept": (i32, [i32, vp, vp, vp, tp, i32, i32, f32, u64, u64, vp, vp, vp, vp, vp, sz, vp]),
         "tree_kv_commit_workspace_size": (sz, []),
@@ -275,6 +278,54 @@ def tree_attention(q, k_cache, v_cache, prefix_len, k_tree, v_tree, tree, scale=
                                                      _ptr(k_tree), _ptr(v_tree), tree.ref(), B, Hq, Hkv, Lmax, D,
                                                      float(scale), dt, _ptr(out), _ptr(lse), _ptr(ws), ws.numel(),
                                                      _stream(stream)))
+    return out, lse
+
+
+def tree_attention_paged_workspace_size(tree, B, Hq, Hkv, max_blocks, block_size, D, dt):
+    n = _lib.tree_attention_paged_workspace_size(tree.ref(), B, Hq, Hkv, max_blocks, block_size, D, dt)
+    if n == 0:
+        raise SpecError("tree_attention_paged_workspace_size", 1, _lib.spec_last_error().decode())
+    return int(n)
+
+
+def tree_attention_paged(q, k_pool, v_pool, block_table, prefix_len, k_tree, v_tree, tree, scale=None, out=None,
+                         lse=None, want_lse=True, ws=None, stream=None):
+    """Tree attention over a paged cache: pools [num_blocks, Hkv, block_size, D], block_table [B, max_blocks] int32."""
+    _need(q, "q", ndim=4)
+    dev = q.device
+    dt = _dtype_code(q)
+    B, Hq, T, D = q.shape
+    _need(k_pool, "k_pool", dtype=q.dtype, ndim=4, device=dev)
+    _need(v_pool, "v_pool", dtype=q.dtype, ndim=4, device=dev)
+    num_blocks, Hkv, bs = k_pool.shape[0], k_pool.shape[1], k_pool.shape[2]
+    if tuple(k_pool.shape) != (num_blocks, Hkv, bs, D) or tuple(v_pool.shape) != (num_blocks, Hkv, bs, D):
+        raise ValueError("pools must be [num_blocks, Hkv, block_size, D]")
+    _need(block_table, "block_table", dtype=torch.int32, ndim=2, device=dev)
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks]")
+    max_blocks = block_table.shape[1]
+    _need(k_tree, "k_tree", dtype=q.dtype, ndim=4, device=dev)
+    _need(v_tree, "v_tree", dtype=q.dtype, ndim=4, device=dev)
+    if tuple(k_tree.shape) != (B, Hkv, T, D) or tuple(v_tree.shape) != (B, Hkv, T, D):
+        raise ValueError("tree keys/values must be [B, Hkv, T, D]")
+    if T != tree.T:
+        raise ValueError(f"q has {T} nodes, the tree {tree.T}")
+    _need(prefix_len, "prefix_len", dtype=torch.int32, ndim=1, device=dev)
+    if scale is None:
+        scale = 1.0 / (D ** 0.5)
+    if out is None:
+        out = torch.empty(B, Hq, T, D, dtype=torch.float32, device=dev)
+    if lse is None and want_lse:
+        lse = torch.empty(B, Hq, T, dtype=torch.float32, device=dev)
+    nws = _lib.tree_attention_paged_workspace_size(tree.ref(), B, Hq, Hkv, max_blocks, bs, D, dt)
+    if nws == 0:
+        raise SpecError("tree_attention_paged_workspace_size", 1, _lib.spec_last_error().decode())
+    ws = _workspace(nws, dev, ws)
+    with torch.cuda.device(dev):
+        _check("tree_attention_paged", _lib.tree_attention_paged(
+            _ptr(q), _ptr(k_pool), _ptr(v_pool), num_blocks, _ptr(block_table), max_blocks, bs, _ptr(prefix_len),
+            _ptr(k_tree), _ptr(v_tree), tree.ref(), B, Hq, Hkv, D, float(scale), dt, _ptr(out), _ptr(lse), _ptr(ws),
+            ws.numel(), _stream(stream)))
     return out, lse
 
 

@@ -33,7 +33,7 @@ __global__ void __launch_bounds__(256) k_attn_fma(const T* __restrict__ q, const
                                                   const T* __restrict__ kt, const T* __restrict__ vt,
                                                   const uint64_t* __restrict__ anc, int Tn, int words, int Hq, int Hkv,
                                                   int Lmax, float scale_log2, int chunk, int n_pre, int n_rowblocks,
-                                                  float* __restrict__ part) {
+                                                  float* __restrict__ part, const tc::KvPages pg, void* ws) {
     constexpr int LD = D + 4;
     constexpr int LP = BC + 4;
     constexpr int DT = D / 16;   // output dims per thread
@@ -94,8 +94,19 @@ __global__ void __launch_bounds__(256) k_attn_fma(const T* __restrict__ q, const
             const int j = j0 + jl;
             float kv[4] = {0.f, 0.f, 0.f, 0.f}, vv[4] = {0.f, 0.f, 0.f, 0.f};
             if (j < k_end) {
-                load4(Kb + static_cast<size_t>(j) * D + c4 * 4, kv);
-                load4(Vb + static_cast<size_t>(j) * D + c4 * 4, vv);
+                if (!tail && pg.table) {   // paged prefix: the key's pool block and row
+                    const int blk = pg.table[static_cast<size_t>(b) * pg.max_blocks + j / pg.bs];
+                    if (blk >= 0 && blk < pg.num_blocks) {
+                        const size_t row = (static_cast<size_t>(blk) * Hkv + kvh) * pg.bs + j % pg.bs;
+                        load4(kc + row * D + c4 * 4, kv);
+                        load4(vc + row * D + c4 * 4, vv);
+                    } else {
+                        flag_status(ws, SPEC_EINVAL);   // the key reads as zeros
+                    }
+                } else {
+                    load4(Kb + static_cast<size_t>(j) * D + c4 * 4, kv);
+                    load4(Vb + static_cast<size_t>(j) * D + c4 * 4, vv);
+                }
             }
             *reinterpret_cast<float4*>(&Ks[jl * LD + c4 * 4]) = make_float4(kv[0], kv[1], kv[2], kv[3]);
             *reinterpret_cast<float4*>(&Vs[jl * LD + c4 * 4]) = make_float4(vv[0], vv[1], vv[2], vv[3]);
@@ -281,7 +292,7 @@ spec_status check_args(const spec_tree* t, int B, int Hq, int Hkv, int Lmax, int
 template <typename T>
 spec_status run_fma(const T* q, const T* kc, const T* vc, const int32_t* prefix_len, const T* kt, const T* vt,
                     const spec_tree* t, int B, int Hq, int Hkv, int Lmax, int D, float scale, float* out, float* lse,
-                    void* ws, const Plan& p, cudaStream_t s) {
+                    void* ws, const Plan& p, cudaStream_t s, const tc::KvPages& pg) {
     float* part = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kWsHeader);
     const dim3 grid(p.n_pre + 1, Hkv * p.n_rowblocks, B);
     const float sl2 = scale * kLog2e;
@@ -289,12 +300,14 @@ spec_status run_fma(const T* q, const T* kc, const T* vc, const int32_t* prefix_
         const size_t smem = sizeof(float) * (BR * 132 + 2 * BC * 132 + BR * (BC + 4));
         SPEC_CUDA_TRY(cudaFuncSetAttribute(k_attn_fma<T, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         SPEC_CUDA_TRY(launch("attn_fma", k_attn_fma<T, 128>, grid, dim3(256), smem, s, q, kc, vc, prefix_len, kt, vt,
-                             t->anc, t->T, t->words, Hq, Hkv, Lmax, sl2, p.chunk, p.n_pre, p.n_rowblocks, part));
+                             t->anc, t->T, t->words, Hq, Hkv, Lmax, sl2, p.chunk, p.n_pre, p.n_rowblocks, part, pg,
+                             ws));
     } else {
         const size_t smem = sizeof(float) * (BR * 68 + 2 * BC * 68 + BR * (BC + 4));
         SPEC_CUDA_TRY(cudaFuncSetAttribute(k_attn_fma<T, 64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem));
         SPEC_CUDA_TRY(launch("attn_fma", k_attn_fma<T, 64>, grid, dim3(256), smem, s, q, kc, vc, prefix_len, kt, vt,
-                             t->anc, t->T, t->words, Hq, Hkv, Lmax, sl2, p.chunk, p.n_pre, p.n_rowblocks, part));
+                             t->anc, t->T, t->words, Hq, Hkv, Lmax, sl2, p.chunk, p.n_pre, p.n_rowblocks, part, pg,
+                             ws));
     }
     const int nrows = B * Hq * t->T;
     SPEC_CUDA_TRY(launch("attn_combine", k_attn_combine, dim3((nrows + 7) / 8), dim3(256), 0, s, part, prefix_len, t->T,
@@ -314,14 +327,15 @@ extern "C" size_t tree_attention_workspace_size(const spec_tree* tree, int32_t B
     return attn::make_plan(tree, B, Hq, Hkv, Lmax, D, dt).total;
 }
 
-extern "C" spec_status tree_attention(const void* q, const void* k_cache, const void* v_cache,
-                                      const int32_t* prefix_len, const void* k_tree, const void* v_tree,
-                                      const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
-                                      int32_t D, float scale, spec_dtype dt, float* out, float* lse, void* ws,
-                                      size_t ws_bytes, spec_stream_t s_) {
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(s_);
-    clear_error();
-    spec_status st = attn::check_args(tree, B, Hq, Hkv, Lmax, D, dt);
+namespace spec {
+namespace attn {
+
+// Both entry points: contiguous caches (pg.table == nullptr) or a paged pool.
+static spec_status run_checked(const void* q, const void* k_cache, const void* v_cache, const int32_t* prefix_len,
+                               const void* k_tree, const void* v_tree, const spec_tree* tree, int32_t B, int32_t Hq,
+                               int32_t Hkv, int32_t Lmax, int32_t D, float scale, spec_dtype dt, float* out, float* lse,
+                               void* ws, size_t ws_bytes, cudaStream_t s, const tc::KvPages& pg) {
+    spec_status st = check_args(tree, B, Hq, Hkv, Lmax, D, dt);
     if (st != SPEC_OK) return st;
     if (!q || !k_cache || !v_cache || !prefix_len || !k_tree || !v_tree || !out)
         return fail(SPEC_EINVAL, "q, caches, prefix_len, tree K/V and out must not be NULL");
@@ -329,7 +343,7 @@ extern "C" spec_status tree_attention(const void* q, const void* k_cache, const 
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_tree) || !aligned16(v_tree) ||
         !aligned16(out) || !aligned4(prefix_len) || (lse && !aligned4(lse)))
         return fail(SPEC_EALIGN, "tensors must be 16-byte aligned (prefix_len and lse 4-byte)");
-    const attn::Plan p = attn::make_plan(tree, B, Hq, Hkv, Lmax, D, dt);
+    const Plan p = make_plan(tree, B, Hq, Hkv, Lmax, D, dt);
     if (!ws || ws_bytes < p.total) return fail(SPEC_EWORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, p.total);
     if (!aligned16(ws)) return fail(SPEC_EALIGN, "workspace must be 16-byte aligned");
     SPEC_CUDA_TRY(reset_device_status(ws, s));
@@ -339,20 +353,74 @@ extern "C" spec_status tree_attention(const void* q, const void* k_cache, const 
             float* part = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kWsHeader);
             st = tc::attn_tc_run(p.tcp, static_cast<const T*>(q), static_cast<const T*>(k_cache),
                                  static_cast<const T*>(v_cache), prefix_len, static_cast<const T*>(k_tree),
-                                 static_cast<const T*>(v_tree), tree, B, Hq, Hkv, Lmax, scale, part, ws, s);
+                                 static_cast<const T*>(v_tree), tree, B, Hq, Hkv, Lmax, scale, part, ws, s, pg);
             if (st != SPEC_OK) return st;
             const int nrows = B * Hq * tree->T;
-            SPEC_CUDA_TRY(launch("attn_combine", attn::k_attn_combine, dim3((nrows + 7) / 8), dim3(256), 0, s, part,
+            SPEC_CUDA_TRY(launch("attn_combine", k_attn_combine, dim3((nrows + 7) / 8), dim3(256), 0, s, part,
                                  prefix_len, tree->T, Hq, D, Lmax, p.tcp.chunk, p.tcp.n_pre, 1, nrows, out, lse));
             return SPEC_OK;
         }
-        return attn::run_fma<T>(static_cast<const T*>(q), static_cast<const T*>(k_cache), static_cast<const T*>(v_cache),
-                                prefix_len, static_cast<const T*>(k_tree), static_cast<const T*>(v_tree), tree, B, Hq,
-                                Hkv, Lmax, D, scale, out, lse, ws, p, s);
+        return run_fma<T>(static_cast<const T*>(q), static_cast<const T*>(k_cache), static_cast<const T*>(v_cache),
+                          prefix_len, static_cast<const T*>(k_tree), static_cast<const T*>(v_tree), tree, B, Hq, Hkv,
+                          Lmax, D, scale, out, lse, ws, p, s, pg);
     }
-    return attn::run_fma<float>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
-                                static_cast<const float*>(v_cache), prefix_len, static_cast<const float*>(k_tree),
-                                static_cast<const float*>(v_tree), tree, B, Hq, Hkv, Lmax, D, scale, out, lse, ws, p, s);
+    return run_fma<float>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
+                          static_cast<const float*>(v_cache), prefix_len, static_cast<const float*>(k_tree),
+                          static_cast<const float*>(v_tree), tree, B, Hq, Hkv, Lmax, D, scale, out, lse, ws, p, s, pg);
+}
+
+// Paged arguments: block size a multiple of 64, table entries checked on the device.
+static spec_status check_pages(int32_t num_blocks, const int32_t* block_table, int32_t max_blocks, int32_t block_size,
+                               int32_t Hkv) {
+    if (block_size < 64 || block_size % 64 != 0) return fail(SPEC_EINVAL, "block_size = %d: a positive multiple of 64", block_size);
+    if (num_blocks < 1 || max_blocks < 1) return fail(SPEC_EINVAL, "num_blocks = %d, max_blocks = %d must be positive", num_blocks, max_blocks);
+    if (static_cast<int64_t>(max_blocks) * block_size > (1 << 22))
+        return fail(SPEC_EINVAL, "max_blocks * block_size = %lld > 2^22", static_cast<long long>(max_blocks) * block_size);
+    if (static_cast<int64_t>(num_blocks) * (Hkv > 0 ? Hkv : 1) * block_size > INT32_MAX)
+        return fail(SPEC_EINVAL, "pool of %d blocks too large (num_blocks * Hkv * block_size rows >= 2^31)", num_blocks);
+    if (!block_table) return fail(SPEC_EINVAL, "block_table must not be NULL");
+    if (!aligned4(block_table)) return fail(SPEC_EALIGN, "block_table must be 4-byte aligned");
+    return SPEC_OK;
+}
+
+}  // namespace attn
+}  // namespace spec
+
+extern "C" spec_status tree_attention(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* prefix_len, const void* k_tree, const void* v_tree,
+                                      const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
+                                      int32_t D, float scale, spec_dtype dt, float* out, float* lse, void* ws,
+                                      size_t ws_bytes, spec_stream_t s_) {
+    clear_error();
+    return attn::run_checked(q, k_cache, v_cache, prefix_len, k_tree, v_tree, tree, B, Hq, Hkv, Lmax, D, scale, dt, out,
+                             lse, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s_), tc::KvPages{});
+}
+
+extern "C" size_t tree_attention_paged_workspace_size(const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv,
+                                                      int32_t max_blocks, int32_t block_size, int32_t D, spec_dtype dt) {
+    clear_error();
+    if (block_size < 64 || block_size % 64 != 0 || max_blocks < 1 ||
+        static_cast<int64_t>(max_blocks) * block_size > (1 << 22))
+        return 0;
+    return tree_attention_workspace_size(tree, B, Hq, Hkv, max_blocks * block_size, D, dt);
+}
+
+extern "C" spec_status tree_attention_paged(const void* q, const void* k_pool, const void* v_pool, int32_t num_blocks,
+                                            const int32_t* block_table, int32_t max_blocks, int32_t block_size,
+                                            const int32_t* prefix_len, const void* k_tree, const void* v_tree,
+                                            const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv, int32_t D,
+                                            float scale, spec_dtype dt, float* out, float* lse, void* ws,
+                                            size_t ws_bytes, spec_stream_t s_) {
+    clear_error();
+    spec_status st = attn::check_pages(num_blocks, block_table, max_blocks, block_size, Hkv);
+    if (st != SPEC_OK) return st;
+    tc::KvPages pg;
+    pg.table = block_table;
+    pg.max_blocks = max_blocks;
+    pg.bs = block_size;
+    pg.num_blocks = num_blocks;
+    return attn::run_checked(q, k_pool, v_pool, prefix_len, k_tree, v_tree, tree, B, Hq, Hkv, max_blocks * block_size, D,
+                             scale, dt, out, lse, ws, ws_bytes, reinterpret_cast<cudaStream_t>(s_), pg);
 }
 
 // ---------------------------------------------------------------- tree_attention without caller scratch

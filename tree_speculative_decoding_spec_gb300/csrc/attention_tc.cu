@@ -58,6 +58,7 @@ struct AttnTcParams {
     const uint64_t* anc;
     float* part;
     void* ws;
+    KvPages pg;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -148,15 +149,36 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                     break;
                 }
                 const bool tree_tile = j >= n_pt;
-                const CUtensorMap* tk = tree_tile ? &tmKt : &tmKc;
-                const CUtensorMap* tv = tree_tile ? &tmVt : &tmVc;
-                const int row = tree_tile ? kvt_row0 + (j - n_pt) * kAKeys : kvc_row0 + j * kAKeys;
                 uint8_t* st = sKV + s * kStageBytes;
                 mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
-                tma_load_2d(st, tk, &kv_full[s], 0, row);
-                tma_load_2d(st + kKVHalf, tk, &kv_full[s], 64, row);
-                tma_load_2d(st + 2 * kKVHalf, tv, &kv_full[s], 0, row);
-                tma_load_2d(st + 3 * kKVHalf, tv, &kv_full[s], 64, row);
+                if (!tree_tile && p.pg.table) {
+                    // paged prefix: two 64-key halves, each inside one pool block (bs is a
+                    // multiple of 64); keys past the prefix read the last used block (they are
+                    // masked, and their V rows zeroed, by the softmax threads)
+                    for (int hh = 0; hh < 2; ++hh) {
+                        const int pos = pre_begin + j * kAKeys + hh * 64;
+                        const int lb = min(pos / p.pg.bs, (L - 1) / p.pg.bs);
+                        int blk = p.pg.table[static_cast<size_t>(b) * p.pg.max_blocks + lb];
+                        if (blk < 0 || blk >= p.pg.num_blocks) {
+                            flag_status(p.ws, SPEC_EINVAL);
+                            blk = 0;
+                        }
+                        const int row = (blk * p.Hkv + kvh) * p.pg.bs + pos % p.pg.bs;
+                        const int off = hh * (kKVHalf / 2);
+                        tma_load_2d(st + off, &tmKc, &kv_full[s], 0, row);
+                        tma_load_2d(st + kKVHalf + off, &tmKc, &kv_full[s], 64, row);
+                        tma_load_2d(st + 2 * kKVHalf + off, &tmVc, &kv_full[s], 0, row);
+                        tma_load_2d(st + 3 * kKVHalf + off, &tmVc, &kv_full[s], 64, row);
+                    }
+                } else {
+                    const CUtensorMap* tk = tree_tile ? &tmKt : &tmKc;
+                    const CUtensorMap* tv = tree_tile ? &tmVt : &tmVc;
+                    const int row = tree_tile ? kvt_row0 + (j - n_pt) * kAKeys : kvc_row0 + j * kAKeys;
+                    tma_load_2d(st, tk, &kv_full[s], 0, row);
+                    tma_load_2d(st + kKVHalf, tk, &kv_full[s], 64, row);
+                    tma_load_2d(st + 2 * kKVHalf, tv, &kv_full[s], 0, row);
+                    tma_load_2d(st + 3 * kKVHalf, tv, &kv_full[s], 64, row);
+                }
                 issued = j + 1;
             }
         }
@@ -436,12 +458,17 @@ AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_c
 spec_status attn_tc_run(const AttnTcPlan& pl, const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
                         const int32_t* prefix_len, const __nv_bfloat16* kt, const __nv_bfloat16* vt,
                         const spec_tree* tree, int B, int Hq, int Hkv, int Lmax, float scale, float* part, void* ws,
-                        cudaStream_t s) {
+                        cudaStream_t s, const KvPages& pg) {
     const int T = tree->T;
     CUtensorMap tq, tkc, tvc, tkt, tvt;
     SPEC_CUDA_TRY(make_tmap_bf16_2d(&tq, q, static_cast<uint64_t>(B) * Hq * T, kAD, kAD, kARows));
-    SPEC_CUDA_TRY(make_tmap_bf16_2d(&tkc, kc, static_cast<uint64_t>(B) * Hkv * Lmax, kAD, kAD, kAKeys));
-    SPEC_CUDA_TRY(make_tmap_bf16_2d(&tvc, vc, static_cast<uint64_t>(B) * Hkv * Lmax, kAD, kAD, kAKeys));
+    if (pg.table) {   // pool rows, boxes of 64 (half a tile: one block holds it)
+        SPEC_CUDA_TRY(make_tmap_bf16_2d(&tkc, kc, static_cast<uint64_t>(pg.num_blocks) * Hkv * pg.bs, kAD, kAD, 64));
+        SPEC_CUDA_TRY(make_tmap_bf16_2d(&tvc, vc, static_cast<uint64_t>(pg.num_blocks) * Hkv * pg.bs, kAD, kAD, 64));
+    } else {
+        SPEC_CUDA_TRY(make_tmap_bf16_2d(&tkc, kc, static_cast<uint64_t>(B) * Hkv * Lmax, kAD, kAD, kAKeys));
+        SPEC_CUDA_TRY(make_tmap_bf16_2d(&tvc, vc, static_cast<uint64_t>(B) * Hkv * Lmax, kAD, kAD, kAKeys));
+    }
     SPEC_CUDA_TRY(make_tmap_bf16_2d(&tkt, kt, static_cast<uint64_t>(B) * Hkv * T, kAD, kAD, kAKeys));
     SPEC_CUDA_TRY(make_tmap_bf16_2d(&tvt, vt, static_cast<uint64_t>(B) * Hkv * T, kAD, kAD, kAKeys));
     AttnTcParams p{};
@@ -459,6 +486,7 @@ spec_status attn_tc_run(const AttnTcPlan& pl, const __nv_bfloat16* q, const __nv
     p.anc = tree->anc;
     p.part = part;
     p.ws = ws;
+    p.pg = pg;
     SPEC_CUDA_TRY(cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem));
     SPEC_CUDA_TRY(launch("attn_tc", k_attn_tc, dim3(pl.n_pre, Hkv * pl.n_rb, B), dim3(kAThreads), kASmem, s, tq, tkc,
                          tvc, tkt, tvt, p));

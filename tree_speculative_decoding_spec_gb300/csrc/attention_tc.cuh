@@ -8,6 +8,17 @@
 namespace spec {
 namespace tc {
 
+// Addressing of the cached prefix.  table == nullptr: contiguous caches
+// [B, Hkv, Lmax, D].  Otherwise a paged pool [num_blocks, Hkv, bs, D]:
+// position j of sequence b lives in pool block table[b * max_blocks + j / bs],
+// row j % bs (bs a multiple of 64).
+struct KvPages {
+    const int32_t* table = nullptr;
+    int max_blocks = 0;
+    int bs = 0;
+    int num_blocks = 0;
+};
+
 struct AttnTcPlan {
     int n_rb = 0;       // 128-row query blocks per KV head
     int chunk = 0;      // prefix keys per split (multiple of 128)
@@ -22,10 +33,12 @@ AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_c
 
 // Queue the split-KV kernel; it writes per-(row, split) partials in the layout
 // the combine kernel of attention.cu reads ([B*Hq*T][n_pre+1][D+4] floats).
+// kc, vc: the contiguous caches, or the pools when pg.table is set (Lmax =
+// pg.max_blocks * pg.bs then).
 spec_status attn_tc_run(const AttnTcPlan& p, const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
                         const int32_t* prefix_len, const __nv_bfloat16* kt, const __nv_bfloat16* vt,
                         const spec_tree* tree, int B, int Hq, int Hkv, int Lmax, float scale, float* part, void* ws,
-                        cudaStream_t s);
+                        cudaStream_t s, const KvPages& pg = KvPages{});
 
 }  // namespace tc
 }  // namespace spec
