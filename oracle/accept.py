@@ -155,3 +155,64 @@ def rejection_accept(logits_p, logits_q, node_tok, tree, temperature, u_accept, 
         out["margin_sample"][b] = float(np.min(np.abs(cdf - t))) / total
         out["margin"][b] = min(out["margin_decide"][b], out["margin_sample"][b])
     return out
+
+
+def typical_accept(logits_p, node_tok, tree, temperature, epsilon, alpha, u_sample):
+    """Medusa's typical acceptance on a tree.
+
+    "Medusa Heads" (ultralytics glossary), section "Tree Attention und
+    Akzeptanz": for sampling, a candidate is kept when its probability under
+    the base model exceeds a threshold tied to the entropy of that
+    distribution; more tokens are accepted, at the price of an inexact
+    distribution ("Speculative Decoding", section "Beyond draft models:
+    Medusa").  The pages give no formula and no constants.  Taken here: with
+    p_u = softmax(logits_p[u] / temperature) and H_u = -sum_x p_u(x) ln p_u(x),
+    the edge into node c with token x is accepted iff
+        p_par(x) > min(epsilon, alpha * exp(-H_par));
+    accepted(c) = accepted(parent) and that test; u* is the deepest accepted
+    node (lowest index on equal depth), and the extra token is drawn from p_u*
+    by inverse CDF in ascending token order with uniform u_sample[b].
+
+    Returns dict as greedy_accept, plus margin_decide (smallest |p - threshold|
+    over edges with an accepted parent), margin_sample (as rejection_accept)
+    and margin = the smaller of the two.
+    """
+    zp = np.asarray(logits_p, dtype=np.float64) / float(temperature)
+    B, T, V = zp.shape
+    parent, depth = tree["parent"], tree["depth"]
+    node_tok = np.asarray(node_tok, dtype=np.int64).reshape(B, T)
+    u_sample = np.asarray(u_sample, dtype=np.float64).reshape(B)
+    maxd = tree["max_depth"]
+    out = {
+        "accept_len": np.zeros(B, dtype=np.int64),
+        "accept_path": np.full((B, maxd + 1), -1, dtype=np.int64),
+        "next_token": np.zeros(B, dtype=np.int64),
+        "margin": np.full(B, np.inf),
+        "margin_decide": np.full(B, np.inf),
+        "margin_sample": np.full(B, np.inf),
+    }
+    for b in range(B):
+        logp = _log_softmax(zp[b])
+        p = np.exp(logp)
+        H = -(p * np.where(p > 0, logp, 0.0)).sum(axis=1)
+        thr = np.minimum(float(epsilon), float(alpha) * np.exp(-H))
+        accepted = np.zeros(T, dtype=bool)
+        accepted[0] = True
+        for c in range(1, T):
+            par = int(parent[c])
+            pc = p[par, int(node_tok[b, c])]
+            accepted[c] = accepted[par] and pc > thr[par]
+            if accepted[par]:
+                out["margin_decide"][b] = min(out["margin_decide"][b], abs(pc - thr[par]))
+        u = _deepest(accepted, depth)
+        cdf = np.cumsum(p[u])
+        total = cdf[-1]
+        t = u_sample[b] * total
+        x = int(np.searchsorted(cdf, t, side="right"))
+        path = _path_to(u, parent)
+        out["accept_len"][b] = depth[u]
+        out["accept_path"][b, : len(path)] = path
+        out["next_token"][b] = x
+        out["margin_sample"][b] = float(np.min(np.abs(cdf - t))) / total
+        out["margin"][b] = min(out["margin_decide"][b], out["margin_sample"][b])
+    return out
