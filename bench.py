@@ -508,6 +508,7 @@ COMPONENTS = {
     "draft-hydra-b4": (3, "draft", None),
     "accept-greedy-vicuna7b": (2, "accept", None),
     "accept-rejection-32k": (5, "accept", None),
+    "accept-typical-32k": (5, "accept_typical", None),
     "attention-paged-70b-b8": (4, "attention_paged", None),
     "kv-commit-vicuna7b": (2, "commit", None),
     "kv-commit-70b-b8": (4, "commit", None),
@@ -597,6 +598,18 @@ def run_component(args):
             d_in = d * (2 if cond[k] else 1)
             abytes += (d * d_in + d + V * d) * s + rows * (d_in + d) * s
             flops += 2.0 * rows * (d_in * d + d * V)
+    elif part == "accept_typical":
+        # Medusa typical acceptance on the long-context workload's target logits (epsilon 0.09, alpha 0.3)
+        rx = wl.rejection_inputs(w, parent, rank_arr)
+        lp, tok = dev_t(rx["logits_p"]), dev_t(rx["node_tok"])
+        abytes = 2.0 * w.B * T * w.V * 4    # the entropy pass reads every row; the walk reads the node rows again
+        outs = [torch.empty(w.B, dtype=torch.int32, device=dev),
+                torch.empty(w.B, tree.max_depth + 1, dtype=torch.int32, device=dev),
+                torch.empty(w.B, dtype=torch.int32, device=dev), torch.empty(w.B, dtype=torch.float32, device=dev)]
+        ws = torch.empty(st.tree_accept_workspace_size(2, tree, w.B, w.V), dtype=torch.uint8, device=dev)
+        call = lambda: st.tree_accept_typical(lp, tok, tree, temperature=w.temperature, epsilon=0.09, alpha=0.3,
+                                              seed=w.philox_seed, accept_len=outs[0], accept_path=outs[1],
+                                              next_token=outs[2], margin=outs[3], ws=ws)
     elif part == "commit":
         # paths from the library's own greedy acceptance on planted target logits (once, untimed)
         ax = wl.attention_inputs(w, T)

@@ -231,7 +231,7 @@ spec_status tree_attention_paged(const void* q, const void* k_pool, const void* 
                                  float scale, spec_dtype dt, float* out, float* lse, void* ws,
                                  size_t ws_bytes, spec_stream_t s);
 
-/* Workspace bytes tree_accept needs (0 on invalid arguments). */
+/* Workspace bytes tree_accept (mode 0 or 1) or tree_accept_typical (mode 2) needs (0 on invalid arguments). */
 size_t tree_accept_workspace_size(int32_t mode, const spec_tree* tree, int32_t B, int32_t V);
 
 /*
@@ -269,6 +269,30 @@ spec_status tree_accept(int32_t mode, const float* logits_p, const float* logits
                         const spec_tree* tree, int32_t B, int32_t V, float temperature,
                         uint64_t seed, uint64_t offset, int32_t* accept_len, int32_t* accept_path,
                         int32_t* next_token, float* margin, void* ws, size_t ws_bytes, spec_stream_t s);
+
+/*
+ * Typical acceptance -- Medusa Heads (ultralytics glossary), section "Tree
+ * Attention und Akzeptanz": for sampling, a candidate is kept when its
+ * probability under the base model exceeds a threshold tied to the entropy of
+ * that distribution (more tokens accepted, the distribution no longer exact;
+ * Speculative Decoding, section "Beyond draft models: Medusa").  The pages give
+ * neither the formula nor the constants; this call takes
+ *     p_u = softmax(logits_p[b, u] / temperature),  H_u = -sum_x p_u(x) ln p_u(x),
+ *     the edge into node c with token x is accepted iff p_par(x) > min(epsilon, alpha * exp(-H_par)),
+ * u* = the deepest accepted node (lowest index on equal depth), and the extra
+ * token drawn from p_u* by inverse CDF in ascending token order with the
+ * uniform u' of tree_accept (word 1 of Philox4x32-10, counter (0, b, offset)).
+ *
+ *   margin  device [B] out or NULL: the smallest |p_par(x) / threshold - 1| over
+ *           edges with an accepted parent, or the draw's distance to a CDF
+ *           breakpoint over the total, whichever is smaller
+ *   the rest as tree_accept; epsilon, alpha >= 0 and finite, temperature > 0;
+ *   the workspace is tree_accept_workspace_size(2, ...).
+ */
+spec_status tree_accept_typical(const float* logits_p, const int32_t* node_tok, const spec_tree* tree,
+                                int32_t B, int32_t V, float temperature, float epsilon, float alpha,
+                                uint64_t seed, uint64_t offset, int32_t* accept_len, int32_t* accept_path,
+                                int32_t* next_token, float* margin, void* ws, size_t ws_bytes, spec_stream_t s);
 
 /*
  * The uniforms tree_accept draws, for inspection: u_accept [B, T] (entry

@@ -173,9 +173,10 @@ def typical_accept(logits_p, node_tok, tree, temperature, epsilon, alpha, u_samp
     node (lowest index on equal depth), and the extra token is drawn from p_u*
     by inverse CDF in ascending token order with uniform u_sample[b].
 
-    Returns dict as greedy_accept, plus margin_decide (smallest |p - threshold|
-    over edges with an accepted parent), margin_sample (as rejection_accept)
-    and margin = the smaller of the two.
+    Returns dict as greedy_accept, plus margin_decide (smallest |p / threshold - 1|
+    over edges with an accepted parent: thresholds can be ~1e-4, so the distance
+    is relative), margin_sample (as rejection_accept) and margin = the smaller
+    of the two.
     """
     zp = np.asarray(logits_p, dtype=np.float64) / float(temperature)
     B, T, V = zp.shape
@@ -202,8 +203,8 @@ def typical_accept(logits_p, node_tok, tree, temperature, epsilon, alpha, u_samp
             par = int(parent[c])
             pc = p[par, int(node_tok[b, c])]
             accepted[c] = accepted[par] and pc > thr[par]
-            if accepted[par]:
-                out["margin_decide"][b] = min(out["margin_decide"][b], abs(pc - thr[par]))
+            if accepted[par] and thr[par] > 0:
+                out["margin_decide"][b] = min(out["margin_decide"][b], abs(pc / thr[par] - 1.0))
         u = _deepest(accepted, depth)
         cdf = np.cumsum(p[u])
         total = cdf[-1]

@@ -137,7 +137,8 @@ def test_workspace_sizes_and_argument_checks(lib):
     assert L.tree_attention_workspace_size(ctypes.byref(t), 1, 4, 3, 128, 64, 0) == 0         # Hq % Hkv
     assert L.tree_attention_workspace_size(ctypes.byref(t), 1, 4, 4, 128, 96, 0) == 0         # D
     assert L.tree_accept_workspace_size(0, ctypes.byref(t), 1, 1000) > 0
-    assert L.tree_accept_workspace_size(2, ctypes.byref(t), 1, 1000) == 0
+    assert L.tree_accept_workspace_size(2, ctypes.byref(t), 1, 1000) > 0       # typical acceptance
+    assert L.tree_accept_workspace_size(3, ctypes.byref(t), 1, 1000) == 0
     assert L.tree_accept_workspace_size(0, ctypes.byref(t), 1, 1) == 0
 
 
@@ -173,6 +174,13 @@ def test_entry_points_reject_before_launch(lib):
     k = (ctypes.c_int32 * 2)(2, 3)
     st = L.hydra_draft(vp(FAKE), vp(FAKE), 2, W, None, W, c, k, vp(FAKE), ctypes.byref(t), 1, 256, 1000, 0,
                        vp(FAKE), vp(FAKE), vp(0), vp(FAKE), 1 << 30, None)
+    assert st == 1
+    # mode 2 goes through tree_accept_typical; typical with a negative epsilon
+    st = L.tree_accept(2, vp(FAKE), vp(0), vp(FAKE), ctypes.byref(t), 1, 1000, 1.0, 0, 0,
+                       vp(FAKE), vp(FAKE), vp(FAKE), vp(0), vp(FAKE), 1 << 30, None)
+    assert st == 1
+    st = L.tree_accept_typical(vp(FAKE), vp(FAKE), ctypes.byref(t), 1, 1000, 1.0, -0.1, 0.3, 0, 0,
+                               vp(FAKE), vp(FAKE), vp(FAKE), vp(0), vp(FAKE), 1 << 30, None)
     assert st == 1
     # a tree struct that was never built
     empty = lib.spec_tree()

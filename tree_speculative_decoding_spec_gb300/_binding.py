@@ -68,6 +68,7 @@ def _load():
                                        vp, vp, vp, sz, vp]),
         "tree_accept_workspace_size": (sz, [i32, tp, i32, i32]),
         "tree_accept": (i32, [i32, vp, vp, vp, tp, i32, i32, f32, u64, u64, vp, vp, vp, vp, vp, sz, vp]),
+        "tree_accept_typical": (i32, [vp, vp, tp, i32, i32, f32, f32, f32, u64, u64, vp, vp, vp, vp, vp, sz, vp]),
         "tree_kv_commit_workspace_size": (sz, []),
         "tree_kv_commit": (i32, [vp, vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, vp, sz, vp]),
         "spec_philox_uniform": (i32, [u64, u64, i32, i32, vp, vp, vp]),
@@ -437,6 +438,38 @@ def tree_kv_commit(k_tree, v_tree, k_cache, v_cache, prefix_len, accept_len, acc
                                                      tree.ref(), B, Hkv, Lmax, D, dt, _ptr(ws), ws.numel(),
                                                      _stream(stream)))
     return ws
+
+
+def tree_accept_typical(logits_p, node_tok, tree, temperature=1.0, epsilon=0.09, alpha=0.3, seed=0, offset=0,
+                        accept_len=None, accept_path=None, next_token=None, margin=None, want_margin=True, ws=None,
+                        stream=None):
+    """Typical acceptance: returns (accept_len, accept_path, next_token, margin)."""
+    _need(logits_p, "logits_p", dtype=torch.float32, ndim=3)
+    dev = logits_p.device
+    B, T, V = logits_p.shape
+    if T != tree.T:
+        raise ValueError(f"logits have {T} nodes, the tree {tree.T}")
+    _need(node_tok, "node_tok", dtype=torch.int32, ndim=2, device=dev)
+    if tuple(node_tok.shape) != (B, T):
+        raise ValueError("node_tok must be [B, T]")
+    if accept_len is None:
+        accept_len = torch.empty(B, dtype=torch.int32, device=dev)
+    if accept_path is None:
+        accept_path = torch.empty(B, tree.max_depth + 1, dtype=torch.int32, device=dev)
+    if next_token is None:
+        next_token = torch.empty(B, dtype=torch.int32, device=dev)
+    if margin is None and want_margin:
+        margin = torch.empty(B, dtype=torch.float32, device=dev)
+    nws = _lib.tree_accept_workspace_size(2, tree.ref(), B, V)
+    if nws == 0:
+        raise SpecError("tree_accept_workspace_size", 1, _lib.spec_last_error().decode())
+    ws = _workspace(nws, dev, ws)
+    with torch.cuda.device(dev):
+        _check("tree_accept_typical", _lib.tree_accept_typical(
+            _ptr(logits_p), _ptr(node_tok), tree.ref(), B, V, float(temperature), float(epsilon), float(alpha),
+            int(seed), int(offset), _ptr(accept_len), _ptr(accept_path), _ptr(next_token), _ptr(margin), _ptr(ws),
+            ws.numel(), _stream(stream)))
+    return accept_len, accept_path, next_token, margin
 
 
 def spec_philox_uniform(seed, offset, B, T, device=None, stream=None):

@@ -129,6 +129,77 @@ __device__ __forceinline__ float2 thread_lse(const float* __restrict__ row, int 
     return make_float2(m, s);
 }
 
+// (m, s, t) with m the max, s = sum exp(x - m) and t = sum exp(x - m) * x over
+// this thread's share: (m + ln s) - t / s is the entropy of softmax(x).
+__device__ __forceinline__ float3 thread_lse_ent(const float* __restrict__ row, int v0, int v1, float inv_temp, bool vec4) {
+    float x[4 * kLseIter];
+    float m = -INFINITY;
+    if (vec4) {
+#pragma unroll
+        for (int it = 0; it < kLseIter; ++it) {
+            const int e = v0 + 4 * (static_cast<int>(threadIdx.x) + kRowThreads * it);
+            float4 q = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            if (e < v1) q = __ldcs(reinterpret_cast<const float4*>(row + e));
+            x[4 * it] = q.x * inv_temp; x[4 * it + 1] = q.y * inv_temp;
+            x[4 * it + 2] = q.z * inv_temp; x[4 * it + 3] = q.w * inv_temp;
+            m = fmaxf(m, fmaxf(fmaxf(x[4 * it], x[4 * it + 1]), fmaxf(x[4 * it + 2], x[4 * it + 3])));
+        }
+    } else {
+#pragma unroll
+        for (int it = 0; it < 4 * kLseIter; ++it) {
+            const int e = v0 + static_cast<int>(threadIdx.x) + kRowThreads * it;
+            x[it] = e < v1 ? row[e] * inv_temp : -INFINITY;
+            m = fmaxf(m, x[it]);
+        }
+    }
+    float sum = 0.f, t = 0.f;
+    if (m != -INFINITY) {
+#pragma unroll
+        for (int i = 0; i < 4 * kLseIter; ++i) {
+            const float e = expf(x[i] - m);
+            sum += e;
+            t += x[i] == -INFINITY ? 0.f : e * x[i];
+        }
+    }
+    return make_float3(m, sum, t);
+}
+
+// Merge (m2, s2, t2) into (m, s, t): s and t are both scaled to the larger maximum.
+__device__ __forceinline__ void lse_ent_merge(float& m, float& s, float& t, float m2, float s2, float t2) {
+    if (m2 == -INFINITY) return;
+    if (m == -INFINITY) { m = m2; s = s2; t = t2; return; }
+    if (m2 > m) {
+        const float a = expf(m - m2);
+        s = s * a + s2;
+        t = t * a + t2;
+        m = m2;
+    } else {
+        const float a = expf(m2 - m);
+        s += s2 * a;
+        t += t2 * a;
+    }
+}
+
+// Typical acceptance: (m, s, t) of every row of logits_p (for entropy and log-sum-exp).
+__global__ void __launch_bounds__(kRowThreads) k_rows_ent(const float* __restrict__ lp, int V, int slice, int slices,
+                                                          float inv_temp, float4* __restrict__ part) {
+    const int sl = blockIdx.x;
+    const size_t row = blockIdx.y;
+    const int v0 = sl * slice, v1 = min(V, v0 + slice);
+    const float3 P = thread_lse_ent(lp + row * V, v0, v1, inv_temp, (V & 3) == 0);
+    float m = P.x, sm = P.y, t = P.z;
+    for (int o = 16; o > 0; o >>= 1)
+        lse_ent_merge(m, sm, t, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, sm, o),
+                      __shfl_xor_sync(0xffffffffu, t, o));
+    __shared__ float4 red[kRowThreads / 32];
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_float4(m, sm, t, 0.f);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        for (int w = 1; w < kRowThreads / 32; ++w) lse_ent_merge(m, sm, t, red[w].x, red[w].y, red[w].z);
+        part[row * slices + sl] = make_float4(m, sm, t, 0.f);
+    }
+}
+
 __global__ void __launch_bounds__(kRowThreads) k_rows_lse(const float* __restrict__ lp, const float* __restrict__ lq,
                                                           const int32_t* __restrict__ child_off, int Tn, int V,
                                                           int slice, int slices, float inv_temp,
@@ -276,7 +347,10 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
                                                               uint64_t offset, int32_t* __restrict__ accept_len,
                                                               int32_t* __restrict__ accept_path,
                                                               int32_t* __restrict__ next_token, float* __restrict__ margin,
-                                                              void* ws) {
+                                                              void* ws, int typical, float eps, float alpha) {
+    // typical == 0: min(1, p/q) rejection with residual resampling; typical == 1:
+    // Medusa typical acceptance (threshold min(eps, alpha exp(-H(p_parent))), extra
+    // token from p at the last accepted node).  lse_q holds that threshold then.
     const int b = blockIdx.x;
     __shared__ float lse_p[SPEC_MAX_T], lse_q[SPEC_MAX_T];
     __shared__ unsigned char pass[SPEC_MAX_T], acc[SPEC_MAX_T];
@@ -285,6 +359,14 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
     __shared__ float fscr[32];
     for (int u = threadIdx.x; u < Tn; u += blockDim.x) {
         const float4* pr = part + (static_cast<size_t>(b) * Tn + u) * slices;
+        if (typical) {
+            float m = -INFINITY, sm = 0.f, t = 0.f;
+            for (int s = 0; s < slices; ++s) lse_ent_merge(m, sm, t, pr[s].x, pr[s].y, pr[s].z);
+            lse_p[u] = m + logf(sm);
+            const float H = lse_p[u] - t / sm;   // entropy of p_u (nats)
+            lse_q[u] = fminf(eps, alpha * expf(-H));
+            continue;
+        }
         float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
         for (int s = 0; s < slices; ++s) { lse_merge(mp, sp, pr[s].x, pr[s].y); lse_merge(mq, sq, pr[s].z, pr[s].w); }
         lse_p[u] = mp + logf(sp);
@@ -303,6 +385,12 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
         }
         const size_t prow = (static_cast<size_t>(b) * Tn + par) * V;
         const float logp = lp[prow + x] * inv_temp - lse_p[par];
+        if (typical) {
+            const float pv = expf(logp);
+            pass[c] = pv > lse_q[par];
+            if (lse_q[par] > 0.f) dmar[c] = fabsf(pv / lse_q[par] - 1.f);   // relative: thresholds can be tiny
+            continue;
+        }
         const float logq = lq[prow + x] * inv_temp - lse_q[par];
         const float ratio = expf(logp - logq);
         const float u = uniform24(spec_draw(seed, offset, static_cast<uint32_t>(c), static_cast<uint32_t>(b)).w[0]);
@@ -322,7 +410,7 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
     const size_t srow = (static_cast<size_t>(b) * Tn + ustar) * V;
     const float lsp = lse_p[ustar], lsq = lse_q[ustar];
     const float* rp = lp + srow;
-    const float* rq = lq + srow;
+    const float* rq = typical ? nullptr : lq + srow;
     // weight of token x: p (leaf, or residual all zero) or max(p - q, 0)
     auto weight = [&](int x, bool resid) -> float {
         const float pv = expf(rp[x] * inv_temp - lsp);
@@ -339,7 +427,7 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
     const int wid = threadIdx.x >> 5, ln = threadIdx.x & 31;
     const int Rw = ((V + 31) / 32 + 31) / 32 * 32;
     const int w0 = min(V, wid * Rw), w1 = min(V, w0 + Rw);
-    bool resid = !leaf;
+    bool resid = !leaf && !typical;
     auto range_sum = [&](bool rs) {
         float acc = 0.f;
         for (int x = w0 + ln; x < w1; x += 32) acc += weight(x, rs);
@@ -434,10 +522,10 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
 spec_status check_args(int mode, const spec_tree* t, int B, int V, float temperature) {
     spec_status st = check_tree(t);
     if (st != SPEC_OK) return st;
-    if (mode != 0 && mode != 1) return fail(SPEC_EINVAL, "mode = %d must be 0 (greedy) or 1 (rejection)", mode);
+    if (mode < 0 || mode > 2) return fail(SPEC_EINVAL, "mode = %d must be 0 (greedy), 1 (rejection) or 2 (typical)", mode);
     if (B < 1 || B > 65535) return fail(SPEC_EINVAL, "B = %d out of 1..65535", B);
     if (V < 2 || V > (1 << 24)) return fail(SPEC_EINVAL, "V = %d out of 2..2^24", V);
-    if (mode == 1 && !(temperature > 0.f && temperature < 1e30f)) return fail(SPEC_EINVAL, "temperature must be positive");
+    if (mode >= 1 && !(temperature > 0.f && temperature < 1e30f)) return fail(SPEC_EINVAL, "temperature must be positive");
     if (static_cast<int64_t>(B) * t->T > 65535) return fail(SPEC_EINVAL, "B * T = %lld rows exceed 65535", (long long)B * t->T);
     return SPEC_OK;
 }
@@ -459,6 +547,7 @@ extern "C" spec_status tree_accept(int32_t mode, const float* logits_p, const fl
                                    float* margin, void* ws, size_t ws_bytes, spec_stream_t s_) {
     cudaStream_t s = reinterpret_cast<cudaStream_t>(s_);
     clear_error();
+    if (mode == 2) return fail(SPEC_EINVAL, "mode 2 (typical acceptance) is tree_accept_typical");
     spec_status st = accept::check_args(mode, tree, B, V, temperature);
     if (st != SPEC_OK) return st;
     if (!logits_p || !node_tok || !accept_len || !accept_path || !next_token)
@@ -487,7 +576,40 @@ extern "C" spec_status tree_accept(int32_t mode, const float* logits_p, const fl
         SPEC_CUDA_TRY(launch("accept_walk_reject", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), 0, s, part,
                              p.slices, logits_p, logits_q, node_tok, tree->parent, tree->depth, tree->child_off,
                              tree->T, tree->max_depth, V, inv_temp, seed, offset, accept_len, accept_path, next_token,
-                             margin, ws));
+                             margin, ws, 0, 0.f, 0.f));
     }
+    return SPEC_OK;
+}
+
+extern "C" spec_status tree_accept_typical(const float* logits_p, const int32_t* node_tok, const spec_tree* tree,
+                                           int32_t B, int32_t V, float temperature, float epsilon, float alpha,
+                                           uint64_t seed, uint64_t offset, int32_t* accept_len, int32_t* accept_path,
+                                           int32_t* next_token, float* margin, void* ws, size_t ws_bytes,
+                                           spec_stream_t s_) {
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(s_);
+    clear_error();
+    spec_status st = accept::check_args(2, tree, B, V, temperature);
+    if (st != SPEC_OK) return st;
+    if (!(epsilon >= 0.f && epsilon < 1e30f) || !(alpha >= 0.f && alpha < 1e30f))
+        return fail(SPEC_EINVAL, "epsilon and alpha must be finite and >= 0");
+    if (!logits_p || !node_tok || !accept_len || !accept_path || !next_token)
+        return fail(SPEC_EINVAL, "logits_p, node_tok and the outputs must not be NULL");
+    if (!aligned16(logits_p)) return fail(SPEC_EALIGN, "logits must be 16-byte aligned");
+    if (!aligned4(node_tok) || !aligned4(accept_len) || !aligned4(accept_path) || !aligned4(next_token) ||
+        (margin && !aligned4(margin)))
+        return fail(SPEC_EALIGN, "token buffers must be 4-byte aligned");
+    const accept::Plan p = accept::make_plan(tree, B, V);
+    if (!ws || ws_bytes < p.total) return fail(SPEC_EWORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, p.total);
+    if (!aligned16(ws)) return fail(SPEC_EALIGN, "workspace must be 16-byte aligned");
+    float4* part = reinterpret_cast<float4*>(static_cast<unsigned char*>(ws) + p.off_part);
+    const dim3 grid(p.slices, B * tree->T);
+    const float inv_temp = 1.0f / temperature;
+    SPEC_CUDA_TRY(reset_device_status(ws, s));
+    SPEC_CUDA_TRY(launch("accept_rows_ent", accept::k_rows_ent, grid, dim3(accept::kRowThreads), 0, s, logits_p, V,
+                         p.slice, p.slices, inv_temp, part));
+    SPEC_CUDA_TRY(launch("accept_walk_typical", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), 0, s, part,
+                         p.slices, logits_p, static_cast<const float*>(nullptr), node_tok, tree->parent, tree->depth,
+                         tree->child_off, tree->T, tree->max_depth, V, inv_temp, seed, offset, accept_len, accept_path,
+                         next_token, margin, ws, 1, epsilon, alpha));
     return SPEC_OK;
 }
