@@ -53,13 +53,23 @@ def hydra_draft(h, E, W1, b1, W2, cond, topk, root_tok, tree, dtype,
     """Fill the candidate tree of every sequence with draft-head tokens.
 
     h [B, d]; E [V, d]; for head k (k = 0 .. K-1, filling depth k+1):
-    W1[k] [d, d_in_k] (d_in_k = d if cond[k] == 0 else 2d), b1[k] [d] or None,
+    W1[k] [d, d_in_k], b1[k] [d] or None,
     W2[k] [V, d]; topk[k] >= 1 + the largest rank among depth-(k+1) nodes.
     Float inputs are float32 arrays (dtype "f32") or bf16 bit patterns as
     uint16 (dtype "bf16").  root_tok [B] is the token of node 0.
 
     teacher_tok [B, T] (optional): tokens to condition later heads on instead of
     the oracle's own picks, so depths after a near tie stay comparable.
+
+    Input of head k for parent node u (depth k), by cond[k]:
+      0: h_b                                  (d_in = d)
+      1: [h_b || E[tok(u)]]                   (d_in = 2d; Hydra Guide, "1. Embedding
+                                               Conditioning Mechanics")
+      2: [h_b || E[tok(a_1)] || ... || E[tok(a_k)]], a_1 .. a_k = u's path below the
+         root, depth 1 first                  (d_in = (k+1) d; Hydra Guide, "2.
+                                               Generalizing to Arbitrary Tree Depths":
+                                               head k reads h and the embeddings of all
+                                               earlier candidate tokens of its path)
 
     Returns dict: node_tok int64 [B, T], node_logit [B, T], node_logprob [B, T]
     (root: its token, 0, 0), topk_gap [B, T] (for each parent row, the smallest
@@ -97,6 +107,13 @@ def hydra_draft(h, E, W1, b1, W2, cond, topk, root_tok, tree, dtype,
         rows = [(b, u) for b in range(B) for u in parents]
         if cond[k] == 0:
             X = np.stack([H[b] for b, _ in rows])
+        elif cond[k] == 2:
+            blocks = [np.stack([H[b] for b, _ in rows])]
+            paths = [[a for a in tree["anc"][u] if a != 0] for _, u in rows]   # depth order (ids grow)
+            for i in range(k):
+                toks = np.array([cond_tok[b, path[i]] for (b, _), path in zip(rows, paths)], dtype=np.int64)
+                blocks.append(_decode(np.asarray(E)[toks], dtype))
+            X = np.concatenate(blocks, axis=1)
         else:
             toks = np.array([cond_tok[b, u] for b, u in rows], dtype=np.int64)
             Erows = _decode(np.asarray(E)[toks], dtype)

@@ -156,3 +156,32 @@ def test_topk_ties_go_to_lower_token():
     out = hydra_draft(h, np.zeros((V, d), np.float32), [np.zeros((d, d), np.float32)], [None], [W2],
                       [0], [3], [0], tree, "f32")
     assert list(out["node_tok"][0, 1:]) == [2, 5, 7]
+
+
+def test_all_ancestor_conditioning_blocks_and_reduction():
+    # Hydra Guide, "2. Generalizing to Arbitrary Tree Depths": head k reads h and the
+    # embeddings of the path's tokens at depths 1..k (cond 2), depth 1 first
+    rng = np.random.default_rng(21)
+    d, V, K = 12, 30, 3
+    tree = _chain(K)
+    h = rng.standard_normal((1, d)).astype(np.float32)
+    E = rng.standard_normal((V, d)).astype(np.float32)
+    W2 = [rng.standard_normal((V, d)).astype(np.float32) for _ in range(K)]
+    A = rng.standard_normal((d, d)).astype(np.float32) * 0.5
+    b = [rng.standard_normal(d).astype(np.float32) * 0.1 for _ in range(K)]
+    Z = np.zeros((d, d), dtype=np.float32)
+    W1 = [rng.standard_normal((d, (k + 1) * d)).astype(np.float32) * 0.3 for k in range(K)]
+    t = lambda a: torch.from_numpy(np.asarray(a)).double()
+    for blocks, pick in [([Z, A, Z], 1), ([Z, Z, A], 2)]:   # head 2 sees only depth-1 / only depth-2 tokens
+        W1b = list(W1)
+        W1b[2] = np.concatenate(blocks, 1)
+        out = hydra_draft(h, E, W1b, b, W2, [2, 2, 2], [1, 1, 1], [3], tree, "f32", keep_logits=True)
+        tok = int(out["node_tok"][0, pick])
+        ref = F.linear(t(h)[0] + F.silu(F.linear(t(E[tok]), t(A), t(b[2]))), t(W2[2]))
+        np.testing.assert_allclose(out["logits"][(0, 2)], ref.numpy(), rtol=1e-12, atol=1e-12)
+    # depth <= 1: cond 2 is cond 0 at head 0 and cond 1 at head 1
+    tree2 = _chain(2)
+    a = hydra_draft(h, E, W1[:2], b[:2], W2[:2], [2, 2], [1, 1], [3], tree2, "f32")
+    c = hydra_draft(h, E, W1[:2], b[:2], W2[:2], [0, 1], [1, 1], [3], tree2, "f32")
+    np.testing.assert_array_equal(a["node_tok"], c["node_tok"])
+    np.testing.assert_allclose(a["node_logit"], c["node_logit"], rtol=0, atol=0)
