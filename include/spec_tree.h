@@ -121,6 +121,9 @@ size_t hydra_draft_workspace_size(const spec_tree* tree, int32_t B, int32_t d, i
  * (filling depth k + 1) and parent node u of sequence b:
  *     u_in = h_b                     if cond[k] == 0   (W1[k] is [d, d])
  *     u_in = [h_b || emb[tok(u)]]    if cond[k] == 1   (W1[k] is [d, 2d])
+ *     u_in = [h_b || emb[tok(a_1)] || ... || emb[tok(a_k)]]   if cond[k] == 2
+ *            (a_1 .. a_k = u's path below the root, depth 1 first; W1[k] is
+ *            [d, (k+1) d]; Hydra Guide, "2. Generalizing to Arbitrary Tree Depths")
  *     z    = h_b + SiLU(W1[k] u_in + b1[k])   (rounded to bf16 when dt is bf16)
  *     l    = W2[k] z                 ([V] logits, never written to memory)
  * A child of rank r gets the (r+1)-th largest logit (ties: lower token id).
@@ -130,7 +133,7 @@ size_t hydra_draft_workspace_size(const spec_tree* tree, int32_t B, int32_t d, i
  *   K          number of heads, >= tree->max_depth, <= SPEC_MAX_DEPTH
  *   W1, b1, W2 host arrays [K] of device pointers: W1[k] [d, d_in_k] (out x in),
  *              b1[k] [d] (a NULL entry or a NULL array means no bias), W2[k] [V, d]
- *   cond, topk host [K]: cond[k] in {0, 1}; topk[k] in 1 .. SPEC_MAX_TOPK and
+ *   cond, topk host [K]: cond[k] in {0, 1, 2}; topk[k] in 1 .. SPEC_MAX_TOPK and
  *              > the largest rank among depth-(k+1) nodes
  *   root_tok   device [B]                     token of node 0 (the base token x_t)
  *   node_tok   device [B, T] out: node 0 = root_tok, others = drafted tokens

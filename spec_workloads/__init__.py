@@ -287,7 +287,10 @@ def _rng(seed, part):
 
 
 def draft_inputs(w, B=None, seed=None):
-    """Draft-head inputs: h [B, d] ~ N(0,1); E [V, d], W1_k [d, d_in_k], b1_k [d], W2_k [V, d] ~ N(0, 0.02^2); root tokens uniform."""
+    """Draft-head inputs: h [B, d] ~ N(0,1); E [V, d], W1_k [d, d_in_k], b1_k [d], W2_k [V, d] ~ N(0, 0.02^2); root tokens uniform.
+
+    d_in_k = d (cond 0), 2d (cond 1), (k + 1) d (cond 2).
+    """
     B = w.B if B is None else B
     s = w.seed if seed is None else seed
     d, V = w.d, w.V
@@ -301,7 +304,8 @@ def draft_inputs(w, B=None, seed=None):
         "root_tok": rng.integers(0, V, size=B).astype(np.int32),
     }
     for k, c in enumerate(w.cond):
-        out["W1"].append(normal((s, 1, 10 + k), (d, d * (2 if c else 1)), 0.02, w.dtype))
+        d_in = d * (2 if c == 1 else k + 1 if c == 2 else 1)   # cond 2: h and the path's k embeddings
+        out["W1"].append(normal((s, 1, 10 + k), (d, d_in), 0.02, w.dtype))
         out["b1"].append(normal((s, 1, 30 + k), (d,), 0.02, w.dtype))
         out["W2"].append(normal((s, 1, 50 + k), (V, d), 0.02, w.dtype))
     return out

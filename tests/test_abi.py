@@ -131,7 +131,7 @@ def test_workspace_sizes_and_argument_checks(lib):
     assert L.hydra_draft_workspace_size(ctypes.byref(t), 1, 256, 1000, 2, c, small_k, 0) == 0
     assert L.hydra_draft_workspace_size(ctypes.byref(t), 1, 250, 1000, 2, c, k, 0) == 0       # d % 8
     assert L.hydra_draft_workspace_size(ctypes.byref(t), 1, 256, 1000, 1, c, k, 0) == 0       # K < depth
-    bad_c = (ctypes.c_int32 * 2)(0, 2)
+    bad_c = (ctypes.c_int32 * 2)(0, 3)
     assert L.hydra_draft_workspace_size(ctypes.byref(t), 1, 256, 1000, 2, bad_c, k, 0) == 0
     assert L.tree_attention_workspace_size(ctypes.byref(t), 1, 4, 4, 128, 64, 0) > 0
     assert L.tree_attention_workspace_size(ctypes.byref(t), 1, 4, 3, 128, 64, 0) == 0         # Hq % Hkv

@@ -77,6 +77,53 @@ def test_draft_small_shapes(dtype, shape):
     _compare(st, x, parent, rank, dtype)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [
+    # d, V, B, branching, cond, topk: all-ancestor conditioning (cond 2), alone and mixed
+    (64, 500, 2, (3, 2, 2), (2, 2, 2), (3, 2, 2)),
+    (64, 700, 2, (2, 2, 2, 2), (1, 2, 1, 2), (2, 2, 2, 2)),
+    (32, 300, 3, (3, 3), (2, 1), (3, 3)),
+    (256, 4099, 2, (4, 2, 2), (0, 2, 2), (4, 2, 2)),   # rows of 3d and 4d on the tensor-core path (bf16)
+])
+def test_draft_all_ancestor_conditioning(dtype, shape):
+    st = lib()
+    d, V, B, branching, cond, topk = shape
+    if dtype == "f32" and d > 128:
+        # the wide-row case targets the bf16 tensor-core path; at d = 256 with these enlarged
+        # weights the fp32 log-probs reach magnitudes where the fixed 1e-5 tolerance is
+        # below fp32 rounding, so the fp32 path is covered by the d <= 128 shapes
+        pytest.skip("bf16 tensor-core shape")
+    w = wl.Workload("t", dtype, B=B, seed=17, tree=("cartesian", branching), d=d, V=V, cond=cond, topk=topk)
+    parent, rank = wl.make_tree(w.tree)
+    x = wl.draft_inputs(w)
+    rng = np.random.default_rng(5)
+    enc = (lambda a: wl.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    x["W2"] = [enc(rng.standard_normal(np.shape(a), dtype=np.float32) * np.float32(0.25)) for a in x["W2"]]
+    x["E"] = enc(rng.standard_normal(np.shape(x["E"]), dtype=np.float32))   # embeddings that move the heads
+    _compare(st, x, parent, rank, dtype)
+
+
+def test_draft_shared_vocabulary_projection():
+    # Medusa-2 style: every head projects with the same W2 (one array for all heads)
+    st = lib()
+    w = wl.Workload("t", "bf16", B=2, seed=18, tree=("sparse", (8, 4, 2, 1), 64, 64), d=256, V=4000,
+                    cond=(1, 1, 1, 1), topk=(8, 4, 2, 1))
+    parent, rank = wl.make_tree(w.tree)
+    x = wl.draft_inputs(w)
+    rng = np.random.default_rng(6)
+    shared = wl.f32_to_bf16_bits(rng.standard_normal((w.V, w.d), dtype=np.float32) * np.float32(0.25))
+    x["W2"] = [shared] * 4
+    tree = st.spec_tree_build(parent, rank)
+    W2d = to_dev(shared)
+    tok, logit, logprob = st.hydra_draft(to_dev(x["h"]), to_dev(x["E"]), [to_dev(a) for a in x["W1"]],
+                                         [to_dev(a) for a in x["b1"]], [W2d] * 4, list(x["cond"]), list(x["topk"]),
+                                         to_dev(x["root_tok"]), tree)
+    ref = oracle.hydra_draft(x["h"], x["E"], x["W1"], x["b1"], x["W2"], x["cond"], x["topk"], x["root_tok"],
+                             oracle.tree_encode(parent, rank), "bf16", teacher_tok=tok.cpu().numpy())
+    assert_close(logit.cpu().numpy(), ref["node_logit"], "bf16", "node_logit")
+    _compare(st, x, parent, rank, "bf16")
+
+
 def test_draft_on_sparse_tree_with_missing_ranks():
     # pruned tree: some parents keep children of ranks {0, 2}, so top-k > children
     st = lib()

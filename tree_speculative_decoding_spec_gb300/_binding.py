@@ -205,8 +205,9 @@ def hydra_draft(h, emb, W1, b1, W2, cond, topk, root_tok, tree, node_tok=None, n
         raise ValueError("W1, b1, W2, cond and topk need one entry per head")
     for k in range(K):
         _need(W1[k], f"W1[{k}]", dtype=h.dtype, ndim=2, device=dev)
-        if tuple(W1[k].shape) != (d, d * (2 if cond[k] else 1)):
-            raise ValueError(f"W1[{k}] must be [d, {'2d' if cond[k] else 'd'}]")
+        d_in = d * (2 if cond[k] == 1 else (k + 1) if cond[k] == 2 else 1)
+        if tuple(W1[k].shape) != (d, d_in):
+            raise ValueError(f"W1[{k}] must be [d, {d_in // d}d] for cond {cond[k]}")
         _need(W2[k], f"W2[{k}]", dtype=h.dtype, ndim=2, device=dev)
         if tuple(W2[k].shape) != (V, d):
             raise ValueError(f"W2[{k}] must be [V, d]")

@@ -226,9 +226,11 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                                                 int nslices, int k, int cond, int n_int, int int_off,
                                                 const int32_t* __restrict__ internal, const int32_t* __restrict__ child_off,
                                                 const int32_t* __restrict__ child_idx, const int32_t* __restrict__ rank,
+                                                const int32_t* __restrict__ parent,
                                                 const int32_t* __restrict__ row_of, int Tn, int V,
                                                 int32_t* __restrict__ node_tok, float* __restrict__ node_logit,
                                                 float* __restrict__ node_logprob, void* ws, int next_n_int,
+                                                int next_cond, int next_ld, int kdepth,
                                                 const T* __restrict__ h, const T* __restrict__ emb, int d,
                                                 T* __restrict__ xin) {
     // Once the projection before this kernel is complete, the next head's MLP may
@@ -342,9 +344,35 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                 c_tok[tid] = topi[rank[c]];
             }
             __syncthreads();
-            const int per = d / (16 / static_cast<int>(sizeof(T)));   // 16-byte chunks per half row
-            // the embedding halves only (the h_b halves were written by the step's first
-            // kernel); every load of a chunk column is issued before any store
+            const int per = d / (16 / static_cast<int>(sizeof(T)));   // 16-byte chunks per d-wide block
+            const size_t row0 = static_cast<size_t>(b) * next_n_int;
+            if (next_cond == 2) {
+                // all-ancestor rows [h_b || E[tok(a_1)] || ... || E[tok(a_k)] || E[tok(c)]]: the
+                // blocks of u's path (depths 1..k, shared by all children) then each child's own
+                __shared__ int anc_tok[SPEC_MAX_DEPTH + 1];
+                if (tid == 0) {
+                    int a = u;
+                    for (int i = kdepth; i >= 1; --i) {
+                        anc_tok[i] = node_tok[static_cast<size_t>(b) * Tn + a];
+                        a = parent[a];
+                    }
+                }
+                __syncthreads();
+                for (int i = 1; i <= kdepth; ++i) {
+                    const uint4* er = reinterpret_cast<const uint4*>(emb + static_cast<size_t>(anc_tok[i]) * d);
+                    for (int w = tid; w < per; w += blockDim.x) {
+                        const uint4 v = er[w];
+#pragma unroll
+                        for (int a = 0; a < KMAX; ++a)
+                            if (a < nc && c_row[a] >= 0)
+                                reinterpret_cast<uint4*>(xin + (row0 + c_row[a]) * next_ld)[i * per + w] = v;
+                    }
+                }
+            }
+            // the children's own embedding blocks (block 1 for cond 1, block k + 1 for cond 2;
+            // the h_b parts were written by the step's first kernel); every load of a chunk
+            // column is issued before any store
+            const int own = next_cond == 2 ? kdepth + 1 : 1;
             for (int w0 = tid; w0 < per; w0 += 2 * blockDim.x) {
                 const int w1 = w0 + blockDim.x;   // second chunk column of this thread (if any)
                 const bool two = w1 < per;
@@ -359,9 +387,9 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
 #pragma unroll
                 for (int a = 0; a < KMAX; ++a) {
                     if (a < nc && c_row[a] >= 0) {
-                        uint4* o = reinterpret_cast<uint4*>(xin + (static_cast<size_t>(b) * next_n_int + c_row[a]) * 2 * d);
-                        o[per + w0] = ev0[a];
-                        if (two) o[per + w1] = ev1[a];
+                        uint4* o = reinterpret_cast<uint4*>(xin + (row0 + c_row[a]) * next_ld) + own * per;
+                        o[w0] = ev0[a];
+                        if (two) o[w1] = ev1[a];
                     }
                 }
             }
@@ -369,24 +397,26 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
     }
 }
 
-// The h_b halves of the conditioned heads' input rows [h_b || E[tok]] at
+// The h_b parts of the conditioned heads' input rows ([h_b || E[...]]) at
 // depths >= 1 depend on no drafted token, so the step's first kernel writes
-// them all; each select then writes only the embedding halves of the next
+// them all; each select then writes only the embedding parts of the next
 // depth.  Depth slot i lists n_int[i] rows per sequence, starting at row
 // first[i] of the per-sequence numbering and at element off[i] of the
-// input-row region (rows of 2d elements, sequence-major).
+// input-row region (rows of ld[i] elements, sequence-major).
 struct HRows {
     int per_seq;
     int n;
     int first[SPEC_MAX_DEPTH];
     int n_int[SPEC_MAX_DEPTH];
+    int ld[SPEC_MAX_DEPTH];
     size_t off[SPEC_MAX_DEPTH];
 };
 
 // CTA (b, 0): node 0 of sequence b -- its token is the root token (clamped to
 // the vocabulary, with SPEC_EINVAL in the status word, so later reads stay in
-// bounds) -- and head 0's whole input row when head 0 is conditioned.  CTA
-// (b, 1 + r): the h_b half of row r of sequence b in HRows.
+// bounds) -- and head 0's whole input row when head 0 is conditioned (cond0 1:
+// [h_b || E[root]], 2: h_b).  CTA (b, 1 + r): the h_b part of row r of
+// sequence b in HRows.
 template <typename T>
 __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn, int V, int32_t* __restrict__ node_tok,
                             float* __restrict__ node_logit, float* __restrict__ node_logprob, void* ws, int cond0,
@@ -400,7 +430,7 @@ __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn,
         while (i + 1 < hr.n && r >= hr.first[i + 1]) ++i;
         const size_t row = static_cast<size_t>(b) * hr.n_int[i] + (r - hr.first[i]);
         const uint4* hs = reinterpret_cast<const uint4*>(h + static_cast<size_t>(b) * d);
-        uint4* o = reinterpret_cast<uint4*>(xbase + hr.off[i] + row * 2 * d);
+        uint4* o = reinterpret_cast<uint4*>(xbase + hr.off[i] + row * hr.ld[i]);
         for (int w = threadIdx.x; w < d / (16 / static_cast<int>(sizeof(T))); w += blockDim.x) o[w] = hs[w];
         return;
     }
@@ -414,8 +444,14 @@ __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn,
         node_logit[static_cast<size_t>(b) * Tn] = 0.f;
         if (node_logprob) node_logprob[static_cast<size_t>(b) * Tn] = 0.f;
     }
-    if (cond0) write_next_row(xin0 + static_cast<size_t>(b) * 2 * d, h + static_cast<size_t>(b) * d,
-                              emb + static_cast<size_t>(tok) * d, d);
+    if (cond0 == 1) {
+        write_next_row(xin0 + static_cast<size_t>(b) * 2 * d, h + static_cast<size_t>(b) * d,
+                       emb + static_cast<size_t>(tok) * d, d);
+    } else if (cond0 == 2) {   // all-ancestor conditioning at depth 0: h_b alone
+        const uint4* hs = reinterpret_cast<const uint4*>(h + static_cast<size_t>(b) * d);
+        uint4* o = reinterpret_cast<uint4*>(xin0 + static_cast<size_t>(b) * d);
+        for (int w = threadIdx.x; w < d / (16 / static_cast<int>(sizeof(T))); w += blockDim.x) o[w] = hs[w];
+    }
 }
 
 // ---------------------------------------------------------------- planning
@@ -437,27 +473,32 @@ inline int rows_of(const spec_tree* t, int k, int cond, int B) {
     return cond ? B * t->n_internal_at_depth[k] : B;
 }
 
-// Lay out every conditioned depth's input rows (B x n_int rows of 2d elements
+// Input width of head k: d (cond 0), 2d (cond 1), (k + 1) d (cond 2).
+inline int d_in_of(int cond, int k, int d) { return d * (cond == 1 ? 2 : cond == 2 ? k + 1 : 1); }
+
+// Lay out every conditioned depth's input rows (B x n_int rows of d_in elements
 // each) one after the other; fills xin_at and the HRows table (depths >= 1).
-// Returns the total row count (at least 1).
-size_t xin_rows(Plan& p, const spec_tree* t, int K, const int32_t* cond, int B) {
-    size_t rows = 0;
+// Returns the total element count (at least 1).
+size_t xin_elems(Plan& p, const spec_tree* t, int K, const int32_t* cond, int B, int d) {
+    size_t elems = 0;
     p.hr = HRows{};
     for (int k = 0; k < K && k <= SPEC_MAX_DEPTH; ++k) {
         p.xin_at[k] = 0;
         const int n_int = t->n_internal_at_depth[k];
         if (!cond[k] || n_int == 0) continue;
-        p.xin_at[k] = rows;   // in rows for now
+        const int ld = d_in_of(cond[k], k, d);
+        p.xin_at[k] = elems;
         if (k >= 1 && p.hr.n < SPEC_MAX_DEPTH) {
             p.hr.first[p.hr.n] = p.hr.per_seq;
             p.hr.n_int[p.hr.n] = n_int;
-            p.hr.off[p.hr.n] = rows;
+            p.hr.ld[p.hr.n] = ld;
+            p.hr.off[p.hr.n] = elems;
             p.hr.per_seq += n_int;
             ++p.hr.n;
         }
-        rows += static_cast<size_t>(B) * n_int;
+        elems += static_cast<size_t>(B) * n_int * ld;
     }
-    return std::max<size_t>(rows, 1);
+    return std::max<size_t>(elems, 1);
 }
 
 Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* cond, const int32_t* topk, spec_dtype dt) {
@@ -476,7 +517,7 @@ Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* co
     if (p.tc) {
         p.tcp = tc::draft_tc_plan(p.max_rows, d, V);
         p.nslices = p.tcp.nslices;
-        p.off_xin = take(es * xin_rows(p, t, K, cond, B) * 2 * d);
+        p.off_xin = take(es * xin_elems(p, t, K, cond, B, d));
         p.off_z = take(es * static_cast<size_t>(p.tcp.rows_pad) * d);
         p.off_scratch = 0;   // unused: the MLP reduces its split-K partials on chip
         p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.max_rows) * p.nslices * p.kmax);
@@ -485,14 +526,12 @@ Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* co
         // at most 1024 slices per row
         p.slice_fma = std::max(4096, static_cast<int>(round_up((V + 1023) / 1024, 256)));
         p.nslices = (V + p.slice_fma - 1) / p.slice_fma;
-        p.off_xin = take(es * xin_rows(p, t, K, cond, B) * 2 * d);
+        p.off_xin = take(es * xin_elems(p, t, K, cond, B, d));
         p.off_z = take(es * static_cast<size_t>(p.max_rows) * d);
         p.off_scratch = take(sizeof(float) * static_cast<size_t>(p.max_rows) * V);
         p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.max_rows) * p.nslices * p.kmax);
         p.off_pl = take(sizeof(float2) * static_cast<size_t>(p.max_rows) * p.nslices);
     }
-    for (int k = 0; k <= SPEC_MAX_DEPTH; ++k) p.xin_at[k] *= 2 * static_cast<size_t>(d);
-    for (int i = 0; i < p.hr.n; ++i) p.hr.off[i] *= 2 * static_cast<size_t>(d);
     p.total = off;
     return p;
 }
@@ -508,7 +547,7 @@ spec_status check_args(const spec_tree* t, int B, int d, int V, int K, const int
     if (K < t->max_depth) return fail(SPEC_EINVAL, "K = %d heads for a tree of depth %d", K, t->max_depth);
     if (!cond || !topk) return fail(SPEC_EINVAL, "cond and topk must not be NULL");
     for (int k = 0; k < K; ++k) {
-        if (cond[k] != 0 && cond[k] != 1) return fail(SPEC_EINVAL, "cond[%d] = %d must be 0 or 1", k, cond[k]);
+        if (cond[k] < 0 || cond[k] > 2) return fail(SPEC_EINVAL, "cond[%d] = %d must be 0, 1 or 2", k, cond[k]);
         if (topk[k] < 1 || topk[k] > SPEC_MAX_TOPK || topk[k] > V)
             return fail(SPEC_EINVAL, "topk[%d] = %d out of 1..min(%d, V)", k, topk[k], SPEC_MAX_TOPK);
         if (k + 1 <= t->max_depth && t->max_rank_at_depth[k + 1] >= topk[k])
@@ -523,11 +562,11 @@ template <int KMAX, typename T>
 spec_status launch_select(bool pdl, const Plan& p, const spec_tree* t, int R, int k, int topk, int cond, int n_int,
                           int int_off, int next_n_int, int V, const Cand* pc, const float2* pl, int32_t* node_tok,
                           float* node_logit, float* node_logprob, void* ws, const T* h, const T* emb, int d, T* xin,
-                          cudaStream_t s) {
+                          int next_cond, int next_ld, cudaStream_t s) {
     SPEC_CUDA_TRY(launch_ex("draft_select", k_select<KMAX, T>, dim3(R), dim3(256), 0, s, pdl, pc, pl, p.nslices, topk, cond,
-                            n_int, int_off, t->internal, t->child_off, t->child_idx, t->rank, t->row_of, t->T, V,
-                            node_tok, node_logit, node_logprob, ws, next_n_int, h, emb, d, xin));
-    (void)k;
+                            n_int, int_off, t->internal, t->child_off, t->child_idx, t->rank, t->parent, t->row_of,
+                            t->T, V, node_tok, node_logit, node_logprob, ws, next_n_int, next_cond, next_ld, k, h, emb,
+                            d, xin));
     return SPEC_OK;
 }
 
@@ -545,20 +584,22 @@ spec_status run(const T* h, const T* emb, int K, const void* const* W1, const vo
     const bool first_cond = t->n_internal_at_depth[0] > 0 && cond[0];
     SPEC_CUDA_TRY(reset_device_status(ws, s));
     SPEC_CUDA_TRY(launch("draft_init_root", k_init_root<T>, dim3(B, 1 + p.hr.per_seq), dim3(128), 0, s, root_tok, B,
-                         t->T, V, node_tok, node_logit, node_logprob, ws, first_cond ? 1 : 0, h, emb, d,
+                         t->T, V, node_tok, node_logit, node_logprob, ws, first_cond ? cond[0] : 0, h, emb, d,
                          xbase + p.xin_at[0], xbase, p.hr));
     int int_off = 0;
     for (int k = 0; k < K; int_off += t->n_internal_at_depth[k], ++k) {
         const int n_int = t->n_internal_at_depth[k];
         if (n_int == 0) continue;   // no node of depth k has children: nothing to draft at depth k+1
         const int R = rows_of(t, k, cond[k], B);
-        const int d_in = d * (cond[k] ? 2 : 1);
+        const int d_in = d_in_of(cond[k], k, d);
         // conditioned rows: h_b halves by the step's first kernel, embedding halves by the previous select
         const T* X = cond[k] ? xbase + p.xin_at[k] : h;
         T* xin = k + 1 <= SPEC_MAX_DEPTH ? xbase + p.xin_at[k + 1] : xbase;   // next depth's rows
-        const int ldx = cond[k] ? 2 * d : d;
+        const int ldx = cond[k] ? d_in : d;
         const int next_n_int = (k + 1 < K && k + 1 <= SPEC_MAX_DEPTH && t->n_internal_at_depth[k + 1] > 0 && cond[k + 1])
                                    ? t->n_internal_at_depth[k + 1] : 0;
+        const int next_cond = next_n_int > 0 ? cond[k + 1] : 0;
+        const int next_ld = next_n_int > 0 ? d_in_of(next_cond, k + 1, d) : 0;
         const T* W1k = static_cast<const T*>(W1[k]);
         const T* b1k = b1 ? static_cast<const T*>(b1[k]) : nullptr;
         const T* W2k = static_cast<const T*>(W2[k]);
@@ -568,9 +609,9 @@ spec_status run(const T* h, const T* emb, int K, const void* const* W1, const vo
                                                    topk[k], p.kmax, cond[k] ? d : d_in, pc, pl, ws, s);
                 if (st != SPEC_OK) return st;
                 st = p.kmax == 8 ? launch_select<8, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
-                                                       pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, s)
+                                                       pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, s)
                                  : launch_select<16, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
-                                                        pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, s);
+                                                        pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, s);
                 if (st != SPEC_OK) return st;
                 continue;
             }
@@ -584,12 +625,12 @@ spec_status run(const T* h, const T* emb, int K, const void* const* W1, const vo
             SPEC_CUDA_TRY(launch("draft_topk_slices", k_topk_slices<8>, dim3(p.nslices, R), dim3(256), 0, s, scratch, V,
                                  topk[k], p.slice_fma, pc, pl, p.nslices));
             st = launch_select<8, T>(false, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V, pc, pl, node_tok,
-                                     node_logit, node_logprob, ws, h, emb, d, xin, s);
+                                     node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, s);
         } else {
             SPEC_CUDA_TRY(launch("draft_topk_slices", k_topk_slices<16>, dim3(p.nslices, R), dim3(256), 0, s, scratch, V,
                                  topk[k], p.slice_fma, pc, pl, p.nslices));
             st = launch_select<16, T>(false, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V, pc, pl, node_tok,
-                                      node_logit, node_logprob, ws, h, emb, d, xin, s);
+                                      node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, s);
         }
         if (st != SPEC_OK) return st;
     }
