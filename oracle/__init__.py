@@ -29,7 +29,7 @@ here is "parity unpinned".
 
 from .bf16 import bf16_bits_to_f64, f64_to_bf16_bits
 from .tree import tree_encode, tree_mask
-from .heads import silu, hydra_draft
+from .heads import silu, hydra_draft, hydra_draft_heads
 from .attention import tree_attention, tree_attention_paged, gather_pages
 from .accept import greedy_accept, rejection_accept, typical_accept
 from .kv_commit import kv_commit
@@ -38,7 +38,7 @@ from .philox import philox4, philox4x32_10, philox_uniform_pair, uniform_from_u3
 __all__ = [
     "bf16_bits_to_f64", "f64_to_bf16_bits",
     "tree_encode", "tree_mask",
-    "silu", "hydra_draft",
+    "silu", "hydra_draft", "hydra_draft_heads",
     "tree_attention", "tree_attention_paged", "gather_pages",
     "greedy_accept", "rejection_accept", "typical_accept", "kv_commit",
     "philox4", "philox4x32_10", "philox_uniform_pair", "uniform_from_u32",

@@ -13,7 +13,15 @@ the head of depth d and a parent node u of sequence b:
     l    = W2_d z                      (logits over the vocabulary)
 
 For bf16 weights z is rounded to bf16 before the projection (the projection
-consumes bf16 operands).  The head output is softmax(l); its top-k equals the
+consumes bf16 operands).
+
+A second head form (form 1) is the one the Hydra Guide prints as code: the
+fusion MLP Linear -> SiLU -> Linear -> LayerNorm followed by a bias-free
+projection (its first head: Linear -> SiLU -> LayerNorm):
+    a = SiLU(W1_d u_in + b1_d)         (rounded to bf16 for bf16 weights when it feeds W1b)
+    y = W1b_d a + b1b_d                 (y = a when there is no W1b)
+    z = (y - mean(y)) / sqrt(var(y) + eps) * gamma_d + beta_d
+with the mean and the biased variance over the d entries of y.  The head output is softmax(l); its top-k equals the
 top-k of l (softmax is monotone).
 
 Tree filling.  Hydra Guide, section "Candidate Tree Construction": head 1 takes
@@ -50,10 +58,20 @@ def _logsumexp(row):
 
 def hydra_draft(h, E, W1, b1, W2, cond, topk, root_tok, tree, dtype,
                 teacher_tok=None, keep_logits=False):
+    """Every head of form 0; see hydra_draft_heads for the arguments and the result."""
+    heads = [dict(form=0, cond=int(cond[k]), topk=int(topk[k]), W1=W1[k], b1=None if b1 is None else b1[k],
+                  W2=W2[k]) for k in range(len(W1))]
+    return hydra_draft_heads(h, E, heads, root_tok, tree, dtype, teacher_tok=teacher_tok, keep_logits=keep_logits)
+
+
+def hydra_draft_heads(h, E, heads, root_tok, tree, dtype, ln_eps=1e-5, teacher_tok=None, keep_logits=False):
     """Fill the candidate tree of every sequence with draft-head tokens.
 
-    h [B, d]; E [V, d]; for head k (k = 0 .. K-1, filling depth k+1):
-    W1[k] [d, d_in_k], b1[k] [d] or None,
+    h [B, d]; E [V, d]; heads: one dict per head k (k = 0 .. K-1, filling
+    depth k+1) with cond, topk, form (0 or 1), W1 [hidden, d_in_k], b1
+    [hidden] or None, W2 [V, d], and for form 1 W1b [d, hidden] or None, b1b,
+    gamma, beta ([d] or None: zeros / ones / zeros); ln_eps the LayerNorm
+    epsilon.  Form 0 has hidden = d.
     W2[k] [V, d]; topk[k] >= 1 + the largest rank among depth-(k+1) nodes.
     Float inputs are float32 arrays (dtype "f32") or bf16 bit patterns as
     uint16 (dtype "bf16").  root_tok [B] is the token of node 0.
@@ -76,7 +94,9 @@ def hydra_draft(h, E, W1, b1, W2, cond, topk, root_tok, tree, dtype,
     gap between consecutive sorted logits over the ranks its children use,
     +inf for rows without children), and, if keep_logits, logits {(b, u): row}.
     """
-    K = len(W1)
+    K = len(heads)
+    cond = [int(hd["cond"]) for hd in heads]
+    topk = [int(hd["topk"]) for hd in heads]
     T = tree["T"]
     parent, rank, depth, children = tree["parent"], tree["rank"], tree["depth"], tree["children"]
     if tree["max_depth"] > K:
@@ -101,9 +121,10 @@ def hydra_draft(h, E, W1, b1, W2, cond, topk, root_tok, tree, dtype,
             for c in children[u]:
                 if rank[c] >= topk[k]:
                     raise ValueError(f"node {c} has rank {rank[c]} >= top-k {topk[k]}")
-        W1k = _decode(W1[k], dtype)
-        W2k = _decode(W2[k], dtype)
-        b1k = np.zeros(d) if b1 is None or b1[k] is None else _decode(b1[k], dtype)
+        hd = heads[k]
+        W1k = _decode(hd["W1"], dtype)
+        W2k = _decode(hd["W2"], dtype)
+        b1k = np.zeros(W1k.shape[0]) if hd.get("b1") is None else _decode(hd["b1"], dtype)
         rows = [(b, u) for b in range(B) for u in parents]
         if cond[k] == 0:
             X = np.stack([H[b] for b, _ in rows])
@@ -119,7 +140,22 @@ def hydra_draft(h, E, W1, b1, W2, cond, topk, root_tok, tree, dtype,
             Erows = _decode(np.asarray(E)[toks], dtype)
             X = np.concatenate([np.stack([H[b] for b, _ in rows]), Erows], axis=1)
         A = X @ W1k.T + b1k
-        Z = np.stack([H[b] for b, _ in rows]) + silu(A)
+        if hd.get("form", 0) == 0:
+            Z = np.stack([H[b] for b, _ in rows]) + silu(A)
+        else:
+            a = silu(A)
+            if hd.get("W1b") is not None:
+                if dtype == "bf16":
+                    a = bf16_bits_to_f64(f64_to_bf16_bits(a))
+                b1b = np.zeros(d) if hd.get("b1b") is None else _decode(hd["b1b"], dtype)
+                Y = a @ _decode(hd["W1b"], dtype).T + b1b
+            else:
+                Y = a
+            gamma = np.ones(d) if hd.get("gamma") is None else _decode(hd["gamma"], dtype)
+            beta = np.zeros(d) if hd.get("beta") is None else _decode(hd["beta"], dtype)
+            mu = Y.mean(axis=1, keepdims=True)
+            var = ((Y - mu) ** 2).mean(axis=1, keepdims=True)
+            Z = (Y - mu) / np.sqrt(var + float(ln_eps)) * gamma + beta
         if dtype == "bf16":
             Z = bf16_bits_to_f64(f64_to_bf16_bits(Z))
         L = Z @ W2k.T

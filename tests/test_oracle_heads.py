@@ -185,3 +185,35 @@ def test_all_ancestor_conditioning_blocks_and_reduction():
     c = hydra_draft(h, E, W1[:2], b[:2], W2[:2], [0, 1], [1, 1], [3], tree2, "f32")
     np.testing.assert_array_equal(a["node_tok"], c["node_tok"])
     np.testing.assert_allclose(a["node_logit"], c["node_logit"], rtol=0, atol=0)
+
+
+def test_layernorm_fusion_head_form():
+    # the head form the Hydra Guide prints as code: Linear -> SiLU -> Linear -> LayerNorm,
+    # then a bias-free projection; its first head Linear -> SiLU -> LayerNorm (no W1b)
+    from oracle import hydra_draft_heads
+    rng = np.random.default_rng(31)
+    d, V, hidden, eps = 16, 50, 24, 1e-5
+    tree = tree_encode(*wl.cartesian_tree((3,)))      # root and three children: one head
+    h = rng.standard_normal((1, d)).astype(np.float32)
+    E = rng.standard_normal((V, d)).astype(np.float32)
+    W2 = rng.standard_normal((V, d)).astype(np.float32)
+    g = rng.standard_normal(d).astype(np.float32)
+    be = rng.standard_normal(d).astype(np.float32)
+    t = lambda a: torch.from_numpy(np.asarray(a)).double()
+    root = 7
+    x = torch.cat([t(h)[0], t(E[root])])               # cond 1: [h || E[root]]
+    # two layers, hidden != d
+    W1 = rng.standard_normal((hidden, 2 * d)).astype(np.float32) * 0.3
+    b1 = rng.standard_normal(hidden).astype(np.float32) * 0.1
+    W1b = rng.standard_normal((d, hidden)).astype(np.float32) * 0.3
+    b1b = rng.standard_normal(d).astype(np.float32) * 0.1
+    head = dict(form=1, cond=1, topk=3, W1=W1, b1=b1, W1b=W1b, b1b=b1b, gamma=g, beta=be, W2=W2)
+    out = hydra_draft_heads(h, E, [head], [root], tree, "f32", ln_eps=eps, keep_logits=True)
+    z = F.layer_norm(F.linear(F.silu(F.linear(x, t(W1), t(b1))), t(W1b), t(b1b)), (d,), t(g), t(be), eps)
+    np.testing.assert_allclose(out["logits"][(0, 0)], F.linear(z, t(W2)).numpy(), rtol=1e-12, atol=1e-12)
+    # one layer (no W1b), unconditioned: the printed first head
+    W1s = rng.standard_normal((d, d)).astype(np.float32) * 0.3
+    head = dict(form=1, cond=0, topk=3, W1=W1s, b1=None, W1b=None, gamma=None, beta=None, W2=W2)
+    out = hydra_draft_heads(h, E, [head], [root], tree, "f32", ln_eps=eps, keep_logits=True)
+    z = F.layer_norm(F.silu(F.linear(t(h)[0], t(W1s))), (d,), eps=eps)
+    np.testing.assert_allclose(out["logits"][(0, 0)], F.linear(z, t(W2)).numpy(), rtol=1e-12, atol=1e-12)
