@@ -506,6 +506,7 @@ COMPONENTS = {
     "attention-32k": (5, "attention", None),
     "attention-32k-t256": (5, "attention", ("dense_prefix", (4, 4, 4, 4), 256)),
     "draft-hydra-b4": (3, "draft", None),
+    "draft-ln-heads-vicuna7b": (2, "draft_ln", ("sparse", (8, 4, 2, 1), 64, 64)),
     "accept-greedy-vicuna7b": (2, "accept", None),
     "accept-rejection-32k": (5, "accept", None),
     "accept-typical-32k": (5, "accept_typical", None),
@@ -598,6 +599,30 @@ def run_component(args):
             d_in = d * (2 if cond[k] else 1)
             abytes += (d * d_in + d + V * d) * s + rows * (d_in + d) * s
             flops += 2.0 * rows * (d_in * d + d * V)
+    elif part == "draft_ln":
+        # the LayerNorm fusion head form at Vicuna-7B shape (d 4096, V 32000, inner width 1024):
+        # head 1 Linear -> SiLU -> LayerNorm, heads 2-4 Linear -> SiLU -> Linear -> LayerNorm on [h || E[parent]]
+        d, V, hid, B = 4096, 32000, 1024, 1
+        nrm = lambda key, shape, std: dev_t(wl.normal((w.seed, 7) + key, shape, std, "bf16"))
+        h, E = nrm((0,), (B, d), 1.0), nrm((1,), (V, d), 0.02)
+        root = dev_t(np.zeros(B, dtype=np.int32))
+        heads = [dict(form=1, cond=0, topk=8, W1=nrm((10,), (d, d), 0.02), b1=nrm((11,), (d,), 0.02),
+                      gamma=nrm((12,), (d,), 1.0), beta=nrm((13,), (d,), 0.02), W2=nrm((14,), (V, d), 0.02))]
+        for k, tk in zip(range(1, 4), (4, 2, 1)):
+            heads.append(dict(form=1, cond=1, topk=tk, W1=nrm((20 + k,), (hid, 2 * d), 0.02),
+                              b1=nrm((30 + k,), (hid,), 0.02), W1b=nrm((40 + k,), (d, hid), 0.02),
+                              b1b=nrm((50 + k,), (d,), 0.02), gamma=nrm((60 + k,), (d,), 1.0),
+                              beta=nrm((70 + k,), (d,), 0.02), W2=nrm((80 + k,), (V, d), 0.02)))
+        nt = torch.empty(B, T, dtype=torch.int32, device=dev)
+        nl = torch.empty(B, T, dtype=torch.float32, device=dev)
+        nlp = torch.empty(B, T, dtype=torch.float32, device=dev)
+        ws = None
+        call = lambda: st.hydra_draft_heads(h, E, heads, root, tree, node_tok=nt, node_logit=nl, node_logprob=nlp)
+        abytes = 0.0
+        for k, hd in enumerate(heads):
+            n_int = tree.struct.n_internal_at_depth[k]
+            abytes += sum(hd[n].numel() * 2 for n in ("W1", "W1b", "W2") if n in hd) + B * n_int * 3 * d * 2
+            flops += 2.0 * B * n_int * sum(hd[n].numel() for n in ("W1", "W1b", "W2") if n in hd)
     elif part == "accept_typical":
         # Medusa typical acceptance on the long-context workload's target logits (epsilon 0.09, alpha 0.3)
         rx = wl.rejection_inputs(w, parent, rank_arr)

@@ -149,6 +149,47 @@ spec_status hydra_draft(const void* h, const void* emb, int32_t K,
                         int32_t* node_tok, float* node_logit, float* node_logprob,
                         void* ws, size_t ws_bytes, spec_stream_t s);
 
+/*
+ * One draft head for hydra_draft_heads.  form 0 is hydra_draft's head; form 1
+ * is the head form that the Hydra Guide prints as code (fusion MLP
+ * Linear -> SiLU -> Linear -> LayerNorm, then a bias-free vocabulary
+ * projection; its first head Linear -> SiLU -> LayerNorm, i.e. no W1b):
+ *   form 0: z = h_b + SiLU(W1 u_in + b1)                         (hidden == d)
+ *   form 1: y = W1b SiLU(W1 u_in + b1) + b1b, or y = SiLU(W1 u_in + b1) when
+ *           W1b is NULL (then hidden == d);
+ *           z = (y - mean(y)) / sqrt(var(y) + ln_eps) * gamma + beta
+ *           (mean and biased variance over the d entries of y)
+ * then l = W2 z as in hydra_draft.  u_in follows cond exactly as in
+ * hydra_draft; with dt bf16, SiLU(W1 u_in + b1) is rounded to bf16 when it
+ * feeds W1b, and z is rounded to bf16.
+ */
+typedef struct {
+    int32_t cond;         /* 0, 1 or 2 (hydra_draft) */
+    int32_t topk;         /* 1 .. SPEC_MAX_TOPK (hydra_draft) */
+    int32_t form;         /* 0 or 1 */
+    int32_t hidden;       /* rows of W1: d for form 0 and for form 1 without W1b */
+    const void* W1;       /* device [hidden, d_in] */
+    const void* b1;       /* device [hidden] or NULL */
+    const void* W1b;      /* form 1: device [d, hidden] or NULL */
+    const void* b1b;      /* form 1: device [d] or NULL */
+    const void* gamma;    /* form 1: device [d] or NULL (ones) */
+    const void* beta;     /* form 1: device [d] or NULL (zeros) */
+    const void* W2;       /* device [V, d] (heads may share one) */
+} spec_head;
+
+/* Workspace bytes hydra_draft_heads needs (0 on invalid arguments). */
+size_t hydra_draft_heads_workspace_size(const spec_tree* tree, int32_t B, int32_t d, int32_t V, int32_t K,
+                                        const spec_head* heads, spec_dtype dt);
+
+/*
+ * hydra_draft with a per-head description (heads: host array [K]); ln_eps > 0
+ * is the LayerNorm epsilon of form-1 heads.  Everything else as hydra_draft.
+ */
+spec_status hydra_draft_heads(const void* h, const void* emb, int32_t K, const spec_head* heads,
+                              const int32_t* root_tok, const spec_tree* tree, int32_t B, int32_t d, int32_t V,
+                              float ln_eps, spec_dtype dt, int32_t* node_tok, float* node_logit,
+                              float* node_logprob, void* ws, size_t ws_bytes, spec_stream_t s);
+
 /* Workspace bytes tree_attention needs for these shapes on the current device (0 on invalid arguments). */
 size_t tree_attention_workspace_size(const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv,
                                      int32_t Lmax, int32_t D, spec_dtype dt);

@@ -26,10 +26,15 @@ def _run(st, x, tree):
 def _compare(st, x, parent, rank, dtype):
     tree = st.spec_tree_build(parent, rank)
     tok, logit, logprob = _run(st, x, tree)
-    tok, logit, logprob = tok.cpu().numpy(), logit.cpu().numpy(), logprob.cpu().numpy()
     to = oracle.tree_encode(parent, rank)
-    ref = oracle.hydra_draft(x["h"], x["E"], x["W1"], x["b1"], x["W2"], x["cond"], x["topk"], x["root_tok"], to,
-                             dtype, teacher_tok=tok, keep_logits=True)
+    ref_fn = lambda teacher: oracle.hydra_draft(x["h"], x["E"], x["W1"], x["b1"], x["W2"], x["cond"], x["topk"],
+                                                x["root_tok"], to, dtype, teacher_tok=teacher, keep_logits=True)
+    return _check(tok, logit, logprob, ref_fn, parent, dtype, x["root_tok"])
+
+
+def _check(tok, logit, logprob, ref_fn, parent, dtype, root_tok):
+    tok, logit, logprob = tok.cpu().numpy(), logit.cpu().numpy(), logprob.cpu().numpy()
+    ref = ref_fn(tok)
     B, T = tok.shape
     near = 0
     for b in range(B):
@@ -44,7 +49,7 @@ def _compare(st, x, parent, rank, dtype):
             diff = abs(row[tok[b, c]] - row[ref["node_tok"][b, c]])
             assert diff <= tol, (b, c, tok[b, c], ref["node_tok"][b, c], diff, tol)
             near += 1
-    assert tok[:, 0].tolist() == list(x["root_tok"])
+    assert tok[:, 0].tolist() == list(root_tok)
     assert_close(logit, ref["node_logit"], dtype, "node_logit")
     assert_close(logprob, ref["node_logprob"], dtype, "node_logprob")
     return near
@@ -179,3 +184,45 @@ def test_medusa_sibling_sets_repeat_on_gpu():
     for b in range(2):
         sets = [tuple(tok[b, to["children"][u]]) for u in to["children"][0]]
         assert all(s == sets[0] for s in sets)
+
+
+@pytest.mark.parametrize("dtype,d,V,hidden", [("f32", 64, 500, 96), ("bf16", 64, 700, 128), ("bf16", 256, 4099, 512)])
+def test_draft_layernorm_fusion_heads(dtype, d, V, hidden):
+    # the head form the Hydra Guide prints as code: head 1 Linear -> SiLU -> LayerNorm (no W1b),
+    # later heads Linear -> SiLU -> Linear -> LayerNorm on [h || E[...]], bias-free projection
+    st = lib()
+    rng = np.random.default_rng(d + hidden)
+    enc = (lambda a: wl.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    n = lambda *shape, sc=1.0: enc(rng.standard_normal(shape, dtype=np.float32) * np.float32(sc))
+    parent, rank = wl.make_tree(("cartesian", (3, 2, 2)))
+    B = 2
+    x = {"h": n(B, d), "E": n(V, d), "root_tok": rng.integers(0, V, size=B).astype(np.int32)}
+    heads = [dict(form=1, cond=0, topk=3, W1=n(d, d, sc=0.1), b1=n(d, sc=0.1), gamma=n(d), beta=n(d, sc=0.1),
+                  W2=n(V, d, sc=0.25)),
+             dict(form=1, cond=1, topk=2, W1=n(hidden, 2 * d, sc=0.1), b1=n(hidden, sc=0.1), W1b=n(d, hidden, sc=0.1),
+                  b1b=n(d, sc=0.1), gamma=n(d), beta=None, W2=n(V, d, sc=0.25)),
+             dict(form=1, cond=2, topk=2, W1=n(hidden, 3 * d, sc=0.1), b1=None, W1b=n(d, hidden, sc=0.1), b1b=None,
+                  gamma=None, beta=n(d, sc=0.1), W2=n(V, d, sc=0.25))]
+    tree = st.spec_tree_build(parent, rank)
+    dev_heads = [{k: (to_dev(v) if isinstance(v, np.ndarray) else v) for k, v in hd.items()} for hd in heads]
+    tok, logit, logprob = st.hydra_draft_heads(to_dev(x["h"]), to_dev(x["E"]), dev_heads, to_dev(x["root_tok"]), tree)
+    to = oracle.tree_encode(parent, rank)
+    ref_fn = lambda teacher: oracle.hydra_draft_heads(x["h"], x["E"], heads, x["root_tok"], to, dtype,
+                                                      teacher_tok=teacher, keep_logits=True)
+    _check(tok, logit, logprob, ref_fn, parent, dtype, x["root_tok"])
+
+
+def test_draft_heads_form0_matches_hydra_draft():
+    # the description entry point with form-0 heads reproduces hydra_draft bit for bit
+    st = lib()
+    w = wl.Workload("t", "bf16", B=2, seed=19, tree=("sparse", (8, 4, 2, 1), 64, 64), d=128, V=3000,
+                    cond=(1, 2, 1, 2), topk=(8, 4, 2, 1))
+    parent, rank = wl.make_tree(w.tree)
+    x = wl.draft_inputs(w)
+    tree = st.spec_tree_build(parent, rank)
+    a = _run(st, x, tree)
+    heads = [dict(form=0, cond=int(x["cond"][k]), topk=int(x["topk"][k]), W1=to_dev(x["W1"][k]), b1=to_dev(x["b1"][k]),
+                  W2=to_dev(x["W2"][k])) for k in range(4)]
+    b = st.hydra_draft_heads(to_dev(x["h"]), to_dev(x["E"]), heads, to_dev(x["root_tok"]), tree)
+    for u, v in zip(a, b):
+        np.testing.assert_array_equal(u.cpu().numpy(), v.cpu().numpy())

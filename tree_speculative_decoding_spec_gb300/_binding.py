@@ -38,6 +38,12 @@ class spec_tree(ctypes.Structure):
     ]
 
 
+class spec_head(ctypes.Structure):
+    _fields_ = [("cond", ctypes.c_int32), ("topk", ctypes.c_int32), ("form", ctypes.c_int32), ("hidden", ctypes.c_int32),
+                ("W1", ctypes.c_void_p), ("b1", ctypes.c_void_p), ("W1b", ctypes.c_void_p), ("b1b", ctypes.c_void_p),
+                ("gamma", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("W2", ctypes.c_void_p)]
+
+
 class spec_trace_entry(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int32), ("total_ms", ctypes.c_double)]
 
@@ -60,6 +66,9 @@ def _load():
         "spec_tree_build": (i32, [vp, vp, i32, vp, sz, tp, vp]),
         "hydra_draft_workspace_size": (sz, [tp, i32, i32, i32, i32, vp, vp, i32]),
         "hydra_draft": (i32, [vp, vp, i32, vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]),
+        "hydra_draft_heads_workspace_size": (sz, [tp, i32, i32, i32, i32, ctypes.POINTER(spec_head), i32]),
+        "hydra_draft_heads": (i32, [vp, vp, i32, ctypes.POINTER(spec_head), vp, tp, i32, i32, i32, f32, i32, vp, vp,
+                                    vp, vp, sz, vp]),
         "tree_attention_workspace_size": (sz, [tp, i32, i32, i32, i32, i32, i32]),
         "tree_attention": (i32, [vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]),
         "tree_attention_noalloc": (i32, [vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp]),
@@ -236,6 +245,59 @@ def hydra_draft(h, emb, W1, b1, W2, cond, topk, root_tok, tree, node_tok=None, n
         _check("hydra_draft", _lib.hydra_draft(_ptr(h), _ptr(emb), K, w1p, b1p, w2p, c, kk, _ptr(root_tok), tree.ref(),
                                                B, d, V, dt, _ptr(node_tok), _ptr(node_logit), _ptr(node_logprob),
                                                _ptr(ws), ws.numel(), _stream(stream)))
+    return node_tok, node_logit, node_logprob
+
+
+def hydra_draft_heads(h, emb, heads, root_tok, tree, ln_eps=1e-5, node_tok=None, node_logit=None, node_logprob=None,
+                      want_logprob=True, ws=None, stream=None):
+    """hydra_draft with one dict per head: cond, topk, form (0/1), W1, W2 and optionally b1, W1b, b1b, gamma, beta.
+
+    Returns (node_tok, node_logit, node_logprob)."""
+    _need(h, "h", ndim=2)
+    dev = h.device
+    dt = _dtype_code(h)
+    B, d = h.shape
+    _need(emb, "emb", dtype=h.dtype, ndim=2, device=dev)
+    V = emb.shape[0]
+    if emb.shape[1] != d:
+        raise ValueError("emb must be [V, d]")
+    K = len(heads)
+    arr = (spec_head * K)()
+    for k, hd in enumerate(heads):
+        W1 = hd["W1"]
+        _need(W1, f"heads[{k}].W1", dtype=h.dtype, ndim=2, device=dev)
+        hidden = W1.shape[0]
+        cond = int(hd["cond"])
+        d_in = d * (2 if cond == 1 else (k + 1) if cond == 2 else 1)
+        if W1.shape[1] != d_in:
+            raise ValueError(f"heads[{k}].W1 must have {d_in} columns for cond {cond}")
+        shapes = {"W2": (V, d), "b1": (hidden,), "W1b": (d, hidden), "b1b": (d,), "gamma": (d,), "beta": (d,)}
+        for name, shp in shapes.items():
+            t = hd.get(name)
+            if t is not None:
+                _need(t, f"heads[{k}].{name}", dtype=h.dtype, ndim=len(shp), device=dev)
+                if tuple(t.shape) != shp:
+                    raise ValueError(f"heads[{k}].{name} must be {shp}")
+        arr[k].cond, arr[k].topk, arr[k].form, arr[k].hidden = cond, int(hd["topk"]), int(hd.get("form", 0)), hidden
+        for name in ("W1", "b1", "W1b", "b1b", "gamma", "beta", "W2"):
+            t = hd.get(name)
+            setattr(arr[k], name, t.data_ptr() if t is not None else None)
+    _need(root_tok, "root_tok", dtype=torch.int32, ndim=1, device=dev)
+    T = tree.T
+    if node_tok is None:
+        node_tok = torch.empty(B, T, dtype=torch.int32, device=dev)
+    if node_logit is None:
+        node_logit = torch.empty(B, T, dtype=torch.float32, device=dev)
+    if node_logprob is None and want_logprob:
+        node_logprob = torch.empty(B, T, dtype=torch.float32, device=dev)
+    nws = _lib.hydra_draft_heads_workspace_size(tree.ref(), B, d, V, K, arr, dt)
+    if nws == 0:
+        raise SpecError("hydra_draft_heads_workspace_size", 1, _lib.spec_last_error().decode())
+    ws = _workspace(nws, dev, ws)
+    with torch.cuda.device(dev):
+        _check("hydra_draft_heads", _lib.hydra_draft_heads(_ptr(h), _ptr(emb), K, arr, _ptr(root_tok), tree.ref(), B, d,
+                                                           V, float(ln_eps), dt, _ptr(node_tok), _ptr(node_logit),
+                                                           _ptr(node_logprob), _ptr(ws), ws.numel(), _stream(stream)))
     return node_tok, node_logit, node_logprob
 
 

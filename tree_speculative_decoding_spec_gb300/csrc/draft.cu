@@ -38,7 +38,8 @@ constexpr int GBM = 64, GBN = 32, GBK = 32;
 template <typename T, int EPI>
 __global__ void __launch_bounds__(256) k_gemm_fma(const T* __restrict__ W, const T* __restrict__ X, int M, int N, int K,
                                                    int ldx, const T* __restrict__ bias, const T* __restrict__ h,
-                                                   int cond, int n_int, T* __restrict__ z_out, float* __restrict__ logits) {
+                                                   int cond, int n_int, T* __restrict__ z_out, float* __restrict__ logits,
+                                                   int act, float* __restrict__ zf) {
     __shared__ float Ws[GBK][GBM + 4];
     __shared__ float Xs[GBK][GBN + 4];
     const int t = threadIdx.x;
@@ -81,15 +82,53 @@ __global__ void __launch_bounds__(256) k_gemm_fma(const T* __restrict__ W, const
         for (int j = 0; j < 2; ++j) {
             const int m = m0 + tx * 4 + i, n = n0 + ty * 2 + j;
             if (m >= M || n >= N) continue;
-            if (EPI == 0) {
+            if (EPI == 0) {   // act(W x + bias) (+ h_b when h is set), to z_out or, if set, fp32 zf
                 const int b = cond ? n / n_int : n;
                 const float a = acc[i][j] + (bias ? to_f32(bias[m]) : 0.f);
-                const float zz = to_f32(h[static_cast<size_t>(b) * M + m]) + a / (1.0f + expf(-a));
-                z_out[static_cast<size_t>(n) * M + m] = from_f32<T>(zz);
+                const float y = act ? a / (1.0f + expf(-a)) : a;
+                const float zz = h ? to_f32(h[static_cast<size_t>(b) * M + m]) + y : y;
+                if (zf) zf[static_cast<size_t>(n) * M + m] = zz;
+                else z_out[static_cast<size_t>(n) * M + m] = from_f32<T>(zz);
             } else {
                 logits[static_cast<size_t>(n) * M + m] = acc[i][j];
             }
         }
+    }
+}
+
+// ---------------------------------------------------------------- LayerNorm (head form 1)
+
+// z[r] = (y[r] - mean) / sqrt(var + eps) * gamma + beta over the d entries of
+// row r (mean and biased variance in fp32, two passes); gamma/beta NULL: 1/0.
+// One CTA per row.
+template <typename T>
+__global__ void __launch_bounds__(256) k_layernorm(const float* __restrict__ y, int d, const T* __restrict__ gamma,
+                                                   const T* __restrict__ beta, float eps, T* __restrict__ z) {
+    __shared__ float red[8];
+    const float* yr = y + static_cast<size_t>(blockIdx.x) * d;
+    auto block_sum = [&](float v) {
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        __syncthreads();
+        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+        __syncthreads();
+        float t = 0.f;
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
+        return t;
+    };
+    float sum = 0.f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) sum += yr[i];
+    const float mean = block_sum(sum) / d;
+    float sq = 0.f;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        const float e = yr[i] - mean;
+        sq += e * e;
+    }
+    const float inv = 1.0f / sqrtf(block_sum(sq) / d + eps);
+    T* zr = z + static_cast<size_t>(blockIdx.x) * d;
+    for (int i = threadIdx.x; i < d; i += blockDim.x) {
+        const float g = gamma ? to_f32(gamma[i]) : 1.f;
+        const float bb = beta ? to_f32(beta[i]) : 0.f;
+        zr[i] = from_f32<T>((yr[i] - mean) * inv * g + bb);
     }
 }
 
@@ -462,7 +501,7 @@ struct Plan {
     int kmax;            // list length of the top-k partials (8 or 16)
     int nslices;         // vocabulary slices per row
     int slice_fma;       // fp32 path: tokens per slice
-    size_t off_xin, off_z, off_scratch, off_pc, off_pl, total;
+    size_t off_xin, off_z, off_scratch, off_pc, off_pl, off_hid, off_y, total;
     size_t xin_at[SPEC_MAX_DEPTH + 1];   // element offset of depth k's input rows (conditioned heads)
     HRows hr;
     bool tc;             // bf16 tensor-core path
@@ -501,7 +540,80 @@ size_t xin_elems(Plan& p, const spec_tree* t, int K, const int32_t* cond, int B,
     return std::max<size_t>(elems, 1);
 }
 
-Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* cond, const int32_t* topk, spec_dtype dt) {
+// Per-head description (host).  Form 0: z = h + SiLU(W1 u + b1); form 1: the
+// LayerNorm fusion head (see spec_head in the header).
+struct Heads {
+    int K = 0;
+    int32_t cond[SPEC_MAX_DEPTH] = {}, topk[SPEC_MAX_DEPTH] = {}, form[SPEC_MAX_DEPTH] = {}, hidden[SPEC_MAX_DEPTH] = {};
+    const void* W1[SPEC_MAX_DEPTH] = {};
+    const void* b1[SPEC_MAX_DEPTH] = {};
+    const void* W1b[SPEC_MAX_DEPTH] = {};
+    const void* b1b[SPEC_MAX_DEPTH] = {};
+    const void* gamma[SPEC_MAX_DEPTH] = {};
+    const void* beta[SPEC_MAX_DEPTH] = {};
+    const void* W2[SPEC_MAX_DEPTH] = {};
+    int hid_width = 0;   // widest form-1 inner layer that feeds W1b (0: none)
+    bool ln = false;     // some head has form 1
+};
+
+Heads heads_from_arrays(int K, const void* const* W1, const void* const* b1, const void* const* W2,
+                        const int32_t* cond, const int32_t* topk, int d) {
+    Heads hs;
+    hs.K = K;
+    for (int k = 0; k < K; ++k) {
+        hs.cond[k] = cond[k];
+        hs.topk[k] = topk[k];
+        hs.hidden[k] = d;
+        hs.W1[k] = W1[k];
+        hs.b1[k] = b1 ? b1[k] : nullptr;
+        hs.W2[k] = W2[k];
+    }
+    return hs;
+}
+
+Heads heads_from_desc(int K, const spec_head* h) {
+    Heads hs;
+    hs.K = K;
+    for (int k = 0; k < K; ++k) {
+        hs.cond[k] = h[k].cond;
+        hs.topk[k] = h[k].topk;
+        hs.form[k] = h[k].form;
+        hs.hidden[k] = h[k].hidden;
+        hs.W1[k] = h[k].W1;
+        hs.b1[k] = h[k].b1;
+        hs.W1b[k] = h[k].W1b;
+        hs.b1b[k] = h[k].b1b;
+        hs.gamma[k] = h[k].gamma;
+        hs.beta[k] = h[k].beta;
+        hs.W2[k] = h[k].W2;
+        if (h[k].form == 1) {
+            hs.ln = true;
+            if (h[k].W1b) hs.hid_width = std::max(hs.hid_width, h[k].hidden);
+        }
+    }
+    return hs;
+}
+
+spec_status check_heads(const Heads& hs, int d) {
+    for (int k = 0; k < hs.K; ++k) {
+        if (hs.form[k] != 0 && hs.form[k] != 1) return fail(SPEC_EINVAL, "head %d: form %d must be 0 or 1", k, hs.form[k]);
+        if (!hs.W1[k] || !hs.W2[k]) return fail(SPEC_EINVAL, "head %d: W1 and W2 must not be NULL", k);
+        if (hs.form[k] == 0 || !hs.W1b[k]) {
+            if (hs.hidden[k] != d) return fail(SPEC_EINVAL, "head %d: hidden = %d must be d = %d here", k, hs.hidden[k], d);
+        } else if (hs.hidden[k] < 8 || hs.hidden[k] > 65536 || hs.hidden[k] % 8) {
+            return fail(SPEC_EINVAL, "head %d: hidden = %d must be a multiple of 8 in 8..65536", k, hs.hidden[k]);
+        }
+        if (hs.form[k] == 0 && (hs.W1b[k] || hs.b1b[k] || hs.gamma[k] || hs.beta[k]))
+            return fail(SPEC_EINVAL, "head %d: form 0 takes no W1b, b1b, gamma or beta", k);
+        const void* ptrs[] = {hs.W1[k], hs.b1[k], hs.W1b[k], hs.b1b[k], hs.gamma[k], hs.beta[k], hs.W2[k]};
+        for (const void* q : ptrs)
+            if (q && !aligned16(q)) return fail(SPEC_EALIGN, "head %d weights must be 16-byte aligned", k);
+    }
+    return SPEC_OK;
+}
+
+Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* cond, const int32_t* topk, spec_dtype dt,
+               const Heads* hs = nullptr) {
     Plan p{};
     p.K = K;
     for (int k = 0; k < K; ++k) {
@@ -531,6 +643,11 @@ Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* co
         p.off_scratch = take(sizeof(float) * static_cast<size_t>(p.max_rows) * V);
         p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.max_rows) * p.nslices * p.kmax);
         p.off_pl = take(sizeof(float2) * static_cast<size_t>(p.max_rows) * p.nslices);
+    }
+    if (hs && hs->ln) {   // form-1 heads: the inner activations and the fp32 rows before LayerNorm
+        const int rows_pad = p.tc ? p.tcp.rows_pad : p.max_rows;
+        p.off_hid = take(es * static_cast<size_t>(rows_pad) * std::max(hs->hid_width, 8));
+        p.off_y = take(sizeof(float) * static_cast<size_t>(rows_pad) * d);
     }
     p.total = off;
     return p;
@@ -571,16 +688,20 @@ spec_status launch_select(bool pdl, const Plan& p, const spec_tree* t, int R, in
 }
 
 template <typename T>
-spec_status run(const T* h, const T* emb, int K, const void* const* W1, const void* const* b1, const void* const* W2,
-                const int32_t* cond, const int32_t* topk, const int32_t* root_tok, const spec_tree* t, int B, int d,
-                int V, int32_t* node_tok, float* node_logit, float* node_logprob, void* ws, const Plan& p,
+spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const int32_t* root_tok, const spec_tree* t,
+                int B, int d, int V, int32_t* node_tok, float* node_logit, float* node_logprob, void* ws, const Plan& p,
                 cudaStream_t s) {
+    const int K = hs.K;
+    const int32_t* cond = hs.cond;
+    const int32_t* topk = hs.topk;
     unsigned char* w = static_cast<unsigned char*>(ws);
     T* xbase = reinterpret_cast<T*>(w + p.off_xin);
     T* z = reinterpret_cast<T*>(w + p.off_z);
     float* scratch = reinterpret_cast<float*>(w + p.off_scratch);
     Cand* pc = reinterpret_cast<Cand*>(w + p.off_pc);
     float2* pl = reinterpret_cast<float2*>(w + p.off_pl);
+    T* hid = reinterpret_cast<T*>(w + p.off_hid);
+    float* yln = reinterpret_cast<float*>(w + p.off_y);
     const bool first_cond = t->n_internal_at_depth[0] > 0 && cond[0];
     SPEC_CUDA_TRY(reset_device_status(ws, s));
     SPEC_CUDA_TRY(launch("draft_init_root", k_init_root<T>, dim3(B, 1 + p.hr.per_seq), dim3(128), 0, s, root_tok, B,
@@ -600,13 +721,34 @@ spec_status run(const T* h, const T* emb, int K, const void* const* W1, const vo
                                    ? t->n_internal_at_depth[k + 1] : 0;
         const int next_cond = next_n_int > 0 ? cond[k + 1] : 0;
         const int next_ld = next_n_int > 0 ? d_in_of(next_cond, k + 1, d) : 0;
-        const T* W1k = static_cast<const T*>(W1[k]);
-        const T* b1k = b1 ? static_cast<const T*>(b1[k]) : nullptr;
-        const T* W2k = static_cast<const T*>(W2[k]);
+        const T* W1k = static_cast<const T*>(hs.W1[k]);
+        const T* b1k = static_cast<const T*>(hs.b1[k]);
+        const T* W2k = static_cast<const T*>(hs.W2[k]);
+        const int dep_k0 = cond[k] ? d : d_in;   // input columns that come from the previous select
+        // form 1: a = SiLU(W1 u + b1) into hid (W1b set) or yln; y = W1b a + b1b into yln;
+        // z = LayerNorm(y) (queued between the MLP and the projection)
+        const bool ln = hs.form[k] == 1;
+        const T* W1bk = static_cast<const T*>(hs.W1b[k]);
+        auto layernorm = [&]() -> spec_status {
+            SPEC_CUDA_TRY(launch("draft_layernorm", k_layernorm<T>, dim3(R), dim3(256), 0, s, yln, d,
+                                 static_cast<const T*>(hs.gamma[k]), static_cast<const T*>(hs.beta[k]), ln_eps, z));
+            return SPEC_OK;
+        };
         if constexpr (std::is_same<T, __nv_bfloat16>::value) {
             if (p.tc) {
-                spec_status st = tc::draft_head_tc(p.tcp, W1k, b1k, W2k, h, X, d_in, ldx, z, R, d, V, cond[k], n_int,
-                                                   topk[k], p.kmax, cond[k] ? d : d_in, pc, pl, ws, s);
+                spec_status st;
+                if (!ln) {
+                    st = tc::draft_head_tc(p.tcp, W1k, b1k, W2k, h, X, d_in, ldx, z, R, d, V, cond[k], n_int, topk[k],
+                                           p.kmax, dep_k0, pc, pl, ws, s);
+                } else {
+                    st = tc::mlp_tc(W1k, b1k, hs.hidden[k], X, d_in, ldx, R, cond[k], n_int, dep_k0, 1, nullptr,
+                                    W1bk ? hid : nullptr, W1bk ? nullptr : yln, ws, s);
+                    if (st == SPEC_OK && W1bk)
+                        st = tc::mlp_tc(W1bk, static_cast<const T*>(hs.b1b[k]), d, hid, hs.hidden[k], hs.hidden[k], R,
+                                        0, 1, 0, 0, nullptr, nullptr, yln, ws, s);
+                    if (st == SPEC_OK) st = layernorm();
+                    if (st == SPEC_OK) st = tc::proj_tc(p.tcp, W2k, z, R, d, V, topk[k], p.kmax, pc, pl, ws, s);
+                }
                 if (st != SPEC_OK) return st;
                 st = p.kmax == 8 ? launch_select<8, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
                                                        pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, s)
@@ -616,10 +758,24 @@ spec_status run(const T* h, const T* emb, int K, const void* const* W1, const vo
                 continue;
             }
         }
-        SPEC_CUDA_TRY(launch("draft_mlp_fma", k_gemm_fma<T, 0>, dim3((d + GBM - 1) / GBM, (R + GBN - 1) / GBN), dim3(256), 0, s,
-                             W1k, X, d, R, d_in, ldx, b1k, h, cond[k], n_int, z, nullptr));
+        if (!ln) {
+            SPEC_CUDA_TRY(launch("draft_mlp_fma", k_gemm_fma<T, 0>, dim3((d + GBM - 1) / GBM, (R + GBN - 1) / GBN), dim3(256),
+                                 0, s, W1k, X, d, R, d_in, ldx, b1k, h, cond[k], n_int, z, nullptr, 1, nullptr));
+        } else {
+            const int hd = hs.hidden[k];
+            SPEC_CUDA_TRY(launch("draft_mlp_fma", k_gemm_fma<T, 0>, dim3((hd + GBM - 1) / GBM, (R + GBN - 1) / GBN),
+                                 dim3(256), 0, s, W1k, X, hd, R, d_in, ldx, b1k, static_cast<const T*>(nullptr), cond[k],
+                                 n_int, W1bk ? hid : nullptr, nullptr, 1, W1bk ? nullptr : yln));
+            if (W1bk)
+                SPEC_CUDA_TRY(launch("draft_mlp_fma", k_gemm_fma<T, 0>, dim3((d + GBM - 1) / GBM, (R + GBN - 1) / GBN),
+                                     dim3(256), 0, s, W1bk, static_cast<const T*>(hid), d, R, hd, hd,
+                                     static_cast<const T*>(hs.b1b[k]), static_cast<const T*>(nullptr), 0, 1,
+                                     static_cast<T*>(nullptr), nullptr, 0, yln));
+            spec_status st = layernorm();
+            if (st != SPEC_OK) return st;
+        }
         SPEC_CUDA_TRY(launch("draft_proj_fma", k_gemm_fma<T, 1>, dim3((V + GBM - 1) / GBM, (R + GBN - 1) / GBN), dim3(256), 0, s,
-                             W2k, z, V, R, d, d, nullptr, nullptr, 0, 1, nullptr, scratch));
+                             W2k, z, V, R, d, d, nullptr, nullptr, 0, 1, nullptr, scratch, 0, nullptr));
         spec_status st;
         if (p.kmax == 8) {
             SPEC_CUDA_TRY(launch("draft_topk_slices", k_topk_slices<8>, dim3(p.nslices, R), dim3(256), 0, s, scratch, V,
@@ -642,6 +798,36 @@ spec_status run(const T* h, const T* emb, int K, const void* const* W1, const vo
 
 using namespace spec;
 
+namespace spec {
+namespace draft {
+
+// Shared by both entry points once the heads are described.
+static spec_status draft_call(const void* h, const void* emb, const Heads& hs, float ln_eps, const int32_t* root_tok,
+                              const spec_tree* tree, int32_t B, int32_t d, int32_t V, spec_dtype dt, int32_t* node_tok,
+                              float* node_logit, float* node_logprob, void* ws, size_t ws_bytes, cudaStream_t s) {
+    spec_status st = check_args(tree, B, d, V, hs.K, hs.cond, hs.topk, dt);
+    if (st != SPEC_OK) return st;
+    st = check_heads(hs, d);
+    if (st != SPEC_OK) return st;
+    if (hs.ln && !(ln_eps > 0.f && ln_eps < 1e30f)) return fail(SPEC_EINVAL, "ln_eps must be positive and finite");
+    if (!h || !emb || !root_tok || !node_tok || !node_logit)
+        return fail(SPEC_EINVAL, "h, emb, root_tok, node_tok and node_logit must not be NULL");
+    if (!aligned16(h) || !aligned16(emb)) return fail(SPEC_EALIGN, "h and emb must be 16-byte aligned");
+    if (!aligned4(root_tok) || !aligned4(node_tok) || !aligned4(node_logit) || (node_logprob && !aligned4(node_logprob)))
+        return fail(SPEC_EALIGN, "token and logit buffers must be 4-byte aligned");
+    const Plan p = make_plan(tree, B, d, V, hs.K, hs.cond, hs.topk, dt, &hs);
+    if (!ws || ws_bytes < p.total) return fail(SPEC_EWORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, p.total);
+    if (!aligned16(ws)) return fail(SPEC_EALIGN, "workspace must be 16-byte aligned");
+    if (dt == SPEC_BF16)
+        return run<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(h), static_cast<const __nv_bfloat16*>(emb), hs, ln_eps,
+                                  root_tok, tree, B, d, V, node_tok, node_logit, node_logprob, ws, p, s);
+    return run<float>(static_cast<const float*>(h), static_cast<const float*>(emb), hs, ln_eps, root_tok, tree, B, d, V,
+                      node_tok, node_logit, node_logprob, ws, p, s);
+}
+
+}  // namespace draft
+}  // namespace spec
+
 extern "C" size_t hydra_draft_workspace_size(const spec_tree* tree, int32_t B, int32_t d, int32_t V, int32_t K,
                                              const int32_t* cond, const int32_t* topk, spec_dtype dt) {
     clear_error();
@@ -654,27 +840,32 @@ extern "C" spec_status hydra_draft(const void* h, const void* emb, int32_t K, co
                                    const int32_t* topk, const int32_t* root_tok, const spec_tree* tree, int32_t B,
                                    int32_t d, int32_t V, spec_dtype dt, int32_t* node_tok, float* node_logit,
                                    float* node_logprob, void* ws, size_t ws_bytes, spec_stream_t s_) {
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(s_);
     clear_error();
-    spec_status st = draft::check_args(tree, B, d, V, K, cond, topk, dt);
-    if (st != SPEC_OK) return st;
-    if (!h || !emb || !W1 || !W2 || !root_tok || !node_tok || !node_logit)
-        return fail(SPEC_EINVAL, "h, emb, W1, W2, root_tok, node_tok and node_logit must not be NULL");
-    if (!aligned16(h) || !aligned16(emb)) return fail(SPEC_EALIGN, "h and emb must be 16-byte aligned");
-    if (!aligned4(root_tok) || !aligned4(node_tok) || !aligned4(node_logit) || (node_logprob && !aligned4(node_logprob)))
-        return fail(SPEC_EALIGN, "token and logit buffers must be 4-byte aligned");
-    for (int k = 0; k < K; ++k) {
-        if (!W1[k] || !W2[k]) return fail(SPEC_EINVAL, "W1[%d] and W2[%d] must not be NULL", k, k);
-        if (!aligned16(W1[k]) || !aligned16(W2[k]) || (b1 && b1[k] && !aligned16(b1[k])))
-            return fail(SPEC_EALIGN, "head %d weights must be 16-byte aligned", k);
-    }
-    const draft::Plan p = draft::make_plan(tree, B, d, V, K, cond, topk, dt);
-    if (!ws || ws_bytes < p.total) return fail(SPEC_EWORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, p.total);
-    if (!aligned16(ws)) return fail(SPEC_EALIGN, "workspace must be 16-byte aligned");
-    if (dt == SPEC_BF16)
-        return draft::run<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(h), static_cast<const __nv_bfloat16*>(emb), K,
-                                         W1, b1, W2, cond, topk, root_tok, tree, B, d, V, node_tok, node_logit,
-                                         node_logprob, ws, p, s);
-    return draft::run<float>(static_cast<const float*>(h), static_cast<const float*>(emb), K, W1, b1, W2, cond, topk,
-                             root_tok, tree, B, d, V, node_tok, node_logit, node_logprob, ws, p, s);
+    if (K < 1 || K > SPEC_MAX_DEPTH) return fail(SPEC_EINVAL, "K = %d out of 1..%d", K, SPEC_MAX_DEPTH);
+    if (!W1 || !W2 || !cond || !topk) return fail(SPEC_EINVAL, "W1, W2, cond and topk must not be NULL");
+    const draft::Heads hs = draft::heads_from_arrays(K, W1, b1, W2, cond, topk, d);
+    return draft::draft_call(h, emb, hs, 0.f, root_tok, tree, B, d, V, dt, node_tok, node_logit, node_logprob, ws,
+                             ws_bytes, reinterpret_cast<cudaStream_t>(s_));
+}
+
+extern "C" size_t hydra_draft_heads_workspace_size(const spec_tree* tree, int32_t B, int32_t d, int32_t V, int32_t K,
+                                                   const spec_head* heads, spec_dtype dt) {
+    clear_error();
+    if (K < 1 || K > SPEC_MAX_DEPTH || !heads) return 0;
+    const draft::Heads hs = draft::heads_from_desc(K, heads);
+    if (draft::check_args(tree, B, d, V, K, hs.cond, hs.topk, dt) != SPEC_OK) return 0;
+    if (draft::check_heads(hs, d) != SPEC_OK) return 0;
+    return draft::make_plan(tree, B, d, V, K, hs.cond, hs.topk, dt, &hs).total;
+}
+
+extern "C" spec_status hydra_draft_heads(const void* h, const void* emb, int32_t K, const spec_head* heads,
+                                         const int32_t* root_tok, const spec_tree* tree, int32_t B, int32_t d,
+                                         int32_t V, float ln_eps, spec_dtype dt, int32_t* node_tok, float* node_logit,
+                                         float* node_logprob, void* ws, size_t ws_bytes, spec_stream_t s_) {
+    clear_error();
+    if (K < 1 || K > SPEC_MAX_DEPTH) return fail(SPEC_EINVAL, "K = %d out of 1..%d", K, SPEC_MAX_DEPTH);
+    if (!heads) return fail(SPEC_EINVAL, "heads must not be NULL");
+    const draft::Heads hs = draft::heads_from_desc(K, heads);
+    return draft::draft_call(h, emb, hs, ln_eps, root_tok, tree, B, d, V, dt, node_tok, node_logit, node_logprob, ws,
+                             ws_bytes, reinterpret_cast<cudaStream_t>(s_));
 }

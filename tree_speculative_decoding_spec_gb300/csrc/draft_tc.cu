@@ -78,7 +78,8 @@ struct UmmaParams {
     float2* part_l;
     int kmax;
     void* ws;           // status word
-    // MLP finish (cluster of a weight tile's splits): z = h + SiLU(sum + b1)
+    // MLP finish (cluster of a weight tile's splits): y = act(sum + bias) (+ h_b when h is
+    // set), written as bf16 to z or, when zf is set, as fp32 to zf
     const __nv_bfloat16* bias;
     const __nv_bfloat16* h;
     __nv_bfloat16* z;
@@ -88,6 +89,8 @@ struct UmmaParams {
     // lies below it (and is not CTA (0, 0), which always waits so that this kernel
     // completes after the previous one) starts without waiting for it
     int dep_k0;
+    int act;            // MLP: 1 SiLU, 0 identity
+    float* zf;          // MLP: fp32 output instead of z
 };
 
 __device__ __forceinline__ bool cbetter(float va, int ia, float vb, int ib) {
@@ -248,8 +251,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
                 for (int sp = 0; sp < kMaxSplits; ++sp) x += v[sp];
                 const int row = p.row0 + n;
                 const int b = p.cond ? row / p.n_int : row;
-                const float zz = __bfloat162float(p.h[static_cast<size_t>(b) * p.M + m]) + x / (1.0f + expf(-x));
-                p.z[static_cast<size_t>(row) * p.M + m] = __float2bfloat16_rn(zz);
+                const float y = p.act ? x / (1.0f + expf(-x)) : x;
+                const float zz = p.h ? __bfloat162float(p.h[static_cast<size_t>(b) * p.M + m]) + y : y;
+                if (p.zf) p.zf[static_cast<size_t>(row) * p.M + m] = zz;
+                else p.z[static_cast<size_t>(row) * p.M + m] = __float2bfloat16_rn(zz);
             }
         }
         cluster_sync();   // the peers have read this CTA's partials
@@ -445,25 +450,24 @@ static spec_status launch_umma(const CUtensorMap& ta, const CUtensorMap& tb, dim
     return SPEC_OK;
 }
 
-spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
-                          const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* X, int d_in, int ldx,
-                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax, int dep_k0,
-                          draft::Cand* pc, float2* pl, void* ws, cudaStream_t s) {
+spec_status mlp_tc(const __nv_bfloat16* W, const __nv_bfloat16* bias, int M, const __nv_bfloat16* X, int d_in, int ldx,
+                   int R, int cond, int n_int, int dep_k0, int act, const __nv_bfloat16* residual, __nv_bfloat16* z,
+                   float* zf, void* ws, cudaStream_t s) {
     const int total_mlp = (d_in + kBKS - 1) / kBKS;
-    // ---- MLP, activation rows in groups of at most 256 (the MMA's largest N)
+    // activation rows in groups of at most 256 (the MMA's largest N)
     for (int g0 = 0; g0 < R; g0 += kMaxN) {
         const int rows = std::min(kMaxN, R - g0);
         const int n_pad = n_pad_of(rows);
         // CTAs per SM by shared memory (228 KB per SM, 1 KB reserved per CTA); at most 2
         const int resident = static_cast<int>(std::max<size_t>(
             1, std::min<size_t>(2, 233472 / (smem_of(n_pad, stages_of(n_pad)) + 1024))));
-        const int splits = mlp_splits(d, d_in, resident);
+        const int splits = mlp_splits(M, d_in, resident);
         const int per_split = (total_mlp + splits - 1) / splits;
         CUtensorMap ta, tb;
-        SPEC_CUDA_TRY(make_tmap_bf16_2d(&ta, W1, d, d_in, d_in, kBM));
+        SPEC_CUDA_TRY(make_tmap_bf16_2d(&ta, W, M, d_in, d_in, kBM));
         SPEC_CUDA_TRY(make_tmap_bf16_2d(&tb, X + static_cast<size_t>(g0) * ldx, rows, d_in, ldx, n_pad));
         UmmaParams p{};
-        p.M = d;
+        p.M = M;
         p.k_iters = per_split;
         p.total_iters = total_mlp;
         p.n_pad = n_pad;
@@ -472,16 +476,22 @@ spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, cons
         p.tmem_cols = tmem_cols_of(n_pad);
         p.ws = ws;
         p.row0 = g0;
-        p.bias = b1;
-        p.h = h;
+        p.bias = bias;
+        p.h = residual;
         p.z = z;
+        p.zf = zf;
+        p.act = act;
         p.cond = cond;
         p.n_int = n_int;
         p.dep_k0 = dep_k0;
-        spec_status st = launch_umma<0, 8>(ta, tb, dim3((d + kBM - 1) / kBM, splits), p, s, "draft_mlp_tc");
+        spec_status st = launch_umma<0, 8>(ta, tb, dim3((M + kBM - 1) / kBM, splits), p, s, "draft_mlp_tc");
         if (st != SPEC_OK) return st;
     }
-    // ---- projection with the top-k epilogue
+    return SPEC_OK;
+}
+
+spec_status proj_tc(const DraftTcPlan& plan, const __nv_bfloat16* W2, const __nv_bfloat16* z, int R, int d, int V, int k,
+                    int kmax, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s) {
     for (int g0 = 0; g0 < R; g0 += kMaxN) {
         const int rows = std::min(kMaxN, R - g0);
         const int n_pad = n_pad_of(rows);
@@ -510,6 +520,15 @@ spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, cons
         if (st != SPEC_OK) return st;
     }
     return SPEC_OK;
+}
+
+spec_status draft_head_tc(const DraftTcPlan& plan, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
+                          const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* X, int d_in, int ldx,
+                          __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax, int dep_k0,
+                          draft::Cand* pc, float2* pl, void* ws, cudaStream_t s) {
+    spec_status st = mlp_tc(W1, b1, d, X, d_in, ldx, R, cond, n_int, dep_k0, 1, h, z, nullptr, ws, s);
+    if (st != SPEC_OK) return st;
+    return proj_tc(plan, W2, z, R, d, V, k, kmax, pc, pl, ws, s);
 }
 
 }  // namespace tc

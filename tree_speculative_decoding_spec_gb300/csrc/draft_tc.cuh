@@ -29,6 +29,19 @@ DraftTcPlan draft_tc_plan(int rows, int d, int V);
 // ldx: the gathered [h || E[tok]] rows, or h itself for an unconditioned head);
 // z receives the bf16 MLP output.  Kernels are launched with programmatic
 // dependent launch.
+// One head layer on the tensor cores for R activation rows:
+//   y[r, m] = act(W[m, :] . X[r, 0:d_in] + bias[m]) (+ residual[b(r), m]),  m < M
+// (act 1: SiLU, 0: identity; b(r) = r / n_int when cond, else r), stored as
+// bf16 in z [R, M] or, when zf is set, as fp32 in zf [R, M].  Input columns
+// >= dep_k0 come from the previous kernel.
+spec_status mlp_tc(const __nv_bfloat16* W, const __nv_bfloat16* bias, int M, const __nv_bfloat16* X, int d_in, int ldx,
+                   int R, int cond, int n_int, int dep_k0, int act, const __nv_bfloat16* residual, __nv_bfloat16* z,
+                   float* zf, void* ws, cudaStream_t s);
+
+// The vocabulary projection with the per-slice top-k / (max, sum exp) epilogue.
+spec_status proj_tc(const DraftTcPlan& plan, const __nv_bfloat16* W2, const __nv_bfloat16* z, int R, int d, int V, int k,
+                    int kmax, draft::Cand* pc, float2* pl, void* ws, cudaStream_t s);
+
 spec_status draft_head_tc(const DraftTcPlan& p, const __nv_bfloat16* W1, const __nv_bfloat16* b1,
                           const __nv_bfloat16* W2, const __nv_bfloat16* h, const __nv_bfloat16* X, int d_in, int ldx,
                           __nv_bfloat16* z, int R, int d, int V, int cond, int n_int, int k, int kmax, int dep_k0,
