@@ -217,3 +217,29 @@ def test_layernorm_fusion_head_form():
     out = hydra_draft_heads(h, E, [head], [root], tree, "f32", ln_eps=eps, keep_logits=True)
     z = F.layer_norm(F.silu(F.linear(t(h)[0], t(W1s))), (d,), eps=eps)
     np.testing.assert_allclose(out["logits"][(0, 0)], F.linear(z, t(W2)).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_layernorm_head_zero_gain_gives_beta():
+    # gamma = 0: every head's z is beta whatever the input, so each node's logits are W2 beta and every
+    # parent's children are the same top-k of that row (closed form, independent of h, E, W1, W1b)
+    from oracle import hydra_draft_heads
+    rng = np.random.default_rng(32)
+    d, V = 8, 40
+    parent, rank = wl.cartesian_tree((3, 2))
+    tree = tree_encode(parent, rank)
+    h = rng.standard_normal((2, d)).astype(np.float32)
+    E = rng.standard_normal((V, d)).astype(np.float32)
+    heads = []
+    for k, tk in enumerate((3, 2)):
+        heads.append(dict(form=1, cond=k, topk=tk, W1=rng.standard_normal((12, d * (k + 1))).astype(np.float32),
+                          b1=None, W1b=rng.standard_normal((d, 12)).astype(np.float32), b1b=None,
+                          gamma=np.zeros(d, dtype=np.float32), beta=rng.standard_normal(d).astype(np.float32),
+                          W2=rng.standard_normal((V, d)).astype(np.float32)))
+    out = hydra_draft_heads(h, E, heads, [1, 2], tree, "f32")
+    for b in range(2):
+        for c in range(1, len(parent)):
+            k = tree["depth"][c] - 1
+            row = heads[k]["W2"].astype(np.float64) @ heads[k]["beta"].astype(np.float64)
+            order = np.argsort(-row, kind="stable")
+            assert out["node_tok"][b, c] == order[rank[c]]
+            np.testing.assert_allclose(out["node_logit"][b, c], row[order[rank[c]]], rtol=1e-12)
