@@ -99,36 +99,63 @@ __global__ void __launch_bounds__(256) k_gemm_fma(const T* __restrict__ W, const
 // ---------------------------------------------------------------- LayerNorm (head form 1)
 
 // z[r] = (y[r] - mean) / sqrt(var + eps) * gamma + beta over the d entries of
-// row r (mean and biased variance in fp32, two passes); gamma/beta NULL: 1/0.
-// One CTA per row.
+// row r (mean and biased variance in fp32, the variance from the deviations);
+// gamma/beta NULL: 1/0.  One CTA of 256 threads per row: the row is read once
+// into registers (kLnVec float4 per thread, d <= 4 * 256 * kLnVec), so the
+// kernel costs one load round trip and two block reductions.  Launched as a
+// programmatic dependent: y comes from the kernel before it.
+constexpr int kLnThreads = 256;
+constexpr int kLnVec = 16;
+static_assert(4 * kLnThreads * kLnVec >= 16384, "a LayerNorm row of the largest d fits the registers");
 template <typename T>
-__global__ void __launch_bounds__(256) k_layernorm(const float* __restrict__ y, int d, const T* __restrict__ gamma,
-                                                   const T* __restrict__ beta, float eps, T* __restrict__ z) {
-    __shared__ float red[8];
-    const float* yr = y + static_cast<size_t>(blockIdx.x) * d;
-    auto block_sum = [&](float v) {
-        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+__global__ void __launch_bounds__(kLnThreads) k_layernorm(const float* __restrict__ y, int d, const T* __restrict__ gamma,
+                                                          const T* __restrict__ beta, float eps, T* __restrict__ z) {
+    __shared__ float red[2][kLnThreads / 32];
+    griddep_wait();
+    griddep_launch();
+    const int n4 = d / 4;
+    const float4* yr = reinterpret_cast<const float4*>(y + static_cast<size_t>(blockIdx.x) * d);
+    float4 v[kLnVec];
+#pragma unroll
+    for (int j = 0; j < kLnVec; ++j) {
+        const int i = threadIdx.x + j * kLnThreads;
+        v[j] = i < n4 ? yr[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    auto block_sum = [&](float t, int slot) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if ((threadIdx.x & 31) == 0) red[slot][threadIdx.x >> 5] = t;
         __syncthreads();
-        if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-        __syncthreads();
-        float t = 0.f;
-        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) t += red[w];
-        return t;
+        float r = 0.f;
+#pragma unroll
+        for (int w = 0; w < kLnThreads / 32; ++w) r += red[slot][w];
+        return r;
     };
     float sum = 0.f;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) sum += yr[i];
-    const float mean = block_sum(sum) / d;
+#pragma unroll
+    for (int j = 0; j < kLnVec; ++j) sum += (v[j].x + v[j].y) + (v[j].z + v[j].w);
+    const float mean = block_sum(sum, 0) / d;
     float sq = 0.f;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) {
-        const float e = yr[i] - mean;
-        sq += e * e;
-    }
-    const float inv = 1.0f / sqrtf(block_sum(sq) / d + eps);
+#pragma unroll
+    for (int j = 0; j < kLnVec; ++j)
+        if (threadIdx.x + j * kLnThreads < n4) {
+            const float a = v[j].x - mean, b = v[j].y - mean, c = v[j].z - mean, e = v[j].w - mean;
+            sq += (a * a + b * b) + (c * c + e * e);
+        }
+    const float inv = 1.0f / sqrtf(block_sum(sq, 1) / d + eps);
     T* zr = z + static_cast<size_t>(blockIdx.x) * d;
-    for (int i = threadIdx.x; i < d; i += blockDim.x) {
-        const float g = gamma ? to_f32(gamma[i]) : 1.f;
-        const float bb = beta ? to_f32(beta[i]) : 0.f;
-        zr[i] = from_f32<T>((yr[i] - mean) * inv * g + bb);
+#pragma unroll
+    for (int j = 0; j < kLnVec; ++j) {
+        const int i = threadIdx.x + j * kLnThreads;
+        if (i < n4) {
+            const float x[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float g = gamma ? to_f32(gamma[4 * i + e]) : 1.f;
+                const float bb = beta ? to_f32(beta[4 * i + e]) : 0.f;
+                zr[4 * i + e] = from_f32<T>((x[e] - mean) * inv * g + bb);
+            }
+        }
     }
 }
 
@@ -260,6 +287,13 @@ __device__ __forceinline__ void write_next_row(T* __restrict__ dst, const T* __r
 // slices than threads are folded in by bitonic merges); k rounds then take the
 // best list head of the CTA -- a warp butterfly and one barrier per round --
 // and pop it from its owner's list.
+//
+// The tree's structure (children, ranks, input rows, ancestors) is written once
+// by spec_tree_build and by none of the kernels this one follows, so a CTA with
+// one parent node (every conditioned head, and the root) reads it before
+// griddep_wait(): the chain of dependent index loads then overlaps the
+// projection still streaming instead of following it.  Tokens and log-probs of
+// earlier depths are read only after the wait.
 template <int KMAX, typename T>
 __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c, const float2* __restrict__ part_l,
                                                 int nslices, int k, int cond, int n_int, int int_off,
@@ -272,18 +306,55 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                                                 int next_cond, int next_ld, int kdepth,
                                                 const T* __restrict__ h, const T* __restrict__ emb, int d,
                                                 T* __restrict__ xin) {
-    // Once the projection before this kernel is complete, the next head's MLP may
-    // launch: it streams its weights and waits for this kernel's outputs (tokens,
-    // input rows) with its own griddep_wait().  Triggering only after the wait keeps
-    // that MLP's CTAs off the SMs while the projection still streams.
-    griddep_wait();
-    griddep_launch();
     const int r = blockIdx.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __shared__ float topv[KMAX];
     __shared__ int topi[KMAX];
     __shared__ float2 wlse[8];
     __shared__ float lse_s;
+    // children of the current parent node: next-depth row, rank (at most k <= KMAX)
+    __shared__ int c_row[KMAX], c_rank[KMAX];
+    __shared__ int anc_node[SPEC_MAX_DEPTH + 1], anc_tok[SPEC_MAX_DEPTH + 1];
+
+    const int b = cond ? r / n_int : r;
+    const int j0 = cond ? r % n_int : 0, j1 = cond ? j0 + 1 : n_int;
+    const bool one = j1 - j0 == 1;
+    const bool rows = next_n_int > 0;
+    const bool anc = rows && next_cond == 2;
+    const size_t bT = static_cast<size_t>(b) * Tn;
+
+    // 0. structure of a single parent node u: thread a < nc holds child a
+    int u1 = 0, nc1 = 0, my_c = 0;
+    if (one) {
+        u1 = internal[int_off + j0];
+        const int a0 = child_off[u1];
+        nc1 = child_off[u1 + 1] - a0;
+        if (tid < nc1) {
+            my_c = child_idx[a0 + tid];
+            c_rank[tid] = rank[my_c];
+            c_row[tid] = rows ? row_of[my_c] : -1;
+        }
+        if (anc && tid == 0) {
+            int a = u1;
+            for (int i = kdepth; i >= 1; --i) {
+                anc_node[i] = a;
+                a = parent[a];
+            }
+        }
+    }
+    __syncthreads();   // anc_node is read by other threads after the wait
+
+    // Once the projection before this kernel is complete, the next head's MLP may
+    // launch: it streams its weights and waits for this kernel's outputs (tokens,
+    // input rows) with its own griddep_wait().  Triggering only after the wait keeps
+    // that MLP's CTAs off the SMs while the projection still streams.
+    griddep_wait();
+    griddep_launch();
+
+    // loads of earlier depths' outputs, issued with the candidate lists below
+    float base1 = 0.f;
+    if (one && node_logprob && tid < nc1) base1 = node_logprob[bT + u1];
+    if (one && anc && tid >= 1 && tid <= kdepth) anc_tok[tid] = node_tok[bT + anc_node[tid]];
 
     // 1. each thread takes the list of slice tid (first k valid, placeholders after)
     // and its (max, sum exp); slices beyond blockDim are folded in by bitonic merges
@@ -358,78 +429,79 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
     }
     __syncthreads();
 
-    // 4. children of this row's parent node(s); next depth's input rows
-    const int b = cond ? r / n_int : r;
-    const int j0 = cond ? r % n_int : 0, j1 = cond ? j0 + 1 : n_int;
+    // 3. children of this row's parent node(s); next depth's input rows
+    const int per = d / (16 / static_cast<int>(sizeof(T)));   // 16-byte chunks per d-wide block
+    const size_t row0 = static_cast<size_t>(b) * next_n_int;
     for (int j = j0; j < j1; ++j) {
-        const int u = internal[int_off + j];
-        const float base = node_logprob ? node_logprob[static_cast<size_t>(b) * Tn + u] : 0.f;
-        for (int a = child_off[u] + tid; a < child_off[u + 1]; a += blockDim.x) {
-            const int c = child_idx[a];
-            const int rr = rank[c];
-            node_tok[static_cast<size_t>(b) * Tn + c] = topi[rr];
-            node_logit[static_cast<size_t>(b) * Tn + c] = topv[rr];
-            if (node_logprob) node_logprob[static_cast<size_t>(b) * Tn + c] = base + (topv[rr] - lse_s);
-        }
-        if (next_n_int > 0) {
-            // next depth's input rows [h_b || E[token]] of all children at once (a node has
-            // at most k <= KMAX children: their rows and tokens go to shared memory first)
-            __shared__ int c_row[KMAX], c_tok[KMAX];
-            const int a0 = child_off[u], nc = min(child_off[u + 1] - a0, KMAX);
-            __syncthreads();
+        int u = u1, nc = nc1;
+        if (one) {
+            if (tid < nc) {
+                const int rr = c_rank[tid];
+                node_tok[bT + my_c] = topi[rr];
+                node_logit[bT + my_c] = topv[rr];
+                if (node_logprob) node_logprob[bT + my_c] = base1 + (topv[rr] - lse_s);
+            }
+        } else {
+            // several parent nodes share this row (an unconditioned head below the root)
+            u = internal[int_off + j];
+            const int a0 = child_off[u];
+            nc = child_off[u + 1] - a0;
+            const float base = node_logprob ? node_logprob[bT + u] : 0.f;
+            __syncthreads();   // the previous parent's c_row / c_rank / anc_tok are consumed
             if (tid < nc) {
                 const int c = child_idx[a0 + tid];
-                c_row[tid] = row_of[c];
-                c_tok[tid] = topi[rank[c]];
+                const int rr = rank[c];
+                node_tok[bT + c] = topi[rr];
+                node_logit[bT + c] = topv[rr];
+                if (node_logprob) node_logprob[bT + c] = base + (topv[rr] - lse_s);
+                c_rank[tid] = rr;
+                c_row[tid] = rows ? row_of[c] : -1;
+            }
+            if (anc && tid == 0) {
+                int a = u;
+                for (int i = kdepth; i >= 1; --i) {
+                    anc_tok[i] = node_tok[bT + a];
+                    a = parent[a];
+                }
             }
             __syncthreads();
-            const int per = d / (16 / static_cast<int>(sizeof(T)));   // 16-byte chunks per d-wide block
-            const size_t row0 = static_cast<size_t>(b) * next_n_int;
-            if (next_cond == 2) {
-                // all-ancestor rows [h_b || E[tok(a_1)] || ... || E[tok(a_k)] || E[tok(c)]]: the
-                // blocks of u's path (depths 1..k, shared by all children) then each child's own
-                __shared__ int anc_tok[SPEC_MAX_DEPTH + 1];
-                if (tid == 0) {
-                    int a = u;
-                    for (int i = kdepth; i >= 1; --i) {
-                        anc_tok[i] = node_tok[static_cast<size_t>(b) * Tn + a];
-                        a = parent[a];
-                    }
-                }
-                __syncthreads();
-                for (int i = 1; i <= kdepth; ++i) {
-                    const uint4* er = reinterpret_cast<const uint4*>(emb + static_cast<size_t>(anc_tok[i]) * d);
-                    for (int w = tid; w < per; w += blockDim.x) {
-                        const uint4 v = er[w];
+        }
+        if (!rows) continue;
+        if (anc) {
+            // all-ancestor rows [h_b || E[tok(a_1)] || ... || E[tok(a_k)] || E[tok(c)]]: the
+            // blocks of u's path (depths 1..k, shared by all children) then each child's own
+            for (int i = 1; i <= kdepth; ++i) {
+                const uint4* er = reinterpret_cast<const uint4*>(emb + static_cast<size_t>(anc_tok[i]) * d);
+                for (int w = tid; w < per; w += blockDim.x) {
+                    const uint4 v = er[w];
 #pragma unroll
-                        for (int a = 0; a < KMAX; ++a)
-                            if (a < nc && c_row[a] >= 0)
-                                reinterpret_cast<uint4*>(xin + (row0 + c_row[a]) * next_ld)[i * per + w] = v;
-                    }
+                    for (int a = 0; a < KMAX; ++a)
+                        if (a < nc && c_row[a] >= 0)
+                            reinterpret_cast<uint4*>(xin + (row0 + c_row[a]) * next_ld)[i * per + w] = v;
                 }
             }
-            // the children's own embedding blocks (block 1 for cond 1, block k + 1 for cond 2;
-            // the h_b parts were written by the step's first kernel); every load of a chunk
-            // column is issued before any store
-            const int own = next_cond == 2 ? kdepth + 1 : 1;
-            for (int w0 = tid; w0 < per; w0 += 2 * blockDim.x) {
-                const int w1 = w0 + blockDim.x;   // second chunk column of this thread (if any)
-                const bool two = w1 < per;
-                uint4 ev0[KMAX], ev1[KMAX];
+        }
+        // the children's own embedding blocks (block 1 for cond 1, block k + 1 for cond 2;
+        // the h_b parts were written by the step's first kernel); every load of a chunk
+        // column is issued before any store
+        const int own = anc ? kdepth + 1 : 1;
+        for (int w0 = tid; w0 < per; w0 += 2 * blockDim.x) {
+            const int w1 = w0 + blockDim.x;   // second chunk column of this thread (if any)
+            const bool two = w1 < per;
+            uint4 ev0[KMAX], ev1[KMAX];
 #pragma unroll
-                for (int a = 0; a < KMAX; ++a)
-                    if (a < nc) {
-                        const uint4* er = reinterpret_cast<const uint4*>(emb + static_cast<size_t>(c_tok[a]) * d);
-                        ev0[a] = er[w0];
-                        if (two) ev1[a] = er[w1];
-                    }
+            for (int a = 0; a < KMAX; ++a)
+                if (a < nc) {
+                    const uint4* er = reinterpret_cast<const uint4*>(emb + static_cast<size_t>(topi[c_rank[a]]) * d);
+                    ev0[a] = er[w0];
+                    if (two) ev1[a] = er[w1];
+                }
 #pragma unroll
-                for (int a = 0; a < KMAX; ++a) {
-                    if (a < nc && c_row[a] >= 0) {
-                        uint4* o = reinterpret_cast<uint4*>(xin + (row0 + c_row[a]) * next_ld) + own * per;
-                        o[w0] = ev0[a];
-                        if (two) o[w1] = ev1[a];
-                    }
+            for (int a = 0; a < KMAX; ++a) {
+                if (a < nc && c_row[a] >= 0) {
+                    uint4* o = reinterpret_cast<uint4*>(xin + (row0 + c_row[a]) * next_ld) + own * per;
+                    o[w0] = ev0[a];
+                    if (two) o[w1] = ev1[a];
                 }
             }
         }
@@ -730,8 +802,8 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
         const bool ln = hs.form[k] == 1;
         const T* W1bk = static_cast<const T*>(hs.W1b[k]);
         auto layernorm = [&]() -> spec_status {
-            SPEC_CUDA_TRY(launch("draft_layernorm", k_layernorm<T>, dim3(R), dim3(256), 0, s, yln, d,
-                                 static_cast<const T*>(hs.gamma[k]), static_cast<const T*>(hs.beta[k]), ln_eps, z));
+            SPEC_CUDA_TRY(launch_ex("draft_layernorm", k_layernorm<T>, dim3(R), dim3(kLnThreads), 0, s, p.tc, yln, d,
+                                    static_cast<const T*>(hs.gamma[k]), static_cast<const T*>(hs.beta[k]), ln_eps, z));
             return SPEC_OK;
         };
         if constexpr (std::is_same<T, __nv_bfloat16>::value) {
