@@ -796,7 +796,11 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
         const T* W1k = static_cast<const T*>(hs.W1[k]);
         const T* b1k = static_cast<const T*>(hs.b1[k]);
         const T* W2k = static_cast<const T*>(hs.W2[k]);
-        const int dep_k0 = cond[k] ? d : d_in;   // input columns that come from the previous select
+        // Input columns that come from the previous kernel: the embedding parts of a
+        // conditioned head's rows (the previous select writes them, the step's first
+        // kernel the h_b parts, long complete by then); every column of the first head's
+        // rows, which that first kernel gathers while the head's MLP starts.
+        const int dep_k0 = !cond[k] ? d_in : k == 0 ? 0 : d;
         // form 1: a = SiLU(W1 u + b1) into hid (W1b set) or yln; y = W1b a + b1b into yln;
         // z = LayerNorm(y) (queued between the MLP and the projection)
         const bool ln = hs.form[k] == 1;
