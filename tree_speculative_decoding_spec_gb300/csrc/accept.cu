@@ -64,6 +64,7 @@ __device__ __forceinline__ void top2_merge(float& v1, int& i1, float& v2, float 
 
 __global__ void __launch_bounds__(kRowThreads) k_rows_greedy(const float* __restrict__ logits, int V, int slice,
                                                              int slices, float4* __restrict__ part) {
+    griddep_launch();   // the walk may start loading the tree while the rows are read
     const int sl = blockIdx.x;
     const size_t row = blockIdx.y;
     const float* x = logits + row * V;
@@ -71,12 +72,23 @@ __global__ void __launch_bounds__(kRowThreads) k_rows_greedy(const float* __rest
     float b1 = -INFINITY, b2 = -INFINITY;
     int i1 = 0x7fffffff;
     if ((V & 3) == 0) {
-        for (int e = v0 + 4 * threadIdx.x; e < v1; e += 4 * kRowThreads) {
-            const float4 q = __ldcs(reinterpret_cast<const float4*>(x + e));
-            top2_push(b1, i1, b2, q.x, e);
-            top2_push(b1, i1, b2, q.y, e + 1);
-            top2_push(b1, i1, b2, q.z, e + 2);
-            top2_push(b1, i1, b2, q.w, e + 3);
+        // every load of the thread's share is issued before any compare (slice <= 4 * kRowThreads * kLseIter)
+        float4 q[kLseIter];
+#pragma unroll
+        for (int it = 0; it < kLseIter; ++it) {
+            const int e = v0 + 4 * (static_cast<int>(threadIdx.x) + kRowThreads * it);
+            q[it] = e < v1 ? __ldcs(reinterpret_cast<const float4*>(x + e))
+                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        }
+#pragma unroll
+        for (int it = 0; it < kLseIter; ++it) {
+            const int e = v0 + 4 * (static_cast<int>(threadIdx.x) + kRowThreads * it);
+            if (e < v1) {
+                top2_push(b1, i1, b2, q[it].x, e);
+                top2_push(b1, i1, b2, q[it].y, e + 1);
+                top2_push(b1, i1, b2, q[it].z, e + 2);
+                top2_push(b1, i1, b2, q[it].w, e + 3);
+            }
         }
     } else {
         for (int e = v0 + threadIdx.x; e < v1; e += kRowThreads) top2_push(b1, i1, b2, x[e], e);
@@ -183,6 +195,7 @@ __device__ __forceinline__ void lse_ent_merge(float& m, float& s, float& t, floa
 // Typical acceptance: (m, s, t) of every row of logits_p (for entropy and log-sum-exp).
 __global__ void __launch_bounds__(kRowThreads) k_rows_ent(const float* __restrict__ lp, int V, int slice, int slices,
                                                           float inv_temp, float4* __restrict__ part) {
+    griddep_launch();   // the walk may start loading the tree while the rows are read
     const int sl = blockIdx.x;
     const size_t row = blockIdx.y;
     const int v0 = sl * slice, v1 = min(V, v0 + slice);
@@ -204,6 +217,7 @@ __global__ void __launch_bounds__(kRowThreads) k_rows_lse(const float* __restric
                                                           const int32_t* __restrict__ child_off, int Tn, int V,
                                                           int slice, int slices, float inv_temp,
                                                           float4* __restrict__ part) {
+    griddep_launch();   // the walk may start loading the tree while the rows are read
     const int sl = blockIdx.x;
     const size_t row = blockIdx.y;
     const int u = static_cast<int>(row % Tn);
@@ -306,6 +320,16 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_greedy(const float4* __re
                                                               int32_t* __restrict__ accept_path,
                                                               int32_t* __restrict__ next_token, float* __restrict__ margin) {
     const int b = blockIdx.x;
+    // The tree and the node tokens are inputs of the call, complete before the rows
+    // kernel started: they are copied to shared memory while that kernel runs.
+    __shared__ int32_t s_par[SPEC_MAX_T], s_dep[SPEC_MAX_T], s_tok[SPEC_MAX_T];
+    for (int u = threadIdx.x; u < Tn; u += blockDim.x) {
+        s_par[u] = parent[u];
+        s_dep[u] = depth[u];
+        s_tok[u] = node_tok[static_cast<size_t>(b) * Tn + u];
+    }
+    __syncthreads();
+    griddep_wait();   // the rows kernel's partials
     __shared__ int amax[SPEC_MAX_T];
     __shared__ float gap[SPEC_MAX_T];
     __shared__ unsigned char pass[SPEC_MAX_T], acc[SPEC_MAX_T];
@@ -321,14 +345,14 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_greedy(const float4* __re
     }
     __syncthreads();
     for (int c = threadIdx.x; c < Tn; c += blockDim.x)
-        pass[c] = (c > 0) && node_tok[static_cast<size_t>(b) * Tn + c] == amax[parent[c]];
+        pass[c] = (c > 0) && s_tok[c] == amax[s_par[c]];
     __syncthreads();
-    const int ustar = resolve_path(parent, depth, Tn, max_depth, acc, pass, iscr);
+    const int ustar = resolve_path(s_par, s_dep, Tn, max_depth, acc, pass, iscr);
     float mg = INFINITY;
     for (int u = threadIdx.x; u < Tn; u += blockDim.x)
         if (acc[u]) mg = fminf(mg, gap[u]);
     mg = block_min_f(mg, fscr);
-    write_path(parent, depth, ustar, b, max_depth, accept_len, accept_path);
+    write_path(s_par, s_dep, ustar, b, max_depth, accept_len, accept_path);
     if (threadIdx.x == 0) {
         next_token[b] = amax[ustar];
         if (margin) margin[b] = mg;
@@ -352,6 +376,7 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
     // Medusa typical acceptance (threshold min(eps, alpha exp(-H(p_parent))), extra
     // token from p at the last accepted node).  lse_q holds that threshold then.
     const int b = blockIdx.x;
+    griddep_wait();   // the rows kernel's partials (launched early: the launch overlaps it)
     __shared__ float lse_p[SPEC_MAX_T], lse_q[SPEC_MAX_T];
     __shared__ unsigned char pass[SPEC_MAX_T], acc[SPEC_MAX_T];
     __shared__ float dmar[SPEC_MAX_T];
@@ -566,14 +591,14 @@ extern "C" spec_status tree_accept(int32_t mode, const float* logits_p, const fl
     if (mode == 0) {
         SPEC_CUDA_TRY(launch("accept_rows_greedy", accept::k_rows_greedy, grid, dim3(accept::kRowThreads), 0, s, logits_p, V,
                              p.slice, p.slices, part));
-        SPEC_CUDA_TRY(launch("accept_walk_greedy", accept::k_walk_greedy, dim3(B), dim3(accept::kWalkThreads), 0, s, part,
+        SPEC_CUDA_TRY(launch_ex("accept_walk_greedy", accept::k_walk_greedy, dim3(B), dim3(accept::kWalkThreads), 0, s, true, part,
                              p.slices, node_tok, tree->parent, tree->depth, tree->T, tree->max_depth, accept_len,
                              accept_path, next_token, margin));
     } else {
         const float inv_temp = 1.0f / temperature;
         SPEC_CUDA_TRY(launch("accept_rows_lse", accept::k_rows_lse, grid, dim3(accept::kRowThreads), 0, s, logits_p, logits_q,
                              tree->child_off, tree->T, V, p.slice, p.slices, inv_temp, part));
-        SPEC_CUDA_TRY(launch("accept_walk_reject", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), 0, s, part,
+        SPEC_CUDA_TRY(launch_ex("accept_walk_reject", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), 0, s, true, part,
                              p.slices, logits_p, logits_q, node_tok, tree->parent, tree->depth, tree->child_off,
                              tree->T, tree->max_depth, V, inv_temp, seed, offset, accept_len, accept_path, next_token,
                              margin, ws, 0, 0.f, 0.f));
@@ -607,7 +632,7 @@ extern "C" spec_status tree_accept_typical(const float* logits_p, const int32_t*
     SPEC_CUDA_TRY(reset_device_status(ws, s));
     SPEC_CUDA_TRY(launch("accept_rows_ent", accept::k_rows_ent, grid, dim3(accept::kRowThreads), 0, s, logits_p, V,
                          p.slice, p.slices, inv_temp, part));
-    SPEC_CUDA_TRY(launch("accept_walk_typical", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), 0, s, part,
+    SPEC_CUDA_TRY(launch_ex("accept_walk_typical", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), 0, s, true, part,
                          p.slices, logits_p, static_cast<const float*>(nullptr), node_tok, tree->parent, tree->depth,
                          tree->child_off, tree->T, tree->max_depth, V, inv_temp, seed, offset, accept_len, accept_path,
                          next_token, margin, ws, 1, epsilon, alpha));

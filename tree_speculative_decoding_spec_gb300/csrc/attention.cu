@@ -34,6 +34,7 @@ __global__ void __launch_bounds__(256) k_attn_fma(const T* __restrict__ q, const
                                                   const uint64_t* __restrict__ anc, int Tn, int words, int Hq, int Hkv,
                                                   int Lmax, float scale_log2, int chunk, int n_pre, int n_rowblocks,
                                                   float* __restrict__ part, const tc::KvPages pg, void* ws) {
+    griddep_launch();   // the combine may start launching: it waits for the partials
     constexpr int LD = D + 4;
     constexpr int LP = BC + 4;
     constexpr int DT = D / 16;   // output dims per thread
@@ -210,6 +211,8 @@ __global__ void __launch_bounds__(256) k_attn_fma(const T* __restrict__ q, const
 // O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c, lse = (M + log2 l) ln 2.
 // Slots read: the non-empty prefix splits, plus the tree slot n_pre unless the
 // tree keys were folded into the last prefix split (tensor-core layout).
+constexpr int kCombineGroup = 4;   // partials whose loads a combine warp issues together
+
 __global__ void __launch_bounds__(256) k_attn_combine(const float* __restrict__ part, const int32_t* __restrict__ prefix_len,
                                                       int Tn, int Hq, int D, int Lmax, int chunk, int n_pre, int folded,
                                                       int nrows, float* __restrict__ out, float* __restrict__ lse) {
@@ -222,20 +225,36 @@ __global__ void __launch_bounds__(256) k_attn_combine(const float* __restrict__ 
     const int nread = folded ? max(nvalid, 1) : nvalid + 1;
     const float* base = part + static_cast<size_t>(row) * (n_pre + 1) * (D + 4);
     auto slot = [&](int i) { return (!folded && i == nvalid) ? n_pre : i; };
-    float M = -INFINITY;
-    for (int i = lane; i < nread; i += 32) M = fmaxf(M, base[static_cast<size_t>(slot(i)) * (D + 4)]);
-    M = warp_max(M);
+    griddep_wait();   // the attention kernel's partials (launched early: the launch overlaps it)
     const bool has = 4 * lane < D;
+    float M = -INFINITY;
     float l = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = 0; i < nread; ++i) {
-        const float* pc = base + static_cast<size_t>(slot(i)) * (D + 4);
-        const float m = pc[0];
-        const float w = m == -INFINITY ? 0.f : exp2f(m - M);
-        l += w * pc[1];
-        if (has && w != 0.f) {
-            const float4 v = *reinterpret_cast<const float4*>(pc + 4 + 4 * lane);
-            o.x += w * v.x; o.y += w * v.y; o.z += w * v.z; o.w += w * v.w;
+    for (int i = lane; i < nread; i += 32) M = fmaxf(M, base[static_cast<size_t>(slot(i)) * (D + 4)]);
+    M = warp_max(M);
+    // the partials in groups of kCombineGroup, each group's loads issued together
+    for (int i0 = 0; i0 < nread; i0 += kCombineGroup) {
+        float pm[kCombineGroup], pl[kCombineGroup];
+        float4 pv[kCombineGroup];
+#pragma unroll
+        for (int j = 0; j < kCombineGroup; ++j) {
+            pm[j] = -INFINITY;
+            pl[j] = 0.f;
+            pv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i0 + j < nread) {
+                const float* pc = base + static_cast<size_t>(slot(i0 + j)) * (D + 4);
+                pm[j] = pc[0];
+                pl[j] = pc[1];
+                if (has) pv[j] = *reinterpret_cast<const float4*>(pc + 4 + 4 * lane);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < kCombineGroup; ++j) {
+            const float w = pm[j] == -INFINITY ? 0.f : exp2f(pm[j] - M);
+            l += w * pl[j];
+            if (has && w != 0.f) {
+                o.x += w * pv[j].x; o.y += w * pv[j].y; o.z += w * pv[j].z; o.w += w * pv[j].w;
+            }
         }
     }
     if (has) {
@@ -310,7 +329,7 @@ spec_status run_fma(const T* q, const T* kc, const T* vc, const int32_t* prefix_
                              ws));
     }
     const int nrows = B * Hq * t->T;
-    SPEC_CUDA_TRY(launch("attn_combine", k_attn_combine, dim3((nrows + 7) / 8), dim3(256), 0, s, part, prefix_len, t->T,
+    SPEC_CUDA_TRY(launch_ex("attn_combine", k_attn_combine, dim3((nrows + 7) / 8), dim3(256), 0, s, true, part, prefix_len, t->T,
                          Hq, D, Lmax, p.chunk, p.n_pre, 0, nrows, out, lse));
     return SPEC_OK;
 }
@@ -356,7 +375,7 @@ static spec_status run_checked(const void* q, const void* k_cache, const void* v
                                  static_cast<const T*>(v_tree), tree, B, Hq, Hkv, Lmax, scale, part, ws, s, pg);
             if (st != SPEC_OK) return st;
             const int nrows = B * Hq * tree->T;
-            SPEC_CUDA_TRY(launch("attn_combine", k_attn_combine, dim3((nrows + 7) / 8), dim3(256), 0, s, part,
+            SPEC_CUDA_TRY(launch_ex("attn_combine", k_attn_combine, dim3((nrows + 7) / 8), dim3(256), 0, s, true, part,
                                  prefix_len, tree->T, Hq, D, Lmax, p.tcp.chunk, p.tcp.n_pre, 1, nrows, out, lse));
             return SPEC_OK;
         }

@@ -131,6 +131,7 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    griddep_launch();   // the combine may start launching: it waits for the partials
     const int kvc_row0 = (b * p.Hkv + kvh) * p.Lmax + pre_begin;   // first prefix key of this split
     const int kvt_row0 = (b * p.Hkv + kvh) * p.T;                  // first tree key
     const int q_row0 = (b * p.Hq + kvh * p.g) * p.T + rb * kARows;
