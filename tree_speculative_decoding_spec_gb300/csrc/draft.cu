@@ -163,6 +163,17 @@ __global__ void __launch_bounds__(kLnThreads) k_layernorm(const float* __restric
 
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) { return va > vb || (va == vb && ia < ib); }
 
+// A 32-bit key that orders like the float (NaN below -inf, -0 equal to +0), and back.
+__device__ __forceinline__ unsigned order_key(float v) {
+    if (v != v) return 0u;
+    if (v == 0.f) v = 0.f;
+    const unsigned b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // Insert (v, i) into a descending list of KMAX candidates (registers, every
 // index static); callers keep KMAX >= k and use the first k.
 template <int KMAX>
@@ -285,7 +296,7 @@ __device__ __forceinline__ void write_next_row(T* __restrict__ dst, const T* __r
 // the row's log-sum-exp, then the children of the row's parent node(s).
 // Merging: each thread holds its slice's sorted list in registers (more
 // slices than threads are folded in by bitonic merges); k rounds then take the
-// best list head of the CTA -- a warp butterfly and one barrier per round --
+// best list head of the CTA -- warp reductions and one barrier per round --
 // and pop it from its owner's list.
 //
 // The tree's structure (children, ranks, input rows, ancestors) is written once
@@ -385,40 +396,35 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
     for (int o = 16; o > 0; o >>= 1) lse_merge(M, S, __shfl_xor_sync(0xffffffffu, M, o), __shfl_xor_sync(0xffffffffu, S, o));
     if (lane == 0) wlse[warp] = make_float2(M, S);
 
-    // 2. k rounds over the list heads: the warp's best head by an xor butterfly, the
-    // CTA's best over the warps' (double-buffered shared slots, one barrier per
-    // round), and the owner of the winning candidate shifts its list.  Candidates are
-    // unique (the slices are disjoint), so the index identifies the owner.
-    __shared__ Cand slot[2][8];
+    // 2. k rounds over the list heads.  A candidate is compared through a 32-bit key
+    // that orders like its logit (NaN lowest, -0 as +0), so the warp's best head is one
+    // max-reduction of keys and one min-reduction of the indices holding that key (lower
+    // token wins ties); the CTA's best is the same two reductions over the warps'
+    // (double-buffered shared slots, one barrier per round); the owner pops it.
+    // Candidates are unique (the slices are disjoint), so the index identifies the owner.
+    __shared__ uint2 slot[2][8];
     const int nw = blockDim.x >> 5;
 #pragma unroll 1
     for (int rr = 0; rr < k; ++rr) {
-        float v = lv[0];
-        int i = li[0];
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float v2 = __shfl_xor_sync(0xffffffffu, v, o);
-            const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
-            if (better(v2, i2, v, i)) { v = v2; i = i2; }
-        }
-        if (lane == 0) slot[rr & 1][warp] = Cand{v, i};
+        const unsigned key = order_key(lv[0]);
+        const unsigned wk = __reduce_max_sync(0xffffffffu, key);
+        const unsigned wi = __reduce_min_sync(0xffffffffu, key == wk ? static_cast<unsigned>(li[0]) : 0xffffffffu);
+        if (lane == 0) slot[rr & 1][warp] = make_uint2(wk, wi);
         __syncthreads();
-        Cand best = slot[rr & 1][0];
-        for (int w = 1; w < nw; ++w) {
-            const Cand c = slot[rr & 1][w];
-            if (better(c.v, c.i, best.v, best.i)) best = c;
-        }
-        if (li[0] == best.i && best.v == lv[0]) {   // this thread's head won: pop it
+        const uint2 c = lane < nw ? slot[rr & 1][lane] : make_uint2(0u, 0xffffffffu);
+        const unsigned bk = __reduce_max_sync(0xffffffffu, c.x);
+        const unsigned bi = __reduce_min_sync(0xffffffffu, c.x == bk ? c.y : 0xffffffffu);
+        if (static_cast<unsigned>(li[0]) == bi) {   // this thread's head won: pop it
 #pragma unroll
             for (int e = 0; e + 1 < KMAX; ++e) { lv[e] = lv[e + 1]; li[e] = li[e + 1]; }
             lv[KMAX - 1] = -INFINITY;
             li[KMAX - 1] = 0x7fffffff;
         }
         if (tid == 0) {
-            int ix = best.i;
+            int ix = static_cast<int>(bi);
             // fewer than k finite logits (NaN/inf weights) leave placeholders: keep tokens in range
             if (ix < 0 || ix >= V) { flag_status(ws, SPEC_EINVAL); ix = 0; }
-            topv[rr] = best.v;
+            topv[rr] = key_value(bk);
             topi[rr] = ix;
         }
     }
