@@ -154,6 +154,17 @@ __device__ __forceinline__ float warp_sum(float v) {
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
+// A 32-bit key that orders like the float (NaN below -inf, -0 equal to +0), and back.
+__device__ __forceinline__ unsigned order_key(float v) {
+    if (v != v) return 0u;
+    if (v == 0.f) v = 0.f;
+    const unsigned b = __float_as_uint(v);
+    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(unsigned k) {
+    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
 // Record a device-detected failure in a workspace's status word (largest code wins).
 __device__ __forceinline__ void flag_status(void* ws, int code) { atomicMax(static_cast<int*>(ws), code); }
 

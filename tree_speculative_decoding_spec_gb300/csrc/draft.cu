@@ -163,17 +163,6 @@ __global__ void __launch_bounds__(kLnThreads) k_layernorm(const float* __restric
 
 __device__ __forceinline__ bool better(float va, int ia, float vb, int ib) { return va > vb || (va == vb && ia < ib); }
 
-// A 32-bit key that orders like the float (NaN below -inf, -0 equal to +0), and back.
-__device__ __forceinline__ unsigned order_key(float v) {
-    if (v != v) return 0u;
-    if (v == 0.f) v = 0.f;
-    const unsigned b = __float_as_uint(v);
-    return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-__device__ __forceinline__ float key_value(unsigned k) {
-    return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
-}
-
 // Insert (v, i) into a descending list of KMAX candidates (registers, every
 // index static); callers keep KMAX >= k and use the first k.
 template <int KMAX>
