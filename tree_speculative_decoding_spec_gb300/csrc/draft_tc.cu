@@ -31,7 +31,6 @@ constexpr int kBM = 128;        // MMA M: weight rows per CTA
 constexpr int kMaxSplits = 8;   // MLP split-K: one cluster (portable size) per weight tile
 // Build-time shape knobs (defaults are the tuned choice):
 //   SPEC_DRAFT_KB        64-column K blocks per pipeline stage
-//   SPEC_DRAFT_SMEM_KB   shared-memory budget per CTA in KB (100 keeps two CTAs per SM)
 //   SPEC_DRAFT_L2PROMO   L2 promotion of the weight loads: 0 none, 1 128 B, 2 256 B
 //   SPEC_DRAFT_EVICT_FIRST  1: weight loads carry the L2 evict-first policy
 //   SPEC_DRAFT_ROTATE    1: each CTA starts its K loop at a different stage (by
@@ -39,9 +38,6 @@ constexpr int kMaxSplits = 8;   // MLP split-K: one cluster (portable size) per 
 //                        activation lines from L2 at the same moment
 #ifndef SPEC_DRAFT_KB
 #define SPEC_DRAFT_KB 2
-#endif
-#ifndef SPEC_DRAFT_SMEM_KB
-#define SPEC_DRAFT_SMEM_KB 100
 #endif
 #ifndef SPEC_DRAFT_ROTATE
 #define SPEC_DRAFT_ROTATE 1
@@ -59,7 +55,6 @@ constexpr int kBKS = kBK * kKB; // K per stage
 constexpr int kThreads = 128;
 constexpr int kStageA = kBM * kBKS * 2;
 constexpr int kBoxA = kBM * kBK * 2;      // one K block of the weight tile
-constexpr int kSmemBudget = SPEC_DRAFT_SMEM_KB * 1024;
 
 struct UmmaParams {
     int M;          // weight rows
@@ -386,7 +381,10 @@ uint32_t tmem_cols_of(int n_pad) {
 
 int stages_of(int n_pad) {
     const int per = kStageA + n_pad * kBKS * 2;
-    return std::max(2, std::min(8, kSmemBudget / per));
+    // as many stages as keep two CTAs per SM (228 KB per SM, 1 KB reserved per CTA; the
+    // fixed part: alignment slack, barriers, flags)
+    const int fixed = 1024 + 17 * 8 + 16;
+    return std::max(2, std::min(8, (233472 / 2 - 1024 - fixed) / per));
 }
 
 size_t smem_of(int n_pad, int stages) {
