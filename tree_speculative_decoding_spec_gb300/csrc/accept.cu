@@ -259,9 +259,6 @@ __device__ __forceinline__ int block_max_int(int v, int* scratch) {
     for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = max(r, scratch[w]);
     return r;
 }
-__device__ __forceinline__ int block_min_int(int v, int* scratch) {
-    return -block_max_int(-v, scratch);
-}
 __device__ __forceinline__ float block_min_f(float v, float* scratch) {
     v = warp_min(v);
     __syncthreads();
@@ -269,15 +266,6 @@ __device__ __forceinline__ float block_min_f(float v, float* scratch) {
     __syncthreads();
     float r = scratch[0];
     for (int w = 1; w < (int)(blockDim.x >> 5); ++w) r = fminf(r, scratch[w]);
-    return r;
-}
-__device__ __forceinline__ float block_sum_f(float v, float* scratch) {
-    v = warp_sum(v);
-    __syncthreads();
-    if ((threadIdx.x & 31) == 0) scratch[threadIdx.x >> 5] = v;
-    __syncthreads();
-    float r = 0.f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) r += scratch[w];
     return r;
 }
 
