@@ -305,8 +305,12 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                                                 float* __restrict__ node_logprob, void* ws, int next_n_int,
                                                 int next_cond, int next_ld, int kdepth,
                                                 const T* __restrict__ h, const T* __restrict__ emb, int d,
-                                                T* __restrict__ xin) {
-    const int r = blockIdx.x;
+                                                T* __restrict__ xin, int cpr) {
+    // cpr CTAs per row (one per child of a single parent that needs next-depth rows): each
+    // computes the row's top-k (the same result) and copies its own child's rows, so the
+    // embedding rows pass through cpr SMs instead of one; CTA 0 of the row writes the
+    // node outputs.
+    const int r = blockIdx.x / cpr, ci = blockIdx.x % cpr;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     __shared__ float topv[KMAX];
     __shared__ int topi[KMAX];
@@ -430,7 +434,7 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
     for (int j = j0; j < j1; ++j) {
         int u = u1, nc = nc1;
         if (one) {
-            if (tid < nc) {
+            if (tid < nc && ci == 0) {
                 const int rr = c_rank[tid];
                 node_tok[bT + my_c] = topi[rr];
                 node_logit[bT + my_c] = topv[rr];
@@ -471,7 +475,7 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                     const uint4 v = er[w];
 #pragma unroll
                     for (int a = 0; a < KMAX; ++a)
-                        if (a < nc && c_row[a] >= 0)
+                        if (a < nc && c_row[a] >= 0 && (cpr == 1 || a == ci))
                             reinterpret_cast<uint4*>(xin + (row0 + c_row[a]) * next_ld)[i * per + w] = v;
                 }
             }
@@ -486,14 +490,14 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
             uint4 ev0[KMAX], ev1[KMAX];
 #pragma unroll
             for (int a = 0; a < KMAX; ++a)
-                if (a < nc) {
+                if (a < nc && (cpr == 1 || a == ci)) {
                     const uint4* er = reinterpret_cast<const uint4*>(emb + static_cast<size_t>(topi[c_rank[a]]) * d);
                     ev0[a] = er[w0];
                     if (two) ev1[a] = er[w1];
                 }
 #pragma unroll
             for (int a = 0; a < KMAX; ++a) {
-                if (a < nc && c_row[a] >= 0) {
+                if (a < nc && c_row[a] >= 0 && (cpr == 1 || a == ci)) {
                     uint4* o = reinterpret_cast<uint4*>(xin + (row0 + c_row[a]) * next_ld) + own * per;
                     o[w0] = ev0[a];
                     if (two) o[w1] = ev1[a];
@@ -747,10 +751,14 @@ spec_status launch_select(bool pdl, const Plan& p, const spec_tree* t, int R, in
                           int int_off, int next_n_int, int V, const Cand* pc, const float2* pl, int32_t* node_tok,
                           float* node_logit, float* node_logprob, void* ws, const T* h, const T* emb, int d, T* xin,
                           int next_cond, int next_ld, cudaStream_t s) {
-    SPEC_CUDA_TRY(launch_ex("draft_select", k_select<KMAX, T>, dim3(R), dim3(256), 0, s, pdl, pc, pl, p.nslices, topk, cond,
-                            n_int, int_off, t->internal, t->child_off, t->child_idx, t->rank, t->parent, t->row_of,
-                            t->T, V, node_tok, node_logit, node_logprob, ws, next_n_int, next_cond, next_ld, k, h, emb,
-                            d, xin));
+    // one CTA per child where each CTA has a single parent node and children get next-depth rows
+    const bool single_parent = cond != 0 || n_int == 1;
+    const int cpr = (next_n_int > 0 && single_parent && k + 1 <= t->max_depth)
+                        ? std::max(1, std::min(topk, t->max_rank_at_depth[k + 1] + 1)) : 1;
+    SPEC_CUDA_TRY(launch_ex("draft_select", k_select<KMAX, T>, dim3(R * cpr), dim3(256), 0, s, pdl, pc, pl, p.nslices, topk,
+                            cond, n_int, int_off, t->internal, t->child_off, t->child_idx, t->rank, t->parent,
+                            t->row_of, t->T, V, node_tok, node_logit, node_logprob, ws, next_n_int, next_cond, next_ld, k,
+                            h, emb, d, xin, cpr));
     return SPEC_OK;
 }
 
