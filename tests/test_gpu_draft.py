@@ -226,3 +226,26 @@ def test_draft_heads_form0_matches_hydra_draft():
     b = st.hydra_draft_heads(to_dev(x["h"]), to_dev(x["E"]), heads, to_dev(x["root_tok"]), tree)
     for u, v in zip(a, b):
         np.testing.assert_array_equal(u.cpu().numpy(), v.cpu().numpy())
+
+
+def test_draft_layernorm_heads_vicuna7b_shape():
+    # the LayerNorm fusion head form at full size: d 4096, V 32000, inner width 1024, batch 1,
+    # the 64-node sparse tree (head 1 without W1b, heads 2-4 conditioned with W1b)
+    st = lib()
+    rng = np.random.default_rng(47)
+    d, V, hidden = 4096, 32000, 1024
+    n = lambda *shape, sc=0.02: wl.f32_to_bf16_bits(rng.standard_normal(shape, dtype=np.float32) * np.float32(sc))
+    parent, rank = wl.make_tree(("sparse", (8, 4, 2, 1), 64, 64))
+    x = {"h": n(1, d, sc=1.0), "E": n(V, d), "root_tok": rng.integers(0, V, size=1).astype(np.int32)}
+    heads = [dict(form=1, cond=0, topk=8, W1=n(d, d), b1=n(d), gamma=n(d, sc=1.0), beta=n(d), W2=n(V, d))]
+    for tk in (4, 2, 1):
+        heads.append(dict(form=1, cond=1, topk=tk, W1=n(hidden, 2 * d), b1=n(hidden), W1b=n(d, hidden), b1b=n(d),
+                          gamma=n(d, sc=1.0), beta=n(d), W2=n(V, d)))
+    tree = st.spec_tree_build(parent, rank)
+    dev_heads = [{k: (to_dev(v) if isinstance(v, np.ndarray) else v) for k, v in hd.items()} for hd in heads]
+    tok, logit, logprob = st.hydra_draft_heads(to_dev(x["h"]), to_dev(x["E"]), dev_heads, to_dev(x["root_tok"]), tree)
+    to = oracle.tree_encode(parent, rank)
+    ref_fn = lambda teacher: oracle.hydra_draft_heads(x["h"], x["E"], heads, x["root_tok"], to, "bf16",
+                                                      teacher_tok=teacher, keep_logits=True)
+    near = _check(tok, logit, logprob, ref_fn, parent, "bf16", x["root_tok"])
+    print(f"layernorm heads at full size: {near} near ties")
