@@ -41,6 +41,10 @@ constexpr int kARows = 128;        // query rows per CTA (MMA M)
 constexpr int kAKeys = 128;        // keys per tile
 constexpr int kAD = 128;           // head dim
 constexpr int kAStages = 3;
+#ifndef SPEC_ATTN_PREFETCH
+#define SPEC_ATTN_PREFETCH 2
+#endif
+constexpr int kAPrefetch = SPEC_ATTN_PREFETCH;   // contiguous prefix tiles prefetched into L2 ahead of their load
 constexpr int kAThreads = 320;
 constexpr int kQBytes = 2 * kARows * 128;         // two 64-column halves of 128 rows
 constexpr int kKVHalf = kAKeys * 128;             // one 64-column half of a 128-key tile
@@ -179,6 +183,16 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                     tma_load_2d(st + kKVHalf, tk, &kv_full[s], 64, row);
                     tma_load_2d(st + 2 * kKVHalf, tv, &kv_full[s], 0, row);
                     tma_load_2d(st + 3 * kKVHalf, tv, &kv_full[s], 64, row);
+                    // the prefix tile kAPrefetch tiles ahead heads for L2 now: the ring's lead
+                    // (its stages free up only as PV finishes) is shorter than a load's latency
+                    const int jp = j + kAPrefetch;
+                    if (kAPrefetch > 0 && jp < n_pt) {
+                        const int rp = kvc_row0 + jp * kAKeys;
+                        tma_prefetch_2d(&tmKc, 0, rp);
+                        tma_prefetch_2d(&tmKc, 64, rp);
+                        tma_prefetch_2d(&tmVc, 0, rp);
+                        tma_prefetch_2d(&tmVc, 64, rp);
+                    }
                 }
                 issued = j + 1;
             }
