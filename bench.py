@@ -194,6 +194,8 @@ def algorithmic_bytes(name, ctx):
     heads = [k for k in range(len(w.cond)) if rows[k] > 0]
     if name.startswith("draft_proj"):
         return sum(V * d * s + rows[k] * d * s for k in heads) / len(heads)
+    if name == "draft_fold_h":   # W1[:, :d] once, h_b in, a (fp32) or z out, per sequence
+        return d * d * s + w.B * d * (s + 4)
     if name.startswith("draft_mlp"):
         return sum(d * 2 * d * s + d * s + rows[k] * 2 * d * s + rows[k] * d * s for k in heads) / len(heads)
     if name.startswith("attn_") and name != "attn_combine":
@@ -259,6 +261,8 @@ def run_ours(args):
     W1 = [dev_t(a) for a in dx["W1"]]
     b1 = [dev_t(a) for a in dx["b1"]]
     W2 = [dev_t(a) for a in dx["W2"]]
+    # weight-load-time preparation (outside every timed region): the folded embedding tables
+    tabs = None if args.no_fold else [st.hydra_fold_embedding(W1[k], E) if c == 1 else None for k, c in enumerate(w.cond)]
     root_tok = dev_t(dx["root_tok"])
     q, kc, vc = dev_t(ax["q"]), dev_t(ax["k_cache"]), dev_t(ax["v_cache"])
     plen, kt, vt = dev_t(ax["prefix_len"]), dev_t(ax["k_tree"]), dev_t(ax["v_tree"])
@@ -280,7 +284,7 @@ def run_ours(args):
 
     def draft():
         st.hydra_draft(h, E, W1, b1, W2, cond, topk, root_tok, tree, node_tok=node_tok, node_logit=node_logit,
-                       node_logprob=node_logprob, ws=ws_d)
+                       node_logprob=node_logprob, ws=ws_d, folded=tabs)
 
     # plant the target logits on the draft's own tokens (the target model itself is out of scope)
     draft()
@@ -405,7 +409,7 @@ def run_ours(args):
 
         def step_e2e():
             st.hydra_draft(h_e, E, W1, b1, W2, cond, topk, root_e, tree, node_tok=tok_e, node_logit=node_logit,
-                           node_logprob=node_logprob, ws=ws_d)
+                           node_logprob=node_logprob, ws=ws_d, folded=tabs)
             st.tree_attention(q_e, kc, vc, plen_e, kt_e, vt_e, tree, out=out, lse=lse, ws=ws_a)
             st.tree_accept(0, lp_e, None, tok_e, tree, accept_len=alen_e, accept_path=apath_e, next_token=nxt_e,
                            margin=mg, ws=ws_c)
@@ -441,6 +445,8 @@ def run_ours(args):
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded; random-init head weights, N(0,1) KV)",
         "config": config_of(w, T),
+        "draft_first_layer": ("whole W1 streamed per step" if args.no_fold else
+                              "folded: W1[:, :d] streamed per step, W1[:, d:] E tabulated once at weight load (fp32)"),
         "tree_node_tokens_per_s": value * B * T,
         "accepted_tokens_per_s": value * B * (accepted + 1),
         "phases_ms": phase_ms,
@@ -602,8 +608,9 @@ def run_component(args):
         nl = torch.empty(w.B, T, dtype=torch.float32, device=dev)
         nlp = torch.empty(w.B, T, dtype=torch.float32, device=dev)
         ws = torch.empty(st.hydra_draft_workspace_size(tree, w.B, w.d, w.V, cond, topk, 1), dtype=torch.uint8, device=dev)
+        tabs = None if args.no_fold else [st.hydra_fold_embedding(W1[k], E) if c == 1 else None for k, c in enumerate(cond)]
         call = lambda: st.hydra_draft(h, E, W1, b1, W2, cond, topk, root, tree, node_tok=nt, node_logit=nl,
-                                      node_logprob=nlp, ws=ws)
+                                      node_logprob=nlp, ws=ws, folded=tabs)
         abytes, d, V = 0.0, w.d, w.V
         for k in range(len(cond)):
             n_int = tree.struct.n_internal_at_depth[k]
@@ -611,8 +618,13 @@ def run_component(args):
                 continue
             rows = w.B * n_int if cond[k] else w.B
             d_in = d * (2 if cond[k] else 1)
-            abytes += (d * d_in + d + V * d) * s + rows * (d_in + d) * s
-            flops += 2.0 * rows * (d_in * d + d * V)
+            if tabs is not None and cond[k] == 1:
+                # folded: the h_b half of W1 per sequence, a table row (fp32) per head-input row
+                abytes += (d * d + d + V * d) * s + w.B * d * (s + 4) + rows * (d * 4 + 2 * d * s)
+                flops += 2.0 * (w.B * d * d + rows * d * V)
+            else:
+                abytes += (d * d_in + d + V * d) * s + rows * (d_in + d) * s
+                flops += 2.0 * rows * (d_in * d + d * V)
     elif part == "draft_ln":
         # the LayerNorm fusion head form at Vicuna-7B shape (d 4096, V 32000, inner width 1024):
         # head 1 Linear -> SiLU -> LayerNorm, heads 2-4 Linear -> SiLU -> Linear -> LayerNorm on [h || E[parent]]
@@ -729,6 +741,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fold", action="store_true",
+                    help="draft heads stream their whole first layer (no folded embedding tables)")
     ap.add_argument("--workload", choices=["step"] + sorted(COMPONENTS), default="step",
                     help="step (default): the headline verification step; otherwise one entry point on one workload")
     args = ap.parse_args()

@@ -149,6 +149,44 @@ spec_status hydra_draft(const void* h, const void* emb, int32_t K,
                         int32_t* node_tok, float* node_logit, float* node_logprob,
                         void* ws, size_t ws_bytes, spec_stream_t s);
 
+/* Bytes of one folded embedding table (V * d fp32), 0 on invalid shapes. */
+size_t hydra_fold_table_bytes(int32_t d, int32_t V);
+
+/*
+ * Fold the embedding half of a cond-1 head's first layer into a per-token
+ * table, once per set of weights (not per step).  Hydra Guide, "1. Embedding
+ * Conditioning Mechanics": the head reads u_in = [h_b || emb[tok]], so
+ *     W1 u_in = W1[:, 0:d] h_b + tab[tok],   tab[v, m] = sum_j W1[m, d + j] emb[v, j]
+ * and the second term depends on the token alone.
+ *
+ *   W1   device [d, 2d] in dt (the head's first layer, out x in)
+ *   emb  device [V, d] in dt
+ *   tab  device fp32 [V, d] out (hydra_fold_table_bytes bytes, caller-owned)
+ * fp32 accumulation in a fixed order per element.  All pointers 16-byte
+ * aligned (SPEC_EALIGN); SPEC_EINVAL on NULL or out-of-range shapes.  Launched
+ * on s, asynchronous.
+ */
+spec_status hydra_fold_embedding(const void* W1, const void* emb, int32_t d, int32_t V, spec_dtype dt,
+                                 float* tab, spec_stream_t s);
+
+/*
+ * hydra_draft with folded first layers: tab is a host array [K] (or NULL) of
+ * device tables from hydra_fold_embedding(W1[k], emb, ...).  On the bf16
+ * tensor-core path a cond-1 head with a table streams only W1[k][:, 0:d] per
+ * step: a[b] = W1[k][:, 0:d] h_b, and the kernel that picks a node's token
+ * writes that node's head input z = h_b + SiLU(a[b] + tab[k][tok] + b1[k])
+ * itself.  NULL entries, other heads and the fp32 path use the whole W1[k].
+ * The results equal hydra_draft's up to fp32 rounding order.  Workspace:
+ * hydra_draft_workspace_size.  Tables must be 16-byte aligned (SPEC_EALIGN);
+ * everything else as hydra_draft.
+ */
+spec_status hydra_draft_folded(const void* h, const void* emb, int32_t K,
+                               const void* const* W1, const void* const* b1, const void* const* W2,
+                               const float* const* tab, const int32_t* cond, const int32_t* topk,
+                               const int32_t* root_tok, const spec_tree* tree, int32_t B, int32_t d,
+                               int32_t V, spec_dtype dt, int32_t* node_tok, float* node_logit,
+                               float* node_logprob, void* ws, size_t ws_bytes, spec_stream_t s);
+
 /*
  * One draft head for hydra_draft_heads.  form 0 is hydra_draft's head; form 1
  * is the head form that the Hydra Guide prints as code (fusion MLP

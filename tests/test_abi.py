@@ -189,6 +189,36 @@ def test_entry_points_reject_before_launch(lib):
     assert st == 1
 
 
+def test_fold_entries_reject_before_launch(lib):
+    # every call here fails a host check, so nothing is queued (no device access)
+    import spec_workloads as wl
+    L = lib._lib
+    vp = ctypes.c_void_p
+    assert L.hydra_fold_table_bytes(4096, 32000) == 4096 * 32000 * 4
+    assert L.hydra_fold_table_bytes(4092, 32000) == 0     # d % 8
+    assert L.hydra_fold_table_bytes(256, 1) == 0          # V
+    assert L.hydra_fold_embedding(vp(FAKE), vp(FAKE), 250, 1000, 0, vp(FAKE), None) == 1
+    assert L.hydra_fold_embedding(vp(FAKE), vp(FAKE), 256, 1, 0, vp(FAKE), None) == 1
+    assert L.hydra_fold_embedding(vp(0), vp(FAKE), 256, 1000, 0, vp(FAKE), None) == 1
+    assert L.hydra_fold_embedding(vp(FAKE), vp(FAKE), 256, 1000, 7, vp(FAKE), None) == 1   # dtype
+    assert L.hydra_fold_embedding(vp(FAKE), vp(FAKE), 256, 1000, 0, vp(FAKE + 4), None) == 3
+    assert L.hydra_fold_embedding(vp(FAKE + 8), vp(FAKE), 256, 1000, 1, vp(FAKE), None) == 3
+    # hydra_draft_folded: a misaligned table is refused after the other checks pass
+    parent, _ = wl.cartesian_tree((2, 3))
+    t = _fake_tree(lib, [int(x) for x in parent])
+    W = (ctypes.c_void_p * 2)(FAKE, FAKE)
+    tab = (ctypes.c_void_p * 2)(0, FAKE + 4)
+    c = (ctypes.c_int32 * 2)(1, 1)
+    k = (ctypes.c_int32 * 2)(2, 3)
+    st = L.hydra_draft_folded(vp(FAKE), vp(FAKE), 2, W, None, W, tab, c, k, vp(FAKE), ctypes.byref(t), 1, 256, 1000, 1,
+                              vp(FAKE), vp(FAKE), vp(0), vp(FAKE), 1 << 30, None)
+    assert st == 3 and "folded table 1" in lib.spec_last_error()
+    W0 = (ctypes.c_void_p * 2)(FAKE, 0)
+    st = L.hydra_draft_folded(vp(FAKE), vp(FAKE), 2, W0, None, W, tab, c, k, vp(FAKE), ctypes.byref(t), 1, 256, 1000, 1,
+                              vp(FAKE), vp(FAKE), vp(0), vp(FAKE), 1 << 30, None)
+    assert st == 1
+
+
 def test_kv_commit_rejects_before_launch(lib):
     # every call here fails a host check, so nothing is queued (no device access)
     import spec_workloads as wl

@@ -249,3 +249,91 @@ def test_draft_layernorm_heads_vicuna7b_shape():
                                                       teacher_tok=teacher, keep_logits=True)
     near = _check(tok, logit, logprob, ref_fn, parent, "bf16", x["root_tok"])
     print(f"layernorm heads at full size: {near} near ties")
+
+
+# ---------------------------------------------------------------- folded first layers (hydra_draft_folded)
+
+def _bf16_to_f64(a):
+    a = np.asarray(a)
+    return (a.astype(np.uint32) << 16).view(np.float32).astype(np.float64) if a.dtype == np.uint16 else a.astype(np.float64)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("d,V", [(64, 500), (256, 4099), (4096, 1000)])
+def test_fold_embedding_is_the_embedding_half_product(dtype, d, V):
+    # tab[v, m] = sum_j W1[m, d + j] E[v, j]: the plain product in fp64 bounds the fp32 table by
+    # the accumulation error, d * 2^-24 relative to sum_j |W1[m, d + j] E[v, j]|
+    st = lib()
+    rng = np.random.default_rng(30 + d)
+    enc = (lambda a: wl.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    W1 = enc(rng.standard_normal((d, 2 * d), dtype=np.float32) * np.float32(0.05))
+    E = enc(rng.standard_normal((V, d), dtype=np.float32))
+    tab = st.hydra_fold_embedding(to_dev(W1), to_dev(E)).cpu().numpy().astype(np.float64)
+    W1e, Ef = _bf16_to_f64(W1)[:, d:], _bf16_to_f64(E)
+    ref = Ef @ W1e.T
+    bound = d * 2.0 ** -24 * (np.abs(Ef) @ np.abs(W1e).T) + 1e-30
+    assert np.all(np.abs(tab - ref) <= bound), np.max(np.abs(tab - ref) / bound)
+
+
+def _run_folded(st, x, tree, fold_mask):
+    W1 = [to_dev(a) for a in x["W1"]]
+    E = to_dev(x["E"])
+    tabs = [st.hydra_fold_embedding(W1[k], E) if (fold_mask[k] and x["cond"][k] == 1) else None
+            for k in range(len(W1))]
+    return st.hydra_draft(to_dev(x["h"]), E, W1, None if x["b1"] is None else [to_dev(a) for a in x["b1"]],
+                          [to_dev(a) for a in x["W2"]], list(x["cond"]), list(x["topk"]), to_dev(x["root_tok"]), tree,
+                          folded=tabs)
+
+
+def _compare_folded(st, x, parent, rank, dtype, fold_mask=None):
+    tree = st.spec_tree_build(parent, rank)
+    K = len(x["W1"])
+    tok, logit, logprob = _run_folded(st, x, tree, fold_mask or [True] * K)
+    to = oracle.tree_encode(parent, rank)
+    ref_fn = lambda teacher: oracle.hydra_draft(x["h"], x["E"], x["W1"], x["b1"], x["W2"], x["cond"], x["topk"],
+                                                x["root_tok"], to, dtype, teacher_tok=teacher, keep_logits=True)
+    return _check(tok, logit, logprob, ref_fn, parent, dtype, x["root_tok"])
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("shape", [
+    # d, V, B, branching, cond, topk, which heads get a table
+    (64, 500, 2, (3, 2, 2), (1, 1, 1), (3, 2, 2), (1, 1, 1)),
+    (128, 4099, 3, (4, 1), (1, 1), (5, 1), (1, 1)),
+    (64, 700, 2, (2, 2, 2, 2), (1, 2, 1, 0), (2, 2, 2, 2), (1, 1, 1, 1)),   # tables only act on cond-1 heads
+    (256, 3000, 2, (3, 2, 2), (1, 1, 1), (3, 2, 2), (0, 1, 0)),             # folded and whole layers mixed
+    (256, 3000, 1, (3, 2, 2), (1, 1, 1), (3, 2, 2), (1, 0, 1)),
+])
+def test_draft_folded_matches_oracle(dtype, shape):
+    st = lib()
+    d, V, B, branching, cond, topk, mask = shape
+    if dtype == "f32" and d > 128:
+        pytest.skip("bf16 tensor-core shape")
+    w = wl.Workload("t", dtype, B=B, seed=21, tree=("cartesian", branching), d=d, V=V, cond=cond, topk=topk)
+    parent, rank = wl.make_tree(w.tree)
+    x = wl.draft_inputs(w)
+    rng = np.random.default_rng(9)
+    enc = (lambda a: wl.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    x["W2"] = [enc(rng.standard_normal(np.shape(a), dtype=np.float32) * np.float32(0.25)) for a in x["W2"]]
+    x["E"] = enc(rng.standard_normal(np.shape(x["E"]), dtype=np.float32))   # embeddings that move the heads
+    _compare_folded(st, x, parent, rank, dtype, list(mask))
+
+
+def test_draft_folded_vicuna7b_workload():
+    """The Vicuna-7B draft (B=1, d=4096, V=32000, 4 cond-1 heads, 64-node tree) with every head folded."""
+    st = lib()
+    w = wl.Workload("vicuna7b-draft", "bf16", B=1, seed=7, tree=wl.WORKLOADS[2].tree, d=4096, V=32000,
+                    cond=(1, 1, 1, 1), topk=(8, 4, 2, 1))
+    parent, rank = wl.make_tree(w.tree)
+    near = _compare_folded(st, wl.draft_inputs(w), parent, rank, "bf16")
+    print(f"vicuna7b folded: {near} near ties")
+
+
+def test_draft_folded_hydra_heads_workload():
+    """The Hydra-heads workload (B=4) folded: several sequences share each a[b] pass."""
+    st = lib()
+    w = wl.WORKLOADS[3]
+    parent, rank = wl.make_tree(w.tree)
+    near = _compare_folded(st, wl.draft_inputs(w), parent, rank, "bf16")
+    print(f"hydra heads folded: {near} near ties")
+

@@ -66,6 +66,10 @@ def _load():
         "spec_tree_build": (i32, [vp, vp, i32, vp, sz, tp, vp]),
         "hydra_draft_workspace_size": (sz, [tp, i32, i32, i32, i32, vp, vp, i32]),
         "hydra_draft": (i32, [vp, vp, i32, vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, vp, vp, vp, vp, sz, vp]),
+        "hydra_draft_folded": (i32, [vp, vp, i32, vp, vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, vp, vp, vp, vp, sz,
+                                     vp]),
+        "hydra_fold_table_bytes": (sz, [i32, i32]),
+        "hydra_fold_embedding": (i32, [vp, vp, i32, i32, i32, vp, vp]),
         "hydra_draft_heads_workspace_size": (sz, [tp, i32, i32, i32, i32, ctypes.POINTER(spec_head), i32]),
         "hydra_draft_heads": (i32, [vp, vp, i32, ctypes.POINTER(spec_head), vp, tp, i32, i32, i32, f32, i32, vp, vp,
                                     vp, vp, sz, vp]),
@@ -198,9 +202,33 @@ def hydra_draft_workspace_size(tree, B, d, V, cond, topk, dtype):
     return int(n)
 
 
+def hydra_fold_embedding(W1, emb, out=None, stream=None):
+    """The folded embedding table of a cond-1 head: fp32 [V, d], tab[v] = W1[:, d:] @ emb[v]."""
+    _need(emb, "emb", ndim=2)
+    dev = emb.device
+    V, d = emb.shape
+    _need(W1, "W1", dtype=emb.dtype, ndim=2, device=dev)
+    if tuple(W1.shape) != (d, 2 * d):
+        raise ValueError("W1 must be [d, 2d]")
+    if _lib.hydra_fold_table_bytes(d, V) == 0:
+        raise SpecError("hydra_fold_table_bytes", 1, _lib.spec_last_error().decode())
+    if out is None:
+        out = torch.empty(V, d, dtype=torch.float32, device=dev)
+    _need(out, "out", dtype=torch.float32, ndim=2, device=dev)
+    if tuple(out.shape) != (V, d):
+        raise ValueError("out must be [V, d]")
+    with torch.cuda.device(dev):
+        _check("hydra_fold_embedding", _lib.hydra_fold_embedding(_ptr(W1), _ptr(emb), d, V, _dtype_code(emb), _ptr(out),
+                                                                 _stream(stream)))
+    return out
+
+
 def hydra_draft(h, emb, W1, b1, W2, cond, topk, root_tok, tree, node_tok=None, node_logit=None,
-                node_logprob=None, want_logprob=True, ws=None, stream=None):
-    """Fill the candidate tree: returns (node_tok [B,T] int32, node_logit [B,T], node_logprob [B,T] or None)."""
+                node_logprob=None, want_logprob=True, ws=None, stream=None, folded=None):
+    """Fill the candidate tree: returns (node_tok [B,T] int32, node_logit [B,T], node_logprob [B,T] or None).
+
+    folded: optional list (one entry per head, None allowed) of hydra_fold_embedding tables; cond-1
+    heads with a table stream only the h_b half of W1 per call (hydra_draft_folded)."""
     _need(h, "h", ndim=2)
     dev = h.device
     dt = _dtype_code(h)
@@ -241,11 +269,30 @@ def hydra_draft(h, emb, W1, b1, W2, cond, topk, root_tok, tree, node_tok=None, n
     if nws == 0:
         raise SpecError("hydra_draft_workspace_size", 1, _lib.spec_last_error().decode())
     ws = _workspace(nws, dev, ws)
+    if folded is not None:
+        if len(folded) != K:
+            raise ValueError("folded needs one entry per head")
+        for k in range(K):
+            if folded[k] is not None:
+                _need(folded[k], f"folded[{k}]", dtype=torch.float32, ndim=2, device=dev)
+                if tuple(folded[k].shape) != (V, d):
+                    raise ValueError(f"folded[{k}] must be [V, d]")
+        tabp = (ctypes.c_void_p * K)(*[(folded[k].data_ptr() if folded[k] is not None else 0) for k in range(K)])
+        with torch.cuda.device(dev):
+            _check("hydra_draft_folded", _lib.hydra_draft_folded(
+                _ptr(h), _ptr(emb), K, w1p, b1p, w2p, tabp, c, kk, _ptr(root_tok), tree.ref(), B, d, V, dt,
+                _ptr(node_tok), _ptr(node_logit), _ptr(node_logprob), _ptr(ws), ws.numel(), _stream(stream)))
+        return node_tok, node_logit, node_logprob
     with torch.cuda.device(dev):
         _check("hydra_draft", _lib.hydra_draft(_ptr(h), _ptr(emb), K, w1p, b1p, w2p, c, kk, _ptr(root_tok), tree.ref(),
                                                B, d, V, dt, _ptr(node_tok), _ptr(node_logit), _ptr(node_logprob),
                                                _ptr(ws), ws.numel(), _stream(stream)))
     return node_tok, node_logit, node_logprob
+
+
+def hydra_draft_folded(h, emb, W1, b1, W2, tab, cond, topk, root_tok, tree, **kw):
+    """hydra_draft with the folded tables tab (one per head, None allowed) from hydra_fold_embedding."""
+    return hydra_draft(h, emb, W1, b1, W2, cond, topk, root_tok, tree, folded=tab, **kw)
 
 
 def hydra_draft_heads(h, emb, heads, root_tok, tree, ln_eps=1e-5, node_tok=None, node_logit=None, node_logprob=None,

@@ -30,13 +30,13 @@ namespace draft {
 
 // ---------------------------------------------------------------- CUDA-core GEMM (fp32 path, small shapes)
 //
-// acc[n][m] = sum_k W[m][k] * X[n][k]; W [M, K], X [N, K] row-major.
+// acc[n][m] = sum_k W[m][k] * X[n][k]; W [M, K] (row stride ldw), X [N, K] (row stride ldx).
 // 64 (m) x 32 (n) tile per CTA, 256 threads, 4 x 2 outputs per thread.
 
 constexpr int GBM = 64, GBN = 32, GBK = 32;
 
 template <typename T, int EPI>
-__global__ void __launch_bounds__(256) k_gemm_fma(const T* __restrict__ W, const T* __restrict__ X, int M, int N, int K,
+__global__ void __launch_bounds__(256) k_gemm_fma(const T* __restrict__ W, int ldw, const T* __restrict__ X, int M, int N, int K,
                                                    int ldx, const T* __restrict__ bias, const T* __restrict__ h,
                                                    int cond, int n_int, T* __restrict__ z_out, float* __restrict__ logits,
                                                    int act, float* __restrict__ zf) {
@@ -52,7 +52,7 @@ __global__ void __launch_bounds__(256) k_gemm_fma(const T* __restrict__ W, const
             const int idx = t + i * 256;
             const int ml = idx / GBK, kl = idx % GBK;
             const int m = m0 + ml, k = k0 + kl;
-            Ws[kl][ml] = (m < M && k < K) ? to_f32(W[static_cast<size_t>(m) * K + k]) : 0.f;
+            Ws[kl][ml] = (m < M && k < K) ? to_f32(W[static_cast<size_t>(m) * ldw + k]) : 0.f;
         }
 #pragma unroll
         for (int i = 0; i < (GBN * GBK) / 256; ++i) {
@@ -265,6 +265,102 @@ __global__ void __launch_bounds__(256) k_topk_slices(const float* __restrict__ l
 }
 
 
+// ---------------------------------------------------------------- folded first layer (conditioned heads)
+//
+// Hydra Guide, "1. Embedding Conditioning Mechanics": a conditioned head's first
+// layer reads u = [h_b || E[tok]], so W1 u = W1[:, :d] h_b + W1[:, d:] E[tok].  The
+// second term depends on the token alone; hydra_fold_embedding tabulates it once
+// per set of weights (tab[v, m] = W1[m, d:] . E[v] in fp32) and a step then streams
+// only the h_b half of W1: k_fold_h forms a[b] = W1[:, :d] h_b, and the select that
+// picks a child's token writes the child's head input z = h_b + SiLU(a[b] + tab[tok]
+// + b1) itself, so the head's MLP leaves the chain between two projections.
+
+// a[b, m] = W1[m, 0:d] . h[b] in fp32, one warp per weight row (16-byte loads, lanes
+// interleaved), up to kFoldB sequences per pass over the row.  With z set (the first
+// head, conditioned on the root token): z[b, m] = h[b, m] + SiLU(a[b, m] + tab[root_b, m]
+// + b1[m]) in bf16 instead.  A programmatic dependent that reads nothing the kernels
+// before it write; it waits for them only before exiting, so a later kernel's wait
+// still covers everything queued ahead of this one.
+constexpr int kFoldB = 8;
+constexpr int kFoldWarps = 8;
+constexpr int kFoldBatch = 8;   // 16-byte weight chunks per lane in flight
+
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+__device__ __forceinline__ float dot8_bf16(const uint4 w, const uint4 x) {
+    const uint32_t wa[4] = {w.x, w.y, w.z, w.w}, xa[4] = {x.x, x.y, x.z, x.w};
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 a = bf2_to_f2(wa[i]), b = bf2_to_f2(xa[i]);
+        acc = fmaf(a.x, b.x, acc);
+        acc = fmaf(a.y, b.y, acc);
+    }
+    return acc;
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+__global__ void __launch_bounds__(kFoldWarps * 32) k_fold_h(const __nv_bfloat16* __restrict__ W1, int ldw,
+                                                            const __nv_bfloat16* __restrict__ h, int B, int d,
+                                                            float* __restrict__ a_out, const float* __restrict__ tab,
+                                                            const __nv_bfloat16* __restrict__ b1,
+                                                            const int32_t* __restrict__ root_tok, int V,
+                                                            __nv_bfloat16* __restrict__ z) {
+    griddep_launch();
+    const int lane = threadIdx.x & 31;
+    const int nchunk = d / 8;   // 16-byte chunks in the h_b half of a weight row
+    const int nw = gridDim.x * kFoldWarps;
+    for (int m = blockIdx.x * kFoldWarps + (threadIdx.x >> 5); m < d; m += nw) {
+        const uint4* wr = reinterpret_cast<const uint4*>(W1 + static_cast<size_t>(m) * ldw);
+        for (int b0 = 0; b0 < B; b0 += kFoldB) {
+            float acc[kFoldB];
+#pragma unroll
+            for (int bb = 0; bb < kFoldB; ++bb) acc[bb] = 0.f;
+            for (int c0 = 0; c0 < nchunk; c0 += 32 * kFoldBatch) {
+                uint4 wv[kFoldBatch];
+#pragma unroll
+                for (int u = 0; u < kFoldBatch; ++u) {
+                    const int c = c0 + u * 32 + lane;
+                    wv[u] = c < nchunk ? __ldcs(wr + c) : make_uint4(0u, 0u, 0u, 0u);
+                }
+#pragma unroll
+                for (int bb = 0; bb < kFoldB; ++bb) {
+                    if (b0 + bb >= B) break;
+                    const uint4* hr = reinterpret_cast<const uint4*>(h + static_cast<size_t>(b0 + bb) * d);
+#pragma unroll
+                    for (int u = 0; u < kFoldBatch; ++u) {
+                        const int c = c0 + u * 32 + lane;
+                        if (c < nchunk) acc[bb] += dot8_bf16(wv[u], __ldg(hr + c));
+                    }
+                }
+            }
+#pragma unroll
+            for (int bb = 0; bb < kFoldB; ++bb)
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) acc[bb] += __shfl_xor_sync(0xffffffffu, acc[bb], o);
+            if (lane == 0) {
+#pragma unroll
+                for (int bb = 0; bb < kFoldB; ++bb) {
+                    const int b = b0 + bb;
+                    if (b >= B) break;
+                    if (!z) {
+                        a_out[static_cast<size_t>(b) * d + m] = acc[bb];
+                    } else {
+                        const int tok = min(max(root_tok[b], 0), V - 1);   // k_init_root flags a bad token
+                        const float x = acc[bb] + tab[static_cast<size_t>(tok) * d + m] + (b1 ? __bfloat162float(b1[m]) : 0.f);
+                        z[static_cast<size_t>(b) * d + m] =
+                            __float2bfloat16_rn(__bfloat162float(h[static_cast<size_t>(b) * d + m]) + silu(x));
+                    }
+                }
+            }
+        }
+    }
+    griddep_wait();
+}
+
 // ---------------------------------------------------------------- select: merge slices, fill children
 
 // Copy the next depth's input row [h_b || E[tok]] (2d elements) with the whole CTA.
@@ -305,7 +401,9 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                                                 float* __restrict__ node_logprob, void* ws, int next_n_int,
                                                 int next_cond, int next_ld, int kdepth,
                                                 const T* __restrict__ h, const T* __restrict__ emb, int d,
-                                                T* __restrict__ xin, int cpr) {
+                                                T* __restrict__ xin, int cpr, const float* __restrict__ ftab,
+                                                const float* __restrict__ fa, const T* __restrict__ fb1,
+                                                T* __restrict__ zf) {
     // cpr CTAs per row (one per child of a single parent that needs next-depth rows): each
     // computes the row's top-k (the same result) and copies its own child's rows, so the
     // embedding rows pass through cpr SMs instead of one; CTA 0 of the row writes the
@@ -466,6 +564,32 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
             __syncthreads();
         }
         if (!rows) continue;
+        if (ftab) {
+            // the next head is folded (cond 1): its input row is z = h_b + SiLU(a[b] +
+            // tab[tok] + b1) itself, 8 elements per thread and chunk
+            const float* ab = fa + static_cast<size_t>(b) * d;
+            const T* hb = h + static_cast<size_t>(b) * d;
+            for (int a = 0; a < nc; ++a) {
+                if (c_row[a] < 0 || (cpr > 1 && a != ci)) continue;
+                const float* tr = ftab + static_cast<size_t>(topi[c_rank[a]]) * d;
+                T* zr = zf + (row0 + c_row[a]) * d;
+                for (int c = tid; c < d / 8; c += blockDim.x) {
+                    const float4 t0 = reinterpret_cast<const float4*>(tr)[2 * c];
+                    const float4 t1 = reinterpret_cast<const float4*>(tr)[2 * c + 1];
+                    const float4 a0 = reinterpret_cast<const float4*>(ab)[2 * c];
+                    const float4 a1 = reinterpret_cast<const float4*>(ab)[2 * c + 1];
+                    const float x[8] = {t0.x + a0.x, t0.y + a0.y, t0.z + a0.z, t0.w + a0.w,
+                                        t1.x + a1.x, t1.y + a1.y, t1.z + a1.z, t1.w + a1.w};
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int m = 8 * c + e;
+                        const float xb = x[e] + (fb1 ? to_f32(fb1[m]) : 0.f);
+                        zr[m] = from_f32<T>(to_f32(hb[m]) + xb / (1.0f + expf(-xb)));
+                    }
+                }
+            }
+            continue;
+        }
         if (anc) {
             // all-ancestor rows [h_b || E[tok(a_1)] || ... || E[tok(a_k)] || E[tok(c)]]: the
             // blocks of u's path (depths 1..k, shared by all children) then each child's own
@@ -572,7 +696,7 @@ struct Plan {
     int kmax;            // list length of the top-k partials (8 or 16)
     int nslices;         // vocabulary slices per row
     int slice_fma;       // fp32 path: tokens per slice
-    size_t off_xin, off_z, off_scratch, off_pc, off_pl, off_hid, off_y, total;
+    size_t off_xin, off_z, off_scratch, off_pc, off_pl, off_hid, off_y, off_fa, total;
     size_t xin_at[SPEC_MAX_DEPTH + 1];   // element offset of depth k's input rows (conditioned heads)
     HRows hr;
     bool tc;             // bf16 tensor-core path
@@ -589,13 +713,13 @@ inline int d_in_of(int cond, int k, int d) { return d * (cond == 1 ? 2 : cond ==
 // Lay out every conditioned depth's input rows (B x n_int rows of d_in elements
 // each) one after the other; fills xin_at and the HRows table (depths >= 1).
 // Returns the total element count (at least 1).
-size_t xin_elems(Plan& p, const spec_tree* t, int K, const int32_t* cond, int B, int d) {
+size_t xin_elems(Plan& p, const spec_tree* t, int K, const int32_t* cond, int B, int d, const bool* fold = nullptr) {
     size_t elems = 0;
     p.hr = HRows{};
     for (int k = 0; k < K && k <= SPEC_MAX_DEPTH; ++k) {
         p.xin_at[k] = 0;
         const int n_int = t->n_internal_at_depth[k];
-        if (!cond[k] || n_int == 0) continue;
+        if (!cond[k] || n_int == 0 || (fold && fold[k])) continue;   // folded heads read z rows
         const int ld = d_in_of(cond[k], k, d);
         p.xin_at[k] = elems;
         if (k >= 1 && p.hr.n < SPEC_MAX_DEPTH) {
@@ -623,6 +747,7 @@ struct Heads {
     const void* gamma[SPEC_MAX_DEPTH] = {};
     const void* beta[SPEC_MAX_DEPTH] = {};
     const void* W2[SPEC_MAX_DEPTH] = {};
+    const float* tab[SPEC_MAX_DEPTH] = {};   // folded embedding tables (cond-1 form-0 heads; NULL: none)
     int hid_width = 0;   // widest form-1 inner layer that feeds W1b (0: none)
     bool ln = false;     // some head has form 1
 };
@@ -683,6 +808,11 @@ spec_status check_heads(const Heads& hs, int d) {
     return SPEC_OK;
 }
 
+// Head k runs folded: the bf16 tensor-core path, a cond-1 form-0 head with a table.
+inline bool folded(const Heads* hs, bool tc, int k) {
+    return tc && hs && hs->tab[k] && hs->cond[k] == 1 && hs->form[k] == 0;
+}
+
 Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* cond, const int32_t* topk, spec_dtype dt,
                const Heads* hs = nullptr) {
     Plan p{};
@@ -700,7 +830,10 @@ Plan make_plan(const spec_tree* t, int B, int d, int V, int K, const int32_t* co
     if (p.tc) {
         p.tcp = tc::draft_tc_plan(p.max_rows, d, V);
         p.nslices = p.tcp.nslices;
-        p.off_xin = take(es * xin_elems(p, t, K, cond, B, d));
+        bool fold[SPEC_MAX_DEPTH] = {};
+        for (int k = 0; k < K; ++k) fold[k] = folded(hs, true, k);
+        p.off_xin = take(es * xin_elems(p, t, K, cond, B, d, fold));
+        p.off_fa = take(sizeof(float) * static_cast<size_t>(K) * B * d);   // a[k][b] of folded heads
         p.off_z = take(es * static_cast<size_t>(p.tcp.rows_pad) * d);
         p.off_scratch = 0;   // unused: the MLP reduces its split-K partials on chip
         p.off_pc = take(sizeof(Cand) * static_cast<size_t>(p.max_rows) * p.nslices * p.kmax);
@@ -750,7 +883,8 @@ template <int KMAX, typename T>
 spec_status launch_select(bool pdl, const Plan& p, const spec_tree* t, int R, int k, int topk, int cond, int n_int,
                           int int_off, int next_n_int, int V, const Cand* pc, const float2* pl, int32_t* node_tok,
                           float* node_logit, float* node_logprob, void* ws, const T* h, const T* emb, int d, T* xin,
-                          int next_cond, int next_ld, cudaStream_t s) {
+                          int next_cond, int next_ld, const float* ftab, const float* fa, const T* fb1, T* zf,
+                          cudaStream_t s) {
     // one CTA per child where each CTA has a single parent node and children get next-depth rows
     const bool single_parent = cond != 0 || n_int == 1;
     const int cpr = (next_n_int > 0 && single_parent && k + 1 <= t->max_depth)
@@ -758,7 +892,7 @@ spec_status launch_select(bool pdl, const Plan& p, const spec_tree* t, int R, in
     SPEC_CUDA_TRY(launch_ex("draft_select", k_select<KMAX, T>, dim3(R * cpr), dim3(256), 0, s, pdl, pc, pl, p.nslices, topk,
                             cond, n_int, int_off, t->internal, t->child_off, t->child_idx, t->rank, t->parent,
                             t->row_of, t->T, V, node_tok, node_logit, node_logprob, ws, next_n_int, next_cond, next_ld, k,
-                            h, emb, d, xin, cpr));
+                            h, emb, d, xin, cpr, ftab, fa, fb1, zf));
     return SPEC_OK;
 }
 
@@ -777,7 +911,10 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
     float2* pl = reinterpret_cast<float2*>(w + p.off_pl);
     T* hid = reinterpret_cast<T*>(w + p.off_hid);
     float* yln = reinterpret_cast<float*>(w + p.off_y);
-    const bool first_cond = t->n_internal_at_depth[0] > 0 && cond[0];
+    float* fa = reinterpret_cast<float*>(w + p.off_fa);
+    bool fold[SPEC_MAX_DEPTH + 1] = {};
+    for (int k = 0; k < K; ++k) fold[k] = folded(&hs, p.tc, k);
+    const bool first_cond = t->n_internal_at_depth[0] > 0 && cond[0] && !fold[0];
     SPEC_CUDA_TRY(reset_device_status(ws, s));
     SPEC_CUDA_TRY(launch("draft_init_root", k_init_root<T>, dim3(B, 1 + p.hr.per_seq), dim3(128), 0, s, root_tok, B,
                          t->T, V, node_tok, node_logit, node_logprob, ws, first_cond ? cond[0] : 0, h, emb, d,
@@ -816,7 +953,16 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
         if constexpr (std::is_same<T, __nv_bfloat16>::value) {
             if (p.tc) {
                 spec_status st;
-                if (!ln) {
+                const bool fnext = next_n_int > 0 && fold[k + 1];
+                const int fold_grid = std::min((d + kFoldWarps - 1) / kFoldWarps, 1024);
+                if (fold[k]) {
+                    // the first head's z from its folded layer (later heads' z come from the select)
+                    if (k == 0)
+                        SPEC_CUDA_TRY(launch_ex("draft_fold_h", k_fold_h, dim3(fold_grid), dim3(kFoldWarps * 32), 0, s, true,
+                                                W1k, 2 * d, h, B, d, static_cast<float*>(nullptr), hs.tab[0], b1k,
+                                                root_tok, V, z));
+                    st = tc::proj_tc(p.tcp, W2k, z, R, d, V, topk[k], p.kmax, pc, pl, ws, s);
+                } else if (!ln) {
                     st = tc::draft_head_tc(p.tcp, W1k, b1k, W2k, h, X, d_in, ldx, z, R, d, V, cond[k], n_int, topk[k],
                                            p.kmax, dep_k0, pc, pl, ws, s);
                 } else {
@@ -829,43 +975,57 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
                     if (st == SPEC_OK) st = tc::proj_tc(p.tcp, W2k, z, R, d, V, topk[k], p.kmax, pc, pl, ws, s);
                 }
                 if (st != SPEC_OK) return st;
+                // the next head's a = W1[:, :d] h_b streams behind this projection; the select then
+                // writes that head's z rows
+                float* fa_next = fa + static_cast<size_t>(k + 1) * B * d;
+                if (fnext)
+                    SPEC_CUDA_TRY(launch_ex("draft_fold_h", k_fold_h, dim3(fold_grid), dim3(kFoldWarps * 32), 0, s, true,
+                                            static_cast<const T*>(hs.W1[k + 1]), 2 * d, h, B, d, fa_next,
+                                            static_cast<const float*>(nullptr), static_cast<const T*>(nullptr),
+                                            static_cast<const int32_t*>(nullptr), V, static_cast<T*>(nullptr)));
+                const float* ftab = fnext ? hs.tab[k + 1] : nullptr;
+                const T* fb1 = fnext ? static_cast<const T*>(hs.b1[k + 1]) : nullptr;
                 st = p.kmax == 8 ? launch_select<8, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
-                                                       pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, s)
+                                                       pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, next_cond,
+                                                       next_ld, ftab, fa_next, fb1, z, s)
                                  : launch_select<16, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
-                                                        pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, s);
+                                                        pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, next_cond,
+                                                        next_ld, ftab, fa_next, fb1, z, s);
                 if (st != SPEC_OK) return st;
                 continue;
             }
         }
         if (!ln) {
             SPEC_CUDA_TRY(launch("draft_mlp_fma", k_gemm_fma<T, 0>, dim3((d + GBM - 1) / GBM, (R + GBN - 1) / GBN), dim3(256),
-                                 0, s, W1k, X, d, R, d_in, ldx, b1k, h, cond[k], n_int, z, nullptr, 1, nullptr));
+                                 0, s, W1k, d_in, X, d, R, d_in, ldx, b1k, h, cond[k], n_int, z, nullptr, 1, nullptr));
         } else {
             const int hd = hs.hidden[k];
             SPEC_CUDA_TRY(launch("draft_mlp_fma", k_gemm_fma<T, 0>, dim3((hd + GBM - 1) / GBM, (R + GBN - 1) / GBN),
-                                 dim3(256), 0, s, W1k, X, hd, R, d_in, ldx, b1k, static_cast<const T*>(nullptr), cond[k],
+                                 dim3(256), 0, s, W1k, d_in, X, hd, R, d_in, ldx, b1k, static_cast<const T*>(nullptr), cond[k],
                                  n_int, W1bk ? hid : nullptr, nullptr, 1, W1bk ? nullptr : yln));
             if (W1bk)
                 SPEC_CUDA_TRY(launch("draft_mlp_fma", k_gemm_fma<T, 0>, dim3((d + GBM - 1) / GBM, (R + GBN - 1) / GBN),
-                                     dim3(256), 0, s, W1bk, static_cast<const T*>(hid), d, R, hd, hd,
+                                     dim3(256), 0, s, W1bk, hd, static_cast<const T*>(hid), d, R, hd, hd,
                                      static_cast<const T*>(hs.b1b[k]), static_cast<const T*>(nullptr), 0, 1,
                                      static_cast<T*>(nullptr), nullptr, 0, yln));
             spec_status st = layernorm();
             if (st != SPEC_OK) return st;
         }
         SPEC_CUDA_TRY(launch("draft_proj_fma", k_gemm_fma<T, 1>, dim3((V + GBM - 1) / GBM, (R + GBN - 1) / GBN), dim3(256), 0, s,
-                             W2k, z, V, R, d, d, nullptr, nullptr, 0, 1, nullptr, scratch, 0, nullptr));
+                             W2k, d, z, V, R, d, d, nullptr, nullptr, 0, 1, nullptr, scratch, 0, nullptr));
         spec_status st;
         if (p.kmax == 8) {
             SPEC_CUDA_TRY(launch("draft_topk_slices", k_topk_slices<8>, dim3(p.nslices, R), dim3(256), 0, s, scratch, V,
                                  topk[k], p.slice_fma, pc, pl, p.nslices));
             st = launch_select<8, T>(false, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V, pc, pl, node_tok,
-                                     node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, s);
+                                     node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, nullptr, nullptr,
+                                     nullptr, z, s);
         } else {
             SPEC_CUDA_TRY(launch("draft_topk_slices", k_topk_slices<16>, dim3(p.nslices, R), dim3(256), 0, s, scratch, V,
                                  topk[k], p.slice_fma, pc, pl, p.nslices));
             st = launch_select<16, T>(false, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V, pc, pl, node_tok,
-                                      node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, s);
+                                      node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, nullptr, nullptr,
+                                      nullptr, z, s);
         }
         if (st != SPEC_OK) return st;
     }
@@ -897,6 +1057,8 @@ static spec_status draft_call(const void* h, const void* emb, const Heads& hs, f
     const Plan p = make_plan(tree, B, d, V, hs.K, hs.cond, hs.topk, dt, &hs);
     if (!ws || ws_bytes < p.total) return fail(SPEC_EWORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, p.total);
     if (!aligned16(ws)) return fail(SPEC_EALIGN, "workspace must be 16-byte aligned");
+    for (int k = 0; k < hs.K; ++k)
+        if (hs.tab[k] && !aligned16(hs.tab[k])) return fail(SPEC_EALIGN, "folded table %d must be 16-byte aligned", k);
     if (dt == SPEC_BF16)
         return run<__nv_bfloat16>(static_cast<const __nv_bfloat16*>(h), static_cast<const __nv_bfloat16*>(emb), hs, ln_eps,
                                   root_tok, tree, B, d, V, node_tok, node_logit, node_logprob, ws, p, s);
@@ -925,6 +1087,62 @@ extern "C" spec_status hydra_draft(const void* h, const void* emb, int32_t K, co
     const draft::Heads hs = draft::heads_from_arrays(K, W1, b1, W2, cond, topk, d);
     return draft::draft_call(h, emb, hs, 0.f, root_tok, tree, B, d, V, dt, node_tok, node_logit, node_logprob, ws,
                              ws_bytes, reinterpret_cast<cudaStream_t>(s_));
+}
+
+extern "C" spec_status hydra_draft_folded(const void* h, const void* emb, int32_t K, const void* const* W1,
+                                          const void* const* b1, const void* const* W2, const float* const* tab,
+                                          const int32_t* cond, const int32_t* topk, const int32_t* root_tok,
+                                          const spec_tree* tree, int32_t B, int32_t d, int32_t V, spec_dtype dt,
+                                          int32_t* node_tok, float* node_logit, float* node_logprob, void* ws,
+                                          size_t ws_bytes, spec_stream_t s_) {
+    clear_error();
+    if (K < 1 || K > SPEC_MAX_DEPTH) return fail(SPEC_EINVAL, "K = %d out of 1..%d", K, SPEC_MAX_DEPTH);
+    if (!W1 || !W2 || !cond || !topk) return fail(SPEC_EINVAL, "W1, W2, cond and topk must not be NULL");
+    draft::Heads hs = draft::heads_from_arrays(K, W1, b1, W2, cond, topk, d);
+    if (tab)
+        for (int k = 0; k < K; ++k) hs.tab[k] = tab[k];
+    return draft::draft_call(h, emb, hs, 0.f, root_tok, tree, B, d, V, dt, node_tok, node_logit, node_logprob, ws,
+                             ws_bytes, reinterpret_cast<cudaStream_t>(s_));
+}
+
+extern "C" size_t hydra_fold_table_bytes(int32_t d, int32_t V) {
+    clear_error();
+    if (d < 8 || d > 16384 || d % 8 || V < 2 || V > (1 << 24)) return 0;
+    return sizeof(float) * static_cast<size_t>(d) * V;
+}
+
+extern "C" spec_status hydra_fold_embedding(const void* W1, const void* emb, int32_t d, int32_t V, spec_dtype dt,
+                                            float* tab, spec_stream_t s_) {
+    clear_error();
+    if (dt != SPEC_F32 && dt != SPEC_BF16) return fail(SPEC_EINVAL, "dtype %d unknown", (int)dt);
+    if (d < 8 || d > 16384 || d % 8) return fail(SPEC_EINVAL, "d = %d must be a multiple of 8 in 8..16384", d);
+    if (V < 2 || V > (1 << 24)) return fail(SPEC_EINVAL, "V = %d out of 2..2^24", V);
+    if (!W1 || !emb || !tab) return fail(SPEC_EINVAL, "W1, emb and tab must not be NULL");
+    if (!aligned16(W1) || !aligned16(emb) || !aligned16(tab)) return fail(SPEC_EALIGN, "W1, emb and tab must be 16-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(s_);
+    // tab[v, m] = W1[m, d:2d] . emb[v]: the CUDA-core GEMM with the embedding half of W1
+    // (row stride 2d) as the weights and the vocabulary as the rows, in chunks of grid rows
+    const int chunk = 65535 * draft::GBN;
+    for (int v0 = 0; v0 < V; v0 += chunk) {
+        const int n = std::min(chunk, V - v0);
+        const dim3 grid((d + draft::GBM - 1) / draft::GBM, (n + draft::GBN - 1) / draft::GBN);
+        if (dt == SPEC_BF16) {
+            using T = __nv_bfloat16;
+            const T* W = static_cast<const T*>(W1) + d;
+            SPEC_CUDA_TRY(launch("fold_embedding", draft::k_gemm_fma<T, 1>, grid, dim3(256), 0, s, W, 2 * d,
+                                 static_cast<const T*>(emb) + static_cast<size_t>(v0) * d, d, n, d, d,
+                                 static_cast<const T*>(nullptr), static_cast<const T*>(nullptr), 0, 1,
+                                 static_cast<T*>(nullptr), tab + static_cast<size_t>(v0) * d, 0, static_cast<float*>(nullptr)));
+        } else {
+            const float* W = static_cast<const float*>(W1) + d;
+            SPEC_CUDA_TRY(launch("fold_embedding", draft::k_gemm_fma<float, 1>, grid, dim3(256), 0, s, W, 2 * d,
+                                 static_cast<const float*>(emb) + static_cast<size_t>(v0) * d, d, n, d, d,
+                                 static_cast<const float*>(nullptr), static_cast<const float*>(nullptr), 0, 1,
+                                 static_cast<float*>(nullptr), tab + static_cast<size_t>(v0) * d, 0,
+                                 static_cast<float*>(nullptr)));
+        }
+    }
+    return SPEC_OK;
 }
 
 extern "C" size_t hydra_draft_heads_workspace_size(const spec_tree* tree, int32_t B, int32_t d, int32_t V, int32_t K,
