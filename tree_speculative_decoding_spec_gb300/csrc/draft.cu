@@ -275,40 +275,34 @@ __global__ void __launch_bounds__(256) k_topk_slices(const float* __restrict__ l
 // picks a child's token writes the child's head input z = h_b + SiLU(a[b] + tab[tok]
 // + b1) itself, so the head's MLP leaves the chain between two projections.
 
-// a[b, m] = W1[m, 0:d] . h[b] in fp32, one warp per weight row (16-byte loads, lanes
-// interleaved), up to kFoldB sequences per pass over the row.  With z set (the first
-// head, conditioned on the root token): z[b, m] = h[b, m] + SiLU(a[b, m] + tab[root_b, m]
-// + b1[m]) in bf16 instead.  A programmatic dependent that reads nothing the kernels
-// before it write; it waits for them only before exiting, so a later kernel's wait
-// still covers everything queued ahead of this one.
-constexpr int kFoldB = 8;
+// a[b, m] = W1[m, 0:d] . h[b] + b1[m] in fp32.  One warp per weight row (16-byte
+// loads, lanes interleaved, kFoldBatch chunks in flight), up to kFoldB sequences per
+// pass over the row, each weight chunk unpacked once for all of them.  With z set
+// (the first head, conditioned on the root token): z[b, m] = h[b, m] + SiLU(a[b, m] +
+// tab[root_b, m]) in bf16 instead.  A programmatic dependent that reads nothing the
+// kernels before it write; it waits for them only before exiting, so a later
+// kernel's wait still covers everything queued ahead of this one.
+constexpr int kFoldB = 4;
 constexpr int kFoldWarps = 8;
 constexpr int kFoldBatch = 8;   // 16-byte weight chunks per lane in flight
 
-__device__ __forceinline__ float2 bf2_to_f2(uint32_t u) {
-    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
-}
-
-__device__ __forceinline__ float dot8_bf16(const uint4 w, const uint4 x) {
-    const uint32_t wa[4] = {w.x, w.y, w.z, w.w}, xa[4] = {x.x, x.y, x.z, x.w};
-    float acc = 0.f;
+__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 a = bf2_to_f2(wa[i]), b = bf2_to_f2(xa[i]);
-        acc = fmaf(a.x, b.x, acc);
-        acc = fmaf(a.y, b.y, acc);
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
-    return acc;
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 
-__global__ void __launch_bounds__(kFoldWarps * 32) k_fold_h(const __nv_bfloat16* __restrict__ W1, int ldw,
-                                                            const __nv_bfloat16* __restrict__ h, int B, int d,
-                                                            float* __restrict__ a_out, const float* __restrict__ tab,
-                                                            const __nv_bfloat16* __restrict__ b1,
-                                                            const int32_t* __restrict__ root_tok, int V,
-                                                            __nv_bfloat16* __restrict__ z) {
+__global__ void __launch_bounds__(kFoldWarps * 32, 4) k_fold_h(const __nv_bfloat16* __restrict__ W1, int ldw,
+                                                               const __nv_bfloat16* __restrict__ h, int B, int d,
+                                                               float* __restrict__ a_out, const float* __restrict__ tab,
+                                                               const __nv_bfloat16* __restrict__ b1,
+                                                               const int32_t* __restrict__ root_tok, int V,
+                                                               __nv_bfloat16* __restrict__ z) {
     griddep_launch();
     const int lane = threadIdx.x & 31;
     const int nchunk = d / 8;   // 16-byte chunks in the h_b half of a weight row
@@ -327,13 +321,18 @@ __global__ void __launch_bounds__(kFoldWarps * 32) k_fold_h(const __nv_bfloat16*
                     wv[u] = c < nchunk ? __ldcs(wr + c) : make_uint4(0u, 0u, 0u, 0u);
                 }
 #pragma unroll
-                for (int bb = 0; bb < kFoldB; ++bb) {
-                    if (b0 + bb >= B) break;
-                    const uint4* hr = reinterpret_cast<const uint4*>(h + static_cast<size_t>(b0 + bb) * d);
+                for (int u = 0; u < kFoldBatch; ++u) {
+                    const int c = c0 + u * 32 + lane;
+                    if (c >= nchunk) break;
+                    float f[8];
+                    bf16x8_to_f32(wv[u], f);
 #pragma unroll
-                    for (int u = 0; u < kFoldBatch; ++u) {
-                        const int c = c0 + u * 32 + lane;
-                        if (c < nchunk) acc[bb] += dot8_bf16(wv[u], __ldg(hr + c));
+                    for (int bb = 0; bb < kFoldB; ++bb) {
+                        if (b0 + bb >= B) break;
+                        float x[8];
+                        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(h + static_cast<size_t>(b0 + bb) * d) + c), x);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) acc[bb] = fmaf(f[e], x[e], acc[bb]);
                     }
                 }
             }
@@ -342,15 +341,17 @@ __global__ void __launch_bounds__(kFoldWarps * 32) k_fold_h(const __nv_bfloat16*
 #pragma unroll
                 for (int o = 16; o > 0; o >>= 1) acc[bb] += __shfl_xor_sync(0xffffffffu, acc[bb], o);
             if (lane == 0) {
+                const float bias = b1 ? __bfloat162float(b1[m]) : 0.f;
 #pragma unroll
                 for (int bb = 0; bb < kFoldB; ++bb) {
                     const int b = b0 + bb;
                     if (b >= B) break;
+                    const float a = acc[bb] + bias;
                     if (!z) {
-                        a_out[static_cast<size_t>(b) * d + m] = acc[bb];
+                        a_out[static_cast<size_t>(b) * d + m] = a;
                     } else {
                         const int tok = min(max(root_tok[b], 0), V - 1);   // k_init_root flags a bad token
-                        const float x = acc[bb] + tab[static_cast<size_t>(tok) * d + m] + (b1 ? __bfloat162float(b1[m]) : 0.f);
+                        const float x = a + tab[static_cast<size_t>(tok) * d + m];
                         z[static_cast<size_t>(b) * d + m] =
                             __float2bfloat16_rn(__bfloat162float(h[static_cast<size_t>(b) * d + m]) + silu(x));
                     }
@@ -362,6 +363,34 @@ __global__ void __launch_bounds__(kFoldWarps * 32) k_fold_h(const __nv_bfloat16*
 }
 
 // ---------------------------------------------------------------- select: merge slices, fill children
+
+// Eight consecutive elements m = 8c .. 8c+7 of a folded head's a[b] (fp32) and h_b
+// (as stored), held raw; store() writes z[m] = h_b[m] + SiLU(a[m] + tab[m]) given
+// the table's two float4 of the chunk.
+constexpr int kZPre = 2;   // chunks per thread loaded before the top-k
+template <typename T>
+struct ZChunk {
+    float4 a0, a1;
+    uint4 hw[sizeof(T) / 2];
+    __device__ __forceinline__ void load(const float* ab, const T* hb, int c) {
+        a0 = reinterpret_cast<const float4*>(ab)[2 * c];
+        a1 = reinterpret_cast<const float4*>(ab)[2 * c + 1];
+#pragma unroll
+        for (int i = 0; i < static_cast<int>(sizeof(T)) / 2; ++i)
+            hw[i] = reinterpret_cast<const uint4*>(hb + 8 * c)[i];
+    }
+    __device__ __forceinline__ void store(T* zr, int c, const float4 t0, const float4 t1) const {
+        const float x[8] = {a0.x + t0.x, a0.y + t0.y, a0.z + t0.z, a0.w + t0.w,
+                            a1.x + t1.x, a1.y + t1.y, a1.z + t1.z, a1.w + t1.w};
+        const T* hv = reinterpret_cast<const T*>(hw);
+        T out[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) out[e] = from_f32<T>(to_f32(hv[e]) + x[e] / (1.0f + expf(-x[e])));
+#pragma unroll
+        for (int i = 0; i < static_cast<int>(sizeof(T)) / 2; ++i)
+            reinterpret_cast<uint4*>(zr + 8 * c)[i] = reinterpret_cast<const uint4*>(out)[i];
+    }
+};
 
 // Copy the next depth's input row [h_b || E[tok]] (2d elements) with the whole CTA.
 template <typename T>
@@ -402,8 +431,7 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                                                 int next_cond, int next_ld, int kdepth,
                                                 const T* __restrict__ h, const T* __restrict__ emb, int d,
                                                 T* __restrict__ xin, int cpr, const float* __restrict__ ftab,
-                                                const float* __restrict__ fa, const T* __restrict__ fb1,
-                                                T* __restrict__ zf) {
+                                                const float* __restrict__ fa, T* __restrict__ zf) {
     // cpr CTAs per row (one per child of a single parent that needs next-depth rows): each
     // computes the row's top-k (the same result) and copies its own child's rows, so the
     // embedding rows pass through cpr SMs instead of one; CTA 0 of the row writes the
@@ -452,6 +480,20 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
     // that MLP's CTAs off the SMs while the projection still streams.
     griddep_wait();
     griddep_launch();
+
+    // a folded next head: a[b] (complete with the kernel before this one) and h_b do not
+    // depend on this kernel's picks, so this thread's first kZPre chunks of them load now,
+    // with the candidate lists; only the table rows wait for the top-k
+    ZChunk<T> zpre[kZPre];
+    if (ftab && rows) {
+        const float* ab = fa + static_cast<size_t>(b) * d;
+        const T* hb = h + static_cast<size_t>(b) * d;
+#pragma unroll
+        for (int j = 0; j < kZPre; ++j) {
+            const int c = tid + j * static_cast<int>(blockDim.x);
+            if (c < d / 8) zpre[j].load(ab, hb, c);
+        }
+    }
 
     // loads of earlier depths' outputs, issued with the candidate lists below
     float base1 = 0.f;
@@ -566,26 +608,25 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
         if (!rows) continue;
         if (ftab) {
             // the next head is folded (cond 1): its input row is z = h_b + SiLU(a[b] +
-            // tab[tok] + b1) itself, 8 elements per thread and chunk
+            // tab[tok]) itself (b1 is inside a), 8 elements per thread and chunk
             const float* ab = fa + static_cast<size_t>(b) * d;
             const T* hb = h + static_cast<size_t>(b) * d;
             for (int a = 0; a < nc; ++a) {
                 if (c_row[a] < 0 || (cpr > 1 && a != ci)) continue;
-                const float* tr = ftab + static_cast<size_t>(topi[c_rank[a]]) * d;
+                const float4* tr = reinterpret_cast<const float4*>(ftab + static_cast<size_t>(topi[c_rank[a]]) * d);
                 T* zr = zf + (row0 + c_row[a]) * d;
-                for (int c = tid; c < d / 8; c += blockDim.x) {
-                    const float4 t0 = reinterpret_cast<const float4*>(tr)[2 * c];
-                    const float4 t1 = reinterpret_cast<const float4*>(tr)[2 * c + 1];
-                    const float4 a0 = reinterpret_cast<const float4*>(ab)[2 * c];
-                    const float4 a1 = reinterpret_cast<const float4*>(ab)[2 * c + 1];
-                    const float x[8] = {t0.x + a0.x, t0.y + a0.y, t0.z + a0.z, t0.w + a0.w,
-                                        t1.x + a1.x, t1.y + a1.y, t1.z + a1.z, t1.w + a1.w};
+                int j = 0;
+                for (int c = tid; c < d / 8; c += blockDim.x, ++j) {
+                    const float4 t0 = tr[2 * c], t1 = tr[2 * c + 1];
+                    ZChunk<T> zc;
+                    if (j < kZPre) {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int m = 8 * c + e;
-                        const float xb = x[e] + (fb1 ? to_f32(fb1[m]) : 0.f);
-                        zr[m] = from_f32<T>(to_f32(hb[m]) + xb / (1.0f + expf(-xb)));
+                        for (int q = 0; q < kZPre; ++q)
+                            if (q == j) zc = zpre[q];
+                    } else {
+                        zc.load(ab, hb, c);
                     }
+                    zc.store(zr, c, t0, t1);
                 }
             }
             continue;
@@ -883,8 +924,7 @@ template <int KMAX, typename T>
 spec_status launch_select(bool pdl, const Plan& p, const spec_tree* t, int R, int k, int topk, int cond, int n_int,
                           int int_off, int next_n_int, int V, const Cand* pc, const float2* pl, int32_t* node_tok,
                           float* node_logit, float* node_logprob, void* ws, const T* h, const T* emb, int d, T* xin,
-                          int next_cond, int next_ld, const float* ftab, const float* fa, const T* fb1, T* zf,
-                          cudaStream_t s) {
+                          int next_cond, int next_ld, const float* ftab, const float* fa, T* zf, cudaStream_t s) {
     // one CTA per child where each CTA has a single parent node and children get next-depth rows
     const bool single_parent = cond != 0 || n_int == 1;
     const int cpr = (next_n_int > 0 && single_parent && k + 1 <= t->max_depth)
@@ -892,7 +932,7 @@ spec_status launch_select(bool pdl, const Plan& p, const spec_tree* t, int R, in
     SPEC_CUDA_TRY(launch_ex("draft_select", k_select<KMAX, T>, dim3(R * cpr), dim3(256), 0, s, pdl, pc, pl, p.nslices, topk,
                             cond, n_int, int_off, t->internal, t->child_off, t->child_idx, t->rank, t->parent,
                             t->row_of, t->T, V, node_tok, node_logit, node_logprob, ws, next_n_int, next_cond, next_ld, k,
-                            h, emb, d, xin, cpr, ftab, fa, fb1, zf));
+                            h, emb, d, xin, cpr, ftab, fa, zf));
     return SPEC_OK;
 }
 
@@ -981,16 +1021,15 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
                 if (fnext)
                     SPEC_CUDA_TRY(launch_ex("draft_fold_h", k_fold_h, dim3(fold_grid), dim3(kFoldWarps * 32), 0, s, true,
                                             static_cast<const T*>(hs.W1[k + 1]), 2 * d, h, B, d, fa_next,
-                                            static_cast<const float*>(nullptr), static_cast<const T*>(nullptr),
+                                            static_cast<const float*>(nullptr), static_cast<const T*>(hs.b1[k + 1]),
                                             static_cast<const int32_t*>(nullptr), V, static_cast<T*>(nullptr)));
                 const float* ftab = fnext ? hs.tab[k + 1] : nullptr;
-                const T* fb1 = fnext ? static_cast<const T*>(hs.b1[k + 1]) : nullptr;
                 st = p.kmax == 8 ? launch_select<8, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
                                                        pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, next_cond,
-                                                       next_ld, ftab, fa_next, fb1, z, s)
+                                                       next_ld, ftab, fa_next, z, s)
                                  : launch_select<16, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
                                                         pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, next_cond,
-                                                        next_ld, ftab, fa_next, fb1, z, s);
+                                                        next_ld, ftab, fa_next, z, s);
                 if (st != SPEC_OK) return st;
                 continue;
             }
@@ -1019,13 +1058,13 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
                                  topk[k], p.slice_fma, pc, pl, p.nslices));
             st = launch_select<8, T>(false, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V, pc, pl, node_tok,
                                      node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, nullptr, nullptr,
-                                     nullptr, z, s);
+                                     z, s);
         } else {
             SPEC_CUDA_TRY(launch("draft_topk_slices", k_topk_slices<16>, dim3(p.nslices, R), dim3(256), 0, s, scratch, V,
                                  topk[k], p.slice_fma, pc, pl, p.nslices));
             st = launch_select<16, T>(false, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V, pc, pl, node_tok,
                                       node_logit, node_logprob, ws, h, emb, d, xin, next_cond, next_ld, nullptr, nullptr,
-                                      nullptr, z, s);
+                                      z, s);
         }
         if (st != SPEC_OK) return st;
     }
