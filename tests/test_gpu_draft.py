@@ -303,6 +303,8 @@ def _compare_folded(st, x, parent, rank, dtype, fold_mask=None):
     (64, 700, 2, (2, 2, 2, 2), (1, 2, 1, 0), (2, 2, 2, 2), (1, 1, 1, 1)),   # tables only act on cond-1 heads
     (256, 3000, 2, (3, 2, 2), (1, 1, 1), (3, 2, 2), (0, 1, 0)),             # folded and whole layers mixed
     (256, 3000, 1, (3, 2, 2), (1, 1, 1), (3, 2, 2), (1, 0, 1)),
+    (64, 500, 10, (3, 2), (1, 1), (3, 2), (1, 1)),                          # more sequences than one MMA pass
+    (200, 999, 3, (2, 2), (1, 1), (2, 2), (1, 1)),                          # d not a multiple of 16 or 64
 ])
 def test_draft_folded_matches_oracle(dtype, shape):
     st = lib()

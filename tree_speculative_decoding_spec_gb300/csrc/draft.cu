@@ -275,89 +275,115 @@ __global__ void __launch_bounds__(256) k_topk_slices(const float* __restrict__ l
 // picks a child's token writes the child's head input z = h_b + SiLU(a[b] + tab[tok]
 // + b1) itself, so the head's MLP leaves the chain between two projections.
 
-// a[b, m] = W1[m, 0:d] . h[b] + b1[m] in fp32.  One warp per weight row (16-byte
-// loads, lanes interleaved, kFoldBatch chunks in flight), up to kFoldB sequences per
-// pass over the row, each weight chunk unpacked once for all of them.  With z set
-// (the first head, conditioned on the root token): z[b, m] = h[b, m] + SiLU(a[b, m] +
-// tab[root_b, m]) in bf16 instead.  A programmatic dependent that reads nothing the
-// kernels before it write; it waits for them only before exiting, so a later
-// kernel's wait still covers everything queued ahead of this one.
-constexpr int kFoldB = 4;
-constexpr int kFoldWarps = 8;
-constexpr int kFoldBatch = 8;   // 16-byte weight chunks per lane in flight
+// a[b, m] = W1[m, 0:d] . h[b] + b1[m] in fp32, on the warp-level tensor-core MMA
+// (m16n8k16, bf16 inputs, fp32 accumulation): weight rows on M, sequences on N
+// (eight per pass).  The work is bound by streaming W1, not by the MMA; the MMA
+// keeps the instruction count flat in the number of sequences.  A dot product
+// does not depend on the order of its k terms, so each lane feeds its fragment
+// registers straight from its own 16-byte loads: in a 64-wide block of k, lane
+// (g = lane / 4, t = lane % 4) loads k in [8t, 8t + 8) and [32 + 8t, 32 + 8t + 8)
+// of weight rows g and g + 8 and of h[b0 + g], and its four MMAs take the 32-bit
+// pairs in that order for both operands (the fragment's k slots {2t, 2t+1,
+// 2t+8, 2t+9} of a thread always meet the same physical k in A and in B).  A CTA
+// covers 16 weight rows; its 16 warps take every 16th 64-wide k block and
+// reduce through shared memory.  With z set (the first head, conditioned on the
+// root token): z[b, m] = h[b, m] + SiLU(a[b, m] + tab[root_b, m]) in bf16
+// instead.  A programmatic dependent that reads nothing the kernels before it
+// write; it waits for them only before exiting, so a later kernel's wait still
+// covers everything queued ahead of this one.
+constexpr int kFoldWarps = 16;
+constexpr int kFoldRows = 16;    // weight rows per CTA (MMA M)
+constexpr int kFoldSeq = 8;      // sequences per pass (MMA N)
+constexpr int kFoldUnroll = 2;   // 64-wide k blocks per warp in flight
 
-__device__ __forceinline__ void bf16x8_to_f32(const uint4 v, float (&f)[8]) {
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = __uint_as_float(w[i] << 16);
-        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
-    }
+__device__ __forceinline__ void mma_16816_bf16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+    asm volatile("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+                 "{%0, %1, %2, %3};"
+                 : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+                 : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 
-__global__ void __launch_bounds__(kFoldWarps * 32, 4) k_fold_h(const __nv_bfloat16* __restrict__ W1, int ldw,
+__global__ void __launch_bounds__(kFoldWarps * 32, 2) k_fold_h(const __nv_bfloat16* __restrict__ W1, int ldw,
                                                                const __nv_bfloat16* __restrict__ h, int B, int d,
                                                                float* __restrict__ a_out, const float* __restrict__ tab,
                                                                const __nv_bfloat16* __restrict__ b1,
                                                                const int32_t* __restrict__ root_tok, int V,
                                                                __nv_bfloat16* __restrict__ z) {
+    __shared__ float4 red[kFoldWarps][32];
     griddep_launch();
-    const int lane = threadIdx.x & 31;
-    const int nchunk = d / 8;   // 16-byte chunks in the h_b half of a weight row
-    const int nw = gridDim.x * kFoldWarps;
-    for (int m = blockIdx.x * kFoldWarps + (threadIdx.x >> 5); m < d; m += nw) {
-        const uint4* wr = reinterpret_cast<const uint4*>(W1 + static_cast<size_t>(m) * ldw);
-        for (int b0 = 0; b0 < B; b0 += kFoldB) {
-            float acc[kFoldB];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int g = lane >> 2, t = lane & 3;
+    const int m0 = blockIdx.x * kFoldRows;
+    const int r0 = m0 + g, r1 = m0 + g + 8;
+    const bool v0 = r0 < d, v1 = r1 < d;
+    const uint4* w0 = reinterpret_cast<const uint4*>(W1 + static_cast<size_t>(v0 ? r0 : 0) * ldw);
+    const uint4* w1 = reinterpret_cast<const uint4*>(W1 + static_cast<size_t>(v1 ? r1 : 0) * ldw);
+    const int nblk = (d + 63) / 64;
+    const int nchunk = d / 8;                      // 16-byte chunks of a row's h_b half
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (int b0 = 0; b0 < B; b0 += kFoldSeq) {
+        const int bq = b0 + g;                     // this lane's B column (sequence)
+        const uint4* hq = reinterpret_cast<const uint4*>(h + static_cast<size_t>(bq < B ? bq : 0) * d);
+        float c[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int k0 = warp; k0 < nblk; k0 += kFoldWarps * kFoldUnroll) {
+            uint4 a[kFoldUnroll][4], x[kFoldUnroll][2];
 #pragma unroll
-            for (int bb = 0; bb < kFoldB; ++bb) acc[bb] = 0.f;
-            for (int c0 = 0; c0 < nchunk; c0 += 32 * kFoldBatch) {
-                uint4 wv[kFoldBatch];
-#pragma unroll
-                for (int u = 0; u < kFoldBatch; ++u) {
-                    const int c = c0 + u * 32 + lane;
-                    wv[u] = c < nchunk ? __ldcs(wr + c) : make_uint4(0u, 0u, 0u, 0u);
-                }
-#pragma unroll
-                for (int u = 0; u < kFoldBatch; ++u) {
-                    const int c = c0 + u * 32 + lane;
-                    if (c >= nchunk) break;
-                    float f[8];
-                    bf16x8_to_f32(wv[u], f);
-#pragma unroll
-                    for (int bb = 0; bb < kFoldB; ++bb) {
-                        if (b0 + bb >= B) break;
-                        float x[8];
-                        bf16x8_to_f32(__ldg(reinterpret_cast<const uint4*>(h + static_cast<size_t>(b0 + bb) * d) + c), x);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) acc[bb] = fmaf(f[e], x[e], acc[bb]);
-                    }
-                }
+            for (int u = 0; u < kFoldUnroll; ++u) {
+                const int blk = k0 + u * kFoldWarps;
+                const int c0 = blk * 8 + t, c1 = blk * 8 + 4 + t;   // chunk indices (8 k each)
+                const bool ok0 = blk < nblk && c0 < nchunk, ok1 = blk < nblk && c1 < nchunk;
+                a[u][0] = ok0 && v0 ? __ldcs(w0 + c0) : zero;
+                a[u][1] = ok1 && v0 ? __ldcs(w0 + c1) : zero;
+                a[u][2] = ok0 && v1 ? __ldcs(w1 + c0) : zero;
+                a[u][3] = ok1 && v1 ? __ldcs(w1 + c1) : zero;
+                x[u][0] = ok0 && bq < B ? __ldg(hq + c0) : zero;
+                x[u][1] = ok1 && bq < B ? __ldg(hq + c1) : zero;
             }
 #pragma unroll
-            for (int bb = 0; bb < kFoldB; ++bb)
+            for (int u = 0; u < kFoldUnroll; ++u) {
+                // word j of this lane's 8-word k set: chunk j / 4, component j % 4
+                const uint32_t ra[8] = {a[u][0].x, a[u][0].y, a[u][0].z, a[u][0].w, a[u][1].x, a[u][1].y, a[u][1].z, a[u][1].w};
+                const uint32_t rb[8] = {a[u][2].x, a[u][2].y, a[u][2].z, a[u][2].w, a[u][3].x, a[u][3].y, a[u][3].z, a[u][3].w};
+                const uint32_t rx[8] = {x[u][0].x, x[u][0].y, x[u][0].z, x[u][0].w, x[u][1].x, x[u][1].y, x[u][1].z, x[u][1].w};
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) acc[bb] += __shfl_xor_sync(0xffffffffu, acc[bb], o);
-            if (lane == 0) {
-                const float bias = b1 ? __bfloat162float(b1[m]) : 0.f;
+                for (int j = 0; j < 4; ++j)
+                    mma_16816_bf16(c, ra[2 * j], rb[2 * j], ra[2 * j + 1], rb[2 * j + 1], rx[2 * j], rx[2 * j + 1]);
+            }
+        }
+        // c[0], c[1]: row g, sequences b0 + 2t, b0 + 2t + 1; c[2], c[3]: row g + 8, the same sequences
+        red[warp][lane] = make_float4(c[0], c[1], c[2], c[3]);
+        __syncthreads();
+        if (warp == 0) {
+            float4 s4 = red[0][lane];
+#pragma unroll 1
+            for (int w = 1; w < kFoldWarps; ++w) {
+                const float4 o = red[w][lane];
+                s4.x += o.x;
+                s4.y += o.y;
+                s4.z += o.z;
+                s4.w += o.w;
+            }
+            const float sv[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
-                for (int bb = 0; bb < kFoldB; ++bb) {
-                    const int b = b0 + bb;
-                    if (b >= B) break;
-                    const float a = acc[bb] + bias;
-                    if (!z) {
-                        a_out[static_cast<size_t>(b) * d + m] = a;
-                    } else {
-                        const int tok = min(max(root_tok[b], 0), V - 1);   // k_init_root flags a bad token
-                        const float x = a + tab[static_cast<size_t>(tok) * d + m];
-                        z[static_cast<size_t>(b) * d + m] =
-                            __float2bfloat16_rn(__bfloat162float(h[static_cast<size_t>(b) * d + m]) + silu(x));
-                    }
+            for (int e = 0; e < 4; ++e) {
+                const int m = (e < 2) ? r0 : r1;
+                const int b = b0 + 2 * t + (e & 1);
+                if (m >= d || b >= B) continue;
+                const float a = sv[e] + (b1 ? __bfloat162float(b1[m]) : 0.f);
+                if (!z) {
+                    a_out[static_cast<size_t>(b) * d + m] = a;
+                } else {
+                    const int tok = min(max(root_tok[b], 0), V - 1);   // k_init_root flags a bad token
+                    const float xx = a + tab[static_cast<size_t>(tok) * d + m];
+                    z[static_cast<size_t>(b) * d + m] =
+                        __float2bfloat16_rn(__bfloat162float(h[static_cast<size_t>(b) * d + m]) + silu(xx));
                 }
             }
         }
+        __syncthreads();   // red is reused by the next pass
     }
     griddep_wait();
 }
@@ -994,7 +1020,7 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
             if (p.tc) {
                 spec_status st;
                 const bool fnext = next_n_int > 0 && fold[k + 1];
-                const int fold_grid = std::min((d + kFoldWarps - 1) / kFoldWarps, 1024);
+                const int fold_grid = (d + kFoldRows - 1) / kFoldRows;
                 if (fold[k]) {
                     // the first head's z from its folded layer (later heads' z come from the select)
                     if (k == 0)
