@@ -77,3 +77,56 @@ def test_misaligned_pointer_is_refused():
     with pytest.raises(st.SpecError) as e:
         st.tree_accept(0, lp, None, tok, tree)
     assert e.value.status == 3   # SPEC_EALIGN
+
+
+@pytest.mark.parametrize("mode", [0, 1, 2])
+def test_accept_status_is_cleared_by_each_call(mode):
+    # the rows kernel clears the status word itself: a workspace whose header holds garbage,
+    # then a call that flags, then a clean call on the same workspace
+    st = lib()
+    parent, rank = wl.chain_tree(3)
+    tree = st.spec_tree_build(parent, rank)
+    V = 16
+    lp = np.zeros((1, 3, V), dtype=np.float32)
+    bad = np.array([[0, 99, 1]], dtype=np.int32)
+    good = np.array([[0, 3, 1]], dtype=np.int32)
+    ws = torch.full((st.tree_accept_workspace_size(mode, tree, 1, V),), 0x7F, dtype=torch.uint8, device="cuda")
+
+    def call(tok):
+        if mode == 2:
+            st.tree_accept_typical(to_dev(lp), to_dev(tok), tree, temperature=1.0, epsilon=0.3, alpha=0.09, ws=ws)
+        else:
+            st.tree_accept(mode, to_dev(lp), to_dev(lp) if mode == 1 else None, to_dev(tok), tree, temperature=1.0,
+                           ws=ws)
+
+    call(good)
+    assert st.spec_read_device_status(ws) == 0
+    if mode != 0:   # the greedy walk compares tokens without indexing by them: nothing to flag
+        call(bad)
+        assert st.spec_read_device_status(ws) == 1
+    call(good)
+    assert st.spec_read_device_status(ws) == 0
+
+
+def test_draft_status_is_cleared_by_each_call():
+    # the root kernel clears the status word itself and flags an out-of-vocabulary root token
+    st = lib()
+    w = wl.Workload("t", "bf16", B=3, seed=5, tree=("cartesian", (3, 2)), d=64, V=500, cond=(1, 1), topk=(3, 2))
+    parent, rank = wl.make_tree(w.tree)
+    tree = st.spec_tree_build(parent, rank)
+    x = wl.draft_inputs(w)
+    args = (to_dev(x["h"]), to_dev(x["E"]), [to_dev(a) for a in x["W1"]], [to_dev(a) for a in x["b1"]],
+            [to_dev(a) for a in x["W2"]], list(x["cond"]), list(x["topk"]))
+    ws = torch.full((st.hydra_draft_workspace_size(tree, 3, 64, 500, [1, 1], [3, 2], 1),), 0x7F, dtype=torch.uint8,
+                    device="cuda")
+    good = to_dev(np.array([1, 2, 3], dtype=np.int32))
+    bad = to_dev(np.array([1, 500, 3], dtype=np.int32))
+    for folded in (False, True):
+        tabs = [st.hydra_fold_embedding(W, args[1]) for W in args[2]] if folded else None
+        st.hydra_draft(*args, good, tree, ws=ws, folded=tabs)
+        assert st.spec_read_device_status(ws) == 0
+        tok, _, _ = st.hydra_draft(*args, bad, tree, ws=ws, folded=tabs)
+        assert st.spec_read_device_status(ws) == 1
+        assert tok.cpu().numpy()[1, 0] == 499        # clamped into the vocabulary
+        st.hydra_draft(*args, good, tree, ws=ws, folded=tabs)
+        assert st.spec_read_device_status(ws) == 0

@@ -63,8 +63,8 @@ __device__ __forceinline__ void top2_merge(float& v1, int& i1, float& v2, float 
 }
 
 __global__ void __launch_bounds__(kRowThreads) k_rows_greedy(const float* __restrict__ logits, int V, int slice,
-                                                             int slices, float4* __restrict__ part) {
-    griddep_launch();   // the walk may start loading the tree while the rows are read
+                                                             int slices, float4* __restrict__ part, void* ws) {
+    clear_status_then_trigger(ws);   // the walk may start loading the tree while the rows are read
     const int sl = blockIdx.x;
     const size_t row = blockIdx.y;
     const float* x = logits + row * V;
@@ -194,8 +194,8 @@ __device__ __forceinline__ void lse_ent_merge(float& m, float& s, float& t, floa
 
 // Typical acceptance: (m, s, t) of every row of logits_p (for entropy and log-sum-exp).
 __global__ void __launch_bounds__(kRowThreads) k_rows_ent(const float* __restrict__ lp, int V, int slice, int slices,
-                                                          float inv_temp, float4* __restrict__ part) {
-    griddep_launch();   // the walk may start loading the tree while the rows are read
+                                                          float inv_temp, float4* __restrict__ part, void* ws) {
+    clear_status_then_trigger(ws);   // the walk may start loading the tree while the rows are read
     const int sl = blockIdx.x;
     const size_t row = blockIdx.y;
     const int v0 = sl * slice, v1 = min(V, v0 + slice);
@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(kRowThreads) k_rows_ent(const float* __restric
 __global__ void __launch_bounds__(kRowThreads) k_rows_lse(const float* __restrict__ lp, const float* __restrict__ lq,
                                                           const int32_t* __restrict__ child_off, int Tn, int V,
                                                           int slice, int slices, float inv_temp,
-                                                          float4* __restrict__ part) {
-    griddep_launch();   // the walk may start loading the tree while the rows are read
+                                                          float4* __restrict__ part, void* ws) {
+    clear_status_then_trigger(ws);   // the walk may start loading the tree while the rows are read
     const int sl = blockIdx.x;
     const size_t row = blockIdx.y;
     const int u = static_cast<int>(row % Tn);
@@ -575,17 +575,17 @@ extern "C" spec_status tree_accept(int32_t mode, const float* logits_p, const fl
     if (!aligned16(ws)) return fail(SPEC_EALIGN, "workspace must be 16-byte aligned");
     float4* part = reinterpret_cast<float4*>(static_cast<unsigned char*>(ws) + p.off_part);
     const dim3 grid(p.slices, B * tree->T);
-    SPEC_CUDA_TRY(reset_device_status(ws, s));
+    // the rows kernel clears the status word (it flags nothing itself; the walk flags after its wait)
     if (mode == 0) {
         SPEC_CUDA_TRY(launch("accept_rows_greedy", accept::k_rows_greedy, grid, dim3(accept::kRowThreads), 0, s, logits_p, V,
-                             p.slice, p.slices, part));
+                             p.slice, p.slices, part, ws));
         SPEC_CUDA_TRY(launch_ex("accept_walk_greedy", accept::k_walk_greedy, dim3(B), dim3(accept::kWalkThreads), 0, s, true, part,
                              p.slices, node_tok, tree->parent, tree->depth, tree->T, tree->max_depth, accept_len,
                              accept_path, next_token, margin));
     } else {
         const float inv_temp = 1.0f / temperature;
         SPEC_CUDA_TRY(launch("accept_rows_lse", accept::k_rows_lse, grid, dim3(accept::kRowThreads), 0, s, logits_p, logits_q,
-                             tree->child_off, tree->T, V, p.slice, p.slices, inv_temp, part));
+                             tree->child_off, tree->T, V, p.slice, p.slices, inv_temp, part, ws));
         SPEC_CUDA_TRY(launch_ex("accept_walk_reject", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), 0, s, true, part,
                              p.slices, logits_p, logits_q, node_tok, tree->parent, tree->depth, tree->child_off,
                              tree->T, tree->max_depth, V, inv_temp, seed, offset, accept_len, accept_path, next_token,
@@ -617,9 +617,9 @@ extern "C" spec_status tree_accept_typical(const float* logits_p, const int32_t*
     float4* part = reinterpret_cast<float4*>(static_cast<unsigned char*>(ws) + p.off_part);
     const dim3 grid(p.slices, B * tree->T);
     const float inv_temp = 1.0f / temperature;
-    SPEC_CUDA_TRY(reset_device_status(ws, s));
+    // the rows kernel clears the status word (it flags nothing itself; the walk flags after its wait)
     SPEC_CUDA_TRY(launch("accept_rows_ent", accept::k_rows_ent, grid, dim3(accept::kRowThreads), 0, s, logits_p, V,
-                         p.slice, p.slices, inv_temp, part));
+                         p.slice, p.slices, inv_temp, part, ws));
     SPEC_CUDA_TRY(launch_ex("accept_walk_typical", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), 0, s, true, part,
                          p.slices, logits_p, static_cast<const float*>(nullptr), node_tok, tree->parent, tree->depth,
                          tree->child_off, tree->T, tree->max_depth, V, inv_temp, seed, offset, accept_len, accept_path,

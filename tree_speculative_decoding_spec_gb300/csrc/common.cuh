@@ -168,6 +168,22 @@ __device__ __forceinline__ float key_value(unsigned k) {
 // Record a device-detected failure in a workspace's status word (largest code wins).
 __device__ __forceinline__ void flag_status(void* ws, int code) { atomicMax(static_cast<int*>(ws), code); }
 
+// Clear a call's status words from the call's first kernel (instead of a memset
+// before it): thread 0 of block 0 stores and fences, then the block meets at a
+// barrier, and only after that does the kernel trigger its dependents.  So no
+// later kernel of the call can flag before the clear; the first kernel itself
+// must flag only from block 0 after this call, or not at all.
+__device__ __forceinline__ void clear_status_then_trigger(void* ws) {
+    if (ws && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0) {
+        if (threadIdx.x == 0) {
+            *static_cast<int4*>(ws) = make_int4(0, 0, 0, 0);
+            __threadfence();
+        }
+        __syncthreads();
+    }
+    griddep_launch();
+}
+
 // Merge two (max, sum of exp(x - max)) pairs.
 __device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
     if (m2 == -INFINITY) return;

@@ -714,8 +714,8 @@ struct HRows {
 };
 
 // CTA (b, 0): node 0 of sequence b -- its token is the root token (clamped to
-// the vocabulary, with SPEC_EINVAL in the status word, so later reads stay in
-// bounds) -- and head 0's whole input row when head 0 is conditioned (cond0 1:
+// the vocabulary so later reads stay in bounds; CTA (0, 0) puts SPEC_EINVAL in
+// the status word for any root token outside it) -- and head 0's whole input row when head 0 is conditioned (cond0 1:
 // [h_b || E[root]], 2: h_b).  CTA (b, 1 + r): the h_b part of row r of
 // sequence b in HRows.
 template <typename T>
@@ -724,7 +724,14 @@ __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn,
                             const T* __restrict__ h, const T* __restrict__ emb, int d, T* __restrict__ xin0,
                             T* __restrict__ xbase, const HRows hr) {
     const int b = blockIdx.x;
-    griddep_launch();   // head 0's MLP may start streaming its weights
+    // Block (0, 0) clears this call's status word before the kernel lets its dependents
+    // (head 0's first kernel streams its weights meanwhile) start, then checks every root
+    // token: the only flags this kernel raises come after the clear.  The other blocks
+    // clamp their token silently.
+    clear_status_then_trigger(ws);
+    if (blockIdx.x == 0 && blockIdx.y == 0)
+        for (int bb = threadIdx.x; bb < B; bb += blockDim.x)
+            if (root_tok[bb] < 0 || root_tok[bb] >= V) flag_status(ws, SPEC_EINVAL);
     if (blockIdx.y > 0) {
         const int r = static_cast<int>(blockIdx.y) - 1;
         int i = 0;
@@ -735,11 +742,7 @@ __global__ void k_init_root(const int32_t* __restrict__ root_tok, int B, int Tn,
         for (int w = threadIdx.x; w < d / (16 / static_cast<int>(sizeof(T))); w += blockDim.x) o[w] = hs[w];
         return;
     }
-    int tok = root_tok[b];
-    if (tok < 0 || tok >= V) {
-        if (threadIdx.x == 0) flag_status(ws, SPEC_EINVAL);
-        tok = min(max(tok, 0), V - 1);
-    }
+    const int tok = min(max(root_tok[b], 0), V - 1);
     if (threadIdx.x == 0) {
         node_tok[static_cast<size_t>(b) * Tn] = tok;
         node_logit[static_cast<size_t>(b) * Tn] = 0.f;
@@ -981,7 +984,7 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
     bool fold[SPEC_MAX_DEPTH + 1] = {};
     for (int k = 0; k < K; ++k) fold[k] = folded(&hs, p.tc, k);
     const bool first_cond = t->n_internal_at_depth[0] > 0 && cond[0] && !fold[0];
-    SPEC_CUDA_TRY(reset_device_status(ws, s));
+    // k_init_root clears the status word (no memset: it would break the launch chain)
     SPEC_CUDA_TRY(launch("draft_init_root", k_init_root<T>, dim3(B, 1 + p.hr.per_seq), dim3(128), 0, s, root_tok, B,
                          t->T, V, node_tok, node_logit, node_logprob, ws, first_cond ? cond[0] : 0, h, emb, d,
                          xbase + p.xin_at[0], xbase, p.hr));
