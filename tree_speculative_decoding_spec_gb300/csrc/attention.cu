@@ -372,8 +372,9 @@ static spec_status run_checked(const void* q, const void* k_cache, const void* v
             float* part = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kWsHeader);
             st = tc::attn_tc_run(p.tcp, static_cast<const T*>(q), static_cast<const T*>(k_cache),
                                  static_cast<const T*>(v_cache), prefix_len, static_cast<const T*>(k_tree),
-                                 static_cast<const T*>(v_tree), tree, B, Hq, Hkv, Lmax, scale, part, ws, s, pg);
+                                 static_cast<const T*>(v_tree), tree, B, Hq, Hkv, Lmax, scale, part, out, lse, ws, s, pg);
             if (st != SPEC_OK) return st;
+            if (p.tcp.fused) return SPEC_OK;   // the splits merged on chip
             const int nrows = B * Hq * tree->T;
             SPEC_CUDA_TRY(launch_ex("attn_combine", k_attn_combine, dim3((nrows + 7) / 8), dim3(256), 0, s, true, part,
                                  prefix_len, tree->T, Hq, D, Lmax, p.tcp.chunk, p.tcp.n_pre, 1, nrows, out, lse));

@@ -52,6 +52,8 @@ constexpr int kStageBytes = 4 * kKVHalf;          // K and V, two halves each
 constexpr size_t kASmem = 1024 + kQBytes + kAStages * kStageBytes + 2048;
 constexpr uint32_t kATmemCols = 512;              // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
 constexpr uint32_t kAO = 2 * kAKeys;              // first O column
+constexpr int kFusedMaxSplits = 8;                // portable cluster size
+constexpr int kFPStride = kAD + 4;                // floats per row of an on-chip partial: m, l, -, -, O[kAD]
 static_assert(kASmem <= 232448, "shared memory of one CTA");
 
 struct AttnTcParams {
@@ -63,6 +65,9 @@ struct AttnTcParams {
     float* part;
     void* ws;
     KvPages pg;
+    int fused;          // cluster of the n_pre splits: merge on chip, write out / lse
+    float* out;
+    float* lse;
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -91,7 +96,7 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     const bool has_tree = (c == max(n_pref - 1, 0));          // this split also takes the tree keys
     const int n_tt = has_tree ? (p.T + kAKeys - 1) / kAKeys : 0;
     const int n_tiles = n_pt + n_tt;
-    if (n_tiles == 0) return;   // whole CTA: nothing allocated yet
+    if (n_tiles == 0 && !p.fused) return;   // whole CTA: nothing allocated yet (a fused one still merges)
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                 return true;
             };
             // S for the first tile of each group, then per tile: PV_j, S_{j+2}
-            if (ok) ok = issue_s(0);
+            if (ok && n_tiles > 0) ok = issue_s(0);
             if (ok && n_tiles > 1) ok = issue_s(1);
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (!mbar_wait_or_abort(&p_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -383,10 +388,14 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             const float a1 = g1.x == -INFINITY ? 0.f : ex2(g1.x - m);
             const bool valid = rg < p.T * p.g;
             float* dst = nullptr;
-            if (valid) {
+            if (p.fused) {   // this CTA's partial stays in its own shared memory (the drained K/V ring)
+                dst = reinterpret_cast<float*>(sKV) + r * kFPStride;
+            } else if (valid) {
                 const int hl = rg / p.T, i = rg % p.T;
                 const size_t row = (static_cast<size_t>(b) * p.Hq + kvh * p.g + hl) * p.T + i;
                 dst = p.part + (row * (p.n_pre + 1) + c) * (kAD + 4);
+            }
+            if (dst) {
                 dst[0] = m;
                 dst[1] = a0 * l + a1 * g1.y;
             }
@@ -396,7 +405,7 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                 tmem_ld32(lane_base + kAO + cc * 32, o0);
                 tmem_ld32(lane_base + kAO + kAD + cc * 32, o1);
                 tmem_ld_wait();
-                if (valid) {
+                if (dst) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         float v[4];
@@ -428,6 +437,65 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
         tc_fence_after();
         tmem_dealloc(tmem, kATmemCols);
     }
+    if (p.fused) {
+        // The n_pre splits of this (KV head, row block, sequence) are one cluster, each
+        // holding its (m, l, O) partial in shared memory (an aborted CTA publishes an empty
+        // one: its own loads have landed by now).  After the cluster barrier CTA c merges
+        // rows c, c + n, ... over every partial through distributed shared memory and
+        // writes out = O / l and lse; a second barrier keeps each partial alive until
+        // every peer has read it.  Every CTA reaches both barriers, also after a timeout.
+        float* fpart = reinterpret_cast<float*>(sKV);
+        if (*abort_flag && threadIdx.x < kARows) {
+            fpart[threadIdx.x * kFPStride] = -INFINITY;
+            fpart[threadIdx.x * kFPStride + 1] = 0.f;
+        }
+        cluster_sync();
+        const int nc = static_cast<int>(gridDim.x);
+        const int cr = static_cast<int>(cluster_ctarank());
+        const uint32_t fbase = smem_u32(fpart);
+        for (int r = cr + nc * warp; r < kARows; r += nc * (kAThreads / 32)) {
+            const int rg = rb * kARows + r;
+            if (rg >= p.T * p.g) break;   // rows only grow along the loop
+            const uint32_t roff = fbase + static_cast<uint32_t>(r * kFPStride) * 4u;
+            // every split's m, then every non-empty split's l and O chunk, each batch of
+            // loads issued together
+            float mj[kFusedMaxSplits], lj[kFusedMaxSplits];
+            float4 vj[kFusedMaxSplits];
+            float M = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kFusedMaxSplits; ++j) {
+                mj[j] = j < nc ? dsmem_ld_f32(dsmem_map(roff, j)) : -INFINITY;
+                M = fmaxf(M, mj[j]);
+            }
+#pragma unroll
+            for (int j = 0; j < kFusedMaxSplits; ++j) {
+                lj[j] = 0.f;
+                vj[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (mj[j] != -INFINITY) {   // an empty split's O is never read
+                    const uint32_t pj = dsmem_map(roff, j);
+                    lj[j] = dsmem_ld_f32(pj + 4u);
+                    vj[j] = dsmem_ld_f32x4(pj + 16u + 16u * lane);
+                }
+            }
+            float lsum = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < kFusedMaxSplits; ++j) {
+                const float w = mj[j] == -INFINITY ? 0.f : exp2f(mj[j] - M);
+                lsum += w * lj[j];
+                o.x += w * vj[j].x;
+                o.y += w * vj[j].y;
+                o.z += w * vj[j].z;
+                o.w += w * vj[j].w;
+            }
+            const int hl = rg / p.T, i = rg % p.T;
+            const size_t row = (static_cast<size_t>(b) * p.Hq + kvh * p.g + hl) * p.T + i;
+            const float inv = 1.f / lsum;
+            *reinterpret_cast<float4*>(p.out + row * kAD + 4 * lane) = make_float4(o.x * inv, o.y * inv, o.z * inv, o.w * inv);
+            if (p.lse && lane == 0) p.lse[row] = (M + log2f(lsum)) * 0.6931471805599453f;
+        }
+        cluster_sync();
+    }
 }
 
 // ---------------------------------------------------------------- host
@@ -438,6 +506,39 @@ bool attn_tc_supported(int rows_per_kv_head, int D) {
     alignas(256) static const uint16_t dummy[kAD * 64] = {};
     // tensor-map encoding must be available (driver entry point); the probe map is never used
     return make_tmap_bf16_2d(&probe, dummy, 64, kAD, kAD, 64) == cudaSuccess;
+}
+
+// Clusters of n CTAs of k_attn_tc that the current device holds at once (0 when
+// unknown, e.g. without a device), cached per device and cluster size.
+static int max_active_clusters(int n) {
+    static int cache[64][kFusedMaxSplits + 1];   // 0: not asked yet, -1: unavailable
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64 || n < 1 || n > kFusedMaxSplits) {
+        cudaGetLastError();
+        return 0;
+    }
+    int& c = cache[dev][n];
+    if (c == 0) {
+        int v = 0;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(n, 1, 1);
+        cfg.blockDim = dim3(kAThreads);
+        cfg.dynamicSmemBytes = kASmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = n;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&v, k_attn_tc, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            v = 0;
+        }
+        c = v > 0 ? v : -1;
+    }
+    return c > 0 ? c : 0;
 }
 
 // Prefix splits: one CTA per (split, KV head x row block, sequence); the last
@@ -465,6 +566,11 @@ AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_c
     }
     p.chunk = static_cast<int>(round_up((Lmax + best - 1) / best, kAKeys));
     p.n_pre = (Lmax + p.chunk - 1) / p.chunk;
+    // merge on chip only when every cluster is resident at once: a cluster starts only when
+    // n_pre SMs of one GPC are free together, so a second wave of clusters leaves SMs idle
+    // (32K prefix, 96 clusters of 3: 203 -> 296 us), and the one-split plans (a cluster of
+    // one) gain nothing over the combine kernel
+    p.fused = p.n_pre > 1 && p.n_pre <= kFusedMaxSplits && base <= max_active_clusters(p.n_pre);
     // partial layout shared with the CUDA-core path: n_pre + 1 slots per row (the last unused here)
     p.part_bytes = sizeof(float) * static_cast<size_t>(B) * Hq * T * (p.n_pre + 1) * (D + 4);
     return p;
@@ -472,8 +578,8 @@ AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_c
 
 spec_status attn_tc_run(const AttnTcPlan& pl, const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
                         const int32_t* prefix_len, const __nv_bfloat16* kt, const __nv_bfloat16* vt,
-                        const spec_tree* tree, int B, int Hq, int Hkv, int Lmax, float scale, float* part, void* ws,
-                        cudaStream_t s, const KvPages& pg) {
+                        const spec_tree* tree, int B, int Hq, int Hkv, int Lmax, float scale, float* part, float* out,
+                        float* lse, void* ws, cudaStream_t s, const KvPages& pg) {
     const int T = tree->T;
     CUtensorMap tq, tkc, tvc, tkt, tvt;
     SPEC_CUDA_TRY(make_tmap_bf16_2d(&tq, q, static_cast<uint64_t>(B) * Hq * T, kAD, kAD, kARows));
@@ -502,9 +608,16 @@ spec_status attn_tc_run(const AttnTcPlan& pl, const __nv_bfloat16* q, const __nv
     p.part = part;
     p.ws = ws;
     p.pg = pg;
+    p.fused = pl.fused ? 1 : 0;
+    p.out = out;
+    p.lse = lse;
     SPEC_CUDA_TRY(cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem));
-    SPEC_CUDA_TRY(launch("attn_tc", k_attn_tc, dim3(pl.n_pre, Hkv * pl.n_rb, B), dim3(kAThreads), kASmem, s, tq, tkc,
-                         tvc, tkt, tvt, p));
+    if (pl.fused)
+        SPEC_CUDA_TRY(launch_cluster("attn_tc", k_attn_tc, dim3(pl.n_pre, Hkv * pl.n_rb, B), dim3(kAThreads), kASmem, s,
+                                     false, dim3(pl.n_pre, 1, 1), tq, tkc, tvc, tkt, tvt, p));
+    else
+        SPEC_CUDA_TRY(launch("attn_tc", k_attn_tc, dim3(pl.n_pre, Hkv * pl.n_rb, B), dim3(kAThreads), kASmem, s, tq,
+                             tkc, tvc, tkt, tvt, p));
     return SPEC_OK;
 }
 

@@ -23,6 +23,7 @@ struct AttnTcPlan {
     int n_rb = 0;       // 128-row query blocks per KV head
     int chunk = 0;      // prefix keys per split (multiple of 128)
     int n_pre = 0;      // prefix splits; split n_pre holds the tree keys
+    bool fused = false; // the splits of a (head, row block, sequence) form one cluster and merge on chip
     size_t part_bytes = 0;
 };
 
@@ -31,14 +32,15 @@ struct AttnTcPlan {
 bool attn_tc_supported(int rows_per_kv_head, int D);
 AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_count);
 
-// Queue the split-KV kernel; it writes per-(row, split) partials in the layout
-// the combine kernel of attention.cu reads ([B*Hq*T][n_pre+1][D+4] floats).
+// Queue the split-KV kernel.  With p.fused it writes out [B*Hq*T][D] and lse
+// (may be NULL) itself; otherwise per-(row, split) partials in the layout the
+// combine kernel of attention.cu reads ([B*Hq*T][n_pre+1][D+4] floats).
 // kc, vc: the contiguous caches, or the pools when pg.table is set (Lmax =
 // pg.max_blocks * pg.bs then).
 spec_status attn_tc_run(const AttnTcPlan& p, const __nv_bfloat16* q, const __nv_bfloat16* kc, const __nv_bfloat16* vc,
                         const int32_t* prefix_len, const __nv_bfloat16* kt, const __nv_bfloat16* vt,
-                        const spec_tree* tree, int B, int Hq, int Hkv, int Lmax, float scale, float* part, void* ws,
-                        cudaStream_t s, const KvPages& pg = KvPages{});
+                        const spec_tree* tree, int B, int Hq, int Hkv, int Lmax, float scale, float* part, float* out,
+                        float* lse, void* ws, cudaStream_t s, const KvPages& pg = KvPages{});
 
 }  // namespace tc
 }  // namespace spec

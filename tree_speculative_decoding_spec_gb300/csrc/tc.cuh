@@ -144,6 +144,15 @@ __device__ __forceinline__ float dsmem_ld_f32(uint32_t cluster_addr) {
     return v;
 }
 
+__device__ __forceinline__ float4 dsmem_ld_f32x4(uint32_t cluster_addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(cluster_addr)
+                 : "memory");
+    return v;
+}
+
 __device__ __forceinline__ int dsmem_ld_s32(uint32_t cluster_addr) {
     int v;
     asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(cluster_addr) : "memory");
