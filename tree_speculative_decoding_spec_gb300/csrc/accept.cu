@@ -579,7 +579,9 @@ extern "C" spec_status tree_accept(int32_t mode, const float* logits_p, const fl
     if (mode == 0) {
         SPEC_CUDA_TRY(launch("accept_rows_greedy", accept::k_rows_greedy, grid, dim3(accept::kRowThreads), 0, s, logits_p, V,
                              p.slice, p.slices, part, ws));
-        SPEC_CUDA_TRY(launch_ex("accept_walk_greedy", accept::k_walk_greedy, dim3(B), dim3(accept::kWalkThreads), 0, s, true, part,
+        // one thread per node is enough here (no vocabulary scans): small trees get cheap barriers
+        const int walk_threads = std::min(accept::kWalkThreads, std::max(32, (tree->T + 31) / 32 * 32));
+        SPEC_CUDA_TRY(launch_ex("accept_walk_greedy", accept::k_walk_greedy, dim3(B), dim3(walk_threads), 0, s, true, part,
                              p.slices, node_tok, tree->parent, tree->depth, tree->T, tree->max_depth, accept_len,
                              accept_path, next_token, margin));
     } else {

@@ -311,9 +311,25 @@ __global__ void __launch_bounds__(kFoldWarps * 32, 2) k_fold_h(const __nv_bfloat
                                                                float* __restrict__ a_out, const float* __restrict__ tab,
                                                                const __nv_bfloat16* __restrict__ b1,
                                                                const int32_t* __restrict__ root_tok, int V,
-                                                               __nv_bfloat16* __restrict__ z) {
+                                                               __nv_bfloat16* __restrict__ z, int32_t* __restrict__ node_tok,
+                                                               float* __restrict__ node_logit,
+                                                               float* __restrict__ node_logprob, int Tn, void* ws) {
     __shared__ float4 red[kFoldWarps][32];
-    griddep_launch();
+    if (node_tok) {
+        // the step's first kernel (no root kernel before it): block 0 clears the status word
+        // before any dependent can start, then checks the root tokens and writes node 0
+        clear_status_then_trigger(ws);
+        if (blockIdx.x == 0)
+            for (int b = threadIdx.x; b < B; b += blockDim.x) {
+                const int t = root_tok[b];
+                if (t < 0 || t >= V) flag_status(ws, SPEC_EINVAL);
+                node_tok[static_cast<size_t>(b) * Tn] = min(max(t, 0), V - 1);
+                node_logit[static_cast<size_t>(b) * Tn] = 0.f;
+                if (node_logprob) node_logprob[static_cast<size_t>(b) * Tn] = 0.f;
+            }
+    } else {
+        griddep_launch();
+    }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int g = lane >> 2, t = lane & 3;
     const int m0 = blockIdx.x * kFoldRows;
@@ -984,10 +1000,14 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
     bool fold[SPEC_MAX_DEPTH + 1] = {};
     for (int k = 0; k < K; ++k) fold[k] = folded(&hs, p.tc, k);
     const bool first_cond = t->n_internal_at_depth[0] > 0 && cond[0] && !fold[0];
-    // k_init_root clears the status word (no memset: it would break the launch chain)
-    SPEC_CUDA_TRY(launch("draft_init_root", k_init_root<T>, dim3(B, 1 + p.hr.per_seq), dim3(128), 0, s, root_tok, B,
-                         t->T, V, node_tok, node_logit, node_logprob, ws, first_cond ? cond[0] : 0, h, emb, d,
-                         xbase + p.xin_at[0], xbase, p.hr));
+    // k_init_root clears the status word (no memset: it would break the launch chain).  When
+    // head 0 is folded and no depth needs h_b rows, the folded first layer of head 0 does the
+    // root kernel's work itself and the chain starts one launch shorter.
+    const bool root_in_fold = fold[0] && t->n_internal_at_depth[0] > 0 && p.hr.per_seq == 0;
+    if (!root_in_fold)
+        SPEC_CUDA_TRY(launch("draft_init_root", k_init_root<T>, dim3(B, 1 + p.hr.per_seq), dim3(128), 0, s, root_tok, B,
+                             t->T, V, node_tok, node_logit, node_logprob, ws, first_cond ? cond[0] : 0, h, emb, d,
+                             xbase + p.xin_at[0], xbase, p.hr));
     int int_off = 0;
     for (int k = 0; k < K; int_off += t->n_internal_at_depth[k], ++k) {
         const int n_int = t->n_internal_at_depth[k];
@@ -1027,9 +1047,10 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
                 if (fold[k]) {
                     // the first head's z from its folded layer (later heads' z come from the select)
                     if (k == 0)
-                        SPEC_CUDA_TRY(launch_ex("draft_fold_h", k_fold_h, dim3(fold_grid), dim3(kFoldWarps * 32), 0, s, true,
-                                                W1k, 2 * d, h, B, d, static_cast<float*>(nullptr), hs.tab[0], b1k,
-                                                root_tok, V, z));
+                        SPEC_CUDA_TRY(launch_ex("draft_fold_h", k_fold_h, dim3(fold_grid), dim3(kFoldWarps * 32), 0, s,
+                                                !root_in_fold, W1k, 2 * d, h, B, d, static_cast<float*>(nullptr), hs.tab[0],
+                                                b1k, root_tok, V, z, root_in_fold ? node_tok : nullptr, node_logit,
+                                                node_logprob, t->T, ws));
                     st = tc::proj_tc(p.tcp, W2k, z, R, d, V, topk[k], p.kmax, pc, pl, ws, s);
                 } else if (!ln) {
                     st = tc::draft_head_tc(p.tcp, W1k, b1k, W2k, h, X, d_in, ldx, z, R, d, V, cond[k], n_int, topk[k],
@@ -1051,7 +1072,9 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
                     SPEC_CUDA_TRY(launch_ex("draft_fold_h", k_fold_h, dim3(fold_grid), dim3(kFoldWarps * 32), 0, s, true,
                                             static_cast<const T*>(hs.W1[k + 1]), 2 * d, h, B, d, fa_next,
                                             static_cast<const float*>(nullptr), static_cast<const T*>(hs.b1[k + 1]),
-                                            static_cast<const int32_t*>(nullptr), V, static_cast<T*>(nullptr)));
+                                            static_cast<const int32_t*>(nullptr), V, static_cast<T*>(nullptr),
+                                            static_cast<int32_t*>(nullptr), static_cast<float*>(nullptr),
+                                            static_cast<float*>(nullptr), t->T, ws));
                 const float* ftab = fnext ? hs.tab[k + 1] : nullptr;
                 st = p.kmax == 8 ? launch_select<8, T>(true, p, t, R, k, topk[k], cond[k], n_int, int_off, next_n_int, V,
                                                        pc, pl, node_tok, node_logit, node_logprob, ws, h, emb, d, xin, next_cond,
