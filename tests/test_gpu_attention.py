@@ -36,6 +36,7 @@ CASES = [
     ("bf16", 1, 32, 32, ("sparse", (8, 4, 2, 1), 64, 64), 128, 1024, [1024]),
     ("bf16", 2, 4, 2, ("random", 200), 128, 700, [333, 700]),       # two tree tiles, four mask words
     ("bf16", 1, 2, 1, ("random", 130), 128, 257, [257]),            # second tree tile: one mask word
+    ("bf16", 2, 2, 2, ("sparse", (8, 4, 2, 1), 64, 64), 128, 1024, [0, 1024]),   # 8 splits merged on chip; empty prefix
 ]
 
 
