@@ -20,8 +20,12 @@
  *    output, and spec_last_error() describes the problem (per host thread).
  *    CUDA launch errors are reported as SPEC_ECUDA.
  *  - Kernels never trap and never wait without bound.  A failure detected on
- *    the device (a bounded wait that ran out) is recorded in the first 16 bytes
- *    of the call's workspace; spec_read_device_status() returns it.
+ *    the device (a bounded wait that ran out, a token or page index out of
+ *    range) is recorded in the first 16 bytes of the call's workspace;
+ *    spec_read_device_status() returns it.  Each call clears those bytes
+ *    before its kernels can record anything (any prior content, including
+ *    garbage in a fresh workspace, is discarded), so a workspace may be reused
+ *    by any later call on the same stream.
  *  - Tokens are int32, logits and outputs float32; inputs of the float tensors
  *    of a call share one spec_dtype (float32 or bfloat16 bit patterns).
  *  - Tensor shapes are given outermost first and are densely packed (row-major).

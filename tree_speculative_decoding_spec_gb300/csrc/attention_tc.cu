@@ -21,7 +21,11 @@
 //             base 2 (O is rescaled in TMEM only when the maximum grows by
 //             more than 2^8) and writes P_j as bf16 pairs over the first 64
 //             columns of its own score buffer.  At the end group 0 merges the
-//             two groups' (max, sum, O) and writes the split's partial.
+//             two groups' (max, sum, O) into the split's partial: in HBM for
+//             the combine kernel, or -- when the splits of a (head, row block,
+//             sequence) run as one thread-block cluster -- in the CTA's own
+//             shared memory, merged across the cluster over distributed shared
+//             memory into out and lse (see the end of the kernel).
 // The tensor pipe runs its MMAs in issue order, so S_{j+2} may overwrite the
 // buffer PV_j reads, and the completion of S_j implies that of PV_{j-2}.
 // Cache rows past the prefix length inside the last prefix tile are zeroed in
