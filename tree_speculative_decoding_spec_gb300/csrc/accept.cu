@@ -62,7 +62,12 @@ __device__ __forceinline__ void top2_merge(float& v1, int& i1, float& v2, float 
     else { v2 = fmaxf(v2, w1); }
 }
 
-__global__ void __launch_bounds__(kRowThreads) k_rows_greedy(const float* __restrict__ logits, int V, int slice,
+// Loads in batches of kGreedyBatch float4 per thread: with 16 in flight the kernel held
+// 102 registers, two CTAs per SM, and the 320-CTA grid of the Vicuna-7B shape ran a
+// second wave of 16 CTAs (a second HBM round trip).
+constexpr int kGreedyBatch = 8;
+
+__global__ void __launch_bounds__(kRowThreads, 3) k_rows_greedy(const float* __restrict__ logits, int V, int slice,
                                                              int slices, float4* __restrict__ part, void* ws) {
     clear_status_then_trigger(ws);   // the walk may start loading the tree while the rows are read
     const int sl = blockIdx.x;
@@ -72,22 +77,24 @@ __global__ void __launch_bounds__(kRowThreads) k_rows_greedy(const float* __rest
     float b1 = -INFINITY, b2 = -INFINITY;
     int i1 = 0x7fffffff;
     if ((V & 3) == 0) {
-        // every load of the thread's share is issued before any compare (slice <= 4 * kRowThreads * kLseIter)
-        float4 q[kLseIter];
+        // each batch of the thread's loads is issued before any compare of it
+        for (int it0 = 0; v0 + 4 * kRowThreads * it0 < v1; it0 += kGreedyBatch) {
+            float4 q[kGreedyBatch];
 #pragma unroll
-        for (int it = 0; it < kLseIter; ++it) {
-            const int e = v0 + 4 * (static_cast<int>(threadIdx.x) + kRowThreads * it);
-            q[it] = e < v1 ? __ldcs(reinterpret_cast<const float4*>(x + e))
-                           : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-        }
+            for (int it = 0; it < kGreedyBatch; ++it) {
+                const int e = v0 + 4 * (static_cast<int>(threadIdx.x) + kRowThreads * (it0 + it));
+                q[it] = e < v1 ? __ldcs(reinterpret_cast<const float4*>(x + e))
+                               : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
 #pragma unroll
-        for (int it = 0; it < kLseIter; ++it) {
-            const int e = v0 + 4 * (static_cast<int>(threadIdx.x) + kRowThreads * it);
-            if (e < v1) {
-                top2_push(b1, i1, b2, q[it].x, e);
-                top2_push(b1, i1, b2, q[it].y, e + 1);
-                top2_push(b1, i1, b2, q[it].z, e + 2);
-                top2_push(b1, i1, b2, q[it].w, e + 3);
+            for (int it = 0; it < kGreedyBatch; ++it) {
+                const int e = v0 + 4 * (static_cast<int>(threadIdx.x) + kRowThreads * (it0 + it));
+                if (e < v1) {
+                    top2_push(b1, i1, b2, q[it].x, e);
+                    top2_push(b1, i1, b2, q[it].y, e + 1);
+                    top2_push(b1, i1, b2, q[it].z, e + 2);
+                    top2_push(b1, i1, b2, q[it].w, e + 3);
+                }
             }
         }
     } else {
