@@ -253,7 +253,7 @@ size_t tree_attention_workspace_size(const spec_tree* tree, int32_t B, int32_t H
  *                     the last 128-key tile of a sequence: they must be readable memory)
  *   prefix_len        device [B], each in 0 .. Lmax (values outside are clamped to it)
  *   k_tree, v_tree    device [B, Hkv, T, D]: keys/values of the tree tokens
- *   scale             > 0 (usually 1/sqrt(D))
+ *   scale             > 0, or 0 for the usual 1/sqrt(D)
  *   out               device [B, Hq, T, D] float32
  *   lse               device [B, Hq, T] float32, or NULL
  * Shapes: Hq % Hkv == 0, D in {64, 128}, 1 <= Lmax <= 2^22.
@@ -282,12 +282,24 @@ spec_status tree_attention(const void* q, const void* k_cache, const void* v_cac
  * before any stream capture.  All calls share the one array and it keeps the
  * last call's contents (each call clears what must start at zero): calls
  * whose work overlaps on the GPU -- on different streams, or from different
- * host threads -- race on it and must not be issued.
+ * host threads -- race on it and must not be issued.  A failure the kernels
+ * detect (a bounded wait that ran out) goes to the status word at the start
+ * of the built-in array; tree_attention_noalloc_status reads it.
  */
 spec_status tree_attention_noalloc(const void* q, const void* k_cache, const void* v_cache,
                                    const int32_t* prefix_len, const void* k_tree, const void* v_tree,
                                    const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv, int32_t Lmax,
                                    int32_t D, float scale, spec_dtype dt, float* out, float* lse, spec_stream_t s);
+
+/*
+ * Device status of the calls that use the built-in scratch (tree_attention_noalloc):
+ * the counterpart of spec_read_device_status for a caller workspace.  Waits on
+ * stream s for the calls queued before it, copies the status word of the
+ * built-in array to *status (host) and returns SPEC_OK, or an error status
+ * when the copy fails.  Like tree_attention_noalloc, it looks up the array's
+ * address with the current device and allocates nothing.
+ */
+spec_status tree_attention_noalloc_status(int32_t* status, spec_stream_t s);
 
 /* Workspace bytes tree_attention_paged needs (0 on invalid arguments). */
 size_t tree_attention_paged_workspace_size(const spec_tree* tree, int32_t B, int32_t Hq, int32_t Hkv,

@@ -236,3 +236,43 @@ def test_temperature_applies_to_both():
     b = rejection_accept(lp * 4, lq * 4, tok, tree, 2.0, u_acc, u_smp)
     for key in ("accept_len", "accept_path", "next_token"):
         assert np.array_equal(a[key], b[key])
+
+
+# ---------------------------------------------------------------- reporting margins, computed by hand
+
+def test_greedy_margin_by_hand():
+    # chain root -> 1 -> 2, V = 4, integer logits so every gap is exact:
+    # row 0 argmax token 1 (gap 5 - 2 = 3); node 1 carries token 1: accepted.
+    # row 1 argmax token 0 (gap 4 - 3.5 = 0.5); node 2 carries token 2: rejected,
+    # so row 2's gap (9) is not an accepted node's and does not count.
+    parent, rank = wl.chain_tree(3)
+    tree = tree_encode(parent, rank)
+    lp = np.array([[[0.0, 5.0, 2.0, 1.0], [4.0, 1.0, 3.5, 0.0], [9.0, 0.0, 0.0, 0.0]]])
+    out = greedy_accept(lp, np.array([[7, 1, 2]]), tree)
+    assert out["accept_len"][0] == 1 and out["next_token"][0] == 0
+    assert out["margin"][0] == 0.5
+
+
+def test_rejection_margins_by_hand():
+    # root with one child carrying token 0; V = 2, temperature 1; p_0 = (.3, .7), q_0 = (.6, .4):
+    # the edge's ratio is .3 / .6 = .5
+    parent, rank = wl.chain_tree(2)
+    tree = tree_encode(parent, rank)
+    lp = np.log(np.array([[[0.3, 0.7], [0.25, 0.75]]]))
+    lq = np.log(np.array([[[0.6, 0.4], [0.5, 0.5]]]))
+    tok = np.array([[5, 0]])
+    # u_c = .45 < .5: accepted, |u - ratio| = .05; the child is a leaf, so the draw is from
+    # p_1 = (.25, .75): u' = .1 -> t = .1, CDF (.25, 1): token 0, nearest breakpoint .15 away
+    out = rejection_accept(lp, lq, tok, tree, 1.0, np.array([[0.0, 0.45]]), np.array([0.1]))
+    assert out["accept_len"][0] == 1 and out["next_token"][0] == 0
+    assert abs(out["margin_decide"][0] - 0.05) < 1e-12
+    assert abs(out["margin_sample"][0] - 0.15) < 1e-12
+    assert abs(out["margin"][0] - 0.05) < 1e-12
+    # u_c = .9 >= .5: rejected, |u - ratio| = .4; the draw is from the residual at the root,
+    # max(p_0 - q_0, 0) = (0, .3), total .3: u' = .5 -> t = .15, CDF (0, .3): token 1,
+    # nearest breakpoint .15 away, .5 of the total
+    out = rejection_accept(lp, lq, tok, tree, 1.0, np.array([[0.0, 0.9]]), np.array([0.5]))
+    assert out["accept_len"][0] == 0 and out["next_token"][0] == 1
+    assert abs(out["margin_decide"][0] - 0.4) < 1e-12
+    assert abs(out["margin_sample"][0] - 0.5) < 1e-12
+    assert abs(out["margin"][0] - 0.4) < 1e-12

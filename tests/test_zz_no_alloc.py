@@ -46,6 +46,7 @@ def test_noalloc_matches_workspace_call_on_two_calls_in_a_row():
         ref_out, ref_lse = st.tree_attention(*args, tree)
         prepared.append((dtype, tree, args, ref_out.cpu().numpy(), ref_lse.cpu().numpy()))
     results = [st.tree_attention_noalloc(*args, tree) for _, tree, args, _, _ in prepared]   # two calls in a row
+    assert st.tree_attention_noalloc_status() == 0    # no failure recorded in the built-in array's status word
     for (dtype, _, _, ref_out, ref_lse), (out, lse) in zip(prepared, results):
         assert_close(out.cpu().numpy(), ref_out, dtype, "out")
         assert_close(lse.cpu().numpy(), ref_lse, dtype, "lse")
@@ -56,8 +57,10 @@ def test_noalloc_refuses_shapes_beyond_its_scratch():
     from tree_speculative_decoding_spec_gb300 import _binding as b
     parent, rank = wl.cartesian_tree((4, 4, 4, 4))
     tree = st.spec_tree_build(parent, rank)
-    fake = ctypes.c_void_p(0x10000)   # never dereferenced: the call must fail before queuing anything
-    status = b._lib.tree_attention_noalloc(fake, fake, fake, fake, fake, fake, tree.ref(), 8, 64, 8, 32768, 128,
-                                           0.088, 1, fake, ctypes.c_void_p(0), None)
+    # NULL tensors: the size check must refuse first; were it to let the call through, the
+    # pointer check behind it would still stop it on the host (SPEC_EINVAL), with nothing queued
+    null = ctypes.c_void_p(0)
+    status = b._lib.tree_attention_noalloc(null, null, null, null, null, null, tree.ref(), 8, 64, 8, 32768, 128,
+                                           0.088, 1, null, null, None)
     assert status == 4   # SPEC_EWORKSPACE
     assert "built-in" in b.spec_last_error()

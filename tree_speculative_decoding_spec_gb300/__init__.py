@@ -10,6 +10,7 @@ __all__ = [
     "spec_tree_build", "spec_tree_device_bytes",
     "hydra_draft", "hydra_draft_workspace_size", "hydra_draft_heads", "hydra_draft_folded", "hydra_fold_embedding",
     "tree_attention", "tree_attention_workspace_size", "tree_attention_noalloc",
+    "tree_attention_noalloc_status",
     "tree_attention_paged", "tree_attention_paged_workspace_size",
     "tree_accept", "tree_accept_workspace_size", "tree_accept_typical",
     "tree_kv_commit", "tree_kv_commit_workspace_size",

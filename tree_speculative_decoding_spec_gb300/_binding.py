@@ -76,6 +76,7 @@ def _load():
         "tree_attention_workspace_size": (sz, [tp, i32, i32, i32, i32, i32, i32]),
         "tree_attention": (i32, [vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp, sz, vp]),
         "tree_attention_noalloc": (i32, [vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, f32, i32, vp, vp, vp]),
+        "tree_attention_noalloc_status": (i32, [_i32p, vp]),
         "tree_attention_paged_workspace_size": (sz, [tp, i32, i32, i32, i32, i32, i32, i32]),
         "tree_attention_paged": (i32, [vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, tp, i32, i32, i32, i32, f32, i32,
                                        vp, vp, vp, sz, vp]),
@@ -375,7 +376,7 @@ def tree_attention(q, k_cache, v_cache, prefix_len, k_tree, v_tree, tree, scale=
         raise ValueError(f"q has {T} nodes, the tree {tree.T}")
     _need(prefix_len, "prefix_len", dtype=torch.int32, ndim=1, device=dev)
     if scale is None:
-        scale = 1.0 / (D ** 0.5)
+        scale = 0.0   # the library's default, 1/sqrt(D)
     if out is None:
         out = torch.empty(B, Hq, T, D, dtype=torch.float32, device=dev)
     if lse is None and want_lse:
@@ -423,7 +424,7 @@ def tree_attention_paged(q, k_pool, v_pool, block_table, prefix_len, k_tree, v_t
         raise ValueError(f"q has {T} nodes, the tree {tree.T}")
     _need(prefix_len, "prefix_len", dtype=torch.int32, ndim=1, device=dev)
     if scale is None:
-        scale = 1.0 / (D ** 0.5)
+        scale = 0.0   # the library's default, 1/sqrt(D)
     if out is None:
         out = torch.empty(B, Hq, T, D, dtype=torch.float32, device=dev)
     if lse is None and want_lse:
@@ -462,7 +463,7 @@ def tree_attention_noalloc(q, k_cache, v_cache, prefix_len, k_tree, v_tree, tree
         raise ValueError(f"q has {T} nodes, the tree {tree.T}")
     _need(prefix_len, "prefix_len", dtype=torch.int32, ndim=1, device=dev)
     if scale is None:
-        scale = 1.0 / (D ** 0.5)
+        scale = 0.0   # the library's default, 1/sqrt(D)
     if out is None:
         out = torch.empty(B, Hq, T, D, dtype=torch.float32, device=dev)
     if lse is None and want_lse:
@@ -472,6 +473,15 @@ def tree_attention_noalloc(q, k_cache, v_cache, prefix_len, k_tree, v_tree, tree
             _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(prefix_len), _ptr(k_tree), _ptr(v_tree), tree.ref(),
             B, Hq, Hkv, Lmax, D, float(scale), dt, _ptr(out), _ptr(lse), _stream(stream)))
     return out, lse
+
+
+def tree_attention_noalloc_status(device=None, stream=None):
+    """Status word of the built-in scratch tree_attention_noalloc uses (0 = no failure)."""
+    v = ctypes.c_int32(0)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _check("tree_attention_noalloc_status", _lib.tree_attention_noalloc_status(ctypes.byref(v), _stream(stream)))
+    return v.value
 
 
 def tree_accept_workspace_size(mode, tree, B, V):

@@ -12,7 +12,7 @@
 // against one chunk with an online softmax and writes (max, sum, unnormalised
 // output) to the workspace; a combine kernel merges the chunks of each row.
 #include <algorithm>
-#include <mutex>
+#include <cmath>
 
 #include "attention_tc.cuh"
 #include "common.cuh"
@@ -358,7 +358,8 @@ static spec_status run_checked(const void* q, const void* k_cache, const void* v
     if (st != SPEC_OK) return st;
     if (!q || !k_cache || !v_cache || !prefix_len || !k_tree || !v_tree || !out)
         return fail(SPEC_EINVAL, "q, caches, prefix_len, tree K/V and out must not be NULL");
-    if (!(scale > 0.f) || !(scale < 1e30f)) return fail(SPEC_EINVAL, "scale must be positive and finite");
+    if (scale == 0.f) scale = 1.f / sqrtf(static_cast<float>(D));   // the usual 1/sqrt(D)
+    if (!(scale > 0.f) || !(scale < 1e30f)) return fail(SPEC_EINVAL, "scale must be positive and finite, or 0");
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(k_tree) || !aligned16(v_tree) ||
         !aligned16(out) || !aligned4(prefix_len) || (lse && !aligned4(lse)))
         return fail(SPEC_EALIGN, "tensors must be 16-byte aligned (prefix_len and lse 4-byte)");
@@ -459,23 +460,16 @@ namespace attn {
 constexpr size_t kNoAllocScratchBytes = size_t(32) << 20;   // 32 MiB
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-// Device address of g_noalloc_scratch on the current device, looked up once per
-// device (host code sees only a host-side stand-in under the array's name).
+// Device address of g_noalloc_scratch on the current device (host code sees only a
+// host-side stand-in under the array's name).  Looked up on every call rather than
+// cached: after a context teardown (cudaDeviceReset) the module reloads and an old
+// address would no longer be valid.  The first lookup on a device loads the module.
 static spec_status noalloc_scratch(void** out) {
-    static std::mutex mu;
-    static void* addr[64] = {};
-    int dev = -1;
-    SPEC_CUDA_TRY(cudaGetDevice(&dev));
-    if (dev < 0 || dev >= 64) return fail(SPEC_EUNSUPPORTED, "device ordinal %d out of range", dev);
-    std::lock_guard<std::mutex> lock(mu);
-    if (!addr[dev]) {
-        void* p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess || !p)
-            return fail(SPEC_ECUDA, "cudaGetSymbolAddress of the built-in scratch failed: %s", cudaGetErrorString(e));
-        addr[dev] = p;
-    }
-    *out = addr[dev];
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || !p)
+        return fail(SPEC_ECUDA, "cudaGetSymbolAddress of the built-in scratch failed: %s", cudaGetErrorString(e));
+    *out = p;
     return SPEC_OK;
 }
 
@@ -501,4 +495,15 @@ extern "C" spec_status tree_attention_noalloc(const void* q, const void* k_cache
     if (st != SPEC_OK) return st;
     return tree_attention(q, k_cache, v_cache, prefix_len, k_tree, v_tree, tree, B, Hq, Hkv, Lmax, D, scale, dt, out,
                           lse, ws, attn::kNoAllocScratchBytes, s);
+}
+
+// Status word of the built-in scratch: what spec_read_device_status returns for a
+// caller workspace, for the calls that use the built-in array instead.
+extern "C" spec_status tree_attention_noalloc_status(int32_t* status, spec_stream_t s) {
+    clear_error();
+    if (!status) return fail(SPEC_EINVAL, "status must not be NULL");
+    void* ws = nullptr;
+    spec_status st = attn::noalloc_scratch(&ws);
+    if (st != SPEC_OK) return st;
+    return spec_read_device_status(ws, status, s);
 }

@@ -45,10 +45,7 @@ constexpr int kARows = 128;        // query rows per CTA (MMA M)
 constexpr int kAKeys = 128;        // keys per tile
 constexpr int kAD = 128;           // head dim
 constexpr int kAStages = 3;
-#ifndef SPEC_ATTN_PREFETCH
-#define SPEC_ATTN_PREFETCH 2
-#endif
-constexpr int kAPrefetch = SPEC_ATTN_PREFETCH;   // contiguous prefix tiles prefetched into L2 ahead of their load
+constexpr int kAPrefetch = 2;     // contiguous prefix tiles prefetched into L2 ahead of their load
 constexpr int kAThreads = 320;
 constexpr int kQBytes = 2 * kARows * 128;         // two 64-column halves of 128 rows
 constexpr int kKVHalf = kAKeys * 128;             // one 64-column half of a 128-key tile

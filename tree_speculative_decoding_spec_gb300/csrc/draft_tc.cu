@@ -29,28 +29,13 @@ namespace tc {
 
 constexpr int kBM = 128;        // MMA M: weight rows per CTA
 constexpr int kMaxSplits = 8;   // MLP split-K: one cluster (portable size) per weight tile
-// Build-time shape knobs (defaults are the tuned choice):
-//   SPEC_DRAFT_KB        64-column K blocks per pipeline stage
-//   SPEC_DRAFT_L2PROMO   L2 promotion of the weight loads: 0 none, 1 128 B, 2 256 B
-//   SPEC_DRAFT_EVICT_FIRST  1: weight loads carry the L2 evict-first policy
-//   SPEC_DRAFT_ROTATE    1: each CTA starts its K loop at a different stage (by
-//                        weight tile), so the CTAs do not all read the same
-//                        activation lines from L2 at the same moment
-#ifndef SPEC_DRAFT_KB
-#define SPEC_DRAFT_KB 2
-#endif
-#ifndef SPEC_DRAFT_ROTATE
-#define SPEC_DRAFT_ROTATE 1
-#endif
-#ifndef SPEC_DRAFT_EVICT_FIRST
-#define SPEC_DRAFT_EVICT_FIRST 1
-#endif
-#ifndef SPEC_DRAFT_L2PROMO
-#define SPEC_DRAFT_L2PROMO 2
-#endif
+constexpr int kKB = 2;          // 64-column K blocks per pipeline stage
+// Weight loads carry the L2 evict-first policy (streamed once per step) and 256-byte L2 promotion.
+constexpr bool kWeightsEvictFirst = true;
+// Each CTA starts its K loop at a different stage (by weight tile), so that the CTAs
+// do not all read the same activation lines from L2 at the same moment.
+constexpr bool kRotateK = true;
 constexpr int kBK = 64;         // K per TMA box: one 128-byte swizzled row of bf16
-constexpr int kKB = SPEC_DRAFT_KB;
-constexpr bool kWeightsEvictFirst = SPEC_DRAFT_EVICT_FIRST != 0;
 constexpr int kBKS = kBK * kKB; // K per stage
 constexpr int kThreads = 128;
 constexpr int kStageA = kBM * kBKS * 2;
@@ -111,7 +96,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
     const int m0 = blockIdx.x * kBM;
     const int it0 = blockIdx.y * p.k_iters;
     // stage i of this CTA covers K stage it0 + (i + rot) mod n_it
-    const int rot = SPEC_DRAFT_ROTATE ? static_cast<int>(blockIdx.x % max(1, min(p.k_iters, p.total_iters - it0))) : 0;
+    const int rot = kRotateK ? static_cast<int>(blockIdx.x % max(1, min(p.k_iters, p.total_iters - it0))) : 0;
     const int n_it = max(0, min(p.k_iters, p.total_iters - it0));
 
     if (threadIdx.x == 0) {
@@ -405,9 +390,7 @@ cudaError_t make_tmap_bf16_2d(CUtensorMap* map, const void* base, uint64_t rows,
     const cuuint32_t estr[2] = {1, 1};
     const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
                           CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          SPEC_DRAFT_L2PROMO == 0 ? CU_TENSOR_MAP_L2_PROMOTION_NONE
-                          : SPEC_DRAFT_L2PROMO == 1 ? CU_TENSOR_MAP_L2_PROMOTION_L2_128B
-                                                    : CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
