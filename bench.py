@@ -240,7 +240,6 @@ def run_ours(args):
     torch.cuda.set_device(dev)
     import __graft_entry__
     __graft_entry__.build()
-    import oracle  # noqa: F401  (cpu baseline leg only)
     import spec_workloads as wl
     import tree_speculative_decoding_spec_gb300 as st
 
@@ -357,6 +356,31 @@ def run_ours(args):
     traced = timed_steps(args.steps)
     torch.cuda.synchronize()
     kernels = st.spec_trace_end(256)
+    # the same step with unfolded first layers (the whole W1 of every head streamed per step)
+    unfolded = None
+    if tabs is not None:
+        def step_unfolded():
+            st.hydra_draft(h, E, W1, b1, W2, cond, topk, root_tok, tree, node_tok=node_tok, node_logit=node_logit,
+                           node_logprob=node_logprob, ws=ws_d)
+            attention()
+            accept()
+        for _ in range(3):
+            step_unfolded()
+            flush()
+        uev = []
+        tu0 = time.time()
+        for _ in range(args.steps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            step_unfolded()
+            b.record(stream)
+            uev.append((a, b))
+            flush()
+        torch.cuda.synchronize()
+        tu1 = time.time()
+        u_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in uev) / len(uev), dev)
+        unfolded = {"value": world * 1000.0 / u_ms, "unit": UNIT, "ms_per_step": u_ms,
+                    "draft_first_layer": "whole W1 streamed per step", "clocks": clocks.summary(tu0, tu1)}
     time.sleep(0.3)
     clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in evs]
@@ -446,10 +470,19 @@ def run_ours(args):
                "ms_per_step": e_mean, "copies_per_step": {"h2d": 2, "d2h": 1},
                "overlap": "the attention/acceptance inputs upload on a copy stream while the draft runs"}
 
-    # CPU baseline: the oracle as it stands, one full step of the same workload
+    # every other config of the parity suite, one entry point per entry, each with its own roofline
+    # and the clock record of its own timed window (rank 0 only)
+    configs = None
+    if rank == 0 and not args.no_configs:
+        tabs = None   # the headline's fold tables (2.1 GB) are not needed any more
+        torch.cuda.empty_cache()
+        configs = run_configs(dev, local, args.steps)
+
+    # CPU baseline: the oracle as it stands, one full step of the same workload, at 1 thread and at
+    # every host thread (separate processes: BLAS threads are fixed when numpy loads)
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = time_oracle_step(w, parent, rank_arr, dx, ax, gx)
+        cpu = cpu_baseline_legs()
 
     if rank != 0:
         return
@@ -466,6 +499,9 @@ def run_ours(args):
         "phases_ms": phase_ms,
         "kernels": kern_table,
         "roofline": roofline,
+        "unfolded_step": unfolded,
+        "fold_tables_bytes": (sum(int(c == 1) for c in cond) * w.V * w.d * 4) if not args.no_fold else 0,
+        "configs": configs,
         "cpu_baseline": cpu,
         "e2e": e2e,
         "ms_per_step_traced": sum(traced_ms) / len(traced_ms),
@@ -475,6 +511,82 @@ def run_ours(args):
         "wall_s_timed": t_wall1 - t_wall0,
     }
     print(json.dumps(line), flush=True)
+
+
+CONFIG_ENTRIES = [
+    # (entry name, component, no_fold): every config of the parity suite that the headline step is not
+    ("1_tiny_fp32_step", "step-tiny-fp32", False),
+    ("2_vicuna7b_attention", "attention-vicuna7b", False),
+    ("2_vicuna7b_greedy_accept", "accept-greedy-vicuna7b", False),
+    ("3_hydra_heads_b4_folded", "draft-hydra-b4", False),
+    ("3_hydra_heads_b4_unfolded", "draft-hydra-b4", True),
+    ("4_70b_gqa_attention", "attention-70b-gqa", False),
+    ("5_long32k_attention_t341", "attention-32k", False),
+    ("5_long32k_attention_t256", "attention-32k-t256", False),
+    ("5_long32k_rejection_accept", "accept-rejection-32k", False),
+]
+
+
+def run_configs(dev, local, steps):
+    import torch
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    flush = L2Flush(dev)
+    out = {}
+    try:
+        for entry, name, no_fold in CONFIG_ENTRIES:
+            comp = make_component(name, dev, no_fold=no_fold)
+            out[entry] = {"component": name}
+            out[entry].update(measure_component(comp, flush, clocks, steps))
+            del comp
+            torch.cuda.synchronize()
+            torch.cuda.empty_cache()
+    finally:
+        clocks.stop()
+    return out
+
+
+def cpu_baseline_legs():
+    """The oracle timed on the host cores at 1 thread and at every thread, each in a child process."""
+    legs = {}
+    n = os.cpu_count() or 1
+    for threads in (1, n):
+        env = dict(os.environ)
+        for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "BLIS_NUM_THREADS"):
+            env[k] = str(threads)
+        env["CUDA_VISIBLE_DEVICES"] = ""
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-step"], env=env, capture_output=True,
+                           text=True, timeout=600)
+        try:
+            legs[threads] = json.loads(r.stdout.strip().splitlines()[-1])
+        except (ValueError, IndexError):
+            legs[threads] = {"error": (r.stderr or r.stdout)[-300:]}
+    full = legs.get(n, {})
+    one = legs.get(1, {})
+    return {"value": full.get("value"), "unit": UNIT, "cores": full.get("cores"), "threads": n,
+            "cores_available": n, "kind": "oracle",
+            "sample": "one full verification step of the same workload (draft heads, attention, greedy acceptance), "
+                      "NumPy float64 on the host cores; cores = CPU time / wall time",
+            "one_thread": {"value": one.get("value"), "cores": one.get("cores"), "threads": 1},
+            "all_threads": {"value": full.get("value"), "cores": full.get("cores"), "threads": n}}
+
+
+def run_oracle_step_child():
+    """Child of cpu_baseline_legs: one oracle step of the headline workload, one JSON line."""
+    import oracle
+    import spec_workloads as wl
+    w = workload(seed=2)
+    parent, rank_arr = wl.make_tree(w.tree)
+    T = len(parent)
+    dx = wl.draft_inputs(w)
+    ax = wl.attention_inputs(w, T)
+    to = oracle.tree_encode(parent, rank_arr)
+    tok = oracle.hydra_draft(dx["h"], dx["E"], dx["W1"], dx["b1"], dx["W2"], dx["cond"], dx["topk"], dx["root_tok"],
+                             to, w.dtype)["node_tok"]
+    gx = wl.greedy_inputs(w, parent, node_tok=tok)
+    r = time_oracle_step(w, parent, rank_arr, dx, ax, gx)
+    print(json.dumps(r), flush=True)
 
 
 def time_oracle_step(w, parent, rank_arr, dx, ax, gx):
@@ -535,6 +647,7 @@ def run_reference(args):
 
 COMPONENTS = {
     # name: (workload id, part, tree override)
+    "step-tiny-fp32": (1, "step", None),
     "attention-vicuna7b": (2, "attention", None),
     "attention-70b-gqa": (4, "attention", None),
     "attention-32k": (5, "attention", None),
@@ -550,18 +663,17 @@ COMPONENTS = {
 }
 
 
-def run_component(args):
-    """Time one entry point on one of the parity workloads (a separate line, not the headline step)."""
+def make_component(name, dev, no_fold=False):
+    """Inputs, outputs and the library call of one entry point on one parity workload.
+
+    Returns a dict: call (one library call), pre (untimed, before every call),
+    abytes / flops (algorithmic work per call), report (extra fields after the
+    measurement: near-tie counts and the like) and the workload facts."""
     import torch
-    _, local, _ = dist_info()
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    import __graft_entry__
-    __graft_entry__.build()
     import spec_workloads as wl
     import tree_speculative_decoding_spec_gb300 as st
 
-    wid, part, tree_spec = COMPONENTS[args.workload]
+    wid, part, tree_spec = COMPONENTS[name]
     w = wl.WORKLOADS[wid]
     parent, rank_arr = wl.make_tree(tree_spec or w.tree)
     T = len(parent)
@@ -575,7 +687,50 @@ def run_component(args):
 
     s = 2 if w.dtype == "bf16" else 4
     flops = 0.0
-    if part == "attention":
+    if part == "step":
+        # the whole verification step of the tiny fp32 workload: draft heads, attention, greedy acceptance
+        dx = wl.draft_inputs(w)
+        h, E, root = dev_t(dx["h"]), dev_t(dx["E"]), dev_t(dx["root_tok"])
+        W1 = [dev_t(a) for a in dx["W1"]]
+        b1 = [dev_t(a) for a in dx["b1"]]
+        W2 = [dev_t(a) for a in dx["W2"]]
+        cond, topk = list(w.cond), list(w.topk)
+        nt = torch.empty(w.B, T, dtype=torch.int32, device=dev)
+        nl = torch.empty(w.B, T, dtype=torch.float32, device=dev)
+        nlp = torch.empty(w.B, T, dtype=torch.float32, device=dev)
+        wsd = torch.empty(st.hydra_draft_workspace_size(tree, w.B, w.d, w.V, cond, topk, 0), dtype=torch.uint8, device=dev)
+        ax = wl.attention_inputs(w, T)
+        q, kc, vc, plen, kt, vt = (dev_t(ax[k]) for k in ("q", "k_cache", "v_cache", "prefix_len", "k_tree", "v_tree"))
+        out = torch.empty(w.B, w.Hq, T, w.D, dtype=torch.float32, device=dev)
+        lse = torch.empty(w.B, w.Hq, T, dtype=torch.float32, device=dev)
+        wsa = torch.empty(st.tree_attention_workspace_size(tree, w.B, w.Hq, w.Hkv, w.Lmax, w.D, 0), dtype=torch.uint8,
+                          device=dev)
+        gx = wl.greedy_inputs(w, parent)
+        lp = dev_t(gx["logits_p"])
+        outs = [torch.empty(w.B, dtype=torch.int32, device=dev),
+                torch.empty(w.B, tree.max_depth + 1, dtype=torch.int32, device=dev),
+                torch.empty(w.B, dtype=torch.int32, device=dev), torch.empty(w.B, dtype=torch.float32, device=dev)]
+        wsc = torch.empty(st.tree_accept_workspace_size(0, tree, w.B, w.V), dtype=torch.uint8, device=dev)
+
+        def call():
+            st.hydra_draft(h, E, W1, b1, W2, cond, topk, root, tree, node_tok=nt, node_logit=nl, node_logprob=nlp,
+                           ws=wsd)
+            st.tree_attention(q, kc, vc, plen, kt, vt, tree, out=out, lse=lse, ws=wsa)
+            st.tree_accept(0, lp, None, nt, tree, accept_len=outs[0], accept_path=outs[1], next_token=outs[2],
+                           margin=outs[3], ws=wsc)
+        d, V, L = w.d, w.V, [int(x) for x in ax["prefix_len"]]
+        abytes = 0.0
+        for k in range(len(cond)):
+            n_int = tree.struct.n_internal_at_depth[k]
+            if n_int:
+                rows = w.B * n_int if cond[k] else w.B
+                d_in = d * (2 if cond[k] else 1)
+                abytes += (d * d_in + d + V * d) * s + rows * (d_in + d) * s
+                flops += 2.0 * rows * (d_in * d + d * V)
+        abytes += (sum(L) * w.Hkv * w.D * 2 * s + w.B * w.Hq * T * w.D * s + w.B * w.Hkv * T * w.D * 2 * s
+                   + w.B * w.Hq * T * (w.D + 1) * 4) + w.B * T * w.V * 4
+        flops += 4.0 * w.D * w.Hq * T * sum(l + T for l in L)
+    elif part == "attention":
         ax = wl.attention_inputs(w, T)
         q, kc, vc, plen, kt, vt = (dev_t(ax[k]) for k in ("q", "k_cache", "v_cache", "prefix_len", "k_tree", "v_tree"))
         out = torch.empty(w.B, w.Hq, T, w.D, dtype=torch.float32, device=dev)
@@ -622,7 +777,7 @@ def run_component(args):
         nl = torch.empty(w.B, T, dtype=torch.float32, device=dev)
         nlp = torch.empty(w.B, T, dtype=torch.float32, device=dev)
         ws = torch.empty(st.hydra_draft_workspace_size(tree, w.B, w.d, w.V, cond, topk, 1), dtype=torch.uint8, device=dev)
-        tabs = None if args.no_fold else [st.hydra_fold_embedding(W1[k], E) if c == 1 else None for k, c in enumerate(cond)]
+        tabs = None if no_fold else [st.hydra_fold_embedding(W1[k], E) if c == 1 else None for k, c in enumerate(cond)]
         call = lambda: st.hydra_draft(h, E, W1, b1, W2, cond, topk, root, tree, node_tok=nt, node_logit=nl,
                                       node_logprob=nlp, ws=ws, folded=tabs)
         abytes, d, V = 0.0, w.d, w.V
@@ -708,10 +863,66 @@ def run_component(args):
         call = lambda: st.tree_accept(mode, lp, lq, tok, tree, temperature=w.temperature, seed=w.philox_seed,
                                       accept_len=outs[0], accept_path=outs[1], next_token=outs[2], margin=outs[3], ws=ws)
 
-    flush = L2Flush(dev)
-    stream = torch.cuda.current_stream()
     if part != "commit":
         pre = lambda: None
+    comp = {"name": name, "config_id": wid, "dtype": w.dtype, "tree_nodes": T, "call": call, "pre": pre,
+            "abytes": abytes, "flops": flops, "report": lambda: {}, "kernel_work": {}}
+    # algorithmic work per launch of the kernels whose roofline the entry reports
+    if part in ("attention", "attention_paged"):
+        comp["kernel_work"]["attn_tc"] = (abytes - w.B * w.Hq * T * (w.D + 1) * 4, flops)
+    elif part == "draft":
+        heads = [k for k in range(len(w.cond)) if tree.struct.n_internal_at_depth[k]]
+        rows = [w.B * tree.struct.n_internal_at_depth[k] if w.cond[k] else w.B for k in heads]
+        comp["kernel_work"]["draft_proj_tc"] = (sum(w.V * w.d * s + r * w.d * s for r in rows) / len(rows),
+                                                sum(2.0 * r * w.d * w.V for r in rows) / len(rows))
+    elif part == "accept":
+        comp["kernel_work"]["accept_rows_greedy" if w.accept == "greedy" else "accept_rows_lse"] = (abytes, 0.0)
+    if part == "draft":
+        def near_ties():
+            # the drafted top-k ranks that sit within the bf16 tie tolerance (1e-3 |logit|) of the
+            # next rank in the GPU's own logits (siblings of consecutive ranks)
+            tok_l = nl.cpu().numpy()
+            ties, pairs = 0, 0
+            for u in range(T):
+                kids = [c for c in range(1, T) if parent[c] == u]
+                by_rank = {int(rank_arr[c]): c for c in kids}
+                for r in by_rank:
+                    if r + 1 in by_rank:
+                        a_, b_ = tok_l[:, by_rank[r]], tok_l[:, by_rank[r + 1]]
+                        pairs += a_.size
+                        ties += int(np.sum(np.abs(a_ - b_) <= 1e-3 * np.abs(a_)))
+            return {"near_ties": ties, "sibling_pairs_checked": pairs,
+                    "near_tie_rule": "consecutive-rank siblings within 1e-3 x |logit| (bf16 tie tolerance)"}
+        comp["report"] = near_ties
+        comp["folded"] = tabs is not None
+    if part == "accept" and w.accept == "rejection":
+        def near_threshold(n_offsets=64):
+            # |u - p/q| < 1e-6 decisions and CDF-breakpoint draws within 1e-6 of the total, over
+            # n_offsets Philox offsets (the margin output is the smallest such distance per sequence)
+            margins, lens = [], []
+            for off in range(n_offsets):
+                st.tree_accept(mode, lp, lq, tok, tree, temperature=w.temperature, seed=w.philox_seed, offset=off,
+                               accept_len=outs[0], accept_path=outs[1], next_token=outs[2], margin=outs[3], ws=ws)
+                margins.append(outs[3].cpu().numpy().copy())
+                lens.append(outs[0].cpu().numpy().copy())
+            m = np.concatenate(margins)
+            return {"offsets": n_offsets, "near_threshold": int(np.sum(m < 1e-6)), "min_margin": float(m.min()),
+                    "near_threshold_rule": "smallest |u - p/q| over decided edges, or the draw's distance to a CDF "
+                                           "breakpoint over the total, below 1e-6",
+                    "mean_accept_len": float(np.concatenate(lens).mean())}
+        comp["report"] = near_threshold
+    if part == "accept" and w.accept == "greedy":
+        comp["report"] = lambda: {"exact_argmax_ties": int(np.sum(outs[3].cpu().numpy() == 0.0))}
+    return comp
+
+
+def measure_component(comp, flush, clocks, steps, min_wall_s=0.4):
+    """CUDA-event time of one call (L2 flushed before each), a traced pass for
+    per-kernel times, the clock record of the timed window, and the roofline."""
+    import torch
+    import tree_speculative_decoding_spec_gb300 as st
+    stream = torch.cuda.current_stream()
+    call, pre = comp["call"], comp["pre"]
 
     def timed(n):
         evs = []
@@ -726,24 +937,65 @@ def run_component(args):
         torch.cuda.synchronize()
         return [a.elapsed_time(b) for a, b in evs]
 
-    timed(max(args.warmup, 3))
-    ms = timed(args.steps)
+    timed(3)
+    ms = []
+    t0 = time.time()
+    while len(ms) < steps or time.time() - t0 < min_wall_s:
+        ms += timed(max(steps // 2, 5))
+    t1 = time.time()
     st.spec_trace_begin(100000)
-    timed(args.steps)
+    timed(max(steps // 2, 5))
     kernels = st.spec_trace_end(64)
     us = 1000.0 * statistics.median(ms)
     hbm, tf_burst, _, src = peaks()
-    line = {
-        "workload": args.workload, "config_id": wid, "impl": "ours", "metric": "calls/s", "value": 1e6 / us,
-        "us_per_call": us, "dtype": w.dtype, "steps": args.steps, "tree_nodes": T,
-        "algorithmic_bytes": abytes, "flops": flops,
-        "hbm_GBps": abytes / us / 1e3, "hbm_frac": abytes / us / 1e3 / hbm,
-        "tensor_TFLOPs": flops / us / 1e6 if flops else None,
-        "tensor_frac": (flops / us / 1e6) / tf_burst if flops else None,
-        "roofline_us": max(abytes / hbm / 1e3, flops / tf_burst / 1e6),
-        "peak_source": src,
-        "kernels": {k: {"launches": n, "us_per_launch": 1000.0 * t / n} for k, (n, t) in kernels.items()},
-    }
+    abytes, flops = comp["abytes"], comp["flops"]
+    t_hbm, t_tc = abytes / hbm / 1e3, (flops / tf_burst / 1e6 if flops else 0.0)
+    bound = "tensor" if t_tc > t_hbm else "hbm"
+    kern = {k: {"launches": n, "us_per_launch": 1000.0 * t / n} for k, (n, t) in kernels.items()}
+    # the kernel roofline: the entry's main kernel, its algorithmic work per launch over its mean
+    # traced launch time; entries without one (the tiny launch-bound step) report the call's
+    work = [(k, kw) for k, kw in comp["kernel_work"].items() if k in kern]
+    if work:
+        dom, (kb, kf) = max(work, key=lambda x: kern[x[0]]["us_per_launch"] * kern[x[0]]["launches"])
+        dom_us = kern[dom]["us_per_launch"]
+    else:
+        dom, kb, kf, dom_us = "whole call", abytes, flops, us
+    k_bound = "tensor" if kf / tf_burst / 1e6 > kb / hbm / 1e3 else "hbm"
+    if k_bound == "tensor":
+        ach = kf / dom_us / 1e6
+        roof = {"bound": "tensor", "kernel": dom, "achieved": ach, "peak": tf_burst, "unit": "TFLOP/s",
+                "frac": ach / tf_burst, "kernel_us": dom_us, "kernel_flops": kf}
+    else:
+        ach = kb / dom_us / 1e3
+        roof = {"bound": "hbm", "kernel": dom, "achieved": ach, "peak": hbm, "unit": "GB/s",
+                "frac": ach / hbm, "kernel_us": dom_us, "kernel_bytes": kb}
+    roof["call_bound"] = bound
+    roof.update({"peak_source": src, "call_hbm_frac": abytes / us / 1e3 / hbm,
+                 "call_tensor_frac": (flops / us / 1e6) / tf_burst if flops else None,
+                 "roofline_us": max(t_hbm, t_tc), "algorithmic_bytes": abytes, "flops": flops})
+    out = {"us_per_call": us, "calls_per_s": 1e6 / us, "calls_timed": len(ms), "kernels": kern, "roofline": roof,
+           "clocks": clocks.summary(t0, t1) if clocks is not None else None}
+    out.update(comp["report"]())
+    return out
+
+
+def run_component(args):
+    """Time one entry point on one of the parity workloads (a separate line, not the headline step)."""
+    import torch
+    _, local, _ = dist_info()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import __graft_entry__
+    __graft_entry__.build()
+    comp = make_component(args.workload, dev, no_fold=args.no_fold)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.5)
+    m = measure_component(comp, L2Flush(dev), clocks, args.steps)
+    clocks.stop()
+    line = {"workload": args.workload, "config_id": comp["config_id"], "impl": "ours", "metric": "calls/s",
+            "value": m["calls_per_s"], "dtype": comp["dtype"], "steps": args.steps, "tree_nodes": comp["tree_nodes"]}
+    line.update(m)
     print(json.dumps(line), flush=True)
 
 
@@ -759,7 +1011,12 @@ def main():
                     help="draft heads stream their whole first layer (no folded embedding tables)")
     ap.add_argument("--workload", choices=["step"] + sorted(COMPONENTS), default="step",
                     help="step (default): the headline verification step; otherwise one entry point on one workload")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-config entries of the default line")
+    ap.add_argument("--oracle-step", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_step:
+        run_oracle_step_child()
+        return
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":

@@ -71,6 +71,32 @@ struct AttnTcParams {
     float* lse;
 };
 
+// Packed two-lane fp32 arithmetic (sm_100 family): one instruction for a pair of
+// scores halves the softmax's FFMA and FADD count, and the 3-input max does the
+// same for the row maximum.
+__device__ __forceinline__ unsigned long long pk2(float a, float b) {
+    unsigned long long r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+__device__ __forceinline__ void upk2(unsigned long long r, float& a, float& b) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ unsigned long long ffma2(unsigned long long a, unsigned long long b, unsigned long long c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ unsigned long long fadd2(unsigned long long a, unsigned long long b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -306,12 +332,10 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             float mx[16];
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-                mx[e] = fmaxf(fmaxf(fmaxf(sv[e], sv[e + 16]), fmaxf(sv[e + 32], sv[e + 48])),
-                              fmaxf(fmaxf(sv[e + 64], sv[e + 80]), fmaxf(sv[e + 96], sv[e + 112])));
-#pragma unroll
-            for (int w2 = 8; w2 > 0; w2 >>= 1)
-#pragma unroll
-                for (int e = 0; e < w2; ++e) mx[e] = fmaxf(mx[e], mx[e + w2]);
+                mx[e] = fmax3(fmax3(sv[e], sv[e + 16], sv[e + 32]), fmax3(sv[e + 48], sv[e + 64], sv[e + 80]),
+                              fmax3(sv[e + 96], sv[e + 112], -INFINITY));
+            mx[0] = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmax3(mx[6], mx[7], mx[8]));
+            mx[0] = fmax3(fmax3(mx[0], mx[9], mx[10]), fmax3(mx[11], mx[12], mx[13]), fmaxf(mx[14], mx[15]));
             const float tmax = mx[0] * p.scale_log2;   // base-2 units
             // lazy rescale: keep the old reference maximum unless the row max grew by > 2^8; the
             // TMEM accesses are warp-collective, so a warp rescales together (alpha = 1 for the rest)
@@ -337,24 +361,29 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                 l *= alpha;
             }
             m_used = m_new;
-            // P = 2^(scale * s - m_used) in bf16 (one FFMA + ex2 per score), written over the
-            // first 64 columns of this group's score buffer; row sum in fp32 over 4 partials
+            // P = 2^(scale * s - m_used) in bf16 (one packed FFMA per pair of scores, one ex2 per
+            // score), written over the first 64 columns of this group's score buffer; row sum in
+            // fp32 over 4 partials of packed adds
             const float nmref = m_used == -INFINITY ? 0.f : -m_used;
             float ps[4];
 #pragma unroll
             for (int qc = 0; qc < 4; ++qc) {
                 uint32_t packed[16];
-                float acc = 0.f;
+                unsigned long long acc2 = pk2(0.f, 0.f);
+                const unsigned long long sc2 = pk2(p.scale_log2, p.scale_log2), nm2 = pk2(nmref, nmref);
 #pragma unroll
                 for (int h2 = 0; h2 < 16; ++h2) {
                     const int e0 = qc * 32 + 2 * h2;
-                    const float a0 = ex2(fmaf(sv[e0], p.scale_log2, nmref));
-                    const float a1 = ex2(fmaf(sv[e0 + 1], p.scale_log2, nmref));
-                    acc += a0 + a1;
+                    float x0, x1;
+                    upk2(ffma2(pk2(sv[e0], sv[e0 + 1]), sc2, nm2), x0, x1);
+                    const float a0 = ex2(x0), a1 = ex2(x1);
+                    acc2 = fadd2(acc2, pk2(a0, a1));
                     const __nv_bfloat162 pr = __floats2bfloat162_rn(a0, a1);   // .x (lower key) low
                     packed[h2] = *reinterpret_cast<const uint32_t*>(&pr);
                 }
-                ps[qc] = acc;
+                float acc0, acc1;
+                upk2(acc2, acc0, acc1);
+                ps[qc] = acc0 + acc1;
                 tmem_st16(lane_base + s_col + qc * 16, packed);
             }
             l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
