@@ -210,8 +210,11 @@ __global__ void __launch_bounds__(256) k_attn_fma(const T* __restrict__ q, const
 // row's split partials (max m_c in base 2, sum l_c, unnormalised O_c):
 // O = sum_c 2^(m_c - M) O_c / sum_c 2^(m_c - M) l_c, lse = (M + log2 l) ln 2.
 // Slots read: the non-empty prefix splits, plus the tree slot n_pre unless the
-// tree keys were folded into the last prefix split (tensor-core layout).
-constexpr int kCombineGroup = 4;   // partials whose loads a combine warp issues together
+// tree keys were folded into the last prefix split (tensor-core layout).  The
+// partials are taken kCombineGroup at a time, every load of a group (m, l and
+// the lane's 4 O values of each partial) issued together, with a running
+// maximum across groups: one memory round trip per group.
+constexpr int kCombineGroup = 4;
 
 __global__ void __launch_bounds__(256) k_attn_combine(const float* __restrict__ part, const int32_t* __restrict__ prefix_len,
                                                       int Tn, int Hq, int D, int Lmax, int chunk, int n_pre, int folded,
@@ -230,9 +233,6 @@ __global__ void __launch_bounds__(256) k_attn_combine(const float* __restrict__ 
     float M = -INFINITY;
     float l = 0.f;
     float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int i = lane; i < nread; i += 32) M = fmaxf(M, base[static_cast<size_t>(slot(i)) * (D + 4)]);
-    M = warp_max(M);
-    // the partials in groups of kCombineGroup, each group's loads issued together
     for (int i0 = 0; i0 < nread; i0 += kCombineGroup) {
         float pm[kCombineGroup], pl[kCombineGroup];
         float4 pv[kCombineGroup];
@@ -243,19 +243,27 @@ __global__ void __launch_bounds__(256) k_attn_combine(const float* __restrict__ 
             pv[j] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (i0 + j < nread) {
                 const float* pc = base + static_cast<size_t>(slot(i0 + j)) * (D + 4);
-                pm[j] = pc[0];
-                pl[j] = pc[1];
+                const float2 ml = *reinterpret_cast<const float2*>(pc);
+                pm[j] = ml.x;
+                pl[j] = ml.y;
                 if (has) pv[j] = *reinterpret_cast<const float4*>(pc + 4 + 4 * lane);
             }
         }
+        float gm = pm[0];
+#pragma unroll
+        for (int j = 1; j < kCombineGroup; ++j) gm = fmaxf(gm, pm[j]);
+        const float Mn = fmaxf(M, gm);
+        if (Mn == -INFINITY) continue;   // nothing but empty partials so far
+        const float sc = M == -INFINITY ? 0.f : exp2f(M - Mn);
+        l *= sc;
+        o.x *= sc; o.y *= sc; o.z *= sc; o.w *= sc;
 #pragma unroll
         for (int j = 0; j < kCombineGroup; ++j) {
-            const float w = pm[j] == -INFINITY ? 0.f : exp2f(pm[j] - M);
+            const float w = pm[j] == -INFINITY ? 0.f : exp2f(pm[j] - Mn);
             l += w * pl[j];
-            if (has && w != 0.f) {
-                o.x += w * pv[j].x; o.y += w * pv[j].y; o.z += w * pv[j].z; o.w += w * pv[j].w;
-            }
+            o.x += w * pv[j].x; o.y += w * pv[j].y; o.z += w * pv[j].z; o.w += w * pv[j].w;
         }
+        M = Mn;
     }
     if (has) {
         const float inv = 1.f / l;
@@ -366,16 +374,15 @@ static spec_status run_checked(const void* q, const void* k_cache, const void* v
     const Plan p = make_plan(tree, B, Hq, Hkv, Lmax, D, dt);
     if (!ws || ws_bytes < p.total) return fail(SPEC_EWORKSPACE, "workspace %zu bytes < %zu needed", ws_bytes, p.total);
     if (!aligned16(ws)) return fail(SPEC_EALIGN, "workspace must be 16-byte aligned");
-    SPEC_CUDA_TRY(reset_device_status(ws, s));
     if (dt == SPEC_BF16) {
         using T = __nv_bfloat16;
+        SPEC_CUDA_TRY(reset_device_status(ws, s));
         if (p.tc) {
             float* part = reinterpret_cast<float*>(static_cast<unsigned char*>(ws) + kWsHeader);
             st = tc::attn_tc_run(p.tcp, static_cast<const T*>(q), static_cast<const T*>(k_cache),
                                  static_cast<const T*>(v_cache), prefix_len, static_cast<const T*>(k_tree),
                                  static_cast<const T*>(v_tree), tree, B, Hq, Hkv, Lmax, scale, part, out, lse, ws, s, pg);
-            if (st != SPEC_OK) return st;
-            if (p.tcp.fused) return SPEC_OK;   // the splits merged on chip
+            if (st != SPEC_OK || p.tcp.fused || p.tcp.n_pre == 1) return st;   // merged on chip, or one split
             const int nrows = B * Hq * tree->T;
             SPEC_CUDA_TRY(launch_ex("attn_combine", k_attn_combine, dim3((nrows + 7) / 8), dim3(256), 0, s, true, part,
                                  prefix_len, tree->T, Hq, D, Lmax, p.tcp.chunk, p.tcp.n_pre, 1, nrows, out, lse));
@@ -385,6 +392,7 @@ static spec_status run_checked(const void* q, const void* k_cache, const void* v
                           prefix_len, static_cast<const T*>(k_tree), static_cast<const T*>(v_tree), tree, B, Hq, Hkv,
                           Lmax, D, scale, out, lse, ws, p, s, pg);
     }
+    SPEC_CUDA_TRY(reset_device_status(ws, s));
     return run_fma<float>(static_cast<const float*>(q), static_cast<const float*>(k_cache),
                           static_cast<const float*>(v_cache), prefix_len, static_cast<const float*>(k_tree),
                           static_cast<const float*>(v_tree), tree, B, Hq, Hkv, Lmax, D, scale, out, lse, ws, p, s, pg);

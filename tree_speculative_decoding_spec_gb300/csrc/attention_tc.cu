@@ -21,11 +21,12 @@
 //             base 2 (O is rescaled in TMEM only when the maximum grows by
 //             more than 2^8) and writes P_j as bf16 pairs over the first 64
 //             columns of its own score buffer.  At the end group 0 merges the
-//             two groups' (max, sum, O) into the split's partial: in HBM for
-//             the combine kernel, or -- when the splits of a (head, row block,
-//             sequence) run as one thread-block cluster -- in the CTA's own
-//             shared memory, merged across the cluster over distributed shared
-//             memory into out and lse (see the end of the kernel).
+//             two groups' (max, sum, O): with a single split it writes out and
+//             lse directly; otherwise the split's partial goes to HBM for the
+//             combine kernel, or -- when the splits of a (head, row block,
+//             sequence) run as one thread-block cluster -- it stays in the
+//             CTA's own shared memory and is merged across the cluster over
+//             distributed shared memory (see the end of the kernel).
 // The tensor pipe runs its MMAs in issue order, so S_{j+2} may overwrite the
 // buffer PV_j reads, and the completion of S_j implies that of PV_{j-2}.
 // Cache rows past the prefix length inside the last prefix tile are zeroed in
@@ -121,6 +122,7 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     const int n_pt = pre_end > pre_begin ? (pre_end - pre_begin + kAKeys - 1) / kAKeys : 0;
     const int n_pref = (L + p.chunk - 1) / p.chunk;          // non-empty prefix splits
     const bool has_tree = (c == max(n_pref - 1, 0));          // this split also takes the tree keys
+    const bool direct = p.n_pre == 1;                         // one split: write out and lse here
     const int n_tt = has_tree ? (p.T + kAKeys - 1) / kAKeys : 0;
     const int n_tiles = n_pt + n_tt;
     if (n_tiles == 0 && !p.fused) return;   // whole CTA: nothing allocated yet (a fused one still merges)
@@ -167,7 +169,7 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    griddep_launch();   // the combine may start launching: it waits for the partials
+    griddep_launch();   // the next kernel on the stream may start launching
     const int kvc_row0 = (b * p.Hkv + kvh) * p.Lmax + pre_begin;   // first prefix key of this split
     const int kvt_row0 = (b * p.Hkv + kvh) * p.T;                  // first tree key
     const int q_row0 = (b * p.Hq + kvh * p.g) * p.T + rb * kARows;
@@ -417,17 +419,24 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             const float a0 = m_used == -INFINITY ? 0.f : ex2(m_used - m);
             const float a1 = g1.x == -INFINITY ? 0.f : ex2(g1.x - m);
             const bool valid = rg < p.T * p.g;
-            float* dst = nullptr;
+            const size_t out_row = (static_cast<size_t>(b) * p.Hq + kvh * p.g + rg / p.T) * p.T + rg % p.T;
+            const float lsum = a0 * l + a1 * g1.y;
+            float* dst = nullptr;   // (m, l, -, -, O[kAD]) partial at dst, or the output row itself when direct
+            int o_off = 4;          // first O float at dst
+            float scale_o = 1.f;
             if (p.fused) {   // this CTA's partial stays in its own shared memory (the drained K/V ring)
                 dst = reinterpret_cast<float*>(sKV) + r * kFPStride;
+            } else if (valid && direct) {
+                dst = p.out + out_row * kAD;
+                o_off = 0;
+                scale_o = 1.f / lsum;
+                if (p.lse) p.lse[out_row] = (m + log2f(lsum)) * 0.6931471805599453f;
             } else if (valid) {
-                const int hl = rg / p.T, i = rg % p.T;
-                const size_t row = (static_cast<size_t>(b) * p.Hq + kvh * p.g + hl) * p.T + i;
-                dst = p.part + (row * (p.n_pre + 1) + c) * (kAD + 4);
+                dst = p.part + (out_row * (p.n_pre + 1) + c) * (kAD + 4);
             }
-            if (dst) {
+            if (dst && !direct) {
                 dst[0] = m;
-                dst[1] = a0 * l + a1 * g1.y;
+                dst[1] = lsum;
             }
 #pragma unroll 1
             for (int cc = 0; cc < kAD / 32; ++cc) {
@@ -442,9 +451,9 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
 #pragma unroll
                         for (int t = 0; t < 4; ++t) {
                             const float x0 = a0 * __uint_as_float(o0[4 * e + t]);
-                            v[t] = a1 != 0.f ? x0 + a1 * __uint_as_float(o1[4 * e + t]) : x0;   // group 1 may own no tile
+                            v[t] = (a1 != 0.f ? x0 + a1 * __uint_as_float(o1[4 * e + t]) : x0) * scale_o;   // group 1 may own no tile
                         }
-                        *reinterpret_cast<float4*>(dst + 4 + cc * 32 + 4 * e) = make_float4(v[0], v[1], v[2], v[3]);
+                        *reinterpret_cast<float4*>(dst + o_off + cc * 32 + 4 * e) = make_float4(v[0], v[1], v[2], v[3]);
                     }
                 }
             }
@@ -575,7 +584,7 @@ static int max_active_clusters(int n) {
 // non-empty split of each sequence also takes the tree keys.  Pick the split
 // count minimising an estimated makespan -- waves of one CTA per SM times the
 // longest CTA (its prefix tiles, the tree tiles, ~2 tiles of fixed cost) --
-// ties to fewer splits (less combine traffic).
+// ties to fewer splits (less partial traffic).
 AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_count) {
     AttnTcPlan p;
     const int g = Hq / Hkv;
@@ -599,10 +608,12 @@ AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_c
     // merge on chip only when every cluster is resident at once: a cluster starts only when
     // n_pre SMs of one GPC are free together, so a second wave of clusters leaves SMs idle
     // (32K prefix, 96 clusters of 3: 203 -> 296 us), and the one-split plans (a cluster of
-    // one) gain nothing over the combine kernel
+    // one) write their output directly anyway
     p.fused = p.n_pre > 1 && p.n_pre <= kFusedMaxSplits && base <= max_active_clusters(p.n_pre);
-    // partial layout shared with the CUDA-core path: n_pre + 1 slots per row (the last unused here)
-    p.part_bytes = sizeof(float) * static_cast<size_t>(B) * Hq * T * (p.n_pre + 1) * (D + 4);
+    // partial layout shared with the CUDA-core path: n_pre + 1 slots per row (the last unused
+    // here); none with a single split or an on-chip merge
+    p.part_bytes = (p.n_pre == 1 || p.fused)
+                       ? 0 : sizeof(float) * static_cast<size_t>(B) * Hq * T * (p.n_pre + 1) * (D + 4);
     return p;
 }
 
