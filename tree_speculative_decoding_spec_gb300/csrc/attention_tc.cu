@@ -104,6 +104,34 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// The sequence of grid slot z: sequences in order of decreasing prefix length
+// (ties to the lower index).  CTAs start in grid order, so the longest work
+// starts first and the shorter fills in behind it as SMs free up
+// (longest-processing-time-first); variable prefix lengths would otherwise
+// leave a second wave led by a long sequence.  Each warp ranks up to 64
+// sequences on its own (two per lane); larger batches keep the identity.
+__device__ __forceinline__ int longest_first(const int32_t* __restrict__ prefix_len, int B, int z) {
+    if (B <= 1 || B > 64) return z;
+    const int lane = threadIdx.x & 31;
+    int found = -1;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int i = lane + 32 * h;
+        int rank = -1;
+        if (i < B) {
+            const int li = prefix_len[i];
+            rank = 0;
+            for (int j = 0; j < B; ++j) {
+                const int lj = prefix_len[j];
+                rank += (lj > li) || (lj == li && j < i);
+            }
+        }
+        const unsigned hit = __ballot_sync(0xffffffffu, rank == z);
+        if (hit) found = 32 * h + __ffs(hit) - 1;
+    }
+    return found < 0 ? z : found;
+}
+
 // Named barrier for the 256 softmax threads (warps 0-7).
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
@@ -115,7 +143,7 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                                                           const AttnTcParams p) {
     const int c = blockIdx.x;
     const int kvh = blockIdx.y / p.n_rb, rb = blockIdx.y % p.n_rb;
-    const int b = blockIdx.z;
+    const int b = longest_first(p.prefix_len, gridDim.z, blockIdx.z);
     const int L = min(max(p.prefix_len[b], 0), p.Lmax);
     const int pre_begin = c * p.chunk;
     const int pre_end = min(L, pre_begin + p.chunk);
