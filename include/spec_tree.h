@@ -166,9 +166,12 @@ size_t hydra_fold_table_bytes(int32_t d, int32_t V);
  *   W1   device [d, 2d] in dt (the head's first layer, out x in)
  *   emb  device [V, d] in dt
  *   tab  device fp32 [V, d] out (hydra_fold_table_bytes bytes, caller-owned)
- * fp32 accumulation in a fixed order per element.  All pointers 16-byte
- * aligned (SPEC_EALIGN); SPEC_EINVAL on NULL or out-of-range shapes.  Launched
- * on s, asynchronous.
+ * fp32 accumulation in a fixed order per element: bf16 inputs on the tensor
+ * cores (256 vocabulary rows per launch), fp32 inputs on the CUDA cores.  All
+ * pointers 16-byte aligned (SPEC_EALIGN); SPEC_EINVAL on NULL or out-of-range
+ * shapes.  Launched on s, asynchronous.  The call has no workspace, so no
+ * device status: its kernels' bounded waits cannot run out unless the GPU
+ * stops making progress, and then the table is left undefined.
  */
 spec_status hydra_fold_embedding(const void* W1, const void* emb, int32_t d, int32_t V, spec_dtype dt,
                                  float* tab, spec_stream_t s);

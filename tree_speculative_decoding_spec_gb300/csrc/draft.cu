@@ -1211,6 +1211,13 @@ extern "C" spec_status hydra_fold_embedding(const void* W1, const void* emb, int
     if (!W1 || !emb || !tab) return fail(SPEC_EINVAL, "W1, emb and tab must not be NULL");
     if (!aligned16(W1) || !aligned16(emb) || !aligned16(tab)) return fail(SPEC_EALIGN, "W1, emb and tab must be 16-byte aligned");
     cudaStream_t s = reinterpret_cast<cudaStream_t>(s_);
+    if (dt == SPEC_BF16 && tc::draft_tc_supported(d, V)) {
+        // tab[v, m] = W1[m, d:2d] . emb[v] on the tensor cores: the head-layer GEMM with the
+        // embedding half of W1 (row stride 2d) as the weights, the vocabulary as the
+        // activation rows (256 per launch) and an identity epilogue writing fp32 rows
+        return tc::mlp_tc(static_cast<const __nv_bfloat16*>(W1) + d, nullptr, d, static_cast<const __nv_bfloat16*>(emb),
+                          d, d, V, 0, 1, 0, 0, nullptr, nullptr, tab, nullptr, s, 2 * d);
+    }
     // tab[v, m] = W1[m, d:2d] . emb[v]: the CUDA-core GEMM with the embedding half of W1
     // (row stride 2d) as the weights and the vocabulary as the rows, in chunks of grid rows
     const int chunk = 65535 * draft::GBN;

@@ -57,7 +57,7 @@ struct UmmaParams {
     draft::Cand* part_c;
     float2* part_l;
     int kmax;
-    void* ws;           // status word
+    void* ws;           // status word (NULL: a timeout goes unrecorded)
     // MLP finish (cluster of a weight tile's splits): y = act(sum + bias) (+ h_b when h is
     // set), written as bf16 to z or, when zf is set, as fp32 to zf
     const __nv_bfloat16* bias;
@@ -70,6 +70,10 @@ struct UmmaParams {
     // completes after the previous one) starts without waiting for it
     int dep_k0;
     int act;            // MLP: 1 SiLU, 0 identity
+    // MLP with more activation rows than one MMA N: grid z indexes groups of group_rows
+    // rows (0: a single group of n_valid rows); rows_total bounds the last group
+    int group_rows;
+    int rows_total;
     float* zf;          // MLP: fp32 output instead of z
 };
 
@@ -95,6 +99,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * kBM;
     const int it0 = blockIdx.y * p.k_iters;
+    const int grow0 = p.group_rows ? static_cast<int>(blockIdx.z) * p.group_rows : 0;   // first row of the group
+    const int n_valid = p.group_rows ? min(p.group_rows, p.rows_total - grow0) : p.n_valid;
+    const int row0 = p.row0 + grow0;
     // stage i of this CTA covers K stage it0 + (i + rot) mod n_it
     const int rot = kRotateK ? static_cast<int>(blockIdx.x % max(1, min(p.k_iters, p.total_iters - it0))) : 0;
     const int n_it = max(0, min(p.k_iters, p.total_iters - it0));
@@ -141,12 +148,12 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
             if (!independent) griddep_wait();
             for (int i = 0; i < pre; ++i)
                 for (int kb = 0; kb < kKB; ++kb)
-                    tma_load_2d(sB + i * stage_b + kb * box_b, &tmB, &full[i], (it0 + (i + rot) % n_it) * kBKS + kb * kBK, 0);
+                    tma_load_2d(sB + i * stage_b + kb * box_b, &tmB, &full[i], (it0 + (i + rot) % n_it) * kBKS + kb * kBK, grow0);
             issued = pre;
             for (int i = pre; i < n_it; ++i) {
                 const int s = i % p.stages;
                 if (!mbar_wait(&empty[s], ((i / p.stages) - 1) & 1)) {
-                    flag_status(p.ws, SPEC_ETIMEOUT);
+                    if (p.ws) flag_status(p.ws, SPEC_ETIMEOUT);
                     *abort_flag = 1;
                     break;
                 }
@@ -155,7 +162,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
                 const int kx = (it0 + (i + rot) % n_it) * kBKS;
                 for (int kb = 0; kb < kKB; ++kb) {
                     load_w(sA + s * kStageA + kb * kBoxA, &full[s], kx + kb * kBK);
-                    tma_load_2d(sB + s * stage_b + kb * box_b, &tmB, &full[s], kx + kb * kBK, 0);
+                    tma_load_2d(sB + s * stage_b + kb * box_b, &tmB, &full[s], kx + kb * kBK, grow0);
                 }
                 issued = i + 1;
             }
@@ -167,7 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
             for (int i = 0; i < n_it; ++i) {
                 const int s = i % p.stages;
                 if (!mbar_wait(&full[s], (i / p.stages) & 1)) {
-                    flag_status(p.ws, SPEC_ETIMEOUT);
+                    if (p.ws) flag_status(p.ws, SPEC_ETIMEOUT);
                     *abort_flag = 1;
                     break;
                 }
@@ -187,7 +194,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
     }
 
     const bool have = mbar_wait(accum, 0);
-    if (!have) flag_status(p.ws, SPEC_ETIMEOUT);
+    if (!have && p.ws) flag_status(p.ws, SPEC_ETIMEOUT);
     tc_fence_after();
     const int all_have = __syncthreads_and(have ? 1 : 0);   // one decision for the whole CTA
     const bool run_epi = all_have && !*abort_flag && n_it > 0;
@@ -201,7 +208,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
         // after a timeout; a CTA whose accumulator is not valid clears its flag and no
         // row is written.
         float* red = reinterpret_cast<float*>(smem);
-        int* ok_flag = reinterpret_cast<int*>(red + p.n_valid * kBM);
+        int* ok_flag = reinterpret_cast<int*>(red + n_valid * kBM);
         if (run_epi) {
             for (int c0 = 0; c0 < p.n_pad; c0 += 32) {
                 uint32_t r[32];
@@ -209,7 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
                 tmem_ld_wait();
 #pragma unroll
                 for (int j = 0; j < 32; ++j)
-                    if (c0 + j < p.n_valid) red[(c0 + j) * kBM + threadIdx.x] = __uint_as_float(r[j]);
+                    if (c0 + j < n_valid) red[(c0 + j) * kBM + threadIdx.x] = __uint_as_float(r[j]);
             }
         }
         if (threadIdx.x == 0) *ok_flag = run_epi ? 1 : 0;
@@ -221,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
         const int m = m0 + threadIdx.x;
         if (all_ok && m < p.M) {
             const float bias = p.bias ? __bfloat162float(p.bias[m]) : 0.f;
-            for (int n = static_cast<int>(rank); n < p.n_valid; n += nsplit) {
+            for (int n = static_cast<int>(rank); n < n_valid; n += nsplit) {
                 const uint32_t a = smem_u32(red + n * kBM + threadIdx.x);
                 float v[kMaxSplits];
 #pragma unroll
@@ -229,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
                 float x = bias;
 #pragma unroll
                 for (int sp = 0; sp < kMaxSplits; ++sp) x += v[sp];
-                const int row = p.row0 + n;
+                const int row = row0 + n;
                 const int b = p.cond ? row / p.n_int : row;
                 const float y = p.act ? x / (1.0f + expf(-x)) : x;
                 const float zz = p.h ? __bfloat162float(p.h[static_cast<size_t>(b) * p.M + m]) + y : y;
@@ -256,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
             // the 4 threads of a column are adjacent lanes and take every branch below together:
             // their shuffles use the group's own mask
             const unsigned gmask = 0xFu << (lane & ~3);
-            if (n < p.n_valid) {
+            if (n < n_valid) {
                 float xs[32];
 #pragma unroll
                 for (int i = 0; i < 32; ++i) xs[i] = v0 + i < p.V ? tile[j * 132 + q * 33 + i] : -INFINITY;
@@ -278,7 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_umma(const __grid_constant__ CU
                     if (M != -INFINITY) sm = sm * expf(mx - M) + s2 * expf(m2 - M);
                     mx = M;
                 }
-                const size_t out = static_cast<size_t>(p.row0 + n) * p.nslices + blockIdx.x;
+                const size_t out = static_cast<size_t>(row0 + n) * p.nslices + blockIdx.x;
                 if (q == 0) p.part_l[out] = make_float2(mx, mx == -INFINITY ? 0.f : sm);
                 // top-k by tournament: k rounds of (tree argmax over the thread's 32 logits,
                 // then over the 4 threads), the winner knocked out; lower index wins ties.
@@ -433,30 +440,39 @@ static spec_status launch_umma(const CUtensorMap& ta, const CUtensorMap& tb, dim
 
 spec_status mlp_tc(const __nv_bfloat16* W, const __nv_bfloat16* bias, int M, const __nv_bfloat16* X, int d_in, int ldx,
                    int R, int cond, int n_int, int dep_k0, int act, const __nv_bfloat16* residual, __nv_bfloat16* z,
-                   float* zf, void* ws, cudaStream_t s) {
+                   float* zf, void* ws, cudaStream_t s, int ldw) {
+    if (ldw == 0) ldw = d_in;
     const int total_mlp = (d_in + kBKS - 1) / kBKS;
-    // activation rows in groups of at most 256 (the MMA's largest N)
-    for (int g0 = 0; g0 < R; g0 += kMaxN) {
-        const int rows = std::min(kMaxN, R - g0);
-        const int n_pad = n_pad_of(rows);
-        // CTAs per SM by shared memory (228 KB per SM, 1 KB reserved per CTA); at most 2
-        const int resident = static_cast<int>(std::max<size_t>(
-            1, std::min<size_t>(2, 233472 / (smem_of(n_pad, stages_of(n_pad)) + 1024))));
-        const int splits = mlp_splits(M, d_in, resident);
-        const int per_split = (total_mlp + splits - 1) / splits;
+    // activation rows in groups of at most 256 (the MMA's largest N): one launch with a
+    // grid z of groups (at most 65535 per launch), the last group partial
+    const int n_pad = n_pad_of(std::min(kMaxN, R));
+    // CTAs per SM by shared memory (228 KB per SM, 1 KB reserved per CTA); at most 2
+    const int resident = static_cast<int>(std::max<size_t>(
+        1, std::min<size_t>(2, 233472 / (smem_of(n_pad, stages_of(n_pad)) + 1024))));
+    // split K only while the weight tiles of one row group leave SMs idle: with many groups
+    // (a table over the whole vocabulary) the groups fill the GPU, unsplit
+    const int64_t tiles_groups = static_cast<int64_t>((M + kBM - 1) / kBM) * ((R + kMaxN - 1) / kMaxN);
+    const int splits = tiles_groups >= static_cast<int64_t>(resident) * device_sm_count() ? 1 : mlp_splits(M, d_in, resident);
+    const int per_split = (total_mlp + splits - 1) / splits;
+    const int64_t rows_per_launch = static_cast<int64_t>(kMaxN) * 65535;
+    for (int64_t g0 = 0; g0 < R; g0 += rows_per_launch) {
+        const int rows = static_cast<int>(std::min<int64_t>(rows_per_launch, R - g0));
+        const int groups = (rows + kMaxN - 1) / kMaxN;
         CUtensorMap ta, tb;
-        SPEC_CUDA_TRY(make_tmap_bf16_2d(&ta, W, M, d_in, d_in, kBM));
+        SPEC_CUDA_TRY(make_tmap_bf16_2d(&ta, W, M, d_in, ldw, kBM));
         SPEC_CUDA_TRY(make_tmap_bf16_2d(&tb, X + static_cast<size_t>(g0) * ldx, rows, d_in, ldx, n_pad));
         UmmaParams p{};
         p.M = M;
         p.k_iters = per_split;
         p.total_iters = total_mlp;
         p.n_pad = n_pad;
-        p.n_valid = rows;
+        p.n_valid = std::min(kMaxN, rows);
+        p.group_rows = groups > 1 ? kMaxN : 0;
+        p.rows_total = rows;
         p.stages = stages_of(n_pad);
         p.tmem_cols = tmem_cols_of(n_pad);
         p.ws = ws;
-        p.row0 = g0;
+        p.row0 = static_cast<int>(g0);
         p.bias = bias;
         p.h = residual;
         p.z = z;
@@ -465,7 +481,8 @@ spec_status mlp_tc(const __nv_bfloat16* W, const __nv_bfloat16* bias, int M, con
         p.cond = cond;
         p.n_int = n_int;
         p.dep_k0 = dep_k0;
-        spec_status st = launch_umma<0, 8>(ta, tb, dim3((M + kBM - 1) / kBM, splits), p, s, "draft_mlp_tc");
+        spec_status st =
+            launch_umma<0, 8>(ta, tb, dim3((M + kBM - 1) / kBM, splits, groups), p, s, "draft_mlp_tc");
         if (st != SPEC_OK) return st;
     }
     return SPEC_OK;

@@ -33,10 +33,11 @@ DraftTcPlan draft_tc_plan(int rows, int d, int V);
 //   y[r, m] = act(W[m, :] . X[r, 0:d_in] + bias[m]) (+ residual[b(r), m]),  m < M
 // (act 1: SiLU, 0: identity; b(r) = r / n_int when cond, else r), stored as
 // bf16 in z [R, M] or, when zf is set, as fp32 in zf [R, M].  Input columns
-// >= dep_k0 come from the previous kernel.
+// >= dep_k0 come from the previous kernel.  W's rows are ldw elements apart
+// (0: d_in); bias, residual and ws (the status word) may be NULL.
 spec_status mlp_tc(const __nv_bfloat16* W, const __nv_bfloat16* bias, int M, const __nv_bfloat16* X, int d_in, int ldx,
                    int R, int cond, int n_int, int dep_k0, int act, const __nv_bfloat16* residual, __nv_bfloat16* z,
-                   float* zf, void* ws, cudaStream_t s);
+                   float* zf, void* ws, cudaStream_t s, int ldw = 0);
 
 // The vocabulary projection with the per-slice top-k / (max, sum exp) epilogue.
 spec_status proj_tc(const DraftTcPlan& plan, const __nv_bfloat16* W2, const __nv_bfloat16* z, int R, int d, int V, int k,
