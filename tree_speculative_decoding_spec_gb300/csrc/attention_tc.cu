@@ -8,13 +8,14 @@
 // One CTA = one (prefix split, KV head x 128-query-row block, sequence); the
 // CTA holding the last non-empty prefix split of a sequence also takes the
 // tree keys.  The query rows of a KV head are its g query heads x T nodes,
-// contiguous in q [B, Hq, T, D], so one 2-D TMA box fetches them.  Ten warps:
+// contiguous in q [B, Hq, T, D], so one 2-D TMA box fetches them.  Eleven warps:
 //   warp 8    TMA: the 128 x 128 Q tile once, then a 3-stage ring of 128-key
 //             K and V tiles (128-byte swizzle), prefix tiles then tree tiles
-//   warp 9    MMA: S_j = Q K_j^T into TMEM score buffer j % 2 (M 128, N 128,
-//             K 128, both operands in shared memory) and O_{j%2} += P_j V_j
-//             (M 128, N 128, K 128) with P_j read from TMEM and V as an
-//             MN-major shared-memory operand
+//   warps 9, 10  MMA, one thread each: warp 9 + g issues the MMAs of the
+//             tiles j with j % 2 == g -- S_j = Q K_j^T into TMEM score buffer g
+//             (M 128, N 128, K 128, both operands in shared memory) and
+//             O_g += P_j V_j (M 128, N 128, K 128) with P_j read from TMEM and
+//             V as an MN-major shared-memory operand
 //   warps 0-3 / 4-7: two softmax groups; group j % 2 owns tile j.  One thread
 //             per query row reads S_j from TMEM, masks (prefix length,
 //             ancestor bits), keeps its group's running maximum and sum in
@@ -27,8 +28,9 @@
 //             sequence) run as one thread-block cluster -- it stays in the
 //             CTA's own shared memory and is merged across the cluster over
 //             distributed shared memory (see the end of the kernel).
-// The tensor pipe runs its MMAs in issue order, so S_{j+2} may overwrite the
-// buffer PV_j reads, and the completion of S_j implies that of PV_{j-2}.
+// A thread's MMAs run in its issue order, so S_{j+2} may overwrite the buffer
+// PV_j reads, and the completion of S_j implies that of PV_{j-2} (same thread);
+// the two threads share only the K/V ring, whose stages free in tile order.
 // Cache rows past the prefix length inside the last prefix tile are zeroed in
 // shared memory before PV reads them (their scores are masked, and a stale
 // non-finite value times a zero weight would still poison O).
@@ -47,7 +49,7 @@ constexpr int kAKeys = 128;        // keys per tile
 constexpr int kAD = 128;           // head dim
 constexpr int kAStages = 3;
 constexpr int kAPrefetch = 2;     // contiguous prefix tiles prefetched into L2 ahead of their load
-constexpr int kAThreads = 320;
+constexpr int kAThreads = 352;
 constexpr int kQBytes = 2 * kARows * 128;         // two 64-column halves of 128 rows
 constexpr int kKVHalf = kAKeys * 128;             // one 64-column half of a 128-key tile
 constexpr int kStageBytes = 4 * kKVHalf;          // K and V, two halves each
@@ -181,7 +183,7 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             mbar_init(&s_full[i], 1);
             mbar_init(&p_full[i], kARows);
         }
-        mbar_init(o_final, 1);
+        mbar_init(o_final, 2);   // one commit from each MMA thread
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmQ);
@@ -260,7 +262,11 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             }
         }
         __syncwarp();
-    } else if (warp == 9) {
+    } else if (warp == 9 || warp == 10) {
+        // two MMA threads, one per softmax group: thread g issues S and PV of the tiles j with
+        // j % 2 == g, so each group's MMAs stay in issue order (the buffer reuse below relies
+        // on that) while one thread's waits and commits overlap the other's MMAs
+        const int g = warp - 9;
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kARows, kAKeys);
             const uint32_t idesc_o = idesc_bf16_f32_bmn(kARows, kAD);
@@ -282,10 +288,9 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                 mma_commit(&s_full[j & 1]);
                 return true;
             };
-            // S for the first tile of each group, then per tile: PV_j, S_{j+2}
-            if (ok && n_tiles > 0) ok = issue_s(0);
-            if (ok && n_tiles > 1) ok = issue_s(1);
-            for (int j = 0; ok && j < n_tiles; ++j) {
+            // S for the group's first tile, then per tile: PV_j, S_{j+2}
+            if (ok && g < n_tiles) ok = issue_s(g);
+            for (int j = g; ok && j < n_tiles; j += 2) {
                 if (!mbar_wait_or_abort(&p_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
                 tc_fence_after();
                 // O_{j%2} += P_j V_j: K = 128 keys in 8 steps of 16.  P_j: bf16 pairs in the first
@@ -497,7 +502,7 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                 mbar_wait(&kv_full[j % kAStages], (j / kAStages) & 1, 100000000ull);
             mbar_wait(q_full, 0, 100000000ull);
         }
-        if (warp == 9 && lane == 0) mbar_wait(o_final, 0, 100000000ull);
+        if ((warp == 9 || warp == 10) && lane == 0) mbar_wait(o_final, 0, 100000000ull);
     }
     __syncthreads();
     if (warp == 0) {
