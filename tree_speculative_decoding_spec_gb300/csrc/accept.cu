@@ -29,6 +29,7 @@ namespace accept {
 constexpr int kRowThreads = 256;
 constexpr int kWalkThreads = 1024;
 constexpr int kLseIter = 16;   // 4-wide loads per thread and operand: a slice holds <= 256*4*16 tokens
+constexpr int kWalkCacheMax = 40960;   // vocabularies up to this size keep the draw's weights in shared memory
 
 struct Plan {
     int slices, slice;
@@ -356,7 +357,7 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_greedy(const float4* __re
 
 // ---------------------------------------------------------------- walk (rejection)
 
-__global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __restrict__ part, int slices,
+__global__ void __launch_bounds__(kWalkThreads, 1) k_walk_reject(const float4* __restrict__ part, int slices,
                                                               const float* __restrict__ lp, const float* __restrict__ lq,
                                                               const int32_t* __restrict__ node_tok,
                                                               const int32_t* __restrict__ parent,
@@ -371,6 +372,16 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
     // Medusa typical acceptance (threshold min(eps, alpha exp(-H(p_parent))), extra
     // token from p at the last accepted node).  lse_q holds that threshold then.
     const int b = blockIdx.x;
+    // The tree and the node tokens are inputs of the call, complete before the rows kernel
+    // started: they are copied to shared memory while that kernel runs.
+    __shared__ int32_t s_par[SPEC_MAX_T], s_dep[SPEC_MAX_T], s_tok[SPEC_MAX_T];
+    __shared__ unsigned char s_int[SPEC_MAX_T];
+    for (int u = threadIdx.x; u < Tn; u += blockDim.x) {
+        s_par[u] = parent[u];
+        s_dep[u] = depth[u];
+        s_tok[u] = node_tok[static_cast<size_t>(b) * Tn + u];
+        s_int[u] = child_off[u + 1] > child_off[u];
+    }
     griddep_wait();   // the rows kernel's partials (launched early: the launch overlaps it)
     __shared__ float lse_p[SPEC_MAX_T], lse_q[SPEC_MAX_T];
     __shared__ unsigned char pass[SPEC_MAX_T], acc[SPEC_MAX_T];
@@ -390,15 +401,15 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
         float mp = -INFINITY, sp = 0.f, mq = -INFINITY, sq = 0.f;
         for (int s = 0; s < slices; ++s) { lse_merge(mp, sp, pr[s].x, pr[s].y); lse_merge(mq, sq, pr[s].z, pr[s].w); }
         lse_p[u] = mp + logf(sp);
-        lse_q[u] = (child_off[u + 1] > child_off[u]) ? mq + logf(sq) : NAN;
+        lse_q[u] = s_int[u] ? mq + logf(sq) : NAN;
     }
     __syncthreads();
     for (int c = threadIdx.x; c < Tn; c += blockDim.x) {
         pass[c] = 0;
         dmar[c] = INFINITY;
         if (c == 0) continue;
-        const int par = parent[c];
-        const int x = node_tok[static_cast<size_t>(b) * Tn + c];
+        const int par = s_par[c];
+        const int x = s_tok[c];
         if (x < 0 || x >= V) {   // a token outside the vocabulary is never accepted
             flag_status(ws, SPEC_EINVAL);
             continue;
@@ -418,15 +429,15 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
         if (ratio < 1.f) dmar[c] = fabsf(u - ratio);
     }
     __syncthreads();
-    const int ustar = resolve_path(parent, depth, Tn, max_depth, acc, pass, iscr);
+    const int ustar = resolve_path(s_par, s_dep, Tn, max_depth, acc, pass, iscr);
     float mg = INFINITY;
     for (int c = threadIdx.x; c < Tn; c += blockDim.x)
-        if (c > 0 && acc[parent[c]]) mg = fminf(mg, dmar[c]);
+        if (c > 0 && acc[s_par[c]]) mg = fminf(mg, dmar[c]);
     mg = block_min_f(mg, fscr);
-    write_path(parent, depth, ustar, b, max_depth, accept_len, accept_path);
+    write_path(s_par, s_dep, ustar, b, max_depth, accept_len, accept_path);
 
     // ---- the extra token: inverse CDF over the vocabulary, ascending token order
-    const bool leaf = child_off[ustar + 1] == child_off[ustar];
+    const bool leaf = !s_int[ustar];
     const size_t srow = (static_cast<size_t>(b) * Tn + ustar) * V;
     const float lsp = lse_p[ustar], lsq = lse_q[ustar];
     const float* rp = lp + srow;
@@ -437,6 +448,12 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
         if (!resid) return pv;
         return fmaxf(pv - expf(rq[x] * inv_temp - lsq), 0.f);
     };
+    // The range sums below compute every token's weight once, 16 loads per lane in flight;
+    // a vocabulary of at most kWalkCacheMax tokens keeps them in shared memory, where the
+    // scans read them (one pass over the two rows instead of a dependent load per 32 tokens)
+    extern __shared__ float wcache[];
+    const bool cached = V <= kWalkCacheMax;
+    auto wt = [&](int x, bool resid) -> float { return cached ? wcache[x] : weight(x, resid); };
     // Draw: warp w owns the contiguous token range [w*Rw, (w+1)*Rw); each warp sums its range
     // with coalesced loads, warp 0 scans the 32 range sums, the warp holding the target
     // scans its range 32 tokens at a time (ascending token order throughout).
@@ -450,7 +467,12 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
     bool resid = !leaf && !typical;
     auto range_sum = [&](bool rs) {
         float acc = 0.f;
-        for (int x = w0 + ln; x < w1; x += 32) acc += weight(x, rs);
+#pragma unroll 16
+        for (int x = w0 + ln; x < w1; x += 32) {
+            const float wv = weight(x, rs);
+            if (cached) wcache[x] = wv;
+            acc += wv;
+        }
         return warp_sum(acc);
     };
     float my = range_sum(resid);
@@ -491,7 +513,7 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
         // target at or beyond the total (rounding): take the last token of positive weight
         int lastx = -1;
         for (int x = threadIdx.x; x < V; x += blockDim.x)
-            if (weight(x, resid) > 0.f) lastx = x;
+            if (wt(x, resid) > 0.f) lastx = x;
         lastx = block_max_int(lastx, iscr);
         if (threadIdx.x == 0) {
             pick = max(lastx, 0);
@@ -503,7 +525,7 @@ __global__ void __launch_bounds__(kWalkThreads) k_walk_reject(const float4* __re
         int found = -1, lastpos = -1;
         for (int base = w0; base < w1; base += 32) {
             const int x = base + ln;
-            const float wv = x < w1 ? weight(x, resid) : 0.f;
+            const float wv = x < w1 ? wt(x, resid) : 0.f;
             float inc = wv;
             for (int o = 1; o < 32; o <<= 1) {
                 const float t = __shfl_up_sync(0xffffffffu, inc, o);
@@ -595,7 +617,10 @@ extern "C" spec_status tree_accept(int32_t mode, const float* logits_p, const fl
         const float inv_temp = 1.0f / temperature;
         SPEC_CUDA_TRY(launch("accept_rows_lse", accept::k_rows_lse, grid, dim3(accept::kRowThreads), 0, s, logits_p, logits_q,
                              tree->child_off, tree->T, V, p.slice, p.slices, inv_temp, part, ws));
-        SPEC_CUDA_TRY(launch_ex("accept_walk_reject", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), 0, s, true, part,
+        const size_t wsmem = V <= accept::kWalkCacheMax ? sizeof(float) * static_cast<size_t>(V) : 0;
+        SPEC_CUDA_TRY(cudaFuncSetAttribute(accept::k_walk_reject, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(sizeof(float) * accept::kWalkCacheMax)));
+        SPEC_CUDA_TRY(launch_ex("accept_walk_reject", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), wsmem, s, true, part,
                              p.slices, logits_p, logits_q, node_tok, tree->parent, tree->depth, tree->child_off,
                              tree->T, tree->max_depth, V, inv_temp, seed, offset, accept_len, accept_path, next_token,
                              margin, ws, 0, 0.f, 0.f));
@@ -629,7 +654,10 @@ extern "C" spec_status tree_accept_typical(const float* logits_p, const int32_t*
     // the rows kernel clears the status word (it flags nothing itself; the walk flags after its wait)
     SPEC_CUDA_TRY(launch("accept_rows_ent", accept::k_rows_ent, grid, dim3(accept::kRowThreads), 0, s, logits_p, V,
                          p.slice, p.slices, inv_temp, part, ws));
-    SPEC_CUDA_TRY(launch_ex("accept_walk_typical", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), 0, s, true, part,
+    const size_t wsmem = V <= accept::kWalkCacheMax ? sizeof(float) * static_cast<size_t>(V) : 0;
+    SPEC_CUDA_TRY(cudaFuncSetAttribute(accept::k_walk_reject, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       static_cast<int>(sizeof(float) * accept::kWalkCacheMax)));
+    SPEC_CUDA_TRY(launch_ex("accept_walk_typical", accept::k_walk_reject, dim3(B), dim3(accept::kWalkThreads), wsmem, s, true, part,
                          p.slices, logits_p, static_cast<const float*>(nullptr), node_tok, tree->parent, tree->depth,
                          tree->child_off, tree->T, tree->max_depth, V, inv_temp, seed, offset, accept_len, accept_path,
                          next_token, margin, ws, 1, epsilon, alpha));
