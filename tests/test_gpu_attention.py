@@ -37,6 +37,15 @@ CASES = [
     ("bf16", 2, 4, 2, ("random", 200), 128, 700, [333, 700]),       # two tree tiles, four mask words
     ("bf16", 1, 2, 1, ("random", 130), 128, 257, [257]),            # second tree tile: one mask word
     ("bf16", 2, 2, 2, ("sparse", (8, 4, 2, 1), 64, 64), 128, 1024, [0, 1024]),   # 8 splits merged on chip; empty prefix
+    # 64 prefix splits, too many to merge on chip: the combine kernel merges 40 partials of one
+    # sequence and 1 of the other, four at a time with a running maximum across the groups
+    ("bf16", 2, 2, 2, ("sparse", (8, 4, 2, 1), 64, 64), 128, 8192, [5000, 77]),
+    # batches whose grid slots are ranked by prefix length (64 sequences, two per lane) and one
+    # past the ranking's reach (65 sequences keep the grid order)
+    ("bf16", 64, 1, 1, ("sparse", (8, 4, 2, 1), 64, 64), 128, 256,
+     [int(x) for x in np.random.default_rng(64).integers(0, 257, 64)]),
+    ("bf16", 65, 1, 1, ("sparse", (8, 4, 2, 1), 64, 64), 128, 256,
+     [int(x) for x in np.random.default_rng(65).integers(0, 257, 65)]),
 ]
 
 
