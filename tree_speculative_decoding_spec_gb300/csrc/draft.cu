@@ -96,6 +96,74 @@ __global__ void __launch_bounds__(256) k_gemm_fma(const T* __restrict__ W, int l
     }
 }
 
+// The same product for a few activation rows (N <= kGemvRows, N * K floats in
+// shared memory): one warp per weight row m, the CTA's rows staged once in
+// shared memory as fp32, each lane taking every 32nd k of the row (coalesced
+// loads, eight in flight) and a shuffle reduction per activation row.  A
+// launch costs about one round trip of loads instead of the tiled kernel's
+// K / 32 dependent ones.  Same epilogues and arguments as k_gemm_fma.
+constexpr int kGemvRows = 16;
+constexpr int kGemvWarps = 8;
+constexpr size_t kGemvSmemMax = 48 * 1024;
+
+inline bool gemv_fits(int N, int K) {
+    return N >= 1 && N <= kGemvRows && static_cast<size_t>(N) * K * sizeof(float) <= kGemvSmemMax;
+}
+
+template <typename T, int EPI>
+__global__ void __launch_bounds__(kGemvWarps * 32) k_gemv_rows(const T* __restrict__ W, int ldw, const T* __restrict__ X,
+                                                               int M, int N, int K, int ldx, const T* __restrict__ bias,
+                                                               const T* __restrict__ h, int cond, int n_int,
+                                                               T* __restrict__ z_out, float* __restrict__ logits, int act,
+                                                               float* __restrict__ zf) {
+    extern __shared__ float xs[];   // [N][K]
+    for (int idx = threadIdx.x; idx < N * K; idx += blockDim.x)
+        xs[idx] = to_f32(X[static_cast<size_t>(idx / K) * ldx + idx % K]);
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const int m = blockIdx.x * kGemvWarps + (threadIdx.x >> 5);
+    if (m >= M) return;
+    const T* wr = W + static_cast<size_t>(m) * ldw;
+    float acc[kGemvRows];
+#pragma unroll
+    for (int n = 0; n < kGemvRows; ++n) acc[n] = 0.f;
+#pragma unroll 8
+    for (int k = lane; k < K; k += 32) {
+        const float wv = to_f32(wr[k]);
+#pragma unroll
+        for (int n = 0; n < kGemvRows; ++n)
+            if (n < N) acc[n] = fmaf(wv, xs[n * K + k], acc[n]);
+    }
+#pragma unroll
+    for (int n = 0; n < kGemvRows; ++n) {
+        if (n >= N) break;
+        const float sum = warp_sum(acc[n]);
+        if (lane != n) continue;
+        if (EPI == 0) {   // act(W x + bias) (+ h_b when h is set), to z_out or, if set, fp32 zf
+            const int b = cond ? n / n_int : n;
+            const float a = sum + (bias ? to_f32(bias[m]) : 0.f);
+            const float y = act ? a / (1.0f + expf(-a)) : a;
+            const float zz = h ? to_f32(h[static_cast<size_t>(b) * M + m]) + y : y;
+            if (zf) zf[static_cast<size_t>(n) * M + m] = zz;
+            else z_out[static_cast<size_t>(n) * M + m] = from_f32<T>(zz);
+        } else {
+            logits[static_cast<size_t>(n) * M + m] = sum;
+        }
+    }
+}
+
+// acc[n][m] = W[m] . X[n] for the fp32 / CUDA-core path: the warp-per-row kernel for a few
+// activation rows, the tiled kernel otherwise.
+template <typename T, int EPI, typename... Args>
+cudaError_t launch_gemm(const char* name, cudaStream_t s, const T* W, int ldw, const T* X, int M, int N, int K, int ldx,
+                        Args... rest) {
+    if (gemv_fits(N, K))
+        return launch(name, k_gemv_rows<T, EPI>, dim3((M + kGemvWarps - 1) / kGemvWarps), dim3(kGemvWarps * 32),
+                      static_cast<size_t>(N) * K * sizeof(float), s, W, ldw, X, M, N, K, ldx, rest...);
+    return launch(name, k_gemm_fma<T, EPI>, dim3((M + GBM - 1) / GBM, (N + GBN - 1) / GBN), dim3(256), 0, s, W, ldw, X,
+                  M, N, K, ldx, rest...);
+}
+
 // ---------------------------------------------------------------- LayerNorm (head form 1)
 
 // z[r] = (y[r] - mean) / sqrt(var + eps) * gamma + beta over the d entries of
@@ -223,14 +291,16 @@ __global__ void __launch_bounds__(256) k_topk_slices(const float* __restrict__ l
         else ssum += expf(v - m);
     }
     __shared__ Cand sc[256 * KMAX];
-    __shared__ float2 sl2[256];
+    __shared__ float2 sl2[8];
 #pragma unroll
     for (int s = 0; s < KMAX; ++s) sc[threadIdx.x * KMAX + s] = Cand{lv[s], li[s]};
-    sl2[threadIdx.x] = make_float2(m, ssum);
+    // (max, sum exp) of the slice: a shuffle reduction per warp, then the warps' results
+    for (int o = 16; o > 0; o >>= 1) lse_merge(m, ssum, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, ssum, o));
+    if ((threadIdx.x & 31) == 0) sl2[threadIdx.x >> 5] = make_float2(m, ssum);
     __syncthreads();
     if (threadIdx.x == 0) {
         float M = -INFINITY, S = 0.f;
-        for (int t = 0; t < blockDim.x; ++t) lse_merge(M, S, sl2[t].x, sl2[t].y);
+        for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) lse_merge(M, S, sl2[w].x, sl2[w].y);
         part_l[static_cast<size_t>(r) * nslices + sl] = make_float2(M, S);
     }
     // k rounds of "best head of the per-thread sorted lists"
@@ -1087,23 +1157,23 @@ spec_status run(const T* h, const T* emb, const Heads& hs, float ln_eps, const i
             }
         }
         if (!ln) {
-            SPEC_CUDA_TRY(launch("draft_mlp_fma", k_gemm_fma<T, 0>, dim3((d + GBM - 1) / GBM, (R + GBN - 1) / GBN), dim3(256),
-                                 0, s, W1k, d_in, X, d, R, d_in, ldx, b1k, h, cond[k], n_int, z, nullptr, 1, nullptr));
+            SPEC_CUDA_TRY((launch_gemm<T, 0>("draft_mlp_fma", s, W1k, d_in, X, d, R, d_in, ldx, b1k, h, cond[k], n_int, z,
+                                             static_cast<float*>(nullptr), 1, static_cast<float*>(nullptr))));
         } else {
             const int hd = hs.hidden[k];
-            SPEC_CUDA_TRY(launch("draft_mlp_fma", k_gemm_fma<T, 0>, dim3((hd + GBM - 1) / GBM, (R + GBN - 1) / GBN),
-                                 dim3(256), 0, s, W1k, d_in, X, hd, R, d_in, ldx, b1k, static_cast<const T*>(nullptr), cond[k],
-                                 n_int, W1bk ? hid : nullptr, nullptr, 1, W1bk ? nullptr : yln));
+            SPEC_CUDA_TRY((launch_gemm<T, 0>("draft_mlp_fma", s, W1k, d_in, X, hd, R, d_in, ldx, b1k,
+                                             static_cast<const T*>(nullptr), cond[k], n_int, W1bk ? hid : nullptr,
+                                             static_cast<float*>(nullptr), 1, W1bk ? static_cast<float*>(nullptr) : yln)));
             if (W1bk)
-                SPEC_CUDA_TRY(launch("draft_mlp_fma", k_gemm_fma<T, 0>, dim3((d + GBM - 1) / GBM, (R + GBN - 1) / GBN),
-                                     dim3(256), 0, s, W1bk, hd, static_cast<const T*>(hid), d, R, hd, hd,
-                                     static_cast<const T*>(hs.b1b[k]), static_cast<const T*>(nullptr), 0, 1,
-                                     static_cast<T*>(nullptr), nullptr, 0, yln));
+                SPEC_CUDA_TRY((launch_gemm<T, 0>("draft_mlp_fma", s, W1bk, hd, static_cast<const T*>(hid), d, R, hd, hd,
+                                                 static_cast<const T*>(hs.b1b[k]), static_cast<const T*>(nullptr), 0, 1,
+                                                 static_cast<T*>(nullptr), static_cast<float*>(nullptr), 0, yln)));
             spec_status st = layernorm();
             if (st != SPEC_OK) return st;
         }
-        SPEC_CUDA_TRY(launch("draft_proj_fma", k_gemm_fma<T, 1>, dim3((V + GBM - 1) / GBM, (R + GBN - 1) / GBN), dim3(256), 0, s,
-                             W2k, d, z, V, R, d, d, nullptr, nullptr, 0, 1, nullptr, scratch, 0, nullptr));
+        SPEC_CUDA_TRY((launch_gemm<T, 1>("draft_proj_fma", s, W2k, d, static_cast<const T*>(z), V, R, d, d,
+                                         static_cast<const T*>(nullptr), static_cast<const T*>(nullptr), 0, 1,
+                                         static_cast<T*>(nullptr), scratch, 0, static_cast<float*>(nullptr))));
         spec_status st;
         if (p.kmax == 8) {
             SPEC_CUDA_TRY(launch("draft_topk_slices", k_topk_slices<8>, dim3(p.nslices, R), dim3(256), 0, s, scratch, V,
