@@ -137,6 +137,12 @@ __device__ __forceinline__ int longest_first(const int32_t* __restrict__ prefix_
 // Named barrier for the 256 softmax threads (warps 0-7).
 __device__ __forceinline__ void softmax_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
 
+// kApart: every CTA's tiles fit in the ring at once (short prefixes); K and V of a stage then
+// complete on separate barriers, so S_j starts as soon as K_j has landed.  In a long stream
+// one barrier covers both (S_j waits for V_j too, which keeps V_j's shared-memory writes off
+// S_j's operand reads); the two forms are separate instantiations so that neither carries
+// the other's waits.
+template <bool kApart>
 __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant__ CUtensorMap tmQ,
                                                           const __grid_constant__ CUtensorMap tmKc,
                                                           const __grid_constant__ CUtensorMap tmVc,
@@ -163,8 +169,9 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     uint8_t* sKV = sQ + kQBytes;                       // stage s: K half0, K half1, V half0, V half1
     uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + kAStages * kStageBytes);
     uint64_t* q_full = bars;
-    uint64_t* kv_full = bars + 1;
-    uint64_t* kv_empty = kv_full + kAStages;
+    uint64_t* k_full = bars + 1;                       // [stage] the stage's K tile (and V, unless kApart) landed
+    uint64_t* v_full = k_full + kAStages;              // [stage] its V tile landed (kApart only)
+    uint64_t* kv_empty = v_full + kAStages;            // [stage] PV of the stage's tile complete
     uint64_t* s_full = kv_empty + kAStages;            // [group]
     uint64_t* p_full = s_full + 2;                     // [group]
     uint64_t* o_final = p_full + 2;
@@ -176,12 +183,13 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         for (int s = 0; s < kAStages; ++s) {
-            mbar_init(&kv_full[s], 1);
+            mbar_init(&k_full[s], 1);
+            mbar_init(&v_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&s_full[i], 1);
-            mbar_init(&p_full[i], kARows);
+            mbar_init(&p_full[i], 4);   // one arrival per softmax warp
         }
         mbar_init(o_final, 2);   // one commit from each MMA thread
         *abort_flag = 0;
@@ -210,20 +218,17 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             mbar_arrive_expect_tx(q_full, kQBytes);
             tma_load_2d(sQ, &tmQ, q_full, 0, q_row0);
             tma_load_2d(sQ + kARows * 128, &tmQ, q_full, 64, q_row0);
+            // a stage frees once PV of its tile is complete
             for (int j = 0; j < n_tiles; ++j) {
                 const int s = j % kAStages;
-                if (j >= kAStages && !mbar_wait_or_abort(&kv_empty[s], ((j / kAStages) - 1) & 1, abort_flag)) {
-                    flag_status(p.ws, SPEC_ETIMEOUT);
-                    *abort_flag = 1;
-                    break;
-                }
                 const bool tree_tile = j >= n_pt;
                 uint8_t* st = sKV + s * kStageBytes;
-                mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
+                // source rows of the tile's two 64-key halves
+                int row_h[2];
                 if (!tree_tile && p.pg.table) {
-                    // paged prefix: two 64-key halves, each inside one pool block (bs is a
-                    // multiple of 64); keys past the prefix read the last used block (they are
-                    // masked, and their V rows zeroed, by the softmax threads)
+                    // paged prefix: each half lies inside one pool block (bs is a multiple of 64);
+                    // keys past the prefix read the last used block (they are masked, and their
+                    // V rows zeroed, by the softmax threads)
                     for (int hh = 0; hh < 2; ++hh) {
                         const int pos = pre_begin + j * kAKeys + hh * 64;
                         const int lb = min(pos / p.pg.bs, (L - 1) / p.pg.bs);
@@ -232,33 +237,47 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                             flag_status(p.ws, SPEC_EINVAL);
                             blk = 0;
                         }
-                        const int row = (blk * p.Hkv + kvh) * p.pg.bs + pos % p.pg.bs;
-                        const int off = hh * (kKVHalf / 2);
-                        tma_load_2d(st + off, &tmKc, &kv_full[s], 0, row);
-                        tma_load_2d(st + kKVHalf + off, &tmKc, &kv_full[s], 64, row);
-                        tma_load_2d(st + 2 * kKVHalf + off, &tmVc, &kv_full[s], 0, row);
-                        tma_load_2d(st + 3 * kKVHalf + off, &tmVc, &kv_full[s], 64, row);
+                        row_h[hh] = (blk * p.Hkv + kvh) * p.pg.bs + pos % p.pg.bs;
                     }
                 } else {
-                    const CUtensorMap* tk = tree_tile ? &tmKt : &tmKc;
-                    const CUtensorMap* tv = tree_tile ? &tmVt : &tmVc;
-                    const int row = tree_tile ? kvt_row0 + (j - n_pt) * kAKeys : kvc_row0 + j * kAKeys;
-                    tma_load_2d(st, tk, &kv_full[s], 0, row);
-                    tma_load_2d(st + kKVHalf, tk, &kv_full[s], 64, row);
-                    tma_load_2d(st + 2 * kKVHalf, tv, &kv_full[s], 0, row);
-                    tma_load_2d(st + 3 * kKVHalf, tv, &kv_full[s], 64, row);
-                    // the prefix tile kAPrefetch tiles ahead heads for L2 now: the ring's lead
-                    // (its stages free up only as PV finishes) is shorter than a load's latency
-                    const int jp = j + kAPrefetch;
-                    if (kAPrefetch > 0 && jp < n_pt) {
-                        const int rp = kvc_row0 + jp * kAKeys;
-                        tma_prefetch_2d(&tmKc, 0, rp);
-                        tma_prefetch_2d(&tmKc, 64, rp);
-                        tma_prefetch_2d(&tmVc, 0, rp);
-                        tma_prefetch_2d(&tmVc, 64, rp);
-                    }
+                    row_h[0] = tree_tile ? kvt_row0 + (j - n_pt) * kAKeys : kvc_row0 + j * kAKeys;
+                    row_h[1] = row_h[0] + 64;
                 }
+                // one 128-key box per 64-column half, or two 64-key boxes when paged
+                auto load = [&](const CUtensorMap* mc, const CUtensorMap* mt, uint64_t* bar, uint8_t* dst) {
+                    if (!tree_tile && p.pg.table) {
+                        for (int hh = 0; hh < 2; ++hh) {
+                            const int off = hh * (kKVHalf / 2);
+                            tma_load_2d(dst + off, mc, bar, 0, row_h[hh]);
+                            tma_load_2d(dst + kKVHalf + off, mc, bar, 64, row_h[hh]);
+                        }
+                    } else {
+                        const CUtensorMap* m = tree_tile ? mt : mc;
+                        tma_load_2d(dst, m, bar, 0, row_h[0]);
+                        tma_load_2d(dst + kKVHalf, m, bar, 64, row_h[0]);
+                    }
+                };
+                if (j >= kAStages && !mbar_wait_or_abort(&kv_empty[s], ((j / kAStages) - 1) & 1, abort_flag)) {
+                    flag_status(p.ws, SPEC_ETIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                uint64_t* vbar = kApart ? &v_full[s] : &k_full[s];
+                mbar_arrive_expect_tx(&k_full[s], kApart ? 2 * kKVHalf : kStageBytes);
+                load(&tmKc, &tmKt, &k_full[s], st);
+                if (kApart) mbar_arrive_expect_tx(vbar, 2 * kKVHalf);
+                load(&tmVc, &tmVt, vbar, st + 2 * kKVHalf);
                 issued = j + 1;
+                // the prefix tile kAPrefetch tiles ahead heads for L2 now: the ring's lead
+                // (its stages free up only as PV finishes) is shorter than a load's latency
+                const int jp = j + kAPrefetch;
+                if (kAPrefetch > 0 && jp < n_pt && !p.pg.table) {
+                    const int rp = kvc_row0 + jp * kAKeys;
+                    tma_prefetch_2d(&tmKc, 0, rp);
+                    tma_prefetch_2d(&tmKc, 64, rp);
+                    tma_prefetch_2d(&tmVc, 0, rp);
+                    tma_prefetch_2d(&tmVc, 64, rp);
+                }
             }
         }
         __syncwarp();
@@ -270,20 +289,23 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
         if (lane == 0) {
             const uint32_t idesc_s = idesc_bf16_f32(kARows, kAKeys);
             const uint32_t idesc_o = idesc_bf16_f32_bmn(kARows, kAD);
-            const uint32_t q0 = smem_u32(sQ);
+            // a descriptor's start-address field is the byte address / 16 in its low 14 bits;
+            // offsets inside shared memory never carry out of it, so the descriptor of an
+            // offset sub-tile is the base descriptor plus offset / 16
+            const uint64_t qd = sdesc_k128(smem_u32(sQ));
             bool ok = mbar_wait_or_abort(q_full, 0, abort_flag);
             // S_j = Q K_j^T: K = 128 in 8 steps of 16 (two 64-column halves)
             auto issue_s = [&](int j) -> bool {
                 const int s = j % kAStages;
-                if (!mbar_wait_or_abort(&kv_full[s], (j / kAStages) & 1, abort_flag)) return false;
+                if (!mbar_wait_or_abort(&k_full[s], (j / kAStages) & 1, abort_flag)) return false;
                 tc_fence_after();
-                const uint32_t k0 = smem_u32(sKV + s * kStageBytes);
+                const uint64_t kd = sdesc_k128(smem_u32(sKV + s * kStageBytes));
                 const uint32_t dst = tmem + (j & 1) * kAKeys;
 #pragma unroll
                 for (int ks = 0; ks < kAD / 16; ++ks) {
                     const uint32_t off = (ks & 3) * 32;
-                    mma_bf16(dst, sdesc_k128(q0 + (ks >> 2) * (kARows * 128) + off),
-                             sdesc_k128(k0 + (ks >> 2) * kKVHalf + off), idesc_s, ks > 0 ? 1u : 0u);
+                    mma_bf16(dst, qd + (((ks >> 2) * (kARows * 128) + off) >> 4), kd + (((ks >> 2) * kKVHalf + off) >> 4),
+                             idesc_s, ks > 0 ? 1u : 0u);
                 }
                 mma_commit(&s_full[j & 1]);
                 return true;
@@ -292,16 +314,19 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             if (ok && g < n_tiles) ok = issue_s(g);
             for (int j = g; ok && j < n_tiles; j += 2) {
                 if (!mbar_wait_or_abort(&p_full[j & 1], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+                if constexpr (kApart) {
+                    if (!mbar_wait_or_abort(&v_full[j % kAStages], 0, abort_flag)) { ok = false; break; }
+                }
                 tc_fence_after();
                 // O_{j%2} += P_j V_j: K = 128 keys in 8 steps of 16.  P_j: bf16 pairs in the first
                 // 64 columns of score buffer j % 2 (8 columns per step).  V is MN-major (d
                 // contiguous): 64-wide d halves kKVHalf apart, 8-key atoms 1 KB apart.
                 const uint32_t pa = tmem + (j & 1) * kAKeys;
-                const uint32_t v0 = smem_u32(sKV + (j % kAStages) * kStageBytes + 2 * kKVHalf);
+                const uint64_t vd = sdesc_mn128(smem_u32(sKV + (j % kAStages) * kStageBytes + 2 * kKVHalf), kKVHalf, 1024);
                 const uint32_t o = tmem + kAO + (j & 1) * kAD;
 #pragma unroll
                 for (int ks = 0; ks < kAKeys / 16; ++ks)
-                    mma_bf16_ts(o, pa + ks * 8, sdesc_mn128(v0 + ks * 2048, kKVHalf, 1024), idesc_o,
+                    mma_bf16_ts(o, pa + ks * 8, vd + ((ks * 2048) >> 4), idesc_o,
                                 (j >= 2 || ks > 0) ? 1u : 0u);
                 mma_commit(&kv_empty[j % kAStages]);
                 // in issue order after PV_j, so S_{j+2} may overwrite P_j
@@ -423,7 +448,12 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             }
             l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
             if (!tree_tile && nvalid < kAKeys) {
-                // zero the V rows past the prefix (both 64-column halves) before PV_j reads them
+                // zero the V rows past the prefix (both 64-column halves) once they have landed
+                // and before PV_j reads them
+                if constexpr (kApart) {
+                    ok = __all_sync(0xffffffffu, mbar_wait_or_abort(&v_full[j % kAStages], 0, abort_flag));
+                    if (!ok) break;
+                }
                 uint8_t* sv_tile = sKV + (j % kAStages) * kStageBytes + 2 * kKVHalf;
                 const int r_in = (warp & 3) * 32 + lane;
                 for (int i = r_in; i < (kAKeys - nvalid) * 16; i += kARows) {
@@ -435,7 +465,8 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             }
             tmem_st_wait();
             tc_fence_before();
-            mbar_arrive(&p_full[grp]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[grp]);
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait_or_abort(o_final, 0, abort_flag));
         if (!ok) {
@@ -498,8 +529,10 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     if (*abort_flag) {
         // a wait ran out: let this CTA's own loads and MMAs land before releasing memory
         if (warp == 8 && lane == 0) {
-            for (int j = max(0, issued - kAStages); j < issued; ++j)
-                mbar_wait(&kv_full[j % kAStages], (j / kAStages) & 1, 100000000ull);
+            for (int j = max(0, issued - kAStages); j < issued; ++j) {
+                mbar_wait(&k_full[j % kAStages], (j / kAStages) & 1, 100000000ull);
+                if (kApart) mbar_wait(&v_full[j % kAStages], 0, 100000000ull);
+            }
             mbar_wait(q_full, 0, 100000000ull);
         }
         if ((warp == 9 || warp == 10) && lane == 0) mbar_wait(o_final, 0, 100000000ull);
@@ -603,8 +636,8 @@ static int max_active_clusters(int n) {
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem) != cudaSuccess ||
-            cudaOccupancyMaxActiveClusters(&v, k_attn_tc, &cfg) != cudaSuccess) {
+        if (cudaFuncSetAttribute(k_attn_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem) != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&v, k_attn_tc<false>, &cfg) != cudaSuccess) {
             cudaGetLastError();
             v = 0;
         }
@@ -685,12 +718,15 @@ spec_status attn_tc_run(const AttnTcPlan& pl, const __nv_bfloat16* q, const __nv
     p.fused = pl.fused ? 1 : 0;
     p.out = out;
     p.lse = lse;
-    SPEC_CUDA_TRY(cudaFuncSetAttribute(k_attn_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem));
+    // every CTA's tiles (its prefix chunk, the tree tiles) fit in the ring at once
+    const bool apart = pl.chunk / kAKeys + (T + kAKeys - 1) / kAKeys <= kAStages;
+    auto kern = apart ? k_attn_tc<true> : k_attn_tc<false>;
+    SPEC_CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kASmem));
     if (pl.fused)
-        SPEC_CUDA_TRY(launch_cluster("attn_tc", k_attn_tc, dim3(pl.n_pre, Hkv * pl.n_rb, B), dim3(kAThreads), kASmem, s,
+        SPEC_CUDA_TRY(launch_cluster("attn_tc", kern, dim3(pl.n_pre, Hkv * pl.n_rb, B), dim3(kAThreads), kASmem, s,
                                      false, dim3(pl.n_pre, 1, 1), tq, tkc, tvc, tkt, tvt, p));
     else
-        SPEC_CUDA_TRY(launch("attn_tc", k_attn_tc, dim3(pl.n_pre, Hkv * pl.n_rb, B), dim3(kAThreads), kASmem, s, tq,
+        SPEC_CUDA_TRY(launch("attn_tc", kern, dim3(pl.n_pre, Hkv * pl.n_rb, B), dim3(kAThreads), kASmem, s, tq,
                              tkc, tvc, tkt, tvt, p));
     return SPEC_OK;
 }
