@@ -521,9 +521,10 @@ __device__ __forceinline__ void write_next_row(T* __restrict__ dst, const T* __r
 // One CTA per row: top-k over the row's sorted per-slice candidate lists and
 // the row's log-sum-exp, then the children of the row's parent node(s).
 // Merging: each thread holds its slice's sorted list in registers (more
-// slices than threads are folded in by bitonic merges); k rounds then take the
-// best list head of the CTA -- warp reductions and one barrier per round --
-// and pop it from its owner's list.
+// slices than threads are folded in by bitonic merges); each warp then takes
+// the top-k of its lists in k rounds of warp reductions (the owner of the best
+// head pops it), and after one barrier warp 0 takes the top-k of the warps'
+// lists the same way.
 //
 // The tree's structure (children, ranks, input rows, ancestors) is written once
 // by spec_tree_build and by none of the kernels this one follows, so a CTA with
@@ -746,18 +747,25 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                 if (c_row[a] < 0 || (cpr > 1 && a != ci)) continue;
                 const float4* tr = reinterpret_cast<const float4*>(ftab + static_cast<size_t>(topi[c_rank[a]]) * d);
                 T* zr = zf + (row0 + c_row[a]) * d;
-                int j = 0;
-                for (int c = tid; c < d / 8; c += blockDim.x, ++j) {
-                    const float4 t0 = tr[2 * c], t1 = tr[2 * c + 1];
-                    ZChunk<T> zc;
-                    if (j < kZPre) {
+                // the table loads of the preloaded chunks are all issued before any store
+                float4 tv[kZPre][2];
 #pragma unroll
-                        for (int q = 0; q < kZPre; ++q)
-                            if (q == j) zc = zpre[q];
-                    } else {
-                        zc.load(ab, hb, c);
+                for (int q = 0; q < kZPre; ++q) {
+                    const int c = tid + q * static_cast<int>(blockDim.x);
+                    if (c < d / 8) {
+                        tv[q][0] = __ldg(tr + 2 * c);
+                        tv[q][1] = __ldg(tr + 2 * c + 1);
                     }
-                    zc.store(zr, c, t0, t1);
+                }
+#pragma unroll
+                for (int q = 0; q < kZPre; ++q) {
+                    const int c = tid + q * static_cast<int>(blockDim.x);
+                    if (c < d / 8) zpre[q].store(zr, c, tv[q][0], tv[q][1]);
+                }
+                for (int c = tid + kZPre * static_cast<int>(blockDim.x); c < d / 8; c += blockDim.x) {
+                    ZChunk<T> zc;
+                    zc.load(ab, hb, c);
+                    zc.store(zr, c, __ldg(tr + 2 * c), __ldg(tr + 2 * c + 1));
                 }
             }
             continue;
