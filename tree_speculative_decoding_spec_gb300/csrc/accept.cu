@@ -70,6 +70,7 @@ constexpr int kGreedyBatch = 8;
 
 __global__ void __launch_bounds__(kRowThreads, 3) k_rows_greedy(const float* __restrict__ logits, int V, int slice,
                                                              int slices, float4* __restrict__ part, void* ws) {
+    griddep_wait();   // launched early behind the previous kernel: its outputs are complete from here
     clear_status_then_trigger(ws);   // the walk may start loading the tree while the rows are read
     const int sl = blockIdx.x;
     const size_t row = blockIdx.y;
@@ -203,6 +204,7 @@ __device__ __forceinline__ void lse_ent_merge(float& m, float& s, float& t, floa
 // Typical acceptance: (m, s, t) of every row of logits_p (for entropy and log-sum-exp).
 __global__ void __launch_bounds__(kRowThreads) k_rows_ent(const float* __restrict__ lp, int V, int slice, int slices,
                                                           float inv_temp, float4* __restrict__ part, void* ws) {
+    griddep_wait();   // launched early behind the previous kernel: its outputs are complete from here
     clear_status_then_trigger(ws);   // the walk may start loading the tree while the rows are read
     const int sl = blockIdx.x;
     const size_t row = blockIdx.y;
@@ -225,6 +227,7 @@ __global__ void __launch_bounds__(kRowThreads) k_rows_lse(const float* __restric
                                                           const int32_t* __restrict__ child_off, int Tn, int V,
                                                           int slice, int slices, float inv_temp,
                                                           float4* __restrict__ part, void* ws) {
+    griddep_wait();   // launched early behind the previous kernel: its outputs are complete from here
     clear_status_then_trigger(ws);   // the walk may start loading the tree while the rows are read
     const int sl = blockIdx.x;
     const size_t row = blockIdx.y;
@@ -606,7 +609,7 @@ extern "C" spec_status tree_accept(int32_t mode, const float* logits_p, const fl
     const dim3 grid(p.slices, B * tree->T);
     // the rows kernel clears the status word (it flags nothing itself; the walk flags after its wait)
     if (mode == 0) {
-        SPEC_CUDA_TRY(launch("accept_rows_greedy", accept::k_rows_greedy, grid, dim3(accept::kRowThreads), 0, s, logits_p, V,
+        SPEC_CUDA_TRY(launch_ex("accept_rows_greedy", accept::k_rows_greedy, grid, dim3(accept::kRowThreads), 0, s, true, logits_p, V,
                              p.slice, p.slices, part, ws));
         // one thread per node is enough here (no vocabulary scans): small trees get cheap barriers
         const int walk_threads = std::min(accept::kWalkThreads, std::max(32, (tree->T + 31) / 32 * 32));
@@ -615,7 +618,7 @@ extern "C" spec_status tree_accept(int32_t mode, const float* logits_p, const fl
                              accept_path, next_token, margin));
     } else {
         const float inv_temp = 1.0f / temperature;
-        SPEC_CUDA_TRY(launch("accept_rows_lse", accept::k_rows_lse, grid, dim3(accept::kRowThreads), 0, s, logits_p, logits_q,
+        SPEC_CUDA_TRY(launch_ex("accept_rows_lse", accept::k_rows_lse, grid, dim3(accept::kRowThreads), 0, s, true, logits_p, logits_q,
                              tree->child_off, tree->T, V, p.slice, p.slices, inv_temp, part, ws));
         const size_t wsmem = V <= accept::kWalkCacheMax ? sizeof(float) * static_cast<size_t>(V) : 0;
         SPEC_CUDA_TRY(cudaFuncSetAttribute(accept::k_walk_reject, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -652,7 +655,7 @@ extern "C" spec_status tree_accept_typical(const float* logits_p, const int32_t*
     const dim3 grid(p.slices, B * tree->T);
     const float inv_temp = 1.0f / temperature;
     // the rows kernel clears the status word (it flags nothing itself; the walk flags after its wait)
-    SPEC_CUDA_TRY(launch("accept_rows_ent", accept::k_rows_ent, grid, dim3(accept::kRowThreads), 0, s, logits_p, V,
+    SPEC_CUDA_TRY(launch_ex("accept_rows_ent", accept::k_rows_ent, grid, dim3(accept::kRowThreads), 0, s, true, logits_p, V,
                          p.slice, p.slices, inv_temp, part, ws));
     const size_t wsmem = V <= accept::kWalkCacheMax ? sizeof(float) * static_cast<size_t>(V) : 0;
     SPEC_CUDA_TRY(cudaFuncSetAttribute(accept::k_walk_reject, cudaFuncAttributeMaxDynamicSharedMemorySize,
