@@ -346,3 +346,41 @@ def test_draft_folded_hydra_heads_workload():
     near = _compare_folded(st, wl.draft_inputs(w), parent, rank, "bf16")
     print(f"hydra heads folded: {near} near ties")
 
+
+
+@pytest.mark.parametrize("dtype,d,V,folded", [("bf16", 256, 32768, False), ("bf16", 256, 32768, True),
+                                               ("f32", 64, 4096, False), ("f32", 64, 4096, True)])
+def test_draft_exact_ties_take_the_lower_token(dtype, d, V, folded):
+    """Every vocabulary row appears four times (tokens v, v + V/4, v + V/2, v + 3V/4), so each
+    logit value is tied exactly four ways, across slices that different threads and warps of the
+    select hold.  The method orders equal logits by token (the lower first): the top-8 of a row is
+    the four copies of the largest value in token order, then the four of the second.  On the
+    tensor-core path the copies sit a multiple of two weight tiles apart, where the projection
+    walks K in the same order, so the GPU's logits of a tied group are equal bit for bit too
+    (copies whose K order differed would tie only up to rounding, a near tie the other tests
+    allow).  Distinct values stay far apart at this scale, so no pick may differ from the
+    oracle's."""
+    st = lib()
+    q = V // 4
+    w = wl.Workload("ties", dtype, B=2, seed=31, tree=("cartesian", (8, 4)), d=d, V=V, cond=(1, 1), topk=(8, 4))
+    parent, rank = wl.make_tree(w.tree)
+    x = wl.draft_inputs(w)
+    rng = np.random.default_rng(31)
+    enc = (lambda a: wl.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    for k in range(2):
+        base = rng.standard_normal((q, d), dtype=np.float32) * np.float32(0.25)
+        x["W2"][k] = enc(np.tile(base, (4, 1)))
+    x["E"] = enc(rng.standard_normal(np.shape(x["E"]), dtype=np.float32))
+    near = (_compare_folded(st, x, parent, rank, dtype) if folded else _compare(st, x, parent, rank, dtype))
+    assert near == 0, near
+    # the picks themselves: each parent's children carry tied tokens in increasing order
+    tree = st.spec_tree_build(parent, rank)
+    tok = (_run_folded(st, x, tree, [True, True]) if folded else _run(st, x, tree))[0].cpu().numpy()
+    for b in range(2):
+        for u in range(len(parent)):
+            kids = [c for c in range(1, len(parent)) if parent[c] == u]
+            kids.sort(key=lambda c: rank[c])
+            t = [int(tok[b, c]) for c in kids]
+            for i in range(0, len(t), 4):
+                grp = t[i:i + 4]
+                assert grp == sorted(grp) and len({g % q for g in grp}) == 1, (b, u, t)
