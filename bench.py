@@ -524,16 +524,22 @@ def run_ours(args):
 
 
 CONFIG_ENTRIES = [
-    # (entry name, component, no_fold): every config of the parity suite that the headline step is not
-    ("1_tiny_fp32_step", "step-tiny-fp32", False),
-    ("2_vicuna7b_attention", "attention-vicuna7b", False),
-    ("2_vicuna7b_greedy_accept", "accept-greedy-vicuna7b", False),
-    ("3_hydra_heads_b4_folded", "draft-hydra-b4", False),
-    ("3_hydra_heads_b4_unfolded", "draft-hydra-b4", True),
-    ("4_70b_gqa_attention", "attention-70b-gqa", False),
-    ("5_long32k_attention_t341", "attention-32k", False),
-    ("5_long32k_attention_t256", "attention-32k-t256", False),
-    ("5_long32k_rejection_accept", "accept-rejection-32k", False),
+    # (entry name, component, no_fold): every workload of the parity suite besides the headline step
+    ("tiny_fp32_step", "step-tiny-fp32", False),
+    ("vicuna7b_attention", "attention-vicuna7b", False),
+    ("vicuna7b_greedy_accept", "accept-greedy-vicuna7b", False),
+    ("hydra_heads_b4_folded", "draft-hydra-b4", False),
+    ("hydra_heads_b4_unfolded", "draft-hydra-b4", True),
+    ("gqa70b_b8_attention", "attention-70b-gqa", False),
+    ("long32k_attention_t341", "attention-32k", False),
+    ("long32k_attention_t256", "attention-32k-t256", False),
+    ("long32k_rejection_accept", "accept-rejection-32k", False),
+    # the entry points past the verification step itself
+    ("long32k_typical_accept", "accept-typical-32k", False),
+    ("gqa70b_b8_paged_attention", "attention-paged-70b-b8", False),
+    ("vicuna7b_layernorm_heads", "draft-ln-heads-vicuna7b", False),
+    ("vicuna7b_kv_commit", "kv-commit-vicuna7b", False),
+    ("gqa70b_b8_kv_commit", "kv-commit-70b-b8", False),
 ]
 
 
