@@ -390,6 +390,16 @@ def run_ours(args):
         u_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in uev) / len(uev), dev)
         unfolded = {"value": world * 1000.0 / u_ms, "unit": UNIT, "ms_per_step": u_ms,
                     "draft_first_layer": "whole W1 streamed per step", "clocks": clocks.summary(tu0, tu1)}
+    # the same step captured once into a CUDA graph and replayed (the per-call host work leaves the step)
+    try:
+        tg0 = time.time()
+        g_list = graph_times(step, lambda: None, flush, args.steps)
+        tg1 = time.time()
+        g_ms = max_over_ranks(sum(g_list) / len(g_list), dev)
+        graph_step = {"value": world * 1000.0 / g_ms, "unit": UNIT, "ms_per_step": g_ms,
+                      "clocks": clocks.summary(tg0, tg1)}
+    except Exception as e:
+        graph_step = {"unavailable": str(e).splitlines()[0][:200]}
     time.sleep(0.3)
     clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in evs]
@@ -509,6 +519,7 @@ def run_ours(args):
         "kernels": kern_table,
         "roofline": roofline,
         "unfolded_step": unfolded,
+        "graph_step": graph_step,
         "fold_tables_bytes": (sum(int(c == 1) for c in cond) * w.V * w.d * 4) if not args.no_fold else 0,
         "fold_table_build_ms_per_head": fold_ms,
         "configs": configs,
@@ -932,6 +943,37 @@ def make_component(name, dev, no_fold=False):
     return comp
 
 
+def graph_times(fn, pre, flush, n):
+    """fn captured once into a CUDA graph (after a warm-up call on the capture stream), then
+    replayed n times, each after pre() and an L2 flush, timed with CUDA events: the device time
+    of the same work without the per-call host work (argument checks, tensor maps, launches)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        pre()
+        fn()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    pre()
+    with torch.cuda.graph(g):
+        fn()
+    evs = []
+    for i in range(n + 3):
+        pre()
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
+        if i >= 3:
+            evs.append((a, b))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
 def measure_component(comp, flush, clocks, steps, min_wall_s=0.4):
     """CUDA-event time of one call (L2 flushed before each), a traced pass for
     per-kernel times, the clock record of the timed window, and the roofline."""
@@ -991,6 +1033,15 @@ def measure_component(comp, flush, clocks, steps, min_wall_s=0.4):
                  "roofline_us": max(t_hbm, t_tc), "algorithmic_bytes": abytes, "flops": flops})
     out = {"us_per_call": us, "calls_per_s": 1e6 / us, "calls_timed": len(ms), "kernels": kern, "roofline": roof,
            "clocks": clocks.summary(t0, t1) if clocks is not None else None}
+    # the same call replayed from a CUDA graph
+    try:
+        tg0 = time.time()
+        gms = graph_times(call, pre, flush, max(steps, 20))
+        tg1 = time.time()
+        out["graph"] = {"us_per_call": 1000.0 * statistics.median(gms), "calls_timed": len(gms),
+                        "clocks": clocks.summary(tg0, tg1) if clocks is not None else None}
+    except Exception as e:   # a call that cannot be captured reports why
+        out["graph"] = {"unavailable": str(e).splitlines()[0][:200]}
     out.update(comp["report"]())
     return out
 
