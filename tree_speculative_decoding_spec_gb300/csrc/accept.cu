@@ -119,10 +119,20 @@ __global__ void __launch_bounds__(kRowThreads, 3) k_rows_greedy(const float* __r
 
 // ---------------------------------------------------------------- rows (rejection)
 
-// (max, sum exp(x - max)) of x = logits * inv_temp over this thread's share of
-// [v0, v1): the values are held in registers, so one HBM pass and no branches.
-__device__ __forceinline__ float2 thread_lse(const float* __restrict__ row, int v0, int v1, float inv_temp, bool vec4) {
-    float x[4 * kLseIter];
+// exp(y) for y <= 0 as 2^(y log2 e) on the special-function unit: each element of a row
+// sum costs one FFMA and one ex2 (the scale and the shift folded into the FFMA); ex2 of
+// -inf is 0.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+constexpr float kLog2e = 1.4426950408889634f;
+
+// This thread's share of [v0, v1) of one logits row, raw, in registers (-inf past v1): one
+// HBM pass, every load issued before any use.
+__device__ __forceinline__ float thread_load(const float* __restrict__ row, int v0, int v1, bool vec4,
+                                             float (&x)[4 * kLseIter]) {
     float m = -INFINITY;
     if (vec4) {
 #pragma unroll
@@ -130,59 +140,52 @@ __device__ __forceinline__ float2 thread_lse(const float* __restrict__ row, int 
             const int e = v0 + 4 * (static_cast<int>(threadIdx.x) + kRowThreads * it);
             float4 q = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
             if (e < v1) q = __ldcs(reinterpret_cast<const float4*>(row + e));
-            x[4 * it] = q.x * inv_temp; x[4 * it + 1] = q.y * inv_temp;
-            x[4 * it + 2] = q.z * inv_temp; x[4 * it + 3] = q.w * inv_temp;
-            m = fmaxf(m, fmaxf(fmaxf(x[4 * it], x[4 * it + 1]), fmaxf(x[4 * it + 2], x[4 * it + 3])));
+            x[4 * it] = q.x; x[4 * it + 1] = q.y; x[4 * it + 2] = q.z; x[4 * it + 3] = q.w;
         }
     } else {
 #pragma unroll
         for (int it = 0; it < 4 * kLseIter; ++it) {
             const int e = v0 + static_cast<int>(threadIdx.x) + kRowThreads * it;
-            x[it] = e < v1 ? row[e] * inv_temp : -INFINITY;
-            m = fmaxf(m, x[it]);
+            x[it] = e < v1 ? row[e] : -INFINITY;
         }
     }
-    float s = 0.f;
-    if (m != -INFINITY) {
 #pragma unroll
-        for (int i = 0; i < 4 * kLseIter; ++i) s += expf(x[i] - m);
+    for (int i = 0; i < 4 * kLseIter; i += 4) m = fmaxf(m, fmaxf(fmaxf(x[i], x[i + 1]), fmaxf(x[i + 2], x[i + 3])));
+    return m;   // raw maximum (inv_temp > 0 keeps the order)
+}
+
+// (max, sum exp(x - max)) of x = logits * inv_temp over this thread's share of [v0, v1).
+__device__ __forceinline__ float2 thread_lse(const float* __restrict__ row, int v0, int v1, float inv_temp, bool vec4) {
+    float x[4 * kLseIter];
+    const float mraw = thread_load(row, v0, v1, vec4, x);
+    if (mraw == -INFINITY) return make_float2(-INFINITY, 0.f);
+    const float m = mraw * inv_temp;
+    const float c = inv_temp * kLog2e, off = -m * kLog2e;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4 * kLseIter; i += 2) {
+        s0 += ex2_approx(fmaf(x[i], c, off));
+        s1 += ex2_approx(fmaf(x[i + 1], c, off));
     }
-    return make_float2(m, s);
+    return make_float2(m, s0 + s1);
 }
 
 // (m, s, t) with m the max, s = sum exp(x - m) and t = sum exp(x - m) * x over
 // this thread's share: (m + ln s) - t / s is the entropy of softmax(x).
 __device__ __forceinline__ float3 thread_lse_ent(const float* __restrict__ row, int v0, int v1, float inv_temp, bool vec4) {
     float x[4 * kLseIter];
-    float m = -INFINITY;
-    if (vec4) {
+    const float mraw = thread_load(row, v0, v1, vec4, x);
+    if (mraw == -INFINITY) return make_float3(-INFINITY, 0.f, 0.f);
+    const float m = mraw * inv_temp;
+    const float c = inv_temp * kLog2e, off = -m * kLog2e;
+    float sum = 0.f, t = 0.f;   // t over the raw values, scaled by inv_temp at the end
 #pragma unroll
-        for (int it = 0; it < kLseIter; ++it) {
-            const int e = v0 + 4 * (static_cast<int>(threadIdx.x) + kRowThreads * it);
-            float4 q = make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            if (e < v1) q = __ldcs(reinterpret_cast<const float4*>(row + e));
-            x[4 * it] = q.x * inv_temp; x[4 * it + 1] = q.y * inv_temp;
-            x[4 * it + 2] = q.z * inv_temp; x[4 * it + 3] = q.w * inv_temp;
-            m = fmaxf(m, fmaxf(fmaxf(x[4 * it], x[4 * it + 1]), fmaxf(x[4 * it + 2], x[4 * it + 3])));
-        }
-    } else {
-#pragma unroll
-        for (int it = 0; it < 4 * kLseIter; ++it) {
-            const int e = v0 + static_cast<int>(threadIdx.x) + kRowThreads * it;
-            x[it] = e < v1 ? row[e] * inv_temp : -INFINITY;
-            m = fmaxf(m, x[it]);
-        }
+    for (int i = 0; i < 4 * kLseIter; ++i) {
+        const float e = ex2_approx(fmaf(x[i], c, off));
+        sum += e;
+        t = x[i] == -INFINITY ? t : fmaf(e, x[i], t);
     }
-    float sum = 0.f, t = 0.f;
-    if (m != -INFINITY) {
-#pragma unroll
-        for (int i = 0; i < 4 * kLseIter; ++i) {
-            const float e = expf(x[i] - m);
-            sum += e;
-            t += x[i] == -INFINITY ? 0.f : e * x[i];
-        }
-    }
-    return make_float3(m, sum, t);
+    return make_float3(m, sum, t * inv_temp);
 }
 
 // Merge (m2, s2, t2) into (m, s, t): s and t are both scaled to the larger maximum.
@@ -618,8 +621,8 @@ extern "C" spec_status tree_accept(int32_t mode, const float* logits_p, const fl
                              accept_path, next_token, margin));
     } else {
         const float inv_temp = 1.0f / temperature;
-        SPEC_CUDA_TRY(launch_ex("accept_rows_lse", accept::k_rows_lse, grid, dim3(accept::kRowThreads), 0, s, true, logits_p, logits_q,
-                             tree->child_off, tree->T, V, p.slice, p.slices, inv_temp, part, ws));
+        SPEC_CUDA_TRY(launch_ex("accept_rows_lse", accept::k_rows_lse, grid, dim3(accept::kRowThreads), 0, s, true, logits_p,
+                                logits_q, tree->child_off, tree->T, V, p.slice, p.slices, inv_temp, part, ws));
         const size_t wsmem = V <= accept::kWalkCacheMax ? sizeof(float) * static_cast<size_t>(V) : 0;
         SPEC_CUDA_TRY(cudaFuncSetAttribute(accept::k_walk_reject, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(sizeof(float) * accept::kWalkCacheMax)));
