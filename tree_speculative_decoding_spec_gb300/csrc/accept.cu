@@ -448,11 +448,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1) k_walk_reject(const float4* _
     const float lsp = lse_p[ustar], lsq = lse_q[ustar];
     const float* rp = lp + srow;
     const float* rq = typical ? nullptr : lq + srow;
-    // weight of token x: p (leaf, or residual all zero) or max(p - q, 0)
+    // weight of token x: p (leaf, or residual all zero) or max(p - q, 0); exp(y) as
+    // 2^(y log2 e), the scale and the shift in one FFMA
+    const float wc = inv_temp * kLog2e, wop = -lsp * kLog2e, woq = -lsq * kLog2e;
     auto weight = [&](int x, bool resid) -> float {
-        const float pv = expf(rp[x] * inv_temp - lsp);
+        const float pv = ex2_approx(fmaf(rp[x], wc, wop));
         if (!resid) return pv;
-        return fmaxf(pv - expf(rq[x] * inv_temp - lsq), 0.f);
+        return fmaxf(pv - ex2_approx(fmaf(rq[x], wc, woq)), 0.f);
     };
     // The range sums below compute every token's weight once, 16 loads per lane in flight;
     // a vocabulary of at most kWalkCacheMax tokens keeps them in shared memory, where the
