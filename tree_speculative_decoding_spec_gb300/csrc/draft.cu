@@ -411,6 +411,21 @@ __global__ void __launch_bounds__(kFoldWarps * 32, 2) k_fold_h(const __nv_bfloat
     const int nchunk = d / 8;                      // 16-byte chunks of a row's h_b half
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     for (int b0 = 0; b0 < B; b0 += kFoldSeq) {
+        // the epilogue's operands that do not depend on the sums (warp 0 with z: the root
+        // tokens' table entries and h) load now, with the weights
+        float tpre[4] = {0.f, 0.f, 0.f, 0.f}, hpre[4] = {0.f, 0.f, 0.f, 0.f};
+        if (z && warp == 0) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int m = (e < 2) ? r0 : r1;
+                const int bb = b0 + 2 * t + (e & 1);
+                if (m < d && bb < B) {
+                    const int tok = min(max(root_tok[bb], 0), V - 1);   // k_init_root flags a bad token
+                    tpre[e] = tab[static_cast<size_t>(tok) * d + m];
+                    hpre[e] = __bfloat162float(h[static_cast<size_t>(bb) * d + m]);
+                }
+            }
+        }
         const int bq = b0 + g;                     // this lane's B column (sequence)
         const uint4* hq = reinterpret_cast<const uint4*>(h + static_cast<size_t>(bq < B ? bq : 0) * d);
         float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -462,10 +477,7 @@ __global__ void __launch_bounds__(kFoldWarps * 32, 2) k_fold_h(const __nv_bfloat
                 if (!z) {
                     a_out[static_cast<size_t>(b) * d + m] = a;
                 } else {
-                    const int tok = min(max(root_tok[b], 0), V - 1);   // k_init_root flags a bad token
-                    const float xx = a + tab[static_cast<size_t>(tok) * d + m];
-                    z[static_cast<size_t>(b) * d + m] =
-                        __float2bfloat16_rn(__bfloat162float(h[static_cast<size_t>(b) * d + m]) + silu(xx));
+                    z[static_cast<size_t>(b) * d + m] = __float2bfloat16_rn(hpre[e] + silu(a + tpre[e]));
                 }
             }
         }
