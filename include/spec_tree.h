@@ -11,7 +11,15 @@
  *    size comes from the matching *_workspace_size call.  Apart from
  *    spec_tree_build (which copies a small host table to the device and waits
  *    for it) no call allocates, frees or synchronises; all work is queued on
- *    the given stream in order.  0 selects the legacy default stream.
+ *    the given stream in order.  0 selects the legacy default stream.  A
+ *    sequence of calls on one stream can therefore be captured into a CUDA
+ *    graph (make one call first, outside the capture, so that one-time setup
+ *    such as kernel attributes happens there) and replayed: the replay
+ *    repeats the same work on the same buffers without the per-call host
+ *    work.  spec_read_device_status synchronises and is not capturable.
+ *    Some kernels launch as programmatic dependents of the kernel before
+ *    them on the stream; they wait for it before reading anything it could
+ *    have written.
  *  - "device" pointers must point to memory of the current CUDA device and be
  *    16-byte aligned (SPEC_EALIGN otherwise); "host" pointers are read during
  *    the call only.
