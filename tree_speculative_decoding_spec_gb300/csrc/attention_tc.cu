@@ -649,8 +649,13 @@ static int max_active_clusters(int n) {
 // Prefix splits: one CTA per (split, KV head x row block, sequence); the last
 // non-empty split of each sequence also takes the tree keys.  Pick the split
 // count minimising an estimated makespan -- waves of one CTA per SM times the
-// longest CTA (its prefix tiles, the tree tiles, ~2 tiles of fixed cost) --
-// ties to fewer splits (less partial traffic).
+// longest CTA (its prefix tiles, the tree tiles, ~4 tiles of fixed cost: setup,
+// the first loads, the epilogue), plus ~14 tiles for the combine kernel when the
+// splits cannot merge on chip -- ties to fewer splits (less partial traffic).
+// Merging on chip needs every cluster of the n splits resident at once.
+constexpr int kPlanFixedTiles = 4;
+constexpr int kPlanCombineTiles = 14;
+
 AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_count) {
     AttnTcPlan p;
     const int g = Hq / Hkv;
@@ -658,12 +663,13 @@ AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_c
     const int64_t base = static_cast<int64_t>(B) * Hkv * p.n_rb;
     const int tiles = (Lmax + kAKeys - 1) / kAKeys;
     const int tree_tiles = (T + kAKeys - 1) / kAKeys;
+    auto fusable = [&](int n) { return n > 1 && n <= kFusedMaxSplits && base <= max_active_clusters(n); };
     int64_t best_cost = INT64_MAX;
     int best = 1;
     for (int n = 1; n <= std::min(tiles, 64); ++n) {
         const int per = (tiles + n - 1) / n;
         const int64_t waves = (base * n + sm_count - 1) / sm_count;
-        const int64_t cost = waves * (per + tree_tiles + 2);
+        const int64_t cost = waves * (per + tree_tiles + kPlanFixedTiles) + ((n > 1 && !fusable(n)) ? kPlanCombineTiles : 0);
         if (cost < best_cost) {
             best_cost = cost;
             best = n;
@@ -675,7 +681,7 @@ AttnTcPlan attn_tc_plan(int B, int Hq, int Hkv, int T, int Lmax, int D, int sm_c
     // n_pre SMs of one GPC are free together, so a second wave of clusters leaves SMs idle
     // (32K prefix, 96 clusters of 3: 203 -> 296 us), and the one-split plans (a cluster of
     // one) write their output directly anyway
-    p.fused = p.n_pre > 1 && p.n_pre <= kFusedMaxSplits && base <= max_active_clusters(p.n_pre);
+    p.fused = fusable(p.n_pre);
     // partial layout shared with the CUDA-core path: n_pre + 1 slots per row (the last unused
     // here); none with a single split or an on-chip merge
     p.part_bytes = (p.n_pre == 1 || p.fused)
