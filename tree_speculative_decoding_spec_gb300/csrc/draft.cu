@@ -411,21 +411,6 @@ __global__ void __launch_bounds__(kFoldWarps * 32, 2) k_fold_h(const __nv_bfloat
     const int nchunk = d / 8;                      // 16-byte chunks of a row's h_b half
     const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
     for (int b0 = 0; b0 < B; b0 += kFoldSeq) {
-        // the epilogue's operands that do not depend on the sums (warp 0 with z: the root
-        // tokens' table entries and h) load now, with the weights
-        float tpre[4] = {0.f, 0.f, 0.f, 0.f}, hpre[4] = {0.f, 0.f, 0.f, 0.f};
-        if (z && warp == 0) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const int m = (e < 2) ? r0 : r1;
-                const int bb = b0 + 2 * t + (e & 1);
-                if (m < d && bb < B) {
-                    const int tok = min(max(root_tok[bb], 0), V - 1);   // k_init_root flags a bad token
-                    tpre[e] = tab[static_cast<size_t>(tok) * d + m];
-                    hpre[e] = __bfloat162float(h[static_cast<size_t>(bb) * d + m]);
-                }
-            }
-        }
         const int bq = b0 + g;                     // this lane's B column (sequence)
         const uint4* hq = reinterpret_cast<const uint4*>(h + static_cast<size_t>(bq < B ? bq : 0) * d);
         float c[4] = {0.f, 0.f, 0.f, 0.f};
@@ -477,7 +462,10 @@ __global__ void __launch_bounds__(kFoldWarps * 32, 2) k_fold_h(const __nv_bfloat
                 if (!z) {
                     a_out[static_cast<size_t>(b) * d + m] = a;
                 } else {
-                    z[static_cast<size_t>(b) * d + m] = __float2bfloat16_rn(hpre[e] + silu(a + tpre[e]));
+                    const int tok = min(max(root_tok[b], 0), V - 1);   // k_init_root flags a bad token
+                    const float xx = a + tab[static_cast<size_t>(tok) * d + m];
+                    z[static_cast<size_t>(b) * d + m] =
+                        __float2bfloat16_rn(__bfloat162float(h[static_cast<size_t>(b) * d + m]) + silu(xx));
                 }
             }
         }
@@ -759,25 +747,18 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
                 if (c_row[a] < 0 || (cpr > 1 && a != ci)) continue;
                 const float4* tr = reinterpret_cast<const float4*>(ftab + static_cast<size_t>(topi[c_rank[a]]) * d);
                 T* zr = zf + (row0 + c_row[a]) * d;
-                // the table loads of the preloaded chunks are all issued before any store
-                float4 tv[kZPre][2];
-#pragma unroll
-                for (int q = 0; q < kZPre; ++q) {
-                    const int c = tid + q * static_cast<int>(blockDim.x);
-                    if (c < d / 8) {
-                        tv[q][0] = __ldg(tr + 2 * c);
-                        tv[q][1] = __ldg(tr + 2 * c + 1);
-                    }
-                }
-#pragma unroll
-                for (int q = 0; q < kZPre; ++q) {
-                    const int c = tid + q * static_cast<int>(blockDim.x);
-                    if (c < d / 8) zpre[q].store(zr, c, tv[q][0], tv[q][1]);
-                }
-                for (int c = tid + kZPre * static_cast<int>(blockDim.x); c < d / 8; c += blockDim.x) {
+                int j = 0;
+                for (int c = tid; c < d / 8; c += blockDim.x, ++j) {
+                    const float4 t0 = tr[2 * c], t1 = tr[2 * c + 1];
                     ZChunk<T> zc;
-                    zc.load(ab, hb, c);
-                    zc.store(zr, c, __ldg(tr + 2 * c), __ldg(tr + 2 * c + 1));
+                    if (j < kZPre) {
+#pragma unroll
+                        for (int q = 0; q < kZPre; ++q)
+                            if (q == j) zc = zpre[q];
+                    } else {
+                        zc.load(ab, hb, c);
+                    }
+                    zc.store(zr, c, t0, t1);
                 }
             }
             continue;
