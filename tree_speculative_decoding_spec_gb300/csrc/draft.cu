@@ -521,10 +521,9 @@ __device__ __forceinline__ void write_next_row(T* __restrict__ dst, const T* __r
 // One CTA per row: top-k over the row's sorted per-slice candidate lists and
 // the row's log-sum-exp, then the children of the row's parent node(s).
 // Merging: each thread holds its slice's sorted list in registers (more
-// slices than threads are folded in by bitonic merges); each warp then takes
-// the top-k of its lists in k rounds of warp reductions (the owner of the best
-// head pops it), and after one barrier warp 0 takes the top-k of the warps'
-// lists the same way.
+// slices than threads are folded in by bitonic merges); k rounds then take the
+// best list head of the CTA -- warp reductions and one barrier per round --
+// and pop it from its owner's list.
 //
 // The tree's structure (children, ranks, input rows, ancestors) is written once
 // by spec_tree_build and by none of the kernels this one follows, so a CTA with
@@ -642,55 +641,36 @@ __global__ void __launch_bounds__(256) k_select(const Cand* __restrict__ part_c,
     for (int o = 16; o > 0; o >>= 1) lse_merge(M, S, __shfl_xor_sync(0xffffffffu, M, o), __shfl_xor_sync(0xffffffffu, S, o));
     if (lane == 0) wlse[warp] = make_float2(M, S);
 
-    // 2. top-k over the list heads in two levels.  A candidate is compared through a
-    // 32-bit key that orders like its logit (NaN lowest, -0 as +0), so a warp's best
-    // head is one max-reduction of keys and one min-reduction of the indices holding
-    // that key (lower token wins ties), and its owner pops it.  (a) Each warp takes the
-    // top-k of its 32 lists by k such rounds, with no barrier; (b) after one barrier
-    // warp 0 holds the warps' sorted lists (lane w: warp w's) and takes the top-k of
-    // those by k more rounds.  The global top-k lies within the warps' top-k.
+    // 2. k rounds over the list heads.  A candidate is compared through a 32-bit key
+    // that orders like its logit (NaN lowest, -0 as +0), so the warp's best head is one
+    // max-reduction of keys and one min-reduction of the indices holding that key (lower
+    // token wins ties); the CTA's best is the same two reductions over the warps'
+    // (double-buffered shared slots, one barrier per round); the owner pops it.
     // Candidates are unique (the slices are disjoint), so the index identifies the owner.
-    __shared__ uint2 wtop[8][KMAX];
+    __shared__ uint2 slot[2][8];
     const int nw = blockDim.x >> 5;
 #pragma unroll 1
     for (int rr = 0; rr < k; ++rr) {
         const unsigned key = order_key(lv[0]);
         const unsigned wk = __reduce_max_sync(0xffffffffu, key);
         const unsigned wi = __reduce_min_sync(0xffffffffu, key == wk ? static_cast<unsigned>(li[0]) : 0xffffffffu);
-        if (static_cast<unsigned>(li[0]) == wi) {   // this thread's head won: pop it
+        if (lane == 0) slot[rr & 1][warp] = make_uint2(wk, wi);
+        __syncthreads();
+        const uint2 c = lane < nw ? slot[rr & 1][lane] : make_uint2(0u, 0xffffffffu);
+        const unsigned bk = __reduce_max_sync(0xffffffffu, c.x);
+        const unsigned bi = __reduce_min_sync(0xffffffffu, c.x == bk ? c.y : 0xffffffffu);
+        if (static_cast<unsigned>(li[0]) == bi) {   // this thread's head won: pop it
 #pragma unroll
             for (int e = 0; e + 1 < KMAX; ++e) { lv[e] = lv[e + 1]; li[e] = li[e + 1]; }
             lv[KMAX - 1] = -INFINITY;
             li[KMAX - 1] = 0x7fffffff;
         }
-        if (lane == 0) wtop[warp][rr] = make_uint2(wk, wi);
-    }
-    __syncthreads();
-    if (warp == 0) {
-        unsigned mk[KMAX], mi[KMAX];
-#pragma unroll
-        for (int e = 0; e < KMAX; ++e) {
-            const uint2 c = (lane < nw && e < k) ? wtop[lane][e] : make_uint2(0u, 0xffffffffu);
-            mk[e] = c.x;
-            mi[e] = c.y;
-        }
-#pragma unroll 1
-        for (int rr = 0; rr < k; ++rr) {
-            const unsigned bk = __reduce_max_sync(0xffffffffu, mk[0]);
-            const unsigned bi = __reduce_min_sync(0xffffffffu, mk[0] == bk ? mi[0] : 0xffffffffu);
-            if (mi[0] == bi) {
-#pragma unroll
-                for (int e = 0; e + 1 < KMAX; ++e) { mk[e] = mk[e + 1]; mi[e] = mi[e + 1]; }
-                mk[KMAX - 1] = 0u;
-                mi[KMAX - 1] = 0xffffffffu;
-            }
-            if (lane == 0) {
-                int ix = static_cast<int>(bi);
-                // fewer than k finite logits (NaN/inf weights) leave placeholders: keep tokens in range
-                if (ix < 0 || ix >= V) { flag_status(ws, SPEC_EINVAL); ix = 0; }
-                topv[rr] = key_value(bk);
-                topi[rr] = ix;
-            }
+        if (tid == 0) {
+            int ix = static_cast<int>(bi);
+            // fewer than k finite logits (NaN/inf weights) leave placeholders: keep tokens in range
+            if (ix < 0 || ix >= V) { flag_status(ws, SPEC_EINVAL); ix = 0; }
+            topv[rr] = key_value(bk);
+            topi[rr] = ix;
         }
     }
     if (tid == 0) {
