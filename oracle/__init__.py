@@ -32,7 +32,7 @@ from .tree import tree_encode, tree_mask
 from .heads import silu, hydra_draft, hydra_draft_heads
 from .attention import tree_attention, tree_attention_paged, gather_pages
 from .accept import greedy_accept, rejection_accept, typical_accept
-from .kv_commit import kv_commit
+from .kv_commit import kv_commit, kv_commit_paged
 from .philox import philox4, philox4x32_10, philox_uniform_pair, uniform_from_u32
 
 __all__ = [
@@ -42,4 +42,5 @@ __all__ = [
     "tree_attention", "tree_attention_paged", "gather_pages",
     "greedy_accept", "rejection_accept", "typical_accept", "kv_commit",
     "philox4", "philox4x32_10", "philox_uniform_pair", "uniform_from_u32",
+    "kv_commit_paged",
 ]

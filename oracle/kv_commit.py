@@ -65,3 +65,53 @@ def kv_commit(k_tree, v_tree, k_cache, v_cache, prefix_len, accept_len, accept_p
             v_cache[b, :, L + i] = v_tree[b, :, node]
         prefix_len[b] = L + m + 1
     return k_cache, v_cache, prefix_len, bad
+
+
+def kv_commit_paged(k_tree, v_tree, k_pool, v_pool, block_table, block_size, prefix_len, accept_len, accept_path,
+                    tree):
+    """The same commit into a paged cache: return (k_pool', v_pool', prefix_len', bad).
+
+    Hydra Guide, "Hydra Production Engineering Checklist", item 3 (KV-Cache
+    Tree Branch Management: the cache lives in pre-allocated static blocks) with
+    the layout read for the paged attention: pool [num_blocks, Hkv, block_size,
+    D], block_table[b, j] the pool block of positions j*block_size ..
+    (j+1)*block_size - 1 of sequence b.  Cache position L + i of sequence b is
+    pool row (block_table[b, (L+i) // block_size], :, (L+i) % block_size), so
+    the accepted node i's rows land there; everything else as ``kv_commit``.
+    Beyond kv_commit's checks a sequence is also left unchanged (and reported)
+    when its commit would pass max_blocks * block_size positions or a block it
+    would write lies outside the pool.
+    """
+    k_pool = np.array(k_pool, copy=True)
+    v_pool = np.array(v_pool, copy=True)
+    k_tree = np.asarray(k_tree)
+    v_tree = np.asarray(v_tree)
+    block_table = np.asarray(block_table, dtype=np.int64)
+    prefix_len = np.array(prefix_len, dtype=np.int64, copy=True).reshape(-1)
+    accept_len = np.asarray(accept_len, dtype=np.int64).reshape(-1)
+    accept_path = np.asarray(accept_path, dtype=np.int64)
+    B, max_blocks = block_table.shape
+    num_blocks = k_pool.shape[0]
+    parent = tree["parent"]
+    bad = np.zeros(B, dtype=bool)
+    for b in range(B):
+        m = int(accept_len[b])
+        if m < 0 or m > tree["max_depth"]:
+            bad[b] = True
+            continue
+        path = [int(x) for x in accept_path[b, :m + 1]]
+        chain = path[0] == 0 and all(0 <= path[i] < tree["T"] and parent[path[i]] == path[i - 1]
+                                     for i in range(1, m + 1))
+        L = int(prefix_len[b])
+        if not chain or L < 0 or L + m + 1 > max_blocks * block_size:
+            bad[b] = True
+            continue
+        blocks = [int(block_table[b, (L + i) // block_size]) for i in range(m + 1)]
+        if any(blk < 0 or blk >= num_blocks for blk in blocks):
+            bad[b] = True
+            continue
+        for i, node in enumerate(path):
+            k_pool[blocks[i], :, (L + i) % block_size] = k_tree[b, :, node]
+            v_pool[blocks[i], :, (L + i) % block_size] = v_tree[b, :, node]
+        prefix_len[b] = L + m + 1
+    return k_pool, v_pool, prefix_len, bad

@@ -116,3 +116,76 @@ def test_invalid_sequences_are_left_alone():
     kc2, vc2, L2, bad = kv_commit(kt, kt, kc, kc, L, alen, apath, tree)
     assert bad.tolist() == [True, True, True, True]
     assert (kc2 == kc).all() and (L2 == L).all()
+
+
+# ---- the paged form: the same commit through a block table
+
+def _paged_case(rng, B, Hkv, T, D, bs, max_blocks, prefix):
+    """A pool holding every sequence's blocks in a shuffled order (plus spare blocks)."""
+    parent, rank = wl.random_tree(rng, T, max_children=3)
+    tree = tree_encode(parent, rank)
+    num_blocks = B * max_blocks + 3
+    order = rng.permutation(num_blocks)
+    table = order[:B * max_blocks].reshape(B, max_blocks).astype(np.int32)
+    k_pool = rng.standard_normal((num_blocks, Hkv, bs, D)).astype(np.float32)
+    v_pool = rng.standard_normal((num_blocks, Hkv, bs, D)).astype(np.float32)
+    k_tree = rng.standard_normal((B, Hkv, T, D)).astype(np.float32)
+    v_tree = rng.standard_normal((B, Hkv, T, D)).astype(np.float32)
+    return tree, table, k_pool, v_pool, k_tree, v_tree, np.array(prefix, dtype=np.int32)
+
+
+@pytest.mark.parametrize("bs", [4, 16])
+def test_paged_commit_equals_the_contiguous_commit(bs):
+    """Gathering the committed pool gives the contiguous commit of the gathered cache (the
+    contiguous commit is pinned above by the path equivalence through torch's SDPA)."""
+    from oracle import gather_pages, kv_commit_paged
+    rng = np.random.default_rng(bs)
+    B, Hkv, T, D, max_blocks = 4, 2, 23, 8, 6
+    prefix = [0, bs - 1, 2 * bs + 3, max_blocks * bs - 5]   # the last one crosses no block boundary
+    tree, table, kp, vp, kt, vt, plen = _paged_case(rng, B, Hkv, T, D, bs, max_blocks, prefix)
+    _, alen, apath = _paths(rng, tree, B)
+    alen[-1] = min(int(alen[-1]), 3)        # keep the last sequence inside its capacity
+    apath[-1, alen[-1] + 1:] = -1
+    full = np.full(B, max_blocks * bs, dtype=np.int32)
+    kc = gather_pages(kp, table, bs, full)
+    vc = gather_pages(vp, table, bs, full)
+    kc2, vc2, L2, bad = kv_commit(kt, vt, kc, vc, plen, alen, apath, tree)
+    kp2, vp2, L3, bad3 = kv_commit_paged(kt, vt, kp, vp, table, bs, plen, alen, apath, tree)
+    np.testing.assert_array_equal(bad, bad3)
+    np.testing.assert_array_equal(L2, L3)
+    assert not bad.any()
+    np.testing.assert_array_equal(gather_pages(kp2, table, bs, full), kc2)
+    np.testing.assert_array_equal(gather_pages(vp2, table, bs, full), vc2)
+    # the spare blocks (in no table) are untouched
+    spare = np.setdiff1d(np.arange(kp.shape[0]), table.reshape(-1))
+    np.testing.assert_array_equal(kp2[spare], kp[spare])
+    np.testing.assert_array_equal(vp2[spare], vp[spare])
+
+
+def test_paged_commit_refusals():
+    """A commit past the table's capacity, or into a block outside the pool, leaves the
+    sequence unchanged and reports it; a bad entry the commit does not reach is harmless."""
+    from oracle import kv_commit_paged
+    rng = np.random.default_rng(7)
+    B, Hkv, T, D, bs, max_blocks = 3, 1, 15, 4, 8, 3
+    tree, table, kp, vp, kt, vt, _ = _paged_case(rng, B, Hkv, T, D, bs, max_blocks, [0, 0, 0])
+    ends = [int(np.argmax(tree["depth"]))] * B
+    m = int(tree["depth"][ends[0]])
+    apath = np.full((B, tree["max_depth"] + 1), -1, dtype=np.int32)
+    for b in range(B):
+        p = _path_to(tree, ends[b])
+        apath[b, :len(p)] = p
+    alen = np.full(B, m, dtype=np.int32)
+    plen = np.array([max_blocks * bs - m - 1,      # the m + 1 rows exactly fit
+                     max_blocks * bs - m,          # one row too many
+                     0], dtype=np.int32)
+    table[2, 0] = kp.shape[0] + 5                  # sequence 2 writes into block 0: outside the pool
+    table[0, 0] = -1                                # sequence 0 does not reach block 0 (m < bs)
+    assert m + 1 <= bs
+    kp2, vp2, L2, bad = kv_commit_paged(kt, vt, kp, vp, table, bs, plen, alen, apath, tree)
+    np.testing.assert_array_equal(bad, [False, True, True])
+    np.testing.assert_array_equal(L2, [plen[0] + m + 1, plen[1], plen[2]])
+    touched = np.zeros(kp.shape[0], dtype=bool)
+    for i in range(m + 1):
+        touched[table[0, (plen[0] + i) // bs]] = True
+    np.testing.assert_array_equal(kp2[~touched], kp[~touched])
