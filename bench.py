@@ -551,6 +551,7 @@ CONFIG_ENTRIES = [
     ("vicuna7b_layernorm_heads", "draft-ln-heads-vicuna7b", False),
     ("vicuna7b_kv_commit", "kv-commit-vicuna7b", False),
     ("gqa70b_b8_kv_commit", "kv-commit-70b-b8", False),
+    ("gqa70b_b8_kv_commit_paged", "kv-commit-paged-70b-b8", False),
 ]
 
 
@@ -687,6 +688,7 @@ COMPONENTS = {
     "attention-paged-70b-b8": (4, "attention_paged", None),
     "kv-commit-vicuna7b": (2, "commit", None),
     "kv-commit-70b-b8": (4, "commit", None),
+    "kv-commit-paged-70b-b8": (4, "commit_paged", None),
 }
 
 
@@ -857,7 +859,7 @@ def make_component(name, dev, no_fold=False):
         call = lambda: st.tree_accept_typical(lp, tok, tree, temperature=w.temperature, epsilon=0.09, alpha=0.3,
                                               seed=w.philox_seed, accept_len=outs[0], accept_path=outs[1],
                                               next_token=outs[2], margin=outs[3], ws=ws)
-    elif part == "commit":
+    elif part in ("commit", "commit_paged"):
         # paths from the library's own greedy acceptance on planted target logits (once, untimed)
         ax = wl.attention_inputs(w, T)
         kc, vc, kt, vt = (dev_t(ax[k]) for k in ("k_cache", "v_cache", "k_tree", "v_tree"))
@@ -870,7 +872,17 @@ def make_component(name, dev, no_fold=False):
         rows = int(alen.sum().item()) + w.B                   # committed rows per head, over the batch
         abytes = 2.0 * 2 * rows * w.Hkv * w.D * s             # K and V, read from the tree and written to the cache
         pre = lambda: plen.copy_(plen0)                       # every call commits onto the same prefix
-        call = lambda: st.tree_kv_commit(kt, vt, kc, vc, plen, alen, apath, tree, ws=ws)
+        if part == "commit_paged":
+            # the same commit into a paged pool: 128-row blocks in a shuffled slot order
+            bs = 128
+            n_blocks = -(-w.Lmax // bs)
+            order = np.random.default_rng(w.seed).permutation(w.B * n_blocks).astype(np.int32)
+            table = dev_t(order.reshape(w.B, n_blocks))
+            kpool = torch.empty(w.B * n_blocks, w.Hkv, bs, w.D, dtype=kc.dtype, device=dev)
+            vpool = torch.empty_like(kpool)
+            call = lambda: st.tree_kv_commit_paged(kt, vt, kpool, vpool, table, bs, plen, alen, apath, tree, ws=ws)
+        else:
+            call = lambda: st.tree_kv_commit(kt, vt, kc, vc, plen, alen, apath, tree, ws=ws)
     else:
         B = w.B
         if w.accept == "greedy":
@@ -890,7 +902,7 @@ def make_component(name, dev, no_fold=False):
         call = lambda: st.tree_accept(mode, lp, lq, tok, tree, temperature=w.temperature, seed=w.philox_seed,
                                       accept_len=outs[0], accept_path=outs[1], next_token=outs[2], margin=outs[3], ws=ws)
 
-    if part != "commit":
+    if part not in ("commit", "commit_paged"):
         pre = lambda: None
     comp = {"name": name, "config_id": wid, "dtype": w.dtype, "tree_nodes": T, "call": call, "pre": pre,
             "abytes": abytes, "flops": flops, "report": lambda: {}, "kernel_work": {}}

@@ -446,6 +446,28 @@ spec_status tree_kv_commit(const void* k_tree, const void* v_tree, void* k_cache
                            const spec_tree* tree, int32_t B, int32_t Hkv, int32_t Lmax, int32_t D,
                            spec_dtype dt, void* ws, size_t ws_bytes, spec_stream_t s);
 
+/*
+ * KV commit into a paged cache -- the same commit as tree_kv_commit (same
+ * sections) with the cache in pre-allocated static blocks (Hydra Guide, "Hydra
+ * Production Engineering Checklist", item 3), the layout tree_attention_paged
+ * reads: cache position L + i of sequence b is row (L + i) % block_size of pool
+ * block block_table[b, (L + i) / block_size] of every KV head.
+ *
+ *   k_pool, v_pool  device [num_blocks, Hkv, block_size, D] (dt), updated in place
+ *   block_table     device [B, max_blocks] int32; only the entries of the blocks
+ *                   the commit writes are read
+ *   block_size      positive; max_blocks * block_size <= 2^22
+ *   the rest as tree_kv_commit (ws >= tree_kv_commit_workspace_size() bytes).
+ * Besides tree_kv_commit's checks, a sequence whose commit would pass
+ * max_blocks * block_size positions or write a block outside 0 .. num_blocks-1
+ * is left unchanged and SPEC_EINVAL goes to the status word.
+ */
+spec_status tree_kv_commit_paged(const void* k_tree, const void* v_tree, void* k_pool, void* v_pool,
+                                 int32_t num_blocks, const int32_t* block_table, int32_t max_blocks,
+                                 int32_t block_size, int32_t* prefix_len, const int32_t* accept_len,
+                                 const int32_t* accept_path, const spec_tree* tree, int32_t B, int32_t Hkv,
+                                 int32_t D, spec_dtype dt, void* ws, size_t ws_bytes, spec_stream_t s);
+
 /* Message of the last failed call on this host thread ("" if none). */
 const char* spec_last_error(void);
 

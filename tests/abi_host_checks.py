@@ -207,3 +207,27 @@ def test_kv_commit_rejects_before_launch(lib):
     assert call(tree=lib.spec_tree()) == 1     # a tree that was never built
 
 
+
+
+def test_kv_commit_paged_rejects_before_launch(lib):
+    # every call here fails a host check, so nothing is queued (no device access)
+    import spec_workloads as wl
+    parent, _ = wl.cartesian_tree((2, 3))
+    t = _fake_tree(lib, [int(x) for x in parent])
+    L = lib._lib
+    vp = ctypes.c_void_p
+
+    def call(k_pool=FAKE, table=FAKE, num_blocks=8, max_blocks=4, bs=64, D=64, dt=1, ws_bytes=256):
+        return L.tree_kv_commit_paged(vp(FAKE), vp(FAKE), vp(k_pool), vp(FAKE), num_blocks, vp(table), max_blocks, bs,
+                                      vp(FAKE), vp(FAKE), vp(FAKE), ctypes.byref(t), 1, 4, D, dt, vp(FAKE), ws_bytes,
+                                      None)
+    assert call(table=0) == 1                  # no block table
+    assert call(num_blocks=0) == 1
+    assert call(bs=0) == 1
+    assert call(max_blocks=1 << 16, bs=128) == 1   # more than 2^22 positions
+    assert call(k_pool=0) == 1                 # NULL pool
+    assert call(k_pool=FAKE + 4) == 3          # misaligned pool
+    assert call(table=FAKE + 2) == 3           # misaligned table
+    assert call(D=4) == 1                      # 8-byte rows
+    assert call(ws_bytes=16) == 4
+    assert call(dt=7) == 5

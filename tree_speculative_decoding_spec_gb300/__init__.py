@@ -13,7 +13,7 @@ __all__ = [
     "tree_attention_noalloc_status",
     "tree_attention_paged", "tree_attention_paged_workspace_size",
     "tree_accept", "tree_accept_workspace_size", "tree_accept_typical",
-    "tree_kv_commit", "tree_kv_commit_workspace_size",
+    "tree_kv_commit", "tree_kv_commit_paged", "tree_kv_commit_workspace_size",
     "spec_philox_uniform", "spec_read_device_status", "spec_last_error", "spec_selftest_timeout",
     "spec_trace_begin", "spec_trace_end", "spec_launch_count",
     "SpecError", "Tree",

@@ -85,6 +85,8 @@ def _load():
         "tree_accept_typical": (i32, [vp, vp, tp, i32, i32, f32, f32, f32, u64, u64, vp, vp, vp, vp, vp, sz, vp]),
         "tree_kv_commit_workspace_size": (sz, []),
         "tree_kv_commit": (i32, [vp, vp, vp, vp, vp, vp, vp, tp, i32, i32, i32, i32, i32, vp, sz, vp]),
+        "tree_kv_commit_paged": (i32, [vp, vp, vp, vp, i32, vp, i32, i32, vp, vp, vp, tp, i32, i32, i32, i32, vp, sz,
+                                       vp]),
         "spec_philox_uniform": (i32, [u64, u64, i32, i32, vp, vp, vp]),
         "spec_last_error": (ctypes.c_char_p, []),
         "spec_read_device_status": (i32, [vp, _i32p, vp]),
@@ -557,6 +559,39 @@ def tree_kv_commit(k_tree, v_tree, k_cache, v_cache, prefix_len, accept_len, acc
                                                      _ptr(prefix_len), _ptr(accept_len), _ptr(accept_path),
                                                      tree.ref(), B, Hkv, Lmax, D, dt, _ptr(ws), ws.numel(),
                                                      _stream(stream)))
+    return ws
+
+
+def tree_kv_commit_paged(k_tree, v_tree, k_pool, v_pool, block_table, block_size, prefix_len, accept_len,
+                         accept_path, tree, ws=None, stream=None):
+    """tree_kv_commit into a paged cache: pool [num_blocks, Hkv, block_size, D], block_table [B, max_blocks]."""
+    _need(k_tree, "k_tree", ndim=4)
+    dev = k_tree.device
+    B, Hkv, T, D = k_tree.shape
+    if T != tree.T:
+        raise ValueError(f"k_tree has {T} nodes, the tree {tree.T}")
+    for name, t in (("v_tree", v_tree), ("k_pool", k_pool), ("v_pool", v_pool)):
+        _need(t, name, dtype=k_tree.dtype, ndim=4, device=dev)
+    if tuple(v_tree.shape) != (B, Hkv, T, D):
+        raise ValueError("v_tree must match k_tree")
+    num_blocks = k_pool.shape[0]
+    if tuple(k_pool.shape) != (num_blocks, Hkv, block_size, D) or tuple(v_pool.shape) != tuple(k_pool.shape):
+        raise ValueError("pools must be [num_blocks, Hkv, block_size, D] with the tree's Hkv and D")
+    _need(block_table, "block_table", dtype=torch.int32, ndim=2, device=dev)
+    if block_table.shape[0] != B:
+        raise ValueError("block_table must be [B, max_blocks]")
+    _need(prefix_len, "prefix_len", dtype=torch.int32, ndim=1, device=dev)
+    _need(accept_len, "accept_len", dtype=torch.int32, ndim=1, device=dev)
+    _need(accept_path, "accept_path", dtype=torch.int32, ndim=2, device=dev)
+    if prefix_len.shape[0] != B or accept_len.shape[0] != B or tuple(accept_path.shape) != (B, tree.max_depth + 1):
+        raise ValueError("prefix_len, accept_len [B] and accept_path [B, max_depth + 1] must match")
+    dt = _dtype_code(k_tree)
+    ws = _workspace(int(_lib.tree_kv_commit_workspace_size()), dev, ws)
+    with torch.cuda.device(dev):
+        _check("tree_kv_commit_paged", _lib.tree_kv_commit_paged(
+            _ptr(k_tree), _ptr(v_tree), _ptr(k_pool), _ptr(v_pool), num_blocks, _ptr(block_table),
+            block_table.shape[1], block_size, _ptr(prefix_len), _ptr(accept_len), _ptr(accept_path), tree.ref(), B, Hkv,
+            D, dt, _ptr(ws), ws.numel(), _stream(stream)))
     return ws
 
 
