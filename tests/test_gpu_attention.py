@@ -137,3 +137,41 @@ def test_attention_ignores_cache_past_prefix(dtype, Hq, Hkv, T):
     O, Lse = oracle.tree_attention(**clean, tree=oracle.tree_encode(parent, rank), dtype=dtype)
     assert_close(out, O, dtype, "out")
     assert_close(lse, Lse, dtype, "lse")
+
+
+def _sweep_cases(n=64, seed=2024):
+    """Seeded random shapes over both paths: bf16 head dim 128 with >= 64 query rows per KV head
+    (tensor cores: split plans of every kind, the K/V completion forms, fused or combined
+    merges) and the CUDA-core path (fp32, or few rows)."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        dtype = "bf16" if rng.random() < 0.75 else "f32"
+        Hkv = int(rng.choice([1, 2, 4, 8]))
+        g = int(rng.choice([1, 2, 4, 8]))
+        T = int(rng.integers(1, 400))
+        D = 128 if dtype == "bf16" and rng.random() < 0.8 else 64
+        B = int(rng.integers(1, 7))
+        Lmax = int(rng.integers(1, 5000))
+        prefix = [int(x) for x in rng.integers(0, Lmax + 1, size=B)]
+        cases.append((i, dtype, B, Hkv * g, Hkv, T, D, Lmax, prefix))
+    return cases
+
+
+@pytest.mark.parametrize("case", _sweep_cases(), ids=lambda c: f"sweep{c[0]}-{c[1]}-B{c[2]}-H{c[3]}/{c[4]}-T{c[5]}-D{c[6]}-L{c[7]}")
+def test_attention_random_sweep(case):
+    """Element by element against the oracle on four sampled (sequence, head) pairs per shape."""
+    st = lib()
+    i, dtype, B, Hq, Hkv, T, D, Lmax, prefix = case
+    rng = np.random.default_rng(1000 + i)
+    parent, rank = wl.random_tree(rng, T, max_children=4)
+    tree = st.spec_tree_build(parent, rank)
+    x = _rand_inputs(rng, dtype, B, Hq, Hkv, len(parent), D, Lmax, prefix)
+    out, lse = _run(st, x, tree, dtype)
+    pairs = [(b, h) for b in range(B) for h in range(Hq)]
+    heads = [pairs[j] for j in rng.choice(len(pairs), size=min(4, len(pairs)), replace=False)]
+    O, L = oracle.tree_attention(**x, tree=oracle.tree_encode(parent, rank), dtype=dtype, heads=heads)
+    sel = ~np.isnan(L)
+    assert sel.any()
+    assert_close(out[sel], O[sel], dtype, "out")
+    assert_close(lse[sel], L[sel], dtype, "lse")
