@@ -208,3 +208,67 @@ def test_out_of_vocabulary_token_is_flagged():
     a, p, n, _ = st.tree_accept(1, to_dev(lp), to_dev(lp), to_dev(tok), tree, temperature=1.0, ws=ws)
     assert st.spec_read_device_status(ws) == 1      # SPEC_EINVAL recorded on the device
     assert int(a.cpu()[0]) == 0
+
+
+def test_rejection_vocabulary_past_the_walk_cache():
+    """V = 50000: above the 40,960 tokens whose draw weights the rejection walk keeps in shared
+    memory, so the draw recomputes them from the logits on every scan."""
+    st = lib()
+    rng = np.random.default_rng(50000)
+    V, B, temp = 50000, 6, 0.8
+    parent, rank = wl.random_tree(rng, 40, max_children=3)
+    T = len(parent)
+    lq = rng.standard_normal((B, T, V), dtype=np.float32) * np.float32(2.0)
+    lp = ((np.float32(0.8) * lq + np.float32(0.6) * rng.standard_normal((B, T, V), dtype=np.float32))
+          * np.float32(2.0)).astype(np.float32)
+    tok = wl.sibling_tokens(rng, parent, B, V)
+    near_total = 0
+    for offset in range(3):
+        near, _ = _compare_rejection(st, lp, lq, tok, parent, rank, temp, 7, offset)
+        near_total += near
+    assert near_total <= 2
+
+
+def _greedy_sweep(n=16, seed=31):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        T = int(rng.integers(1, 300))
+        V = int(rng.choice([2, 3, 17, 1000, 32000, 50001]))
+        B = int(rng.integers(1, 9))
+        out.append((i, T, V, B))
+    return out
+
+
+@pytest.mark.parametrize("case", _greedy_sweep(), ids=lambda c: f"sweep{c[0]}-T{c[1]}-V{c[2]}-B{c[3]}")
+def test_greedy_random_sweep(case):
+    """Random trees, vocabularies (odd sizes and past 2^15) and batches, target logits planted to
+    accept random paths, plus exact ties between the planted token and a rival: bit-exact."""
+    st = lib()
+    i, T, V, B = case
+    rng = np.random.default_rng(100 + i)
+    parent, rank = wl.random_tree(rng, T, max_children=4)
+    T = len(parent)
+    tree = st.spec_tree_build(parent, rank)
+    tok = wl.sibling_tokens(rng, parent, B, V) if V >= 5 else rng.integers(0, V, size=(B, T)).astype(np.int32)
+    lp = rng.standard_normal((B, T, V), dtype=np.float32)
+    # plant: along a random path each node's row prefers its chosen child's token, some by an
+    # exact tie with a lower-numbered rival (which then wins)
+    for b in range(B):
+        u = 0
+        while True:
+            kids = [c for c in range(1, T) if parent[c] == u]
+            if not kids or rng.random() < 0.25:
+                break
+            c = kids[int(rng.integers(0, len(kids)))]
+            top = float(lp[b, u].max()) + 1.0
+            lp[b, u, tok[b, c]] = top
+            if rng.random() < 0.3 and V > 1:
+                rival = int(rng.integers(0, V))
+                lp[b, u, rival] = top
+            u = c
+    a, p, n, _ = _greedy(st, lp, tok, tree)
+    ref = oracle.greedy_accept(lp, tok, oracle.tree_encode(parent, rank))
+    assert np.array_equal(a, ref["accept_len"])
+    assert np.array_equal(p, ref["accept_path"])
+    assert np.array_equal(n, ref["next_token"])

@@ -384,3 +384,39 @@ def test_draft_exact_ties_take_the_lower_token(dtype, d, V, folded):
             for i in range(0, len(t), 4):
                 grp = t[i:i + 4]
                 assert grp == sorted(grp) and len({g % q for g in grp}) == 1, (b, u, t)
+
+
+def _draft_sweep(n=20, seed=77):
+    """Seeded random draft shapes: width, vocabulary, batch, branching, conditioning and top-k,
+    folded or not (bf16 widths of 128 and up take the tensor-core path)."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for i in range(n):
+        dtype = "bf16" if rng.random() < 0.6 else "f32"
+        d = int(rng.choice([64, 128, 256] if dtype == "bf16" else [32, 64, 96]))
+        V = int(rng.integers(50, 6000))
+        B = int(rng.integers(1, 4))
+        K = int(rng.integers(1, 4))
+        branching = tuple(int(x) for x in rng.integers(1, 5, size=K))
+        cond = tuple(int(x) for x in rng.choice([0, 1, 2], size=K))
+        topk = tuple(int(max(b, rng.integers(1, 9))) for b in branching)
+        folded = bool(rng.random() < 0.3)
+        cases.append((i, dtype, d, V, B, branching, cond, topk, folded))
+    return cases
+
+
+@pytest.mark.parametrize("case", _draft_sweep(), ids=lambda c: f"sweep{c[0]}-{c[1]}-d{c[2]}-V{c[3]}-B{c[4]}-K{len(c[5])}{'-fold' if c[8] else ''}")
+def test_draft_random_sweep(case):
+    st = lib()
+    i, dtype, d, V, B, branching, cond, topk, folded = case
+    w = wl.Workload("sweep", dtype, B=B, seed=500 + i, tree=("cartesian", branching), d=d, V=V, cond=cond, topk=topk)
+    parent, rank = wl.make_tree(w.tree)
+    x = wl.draft_inputs(w)
+    rng = np.random.default_rng(900 + i)
+    enc = (lambda a: wl.f32_to_bf16_bits(a)) if dtype == "bf16" else (lambda a: a)
+    x["W2"] = [enc(rng.standard_normal(np.shape(a), dtype=np.float32) * np.float32(0.25)) for a in x["W2"]]
+    x["E"] = enc(rng.standard_normal(np.shape(x["E"]), dtype=np.float32))
+    if folded:
+        _compare_folded(st, x, parent, rank, dtype)
+    else:
+        _compare(st, x, parent, rank, dtype)

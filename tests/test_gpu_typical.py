@@ -105,3 +105,19 @@ def test_typical_equal_logits():
     _, us = acceptance_uniforms(42, 3, B, T)
     assert (a.cpu().numpy() == 2).all()
     np.testing.assert_array_equal(n.cpu().numpy(), np.floor(np.asarray(us) * V).astype(int))
+
+
+def test_typical_vocabulary_past_the_walk_cache():
+    """V = 50000: the extra token's draw weights are recomputed from the logits on every scan."""
+    st = lib()
+    rng = np.random.default_rng(50001)
+    V, B = 50000, 6
+    parent, rank = wl.random_tree(rng, 40, max_children=3)
+    T = len(parent)
+    lp = rng.standard_normal((B, T, V), dtype=np.float32) * np.float32(3.0)
+    tok = wl.sibling_tokens(rng, parent, B, V)
+    near_total = 0
+    for offset in range(3):
+        near, _ = _compare(st, lp, tok, parent, rank, 0.7, 0.09, 0.3, 11, offset)
+        near_total += near
+    assert near_total <= 2
