@@ -124,3 +124,43 @@ def test_paged_70b_gqa_sampled():
     for b, h in heads:
         assert_close(out[b, h], O[b, h], "bf16", f"out[{b},{h}]")
         assert_close(lse[b, h], L[b, h], "bf16", f"lse[{b},{h}]")
+
+
+def _paged_sweep(n=24, seed=4242):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n):
+        dtype = "bf16" if rng.random() < 0.75 else "f32"
+        bs = int(rng.choice([64, 128, 192, 256]))
+        Hkv = int(rng.choice([1, 2, 4]))
+        g = int(rng.choice([1, 2, 4, 8]))
+        T = int(rng.integers(1, 260))
+        D = 128 if dtype == "bf16" and rng.random() < 0.8 else 64
+        B = int(rng.integers(1, 5))
+        Lmax = bs * int(rng.integers(1, 14))
+        prefix = [int(x) for x in rng.integers(0, Lmax + 1, size=B)]
+        out.append((i, dtype, B, Hkv * g, Hkv, T, D, Lmax, prefix, bs))
+    return out
+
+
+@pytest.mark.parametrize("case", _paged_sweep(), ids=lambda c: f"sweep{c[0]}-{c[1]}-B{c[2]}-H{c[3]}/{c[4]}-T{c[5]}-D{c[6]}-bs{c[9]}")
+def test_paged_random_sweep(case):
+    """Random shapes and block sizes: the paged call reproduces the contiguous call bit for bit on
+    the same logical data, and matches the oracle on four sampled (sequence, head) pairs."""
+    st = lib()
+    i, dtype, B, Hq, Hkv, T, D, Lmax, prefix, bs = case
+    parent, rank, x, kpool, vpool, table = _case(dtype, B, Hq, Hkv, T, D, Lmax, prefix, bs, 7000 + i)
+    tree = st.spec_tree_build(parent, rank)
+    out_p, lse_p = st.tree_attention_paged(to_dev(x["q"]), to_dev(kpool), to_dev(vpool), to_dev(table),
+                                           to_dev(x["prefix_len"]), to_dev(x["k_tree"]), to_dev(x["v_tree"]), tree)
+    out_c, lse_c = st.tree_attention(to_dev(x["q"]), to_dev(x["k_cache"]), to_dev(x["v_cache"]), to_dev(x["prefix_len"]),
+                                     to_dev(x["k_tree"]), to_dev(x["v_tree"]), tree)
+    out_p, lse_p, out_c, lse_c = (t.cpu().numpy() for t in (out_p, lse_p, out_c, lse_c))
+    assert np.array_equal(out_p, out_c) and np.array_equal(lse_p, lse_c)
+    rng = np.random.default_rng(i)
+    pairs = [(b, h) for b in range(B) for h in range(Hq)]
+    heads = [pairs[j] for j in rng.choice(len(pairs), size=min(4, len(pairs)), replace=False)]
+    O, L = oracle.tree_attention(**x, tree=oracle.tree_encode(parent, rank), dtype=dtype, heads=heads)
+    sel = ~np.isnan(L)
+    assert_close(out_p[sel], O[sel], dtype, "out")
+    assert_close(lse_p[sel], L[sel], dtype, "lse")
