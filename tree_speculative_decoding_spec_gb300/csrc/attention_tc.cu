@@ -48,6 +48,13 @@ constexpr int kARows = 128;        // query rows per CTA (MMA M)
 constexpr int kAKeys = 128;        // keys per tile
 constexpr int kAD = 128;           // head dim
 constexpr int kAStages = 3;
+// Landing barriers of the K/V ring: tile j signals k_full[j % kKFull].  The stages
+// alternate between the two MMA threads (tile j belongs to thread j % 2), so with
+// one barrier per stage a thread would wait on a phase whose predecessor the other
+// thread consumed -- and a parity wait cannot tell a phase still open from one two
+// phases back (a tile landing out of order would pass it early).  With 2 x kAStages
+// barriers each belongs to one thread, which waits on every phase of it in order.
+constexpr int kKFull = 2 * kAStages;
 constexpr int kAPrefetch = 2;     // contiguous prefix tiles prefetched into L2 ahead of their load
 constexpr int kAThreads = 352;
 constexpr int kQBytes = 2 * kARows * 128;         // two 64-column halves of 128 rows
@@ -169,8 +176,8 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     uint8_t* sKV = sQ + kQBytes;                       // stage s: K half0, K half1, V half0, V half1
     uint64_t* bars = reinterpret_cast<uint64_t*>(sKV + kAStages * kStageBytes);
     uint64_t* q_full = bars;
-    uint64_t* k_full = bars + 1;                       // [stage] the stage's K tile (and V, unless kApart) landed
-    uint64_t* v_full = k_full + kAStages;              // [stage] its V tile landed (kApart only)
+    uint64_t* k_full = bars + 1;                       // [j % kKFull] tile j's K (and V, unless kApart) landed
+    uint64_t* v_full = k_full + kKFull;                // [stage] its V tile landed (kApart only)
     uint64_t* kv_empty = v_full + kAStages;            // [stage] PV of the stage's tile complete
     uint64_t* s_full = kv_empty + kAStages;            // [group]
     uint64_t* p_full = s_full + 2;                     // [group]
@@ -178,12 +185,13 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(o_final + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     float2* merge = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(bars) + 256);   // [128] group 1's (m, l)
+    static_assert((1 + kKFull + 2 * kAStages + 5) * 8 + 8 <= 256, "barriers and flags end before the merge buffer");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        for (int s = 0; s < kKFull; ++s) mbar_init(&k_full[s], 1);
         for (int s = 0; s < kAStages; ++s) {
-            mbar_init(&k_full[s], 1);
             mbar_init(&v_full[s], 1);
             mbar_init(&kv_empty[s], 1);
         }
@@ -262,9 +270,10 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
                     *abort_flag = 1;
                     break;
                 }
-                uint64_t* vbar = kApart ? &v_full[s] : &k_full[s];
-                mbar_arrive_expect_tx(&k_full[s], kApart ? 2 * kKVHalf : kStageBytes);
-                load(&tmKc, &tmKt, &k_full[s], st);
+                uint64_t* kbar = &k_full[j % kKFull];
+                uint64_t* vbar = kApart ? &v_full[s] : kbar;
+                mbar_arrive_expect_tx(kbar, kApart ? 2 * kKVHalf : kStageBytes);
+                load(&tmKc, &tmKt, kbar, st);
                 if (kApart) mbar_arrive_expect_tx(vbar, 2 * kKVHalf);
                 load(&tmVc, &tmVt, vbar, st + 2 * kKVHalf);
                 issued = j + 1;
@@ -294,10 +303,19 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
             // offset sub-tile is the base descriptor plus offset / 16
             const uint64_t qd = sdesc_k128(smem_u32(sQ));
             bool ok = mbar_wait_or_abort(q_full, 0, abort_flag);
+            // this thread's landing barrier and phase for its next S (j = g, g + 2, ...), kept
+            // as counters: no division on the issue path
+            int kf = g;
+            uint32_t kf_phase = 0;
             // S_j = Q K_j^T: K = 128 in 8 steps of 16 (two 64-column halves)
             auto issue_s = [&](int j) -> bool {
                 const int s = j % kAStages;
-                if (!mbar_wait_or_abort(&k_full[s], (j / kAStages) & 1, abort_flag)) return false;
+                if (!mbar_wait_or_abort(&k_full[kf], kf_phase, abort_flag)) return false;
+                kf += 2;
+                if (kf >= kKFull) {
+                    kf -= kKFull;
+                    kf_phase ^= 1u;
+                }
                 tc_fence_after();
                 const uint64_t kd = sdesc_k128(smem_u32(sKV + s * kStageBytes));
                 const uint32_t dst = tmem + (j & 1) * kAKeys;
@@ -530,7 +548,7 @@ __global__ void __launch_bounds__(kAThreads, 1) k_attn_tc(const __grid_constant_
         // a wait ran out: let this CTA's own loads and MMAs land before releasing memory
         if (warp == 8 && lane == 0) {
             for (int j = max(0, issued - kAStages); j < issued; ++j) {
-                mbar_wait(&k_full[j % kAStages], (j / kAStages) & 1, 100000000ull);
+                mbar_wait(&k_full[j % kKFull], (j / kKFull) & 1, 100000000ull);
                 if (kApart) mbar_wait(&v_full[j % kAStages], 0, 100000000ull);
             }
             mbar_wait(q_full, 0, 100000000ull);
